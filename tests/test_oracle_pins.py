@@ -1,0 +1,321 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each oracle step is checked against an independent statement of the same fact: a library
+conversion, a float64 evaluation, brute-force enumeration, an independent full sort, a
+textbook argsort, a stable library sort, invariants, and hand-worked examples whose values
+were computed on paper (tests/golden/).  A plausible slip in the oracle -- a dropped bias,
+a wrong sign, max instead of the top-2 sum, the biased key in the weights, an unstable
+placement, a wrong sentinel -- fails at least one of these.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _support import check_sort_invariants, load_golden
+from moe_expert_routing_sort_gb300 import datagen
+
+ALL_BF16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+
+
+def _finite_bf16():
+    f = torch.from_numpy(ALL_BF16.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    return ALL_BF16[np.isfinite(f)], f[np.isfinite(f)]
+
+
+def _ulp32(x):
+    x = np.abs(np.asarray(x, np.float32))
+    return np.spacing(x).astype(np.float64)
+
+
+# ------------------------------------------------------------------- O1: bf16 decode
+def test_bf16_decode_matches_torch_all_patterns(oracle_mod):
+    got = oracle_mod.bf16_to_float_array(ALL_BF16).view(np.uint32)
+    ref = (torch.from_numpy(ALL_BF16.view(np.int16).copy()).view(torch.bfloat16)
+           .float().numpy().view(np.uint32))
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ O2: sigmoid score
+def test_sigmoid_special_values(oracle_mod):
+    assert oracle_mod.sigmoid(0.0) == 0.5
+    assert oracle_mod.sigmoid(-0.0) == 0.5
+    assert oracle_mod.sigmoid(math.inf) == 1.0
+    assert oracle_mod.sigmoid(-math.inf) == 0.0
+    assert oracle_mod.sigmoid(100.0) == 1.0
+    assert oracle_mod.sigmoid(-100.0) == 0.0
+
+
+def test_sigmoid_vs_float64_all_finite_bf16(oracle_mod):
+    _, x = _finite_bf16()
+    s32 = oracle_mod.sigmoid_array(x).astype(np.float64)
+    with np.errstate(over="ignore"):
+        e64 = np.exp(-x.astype(np.float64))
+    s64 = 1.0 / (1.0 + e64)
+    # where expf(-x) overflows binary32 (x < -88.72) the formula's value is exactly 0
+    overflow = e64 > np.finfo(np.float32).max
+    assert np.all(s32[overflow] == 0.0)
+    # elsewhere: expf (<= 1 ulp), the add and the divide (<= 0.5 ulp each) keep the result
+    # within 2 ulp; below the normal range an absolute floor of a few subnormal steps
+    tol = np.maximum(2.0 * _ulp32(s64), 4e-45)
+    ok = ~overflow
+    assert np.all(np.abs(s32[ok] - s64[ok]) <= tol[ok])
+
+
+def test_sigmoid_monotone_and_symmetric(oracle_mod):
+    _, x = _finite_bf16()
+    order = np.argsort(x, kind="stable")
+    s = oracle_mod.sigmoid_array(x[order])
+    assert np.all(np.diff(s.astype(np.float64)) >= 0.0)
+    xs = x[order]
+    mid = np.abs(xs) < 30
+    sp = oracle_mod.sigmoid_array(xs[mid]).astype(np.float64)
+    sn = oracle_mod.sigmoid_array(-xs[mid]).astype(np.float64)
+    assert np.all(np.abs(sp + sn - 1.0) <= 2.5e-7)
+
+
+def test_sigmoid_vs_torch_float32(oracle_mod):
+    _, x = _finite_bf16()
+    s = oracle_mod.sigmoid_array(x).astype(np.float64)
+    ref = torch.sigmoid(torch.from_numpy(x)).double().numpy()
+    tol = np.maximum(3.0 * _ulp32(ref), 4e-45)
+    assert np.all(np.abs(s - ref) <= tol)
+
+
+# ------------------------------------------------------------------------ keys (R2)
+def test_keys_add_bias_to_unbiased_score(oracle_mod):
+    rng = np.random.default_rng(11)
+    E = 512
+    row = datagen.float32_to_bf16_bits(rng.standard_normal(E).astype(np.float32) * 2)
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    s, key = oracle_mod.scores_row(row, bias)
+    x = oracle_mod.bf16_to_float_array(row).astype(np.float64)
+    s64 = 1.0 / (1.0 + np.exp(-x))
+    assert np.all(np.abs(s - s64) <= 2 * _ulp32(s64))
+    k64 = s64 + bias.astype(np.float64)
+    # the score's own error (<= 2 ulp of s) carries over; the add rounds once more
+    assert np.all(np.abs(key - k64) <= 2 * _ulp32(s64) + _ulp32(k64))
+
+
+# ------------------------------------------------------------- O3: group scores (R3)
+@pytest.mark.parametrize("E,G", [(16, 4), (24, 8), (12, 12), (30, 5), (8, 1)])
+def test_group_score_is_best_pair_sum(oracle_mod, E, G):
+    rng = np.random.default_rng(E * 100 + G)
+    g = E // G
+    for _ in range(20):
+        key = rng.uniform(0.3, 1.1, E).astype(np.float32)
+        if rng.random() < 0.3:  # plant exact ties inside groups
+            key[1::3] = key[0]
+        gs = oracle_mod.group_scores_row(key, G)
+        for j in range(G):
+            grp = key[j * g:(j + 1) * g]
+            if g == 1:
+                ref = grp[0]
+            else:
+                ref = max(np.float32(grp[a]) + np.float32(grp[b])
+                          for a, b in itertools.combinations(range(g), 2))
+            assert gs[j] == np.float32(ref)
+
+
+# ---------------------------------------------------------- O4: kept groups (R4)
+def _beats(gs, a, b):
+    return gs[a] > gs[b] or (gs[a] == gs[b] and a < b)
+
+
+@pytest.mark.parametrize("G,Kg", [(8, 4), (8, 1), (8, 8), (6, 3), (5, 2), (1, 1)])
+def test_kept_groups_by_subset_enumeration(oracle_mod, G, Kg):
+    rng = np.random.default_rng(G * 10 + Kg)
+    for trial in range(40):
+        gs = rng.uniform(0.5, 2.2, G).astype(np.float32)
+        if trial % 4 == 0:  # ties between groups
+            gs[rng.integers(0, G, G // 2 + 1)] = gs[0]
+        winners = [
+            set(S) for S in itertools.combinations(range(G), Kg)
+            if all(_beats(gs, a, b) for a in S for b in range(G) if b not in S)
+        ]
+        assert len(winners) == 1
+        kept = oracle_mod.kept_groups_row(gs, Kg)
+        assert set(np.nonzero(kept)[0]) == winners[0]
+
+
+# ---------------------------------------------------------------- O5: top-k (R4, R5)
+@pytest.mark.parametrize("E,G,Kg,K", [(64, 8, 4, 6), (24, 4, 2, 5), (12, 6, 3, 6),
+                                      (32, 1, 1, 7), (16, 16, 5, 5)])
+def test_topk_matches_independent_full_sort(oracle_mod, E, G, Kg, K):
+    rng = np.random.default_rng(E + G + Kg + K)
+    g = E // G
+    for trial in range(30):
+        key = rng.uniform(0.2, 1.1, E).astype(np.float32)
+        if trial % 3 == 0:
+            key[rng.integers(0, E, E // 3)] = key[1]  # exact ties
+        gs = oracle_mod.group_scores_row(key, G)
+        kept = oracle_mod.kept_groups_row(gs, Kg)
+        ids = oracle_mod.topk_row(key, G, kept, K)
+        everything = sorted(range(E), key=lambda e: (-float(key[e]), e))
+        ref = [e for e in everything if kept[e // g]][:K]
+        assert list(ids) == ref
+        assert len(set(ids.tolist())) == K
+        assert all(kept[e // g] for e in ids)
+
+
+def test_topk_single_group_is_textbook_argsort(oracle_mod):
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        E, K = 896, 16
+        key = rng.uniform(0.2, 1.1, E).astype(np.float32)
+        key[rng.integers(0, E, 40)] = key[3]
+        kept = np.ones(1, np.int32)
+        ids = oracle_mod.topk_row(key, 1, kept, K)
+        ref = np.argsort(-key, kind="stable")[:K]
+        assert np.array_equal(ids, ref)
+
+
+# ------------------------------------------------------------------ O6: weights (R6)
+def test_weights_use_unbiased_scores_and_sum_to_scale(oracle_mod):
+    rng = np.random.default_rng(9)
+    w_ = datagen.workload("prefill_T512_E896")
+    inp = datagen.make_inputs(w_, T=64)
+    ids, w = oracle_mod.route(inp.logits_bf16, inp.bias, w_.n_group, w_.topk_group, w_.topk,
+                              w_.routed_scale)
+    x = oracle_mod.bf16_to_float_array(inp.logits_bf16).astype(np.float64)
+    s64 = 1.0 / (1.0 + np.exp(-x))
+    for t in range(ids.shape[0]):
+        sel = s64[t, ids[t]]
+        ref = sel / sel.sum() * w_.routed_scale
+        assert np.all(np.abs(w[t] - ref) <= 1e-6)
+        assert abs(float(w[t].astype(np.float64).sum()) - w_.routed_scale) <= \
+            w_.topk * 2 * np.spacing(np.float32(w_.routed_scale))
+        assert np.all(w[t] > 0) and np.all(w[t] <= w_.routed_scale)
+    del rng
+
+
+# ------------------------------------------------------------- whole route step
+@pytest.mark.parametrize("name", ["tiny_T4_E64", "decode_T1_E896_G8", "decode_T1_E896_G1",
+                                  "prefill_T512_E896", "skewed_T8192_E896",
+                                  "wide_T16384_E4096"])
+def test_route_invariants_on_workloads(oracle_mod, name):
+    w_ = datagen.workload(name)
+    inp = datagen.make_inputs(w_, T=min(w_.T, 48))
+    ids, wts = oracle_mod.route(inp.logits_bf16, inp.bias, w_.n_group, w_.topk_group,
+                                w_.topk, w_.routed_scale)
+    g = w_.E // w_.n_group
+    for t in range(ids.shape[0]):
+        s, key = oracle_mod.scores_row(inp.logits_bf16[t], inp.bias)
+        gs = oracle_mod.group_scores_row(key, w_.n_group)
+        kept = oracle_mod.kept_groups_row(gs, w_.topk_group)
+        assert len(set(ids[t].tolist())) == w_.topk
+        assert all(kept[e // g] for e in ids[t])
+        assert kept.sum() == w_.topk_group
+        ks = key[ids[t]]
+        assert np.all(ks[:-1] >= ks[1:])
+        # nothing outside the selection (inside the kept groups) beats the last slot
+        cand = [e for e in range(w_.E) if kept[e // g] and e not in set(ids[t].tolist())]
+        last = (float(ks[-1]), int(ids[t][-1]))
+        assert all((float(key[e]), -e) < (last[0], -last[1]) for e in cand)
+
+
+def test_route_golden_worked_examples(oracle_mod):
+    for name, c in load_golden("route_sort_worked_examples.txt").items():
+        logits = c["logits_bf16"].reshape(c["T"], c["E"])
+        res = oracle_mod.route_sort(logits, c["bias"], c["n_group"], c["topk_group"],
+                                    c["topk"], c["routed_scale"], c["block_m"])
+        assert np.array_equal(res.topk_ids.reshape(-1), c["topk_ids"]), name
+        assert np.array_equal(res.topk_weights.reshape(-1), c["topk_weights"]), name
+        assert res.num_tokens_post_pad == c["num_tokens_post_pad"], name
+        assert np.array_equal(res.sorted_token_ids, c["sorted_token_ids"]), name
+        assert np.array_equal(res.sorted_weights, c["sorted_weights"]), name
+        assert np.array_equal(res.expert_ids, c["expert_ids"]), name
+
+
+# --------------------------------------------------------------- O7/O8: sort step
+def test_sort_golden_worked_examples(oracle_mod):
+    for name, c in load_golden("sort_worked_examples.txt").items():
+        ids = c["topk_ids"].reshape(c["T"], c["topk"])
+        w = c["topk_weights"].reshape(c["T"], c["topk"])
+        res = oracle_mod.sort(ids, w, c["E"], c["block_m"])
+        assert res.num_tokens_post_pad == c["num_tokens_post_pad"], name
+        assert np.array_equal(res.sorted_token_ids, c["sorted_token_ids"]), name
+        assert np.array_equal(res.sorted_weights, c["sorted_weights"]), name
+        assert np.array_equal(res.expert_ids, c["expert_ids"]), name
+        assert res.flags == c["flags"], name
+
+
+def _stable_sort_reference(ids, w, E, B):
+    """Segments from Python's stable sort of the valid routes by expert."""
+    flat = ids.reshape(-1)
+    N = flat.size
+    valid = [r for r in range(N) if 0 <= flat[r] < E]
+    order = sorted(valid, key=lambda r: flat[r])  # stable: keeps (token, slot) order
+    out_ids, out_w, owners = [], [], []
+    for e in range(E):
+        seg = [r for r in order if flat[r] == e]
+        if not seg:
+            continue
+        padded = seg + [N] * ((-len(seg)) % B)
+        out_ids += padded
+        out_w += [float(w.reshape(-1)[r]) for r in seg] + [0.0] * (len(padded) - len(seg))
+        owners += [e] * (len(padded) // B)
+    return (np.array(out_ids, np.int32), np.array(out_w, np.float32),
+            np.array(owners, np.int32))
+
+
+@pytest.mark.parametrize("dist", ["uniform", "shared", "one_expert", "every_third_dropped",
+                                  "dup_in_token"])
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_sort_matches_stable_sort(oracle_mod, dist, B):
+    rng = np.random.default_rng(hash((dist, B)) % 2**32)
+    T, K, E = 37, 5, 29
+    if dist == "uniform":
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+    elif dist == "shared":
+        ids = np.stack([np.concatenate([[0], 1 + rng.permutation(E - 1)[:K - 1]])
+                        for _ in range(T)])
+    elif dist == "one_expert":
+        ids = np.full((T, K), 7)
+    elif dist == "every_third_dropped":
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+        ids.reshape(-1)[::3] = -1
+    else:
+        ids = rng.integers(0, E, (T, K))
+    ids = ids.astype(np.int32)
+    w = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
+    res = oracle_mod.sort(ids, w, E, B)
+    ref_ids, ref_w, ref_owner = _stable_sort_reference(ids, w, E, B)
+    assert np.array_equal(res.sorted_token_ids, ref_ids)
+    assert np.array_equal(res.sorted_weights, ref_w)
+    assert np.array_equal(res.expert_ids, ref_owner)
+    check_sort_invariants(ids, E, B, res.sorted_token_ids, res.expert_ids,
+                          res.num_tokens_post_pad, res.sorted_weights, w)
+
+
+def test_sort_empty_and_max_padded(oracle_mod):
+    ids = np.zeros((0, 4), np.int32)
+    res = oracle_mod.sort(ids, np.zeros((0, 4), np.float32), 16, 8)
+    assert res.num_tokens_post_pad == 0 and res.flags == 0
+    # worst case: N routes over min(E, N) experts, each padded by B-1
+    assert oracle_mod.max_padded(1, 896, 16, 32) == 16 + 16 * 31
+    assert oracle_mod.max_padded(16384, 4096, 8, 128) == 131072 + 4096 * 127
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        T, K, E, B = (int(rng.integers(1, 9)), int(rng.integers(1, 5)),
+                      int(rng.integers(1, 40)), int(2 ** rng.integers(0, 5)))
+        ids = rng.integers(0, E, (T, K)).astype(np.int32)
+        res = oracle_mod.sort(ids, np.ones((T, K), np.float32), E, B)
+        assert res.num_tokens_post_pad <= oracle_mod.max_padded(T, E, K, B)
+
+
+# ---------------------------------------------------------- near-tie margin helper
+def test_margins_detect_planted_ties(oracle_mod):
+    w_ = datagen.workload("decode_T1_E896_G1")
+    inp = datagen.make_inputs(w_, T=4)
+    m = oracle_mod.margins(inp.logits_bf16, inp.bias, 1, 1, 16)
+    assert np.all(m > 0)
+    # make experts 10 and 11 tie exactly and both land in the top-16 of token 0
+    logits = inp.logits_bf16.copy()
+    bias = inp.bias.copy()
+    logits[0, 10] = logits[0, 11] = datagen.float32_to_bf16_bits(np.float32([6.0]))[0]
+    bias[10] = bias[11] = 0.0
+    m2 = oracle_mod.margins(logits, bias, 1, 1, 16)
+    assert m2[0] == 0.0
