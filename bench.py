@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE route-sort path (one JSON line on stdout).
+
+Headline workload: Kimi-K3-shaped TP8 decode, T=1 token, E=896 experts, n_group=8,
+topk_group=4, top-16, block_m=32 (``decode_T1_E896_G8``); value = device microseconds per
+route-sort call.  The large-T workloads (T=512/E=896, T=8192/E=896 skewed,
+T=16384/E=4096) are measured in the same run and reported under ``configs`` as routed
+tokens/s and fraction of the HBM roofline.
+
+Timing: a step is one CUDA graph of C calls, each the whole path (route step + both sort
+phases) on its own input set and output set; the sets rotate so that their total is larger
+than twice the L2, and L2 is flushed (a 256 MiB write) before every timed step.  Each step
+is bracketed by CUDA events on the launching stream; warm-up steps are not timed.  Under
+torchrun each rank times its own replica (the path does not shard: replicas only), the step
+times are reduced with MAX over ranks and ``value`` is the per-call time of the whole job.
+
+``--impl reference`` times the CPU oracle (single thread, the slow plain definition) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_expert_routing_sort_gb300 import datagen  # noqa: E402
+
+HEADLINE = "decode_T1_E896_G8"
+SECONDARY = ["prefill_T512_E896", "skewed_T8192_E896", "wide_T16384_E4096"]
+L2_BYTES = 129 * 1024 * 1024
+FLUSH_BYTES = 256 * 1024 * 1024
+METRIC = "route-sort µs/call at T=1 E=896; routed tokens/s and % HBM roofline at T≥512"
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=HEADLINE, choices=list(datagen.WORKLOADS))
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the large-T workloads reported under 'configs'")
+    p.add_argument("--cpu-budget", type=float, default=10.0,
+                   help="seconds of oracle work for the CPU baseline of the headline workload")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------- helpers
+def algorithmic_bytes(w, npp: int) -> int:
+    """Logits + bias read, top-k ids/weights, sorted ids/weights, block owners, npp written."""
+    return (2 * w.T * w.E + 4 * w.E + 8 * w.T * w.topk + 8 * npp + 4 * (npp // w.block_m) + 4)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def dist_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- GPU timing
+class Replica:
+    """Rotating input/output sets of one workload on the current device."""
+
+    def __init__(self, w, n_sets: int):
+        import torch
+
+        import moe_expert_routing_sort_gb300 as mrs
+
+        self.w = w
+        self.sets = []
+        for i in range(n_sets):
+            inp = datagen.make_inputs(datagen.workload(w.name, seed=w.seed + i) if w.name in
+                                      datagen.WORKLOADS else w)
+            logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).cuda()
+            bias = torch.from_numpy(inp.bias).cuda()
+            out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
+            self.sets.append((logits, bias, out))
+        self.mrs = mrs
+
+    def call(self, i: int, stream=None):
+        logits, bias, out = self.sets[i]
+        w = self.w
+        self.mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                            w.block_m, out=out, stream=stream)
+
+    def npp(self) -> list:
+        return [int(o.num_tokens_post_pad.item()) for _, _, o in self.sets]
+
+
+def launches_per_call(w) -> int:
+    return 1 if w.T <= 64 else 3
+
+
+def time_graph_steps(rep: Replica, steps: int, warmup: int, world: int, clocks=None):
+    """Time `steps` graph replays (all sets once per step), L2 flushed before each step."""
+    import torch
+
+    s = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(s):
+        for i in range(len(rep.sets)):
+            rep.call(i)  # first calls outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(len(rep.sets)):
+            rep.call(i)
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            flush.fill_(1)
+            g.replay()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        # soak: keep the same work running ~1 s so the sampled clocks reflect it
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    flush.fill_(2)
+                    g.replay()
+            torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            starts[k].record(s)
+            g.replay()
+            ends[k].record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = dist_max(sum(step_ms), world)
+    return total_ms, step_ms
+
+
+def e2e_time(w, steps: int, warmup: int, world: int):
+    """Whole calls through the public API with host buffers: pinned H2D of the logits, the
+    route-sort call, D2H of every output (full buffers), timed with events on the stream."""
+    import torch
+
+    import moe_expert_routing_sort_gb300 as mrs
+
+    inp = datagen.make_inputs(w)
+    h_logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    bias = torch.from_numpy(inp.bias).cuda()  # router parameter, resident
+    d_logits = torch.empty_like(h_logits, device="cuda")
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
+    outs = [out.topk_ids, out.topk_weights, out.sorted_token_ids, out.sorted_weights,
+            out.expert_ids, out.num_tokens_post_pad]
+    h_outs = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    s = torch.cuda.Stream()
+
+    def one():
+        with torch.cuda.stream(s):
+            d_logits.copy_(h_logits, non_blocking=True)
+            mrs.route_sort(d_logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                           w.block_m, out=out)
+            for h, d in zip(h_outs, outs):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record(s)
+    for _ in range(steps):
+        one()
+    with torch.cuda.stream(s):
+        b.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = dist_max(a.elapsed_time(b), world)
+    h2d = h_logits.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return ms, h2d, d2h
+
+
+def n_sets_for(w) -> int:
+    per = 2 * w.T * w.E
+    return int(min(64, max(2, math.ceil(2 * L2_BYTES / max(per, 1)))))
+
+
+def measure_workload(w, steps, warmup, world, peak_gbs, clocks=None):
+    n_sets = n_sets_for(w) if w.T > 1 else 32
+    rep = Replica(w, n_sets)
+    total_ms, step_ms = time_graph_steps(rep, steps, warmup, world, clocks)
+    calls = steps * n_sets
+    us_per_call = total_ms * 1e3 / calls
+    npps = rep.npp()
+    bytes_per_call = float(np.mean([algorithmic_bytes(w, n) for n in npps]))
+    achieved = bytes_per_call / (us_per_call * 1e-6) / 1e9
+    return {
+        "us_per_call": us_per_call,
+        "ms_per_step": total_ms / steps,
+        "calls_per_step": n_sets,
+        "tokens_per_s": w.T / (us_per_call * 1e-6),
+        "routes_per_s": w.T * w.topk / (us_per_call * 1e-6),
+        "algorithmic_bytes_per_call": bytes_per_call,
+        "achieved_gbs": achieved,
+        "roofline_frac": achieved / peak_gbs,
+        "launches": steps * n_sets * launches_per_call(w),
+        "npp_mean": float(np.mean(npps)),
+    }
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_oracle_rate(w, budget_s: float):
+    """Time the oracle on a bounded sample of workload w: (seconds per token, sample text)."""
+    import oracle
+
+    oracle.build()
+    if w.T == 1:
+        inp = datagen.make_inputs(w)
+        n = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                              w.routed_scale, w.block_m)
+            n += 1
+        dt = time.perf_counter() - t0
+        return dt / n, f"{n} whole calls on the T=1 input ({dt:.1f} s)"
+    # a token sample of the full workload: route step on the sample, sort step scaled
+    inp = datagen.make_inputs(w, T=min(w.T, 64))
+    t0 = time.perf_counter()
+    oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                      w.routed_scale, w.block_m)
+    per_tok = (time.perf_counter() - t0) / inp.logits_bf16.shape[0]
+    n_tok = int(max(16, min(w.T, budget_s / max(per_tok, 1e-7))))
+    inp = datagen.make_inputs(w, T=n_tok)
+    t0 = time.perf_counter()
+    oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                      w.routed_scale, w.block_m)
+    dt = time.perf_counter() - t0
+    return dt / n_tok, f"first {n_tok} of {w.T} tokens, whole path ({dt:.1f} s)"
+
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on this host (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    if w.T <= 64:
+        inp = datagen.make_inputs(w)
+        sample = f"the whole {w.name} call per step (T={w.T})"
+    else:
+        inp = datagen.make_inputs(w, T=64)
+        sample = f"first 64 of {w.T} tokens per step, scaled to the full call"
+    scale = w.T / inp.logits_bf16.shape[0]
+    t_steps = []
+    for k in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                          w.routed_scale, w.block_m)
+        el = (time.perf_counter() - t0) * scale
+        if k >= args.warmup:
+            t_steps.append(el)
+    us = sum(t_steps) / len(t_steps) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "E": w.E, "n_group": w.n_group,
+                   "topk_group": w.topk_group, "topk": w.topk, "block_m": w.block_m,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "cpu_baseline": {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = datagen.workload(args.workload)
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+
+    import moe_expert_routing_sort_gb300 as mrs
+
+    mrs.load()  # fails loudly if the CUDA library is missing
+    torch.cuda.set_device(local)
+    peak, peak_kind = load_peaks()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    head = measure_workload(w, args.steps, args.warmup, world, peak, clocks=True)
+    clocks = sampler.stop()
+    e2e_ms, h2d, d2h = e2e_time(w, args.steps * 32, args.warmup, world)
+    e2e_us = e2e_ms * 1e3 / (args.steps * 32)
+
+    configs = {}
+    if not args.no_secondary:
+        for name in SECONDARY:
+            ws = datagen.workload(name)
+            r = measure_workload(ws, max(3, min(args.steps, 10)), args.warmup, world, peak)
+            configs[name] = {k: r[k] for k in ("us_per_call", "tokens_per_s", "routes_per_s",
+                                                 "achieved_gbs", "roofline_frac",
+                                                 "algorithmic_bytes_per_call", "calls_per_step")}
+
+    cpu = None
+    if rank == 0:
+        secs, sample = cpu_oracle_rate(w, args.cpu_budget)
+        cpu = {"value": secs * 1e6, "unit": "us/call", "cores": 1, "kind": "oracle",
+               "sample": sample}
+        for name in configs:
+            ws = datagen.workload(name)
+            s2, samp2 = cpu_oracle_rate(ws, 3.0)
+            configs[name]["cpu_oracle_tokens_per_s"] = 1.0 / s2
+            configs[name]["cpu_oracle_sample"] = samp2
+
+    if rank != 0:
+        return 0
+    value = head["us_per_call"] / world
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "E": w.E, "n_group": w.n_group,
+                   "topk_group": w.topk_group, "topk": w.topk, "block_m": w.block_m,
+                   "routed_scale": w.routed_scale, "calls_per_step": head["calls_per_step"],
+                   "l2": "flushed (256 MiB write) before every step; rotating input sets",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": "moe_route_sort (whole call)",
+                     "achieved": head["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": head["roofline_frac"], "peak_kind": peak_kind,
+                     "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": head["launches"],
+        "clocks": clocks,
+        "configs": configs,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,133 @@
+/*
+ * moe_route_sort.h -- C ABI of the GB300 (sm_103a) MoE route-sort library.
+ *
+ * Route-sort turns router logits into the expert-grouped dispatch metadata a grouped MoE
+ * GEMM consumes.  Source of the operation: "perf(flydsl): Kimi-K3 B1 route-sort +
+ * prepared-MoE handoff (stack)", Summary -- one kernel converts the logits to FP32, applies
+ * the correction bias, runs grouped top-k and both sort phases, and its prepared metadata
+ * is consumed by the MoE GEMMs with no second top-k or sort.  Sort-phase contracts (dropped
+ * routes, caller-owned integer capacity): "Summary -- general gfx1250 ordinary-TP route
+ * optimization" (ROCm/aiter pull 7095), section "Dispatch and contracts".
+ *
+ * Notation: T tokens, E experts, G = n_group groups of g = E/G consecutive experts,
+ * Kg = topk_group kept groups, K = topk experts per token, R = routed_scale,
+ * B = block_m, N = T*K routes.
+ *
+ * What is computed, per token t (all fp32, IEEE expf, IEEE division, no fast-math):
+ *   x_e   = float(bf16 logit)                       (exact)
+ *   s_e   = 1 / (1 + expf(-x_e))                    sigmoid score
+ *   key_e = s_e + bias_e                            selection key (bias steers selection only)
+ *   group score of group j = the sum of its two largest keys (its one key when g == 1)
+ *   kept groups = the Kg best group scores (equal scores: lower group index first)
+ *   topk_ids[t,0..K) = the K best keys among experts of kept groups, best first
+ *                      (equal keys: lower expert index first)
+ *   topk_weights[t,k] = (s_{id_k} / (s_{id_0} + ... + s_{id_{K-1}})) * R  (sum in slot order)
+ * Sort, over the routes r = t*K + k in token-then-slot order:
+ *   cnt_e = routes of expert e; pad_e = ceil(cnt_e / B) * B; off_e = sum of pad over
+ *   experts below e; num_tokens_post_pad = npp = sum of pad_e;
+ *   sorted_token_ids[off_e + i] = the i-th route of expert e (its flat index r),
+ *   rows [off_e + cnt_e, off_e + pad_e) = sentinel N with sorted_weights 0,
+ *   sorted_weights[p] = topk_weights of the route at row p,
+ *   expert_ids[b] = the expert owning rows [b*B, (b+1)*B), for b < npp / B.
+ * Entries of sorted_token_ids / sorted_weights at or past npp, and of expert_ids at or
+ * past npp / B, are not written.
+ *
+ * Layouts and ownership: every pointer is DEVICE memory owned by the caller, row-major and
+ * contiguous.  logits_bf16: [T, E] bf16 (16-byte aligned base); bias: [E] fp32;
+ * topk_ids, topk_weights: [T, K]; sorted_token_ids, sorted_weights:
+ * [moe_sort_max_padded(T,E,K,B)]; expert_ids: [moe_sort_max_blocks(T,E,K,B)];
+ * num_tokens_post_pad: [1].  The library allocates nothing and keeps no device state
+ * between calls; inputs are never written.  Calls only enqueue work on `stream` (no host
+ * synchronisation), so they can be captured in a CUDA graph once the first call on the
+ * current device has been made outside capture (that call caches device attributes).
+ *
+ * Limits: 1 <= E <= 4096, 1 <= G <= 64, E % G == 0, 1 <= Kg <= G, 1 <= K <= 32,
+ * K <= Kg * g, B a power of two in [1, 1024], T >= 0, N and the padded length fit in
+ * int32.  Logits must be finite (NaN logits give unspecified selections).
+ *
+ * Errors: every entry point returns MOE_RS_OK (0) or a negative status and, on a negative
+ * status, writes nothing and launches nothing (except MOE_RS_ERR_LAUNCH, raised when the
+ * CUDA runtime refuses a launch).  Problems only the device can see are reported in the
+ * workspace's status word (the first int32 of the workspace, MOE_RS_DEVICE_* bits), valid
+ * once the call has completed on the stream; read it with cudaMemcpyAsync if wanted.
+ */
+#ifndef MOE_ROUTE_SORT_H_
+#define MOE_ROUTE_SORT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side status codes (return values). */
+#define MOE_RS_OK 0
+#define MOE_RS_ERR_NULL_POINTER (-1)      /* a required pointer is NULL (with T > 0)        */
+#define MOE_RS_ERR_BAD_EXPERTS (-2)       /* E outside [1, 4096]                           */
+#define MOE_RS_ERR_BAD_GROUPS (-3)        /* G outside [1, 64], E % G != 0, Kg outside [1,G] */
+#define MOE_RS_ERR_BAD_TOPK (-4)          /* K outside [1, 32] or K > Kg * g               */
+#define MOE_RS_ERR_BAD_BLOCK_M (-5)       /* B not a power of two in [1, 1024]             */
+#define MOE_RS_ERR_BAD_TOKENS (-6)        /* T < 0                                         */
+#define MOE_RS_ERR_OVERFLOW (-7)          /* N or the padded length does not fit in int32  */
+#define MOE_RS_ERR_MISALIGNED (-8)        /* logits not 16-byte aligned, or another buffer
+                                             not aligned to its element size (workspace: 16) */
+#define MOE_RS_ERR_ALIAS (-9)             /* an output overlaps an input or another output */
+#define MOE_RS_ERR_WORKSPACE (-10)        /* workspace NULL or smaller than required       */
+#define MOE_RS_ERR_BAD_SCALE (-11)        /* routed_scale not finite                       */
+#define MOE_RS_ERR_LAUNCH (-12)           /* the CUDA runtime rejected a kernel launch     */
+
+/* Device-side status bits, written to the first int32 of the workspace by every call. */
+#define MOE_RS_DEVICE_BAD_EXPERT_ID 0x1   /* moe_sort saw an id >= E; those routes dropped */
+
+/* ---------------------------------------------------------------- size queries */
+
+/* Worst-case padded length: N + min(E, N) * (B - 1) (each nonempty expert pads by at most
+ * B - 1 rows).  Length of sorted_token_ids and sorted_weights.  0 for invalid arguments. */
+size_t moe_sort_max_padded(int T, int E, int topk, int block_m);
+
+/* Worst-case number of blocks: floor(moe_sort_max_padded / B).  Length of expert_ids. */
+size_t moe_sort_max_blocks(int T, int E, int topk, int block_m);
+
+/* Bytes of device workspace that moe_route_sort and moe_sort need for this shape (16-byte
+ * aligned, any contents; the library overwrites what it uses).  One workspace must not be
+ * used by two calls that can run at the same time. */
+size_t moe_route_sort_workspace_bytes(int T, int E, int topk, int block_m);
+
+/* Static text for a status code (host codes above). */
+const char* moe_route_sort_strerror(int status);
+
+/* ------------------------------------------------------------------ operations */
+
+/* The whole path: route step (scores, grouped top-k, weights) then sort step.
+ * Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary.
+ * Outputs: topk_ids/topk_weights [T,K]; sorted metadata as described above. */
+int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int n_group,
+                   int topk_group, int topk, float routed_scale, int block_m,
+                   int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
+                   float* sorted_weights, int32_t* expert_ids,
+                   int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/* Route step only ("grouped top-k" of the same Summary): topk_ids/topk_weights [T,K]. */
+int moe_topk(const void* logits_bf16, const float* bias, int T, int E, int n_group,
+             int topk_group, int topk, float routed_scale, int32_t* topk_ids,
+             float* topk_weights, cudaStream_t stream);
+
+/* Sort step only ("both sort phases" of the same Summary) from caller-given routes.
+ * topk_ids [T,K] int32: an id < 0 is a dropped route (no slot, not counted: "Summary --
+ * general gfx1250 ordinary-TP route optimization", Dispatch and contracts); an id >= E is
+ * invalid, dropped, and sets MOE_RS_DEVICE_BAD_EXPERT_ID.  Ids may repeat within a token.
+ * topk_weights [T,K] fp32 are copied to the sorted rows. */
+int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, int topk,
+             int block_m, int32_t* sorted_token_ids, float* sorted_weights,
+             int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
+             size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_SORT_H_ */

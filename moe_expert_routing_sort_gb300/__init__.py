@@ -1,2 +1,23 @@
-"""GB300-native MoE route-sort (placeholder; the CUDA binding is added with the library)."""
+"""GB300-native (sm_103a) MoE route-sort: router logits -> expert-grouped dispatch metadata.
+
+The compute path is the CUDA library ``libmoe_route_sort.so`` (C ABI in
+``include/moe_route_sort.h``); this package holds its thin ctypes binding, the build script
+and the seeded input generator used by the tests and the benchmark.
+"""
 from . import datagen  # noqa: F401
+from ._build import build  # noqa: F401
+from .binding import (  # noqa: F401
+    DEVICE_BAD_EXPERT_ID,
+    RouteSortBuffers,
+    RouteSortError,
+    library_path,
+    load,
+    moe_route_sort,
+    moe_route_sort_workspace_bytes,
+    moe_sort,
+    moe_sort_max_blocks,
+    moe_sort_max_padded,
+    moe_topk,
+    route_sort,
+    strerror,
+)

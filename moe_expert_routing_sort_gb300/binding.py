@@ -1,0 +1,207 @@
+"""Thin Python binding of the route-sort C ABI (ctypes; argument marshalling only).
+
+Each function has the name of its C entry point, takes torch CUDA tensors for the device
+buffers, passes their data pointers and the current (or given) CUDA stream, and raises
+``RouteSortError`` on a negative status.  Every step of the path runs in the library's
+CUDA kernels; if the library has not been built this module raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from ._build import LIB_PATH
+
+DEVICE_BAD_EXPERT_ID = 0x1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class RouteSortError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed with status {status}: {strerror(status)}")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load ``libmoe_route_sort.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')"
+            )
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.moe_sort_max_padded.argtypes = [I, I, I, I]
+        lib.moe_sort_max_padded.restype = S
+        lib.moe_sort_max_blocks.argtypes = [I, I, I, I]
+        lib.moe_sort_max_blocks.restype = S
+        lib.moe_route_sort_workspace_bytes.argtypes = [I, I, I, I]
+        lib.moe_route_sort_workspace_bytes.restype = S
+        lib.moe_route_sort_strerror.argtypes = [I]
+        lib.moe_route_sort_strerror.restype = ctypes.c_char_p
+        lib.moe_route_sort.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P, S, P]
+        lib.moe_route_sort.restype = I
+        lib.moe_topk.argtypes = [P, P, I, I, I, I, I, F, P, P, P]
+        lib.moe_topk.restype = I
+        lib.moe_sort.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P]
+        lib.moe_sort.restype = I
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ size queries
+def moe_sort_max_padded(T: int, E: int, topk: int, block_m: int) -> int:
+    return int(load().moe_sort_max_padded(T, E, topk, block_m))
+
+
+def moe_sort_max_blocks(T: int, E: int, topk: int, block_m: int) -> int:
+    return int(load().moe_sort_max_blocks(T, E, topk, block_m))
+
+
+def moe_route_sort_workspace_bytes(T: int, E: int, topk: int, block_m: int) -> int:
+    return int(load().moe_route_sort_workspace_bytes(T, E, topk, block_m))
+
+
+def strerror(status: int) -> str:
+    return load().moe_route_sort_strerror(int(status)).decode()
+
+
+# ------------------------------------------------------------------ marshalling
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise RouteSortError(rc, what)
+
+
+# -------------------------------------------------------------------- operations
+def moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
+                   topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
+                   num_tokens_post_pad, workspace, stream=None) -> None:
+    """Whole path into caller-owned buffers (see include/moe_route_sort.h)."""
+    T, E = logits.shape
+    _need(logits, torch.bfloat16, "logits")
+    _need(bias, torch.float32, "bias")
+    for t, dt, n in [(topk_ids, torch.int32, "topk_ids"), (topk_weights, torch.float32,
+                     "topk_weights"), (sorted_token_ids, torch.int32, "sorted_token_ids"),
+                     (sorted_weights, torch.float32, "sorted_weights"),
+                     (expert_ids, torch.int32, "expert_ids"),
+                     (num_tokens_post_pad, torch.int32, "num_tokens_post_pad"),
+                     (workspace, torch.uint8, "workspace")]:
+        _need(t, dt, n)
+    rc = load().moe_route_sort(
+        _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
+        block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
+        _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream))
+    _check(rc, "moe_route_sort")
+
+
+def moe_topk(logits, bias, n_group, topk_group, topk, routed_scale, topk_ids, topk_weights,
+             stream=None) -> None:
+    T, E = logits.shape
+    _need(logits, torch.bfloat16, "logits")
+    _need(bias, torch.float32, "bias")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    rc = load().moe_topk(_ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk,
+                         float(routed_scale), _ptr(topk_ids), _ptr(topk_weights),
+                         _stream_handle(stream))
+    _check(rc, "moe_topk")
+
+
+def moe_sort(topk_ids, topk_weights, E, block_m, sorted_token_ids, sorted_weights, expert_ids,
+             num_tokens_post_pad, workspace, stream=None) -> None:
+    T, K = topk_ids.shape
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    _need(sorted_token_ids, torch.int32, "sorted_token_ids")
+    _need(sorted_weights, torch.float32, "sorted_weights")
+    _need(expert_ids, torch.int32, "expert_ids")
+    _need(num_tokens_post_pad, torch.int32, "num_tokens_post_pad")
+    _need(workspace, torch.uint8, "workspace")
+    rc = load().moe_sort(_ptr(topk_ids), _ptr(topk_weights), T, E, K, block_m,
+                         _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
+                         _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(),
+                         _stream_handle(stream))
+    _check(rc, "moe_sort")
+
+
+# ---------------------------------------------------------- convenience buffers
+@dataclass
+class RouteSortBuffers:
+    """Caller-owned output buffers plus workspace for one (T, E, topk, block_m) shape."""
+
+    topk_ids: torch.Tensor
+    topk_weights: torch.Tensor
+    sorted_token_ids: torch.Tensor
+    sorted_weights: torch.Tensor
+    expert_ids: torch.Tensor
+    num_tokens_post_pad: torch.Tensor
+    workspace: torch.Tensor
+
+    @classmethod
+    def allocate(cls, T, E, topk, block_m, device="cuda") -> "RouteSortBuffers":
+        P = max(moe_sort_max_padded(T, E, topk, block_m), 1)
+        NB = max(moe_sort_max_blocks(T, E, topk, block_m), 1)
+        ws = moe_route_sort_workspace_bytes(T, E, topk, block_m)
+        if ws == 0:
+            raise ValueError("invalid shape for route-sort buffers")
+        kw = dict(device=device)
+        return cls(
+            topk_ids=torch.empty((T, topk), dtype=torch.int32, **kw),
+            topk_weights=torch.empty((T, topk), dtype=torch.float32, **kw),
+            sorted_token_ids=torch.empty(P, dtype=torch.int32, **kw),
+            sorted_weights=torch.empty(P, dtype=torch.float32, **kw),
+            expert_ids=torch.empty(NB, dtype=torch.int32, **kw),
+            num_tokens_post_pad=torch.empty(1, dtype=torch.int32, **kw),
+            workspace=torch.empty(ws, dtype=torch.uint8, **kw),
+        )
+
+    def status_word(self) -> int:
+        """Device status bits of the last completed call (synchronises the device)."""
+        return int(self.workspace[:4].view(torch.int32).item())
+
+
+def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
+               out: Optional[RouteSortBuffers] = None, stream=None) -> RouteSortBuffers:
+    """Allocate (unless ``out`` is given) and run moe_route_sort; returns the buffers."""
+    T, E = logits.shape
+    if out is None:
+        out = RouteSortBuffers.allocate(T, E, topk, block_m, device=logits.device)
+    moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
+                   out.topk_ids, out.topk_weights, out.sorted_token_ids, out.sorted_weights,
+                   out.expert_ids, out.num_tokens_post_pad, out.workspace, stream=stream)
+    return out

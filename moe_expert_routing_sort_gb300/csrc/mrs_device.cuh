@@ -1,0 +1,345 @@
+// mrs_device.cuh -- device helpers and the warp-level route step of MoE route-sort.
+//
+// One warp routes one token: group scores -> kept groups -> top-K inside the kept groups ->
+// renormalised weights.  Source of the step: "perf(flydsl): Kimi-K3 B1 route-sort +
+// prepared-MoE handoff (stack)", Summary (FP32 logits, correction bias, grouped top-k).
+//
+// The selection reads keys through a "key source" with two views of expert e:
+//   proxy(e)        a value within kDelta of the exact key (equal to it when kDelta == 0)
+//   exact(e, s)     the exact key s_e + bias_e, and the exact score s_e through s
+// Every decision is taken on exact keys: proxies only prune, with windows widened by
+// 2*kDelta so that no element that can still win is pruned (see topk_in_kept).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mrs {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxExperts = 4096;
+constexpr int kMaxGroups = 64;
+constexpr int kMaxTopk = 32;
+constexpr int kCandCap = 64;  // survivors kept for the exact ranking before the fallback
+
+// ------------------------------------------------------------------ scalar helpers
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h16) {
+  return __uint_as_float(h16 << 16);
+}
+
+// Sigmoid score with CUDA's full-precision expf and a correctly rounded reciprocal (the
+// same value as the IEEE quotient 1.0f / (1.0f + e)).  Built without fast-math.
+__device__ __forceinline__ float exact_score(float x) {
+  return __frcp_rn(__fadd_rn(1.0f, expf(-x)));
+}
+
+// Order-preserving map of a float onto uint32 (for non-NaN values; -0 sorts below +0,
+// which never matters here because keys are never -0).
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (key desc, expert asc) as one integer: larger composite = better route.
+__device__ __forceinline__ unsigned long long composite(float key, int e) {
+  return (static_cast<unsigned long long>(ordered_bits(key)) << 32) |
+         static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ int composite_expert(unsigned long long c) {
+  return static_cast<int>(0xffffffffu - static_cast<uint32_t>(c & 0xffffffffull));
+}
+
+__device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) - 1u; }
+
+__device__ __forceinline__ int warp_inclusive_sum(int v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(kFull, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+// Bitonic sort of one float per lane into descending order across the warp.
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(kFull, v, j);
+      const bool desc = (lane & k) == 0;
+      const bool lower = (lane & j) == 0;
+      v = (desc == lower) ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return v;
+}
+
+// ------------------------------------------------------------------ route shape
+struct RouteShape {
+  int E, G, g, Kg, K;
+  int L;       // lanes per group in the group pass (power of two)
+  int log2L;
+  int gpr;     // groups per round = 32 / L
+  int rounds;  // ceil(G / gpr)
+  float R;     // routed_scale
+};
+
+// Per-warp shared scratch of the route step.
+struct __align__(16) WarpScratch {
+  unsigned long long cand[kCandCap];
+  float cand_s[kCandCap];
+  float gs[kMaxGroups];
+  float p2[kMaxGroups];
+  int kept[kMaxGroups];
+  int sel_id[kMaxTopk];
+  float sel_s[kMaxTopk];
+};
+
+// ----------------------------------------------------------- step 1: group scores
+// Group score = sum of the two largest keys of the group (the one key when g == 1).
+// Lanes are split into 32/L slots of L lanes; slot i of round r owns group r*(32/L) + i.
+template <class Src>
+__device__ __forceinline__ void group_scores_proxy(const Src& src, const RouteShape& sh,
+                                                   WarpScratch& ws, int lane) {
+  const int q = lane & (sh.L - 1);
+  const int slot = lane >> sh.log2L;
+  for (int r = 0; r < sh.rounds; ++r) {
+    const int j = r * sh.gpr + slot;
+    float m1 = -INFINITY, m2 = -INFINITY;
+    if (j < sh.G) {
+      const int base = j * sh.g;
+      for (int i = q; i < sh.g; i += sh.L) {
+        const float v = src.proxy(base + i);
+        m2 = fmaxf(m2, fminf(m1, v));
+        m1 = fmaxf(m1, v);
+      }
+    }
+    for (int d = 1; d < sh.L; d <<= 1) {
+      const float o1 = __shfl_xor_sync(kFull, m1, d);
+      const float o2 = __shfl_xor_sync(kFull, m2, d);
+      m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+      m1 = fmaxf(m1, o1);
+    }
+    if (j < sh.G && q == 0) {
+      ws.gs[j] = (sh.g >= 2) ? __fadd_rn(m1, m2) : m1;
+      ws.p2[j] = (sh.g >= 2) ? m2 : m1;
+    }
+  }
+  __syncwarp();
+}
+
+// Exact group scores: the exact top-2 of group j lie in the window proxy >= p2_j - 2*delta
+// (order statistics of the proxies are within delta of those of the keys).
+template <class Src>
+__device__ __forceinline__ void group_scores_exact(const Src& src, const RouteShape& sh,
+                                                   WarpScratch& ws, int lane) {
+  const int q = lane & (sh.L - 1);
+  const int slot = lane >> sh.log2L;
+  for (int r = 0; r < sh.rounds; ++r) {
+    const int j = r * sh.gpr + slot;
+    float m1 = -INFINITY, m2 = -INFINITY;
+    if (j < sh.G) {
+      const int base = j * sh.g;
+      const float lo = ws.p2[j] - 2.0f * Src::kDelta;
+      for (int i = q; i < sh.g; i += sh.L) {
+        if (src.proxy(base + i) >= lo) {
+          float s;
+          const float v = src.exact(base + i, s);
+          m2 = fmaxf(m2, fminf(m1, v));
+          m1 = fmaxf(m1, v);
+        }
+      }
+    }
+    for (int d = 1; d < sh.L; d <<= 1) {
+      const float o1 = __shfl_xor_sync(kFull, m1, d);
+      const float o2 = __shfl_xor_sync(kFull, m2, d);
+      m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+      m1 = fmaxf(m1, o1);
+    }
+    if (j < sh.G && q == 0) ws.gs[j] = (sh.g >= 2) ? __fadd_rn(m1, m2) : m1;
+  }
+  __syncwarp();
+}
+
+// --------------------------------------------------------- step 2: kept groups
+// Rank of group j = number of groups that beat it (higher score, or equal score and lower
+// index); kept iff rank < Kg.  Writes the kept groups in ascending order to ws.kept.
+// Returns false when `margin` >= 0 and the Kg-th and (Kg+1)-th scores are within `margin`
+// (approximate scores cannot decide the kept set).
+__device__ __forceinline__ bool rank_groups(const RouteShape& sh, WarpScratch& ws, int lane,
+                                            float margin) {
+  int r0 = 0x7fffffff, r1 = 0x7fffffff;
+  float v0 = 0.0f, v1 = 0.0f;
+  if (lane < sh.G) {
+    v0 = ws.gs[lane];
+    r0 = 0;
+    for (int j = 0; j < sh.G; ++j) {
+      const float o = ws.gs[j];
+      r0 += (o > v0) || (o == v0 && j < lane);
+    }
+  }
+  if (lane + 32 < sh.G) {
+    v1 = ws.gs[lane + 32];
+    r1 = 0;
+    for (int j = 0; j < sh.G; ++j) {
+      const float o = ws.gs[j];
+      r1 += (o > v1) || (o == v1 && j < lane + 32);
+    }
+  }
+  bool certain = true;
+  if (margin >= 0.0f) {
+    const unsigned ha = __ballot_sync(kFull, r0 == sh.Kg - 1 || r1 == sh.Kg - 1);
+    const unsigned hb = __ballot_sync(kFull, r0 == sh.Kg || r1 == sh.Kg);
+    const float va = __shfl_sync(kFull, r0 == sh.Kg - 1 ? v0 : v1, __ffs(ha) - 1);
+    const float vb = __shfl_sync(kFull, r0 == sh.Kg ? v0 : v1, __ffs(hb) - 1);
+    certain = (va - vb) > margin;  // Kg < G, so both ranks exist
+  }
+  __syncwarp();
+  const bool k0 = r0 < sh.Kg, k1 = r1 < sh.Kg;
+  const unsigned b0 = __ballot_sync(kFull, k0);
+  const unsigned b1 = __ballot_sync(kFull, k1);
+  if (k0) ws.kept[__popc(b0 & lanemask_lt(lane))] = lane;
+  if (k1) ws.kept[__popc(b0) + __popc(b1 & lanemask_lt(lane))] = lane + 32;
+  __syncwarp();
+  return certain;
+}
+
+// --------------------------------------------- step 3: top-K inside the kept groups
+// tau = K-th largest of the 32 per-lane maxima of the proxies: at least K candidates have
+// a proxy >= tau, so the K-th best exact key is >= tau - delta and every member of the
+// exact top-K has proxy >= tau - 2*delta.  Those survivors get exact keys and are ranked
+// by (key desc, expert asc); more than kCandCap survivors take a slower exact path.
+template <class Src>
+__device__ __forceinline__ void topk_in_kept(const Src& src, const RouteShape& sh,
+                                             WarpScratch& ws, int lane) {
+  const int g = sh.g;
+  const bool all_kept = (sh.Kg == sh.G);
+  // every slot gets a value even if non-finite keys leave fewer than K survivors
+  if (lane < sh.K) {
+    ws.sel_id[lane] = -1;
+    ws.sel_s[lane] = 0.0f;
+  }
+  __syncwarp();
+  float M = -INFINITY;
+  for (int i = 0; i < sh.Kg; ++i) {
+    const int base = (all_kept ? i : ws.kept[i]) * g;
+    for (int c = lane; c < g; c += 32) M = fmaxf(M, src.proxy(base + c));
+  }
+  const float tau = __shfl_sync(kFull, warp_sort_desc(M, lane), sh.K - 1);
+  const float theta = (Src::kDelta > 0.0f) ? tau - 2.0f * Src::kDelta : tau;
+
+  int cnt = 0;
+  for (int i = 0; i < sh.Kg; ++i) {
+    const int base = (all_kept ? i : ws.kept[i]) * g;
+    for (int c = lane; c < g; c += 32) cnt += (src.proxy(base + c) >= theta) ? 1 : 0;
+  }
+  const int total = __reduce_add_sync(kFull, cnt);
+
+  if (total <= kCandCap) {
+    int w = warp_inclusive_sum(cnt, lane) - cnt;
+    for (int i = 0; i < sh.Kg; ++i) {
+      const int base = (all_kept ? i : ws.kept[i]) * g;
+      for (int c = lane; c < g; c += 32) {
+        const int e = base + c;
+        if (src.proxy(e) >= theta) {
+          float s;
+          const float k = src.exact(e, s);
+          ws.cand[w] = composite(k, e);
+          ws.cand_s[w] = s;
+          ++w;
+        }
+      }
+    }
+    __syncwarp();
+    for (int a = lane; a < total; a += 32) {
+      const unsigned long long me = ws.cand[a];
+      int rank = 0;
+      for (int b = 0; b < total; ++b) rank += (ws.cand[b] > me) ? 1 : 0;
+      if (rank < sh.K) {
+        ws.sel_id[rank] = composite_expert(me);
+        ws.sel_s[rank] = ws.cand_s[a];
+      }
+    }
+  } else {
+    // K rounds: the best exact composite strictly below the previous winner.
+    unsigned long long prev = ~0ull;
+    for (int k = 0; k < sh.K; ++k) {
+      unsigned long long best = 0ull;
+      float best_s = 0.0f;
+      for (int i = 0; i < sh.Kg; ++i) {
+        const int base = (all_kept ? i : ws.kept[i]) * g;
+        for (int c = lane; c < g; c += 32) {
+          const int e = base + c;
+          if (src.proxy(e) >= theta) {
+            float s;
+            const float key = src.exact(e, s);
+            const unsigned long long cc = composite(key, e);
+            if (cc < prev && cc > best) {
+              best = cc;
+              best_s = s;
+            }
+          }
+        }
+      }
+      unsigned long long wb = best;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(kFull, wb, d);
+        wb = (o > wb) ? o : wb;
+      }
+      const unsigned owner = __ballot_sync(kFull, best == wb);
+      const float ws_s = __shfl_sync(kFull, best_s, __ffs(owner) - 1);
+      if (lane == 0) {
+        ws.sel_id[k] = composite_expert(wb);
+        ws.sel_s[k] = ws_s;
+      }
+      prev = wb;
+    }
+  }
+  __syncwarp();
+}
+
+// --------------------------------------------------------------- the whole route step
+// On return lane k < K holds the k-th selected expert in `id` and its weight in `w`
+// (lanes >= K get id = -1, w = 0).
+template <class Src>
+__device__ __forceinline__ void route_token(const Src& src, const RouteShape& sh,
+                                            WarpScratch& ws, int lane, int& id, float& w) {
+  if (sh.Kg < sh.G) {
+    group_scores_proxy(src, sh, ws, lane);
+    if (Src::kDelta > 0.0f) {
+      // approximate scores are within 2*delta (+ two roundings) of the exact ones
+      const float margin = 2.0f * (2.0f * Src::kDelta + 1e-6f);
+      if (!rank_groups(sh, ws, lane, margin)) {
+        group_scores_exact(src, sh, ws, lane);
+        rank_groups(sh, ws, lane, -1.0f);
+      }
+    } else {
+      rank_groups(sh, ws, lane, -1.0f);
+    }
+  }
+  topk_in_kept(src, sh, ws, lane);
+  const bool mine = lane < sh.K;
+  const float s = mine ? ws.sel_s[lane] : 0.0f;
+  id = mine ? ws.sel_id[lane] : -1;
+  float sum = 0.0f;
+  for (int k = 0; k < sh.K; ++k) sum = __fadd_rn(sum, __shfl_sync(kFull, s, k));
+  w = mine ? __fmul_rn(__fdiv_rn(s, sum), sh.R) : 0.0f;
+  __syncwarp();
+}
+
+// Key source over exact keys and scores already in shared memory.
+struct SmemExactSrc {
+  static constexpr float kDelta = 0.0f;
+  const float* key;
+  const float* s;
+  __device__ __forceinline__ float proxy(int e) const { return key[e]; }
+  __device__ __forceinline__ float exact(int e, float& se) const {
+    se = s[e];
+    return key[e];
+  }
+};
+
+}  // namespace mrs

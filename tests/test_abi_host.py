@@ -1,0 +1,121 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, answers size
+queries, and rejects bad arguments before touching any device (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import moe_expert_routing_sort_gb300 as mrs
+from moe_expert_routing_sort_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mrs.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(moe_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"moe_route_sort", "moe_topk", "moe_sort"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_size_queries():
+    assert mrs.moe_sort_max_padded(1, 896, 16, 32) == 16 + 16 * 31
+    assert mrs.moe_sort_max_padded(16384, 4096, 8, 128) == 131072 + 4096 * 127
+    assert mrs.moe_sort_max_blocks(1, 896, 16, 32) == (16 + 16 * 31) // 32
+    assert mrs.moe_sort_max_padded(0, 64, 6, 16) == 0
+    assert mrs.moe_sort_max_padded(4, 64, 6, 3) == 0  # block_m not a power of two
+    for E in range(1, 4097, 37):
+        assert mrs.moe_route_sort_workspace_bytes(512, E, 8, 64) >= 4 * E
+    assert mrs.moe_route_sort_workspace_bytes(1, 0, 1, 1) == 0
+    assert mrs.moe_route_sort_workspace_bytes(1, 4097, 1, 1) == 0
+    assert mrs.moe_route_sort_workspace_bytes(16384, 4096, 8, 128) % 16 == 0
+
+
+def test_strerror_covers_codes():
+    for code in range(-12, 1):
+        assert mrs.strerror(code) != "unknown status"
+    assert mrs.strerror(-99) == "unknown status"
+
+
+# Host-side validation runs before any CUDA call, so fake device addresses are safe here:
+# every call below must be rejected without dereferencing anything.
+BASE = 0x7F0000000000
+
+
+def _route_sort(lib, T=4, E=64, G=8, Kg=4, K=6, R=2.5, B=16, logits=BASE, bias=BASE + 0x10000,
+                ids=BASE + 0x20000, w=BASE + 0x30000, sid=BASE + 0x40000, sw=BASE + 0x80000,
+                eid=BASE + 0xC0000, npp=BASE + 0xD0000, ws=BASE + 0x100000, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = mrs.moe_route_sort_workspace_bytes(max(T, 0), E, K, B) if E > 0 else 1 << 20
+    return lib.moe_route_sort(logits, bias, T, E, G, Kg, K, R, B, ids, w, sid, sw, eid, npp, ws,
+                              ws_bytes, None)
+
+
+def test_route_sort_rejects_bad_shapes(lib):
+    assert _route_sort(lib, E=0) == -2
+    assert _route_sort(lib, E=4097) == -2
+    assert _route_sort(lib, G=7) == -3  # 64 % 7 != 0
+    assert _route_sort(lib, E=128, G=128, Kg=4, K=4) == -3  # more than 64 groups
+    assert _route_sort(lib, Kg=9) == -3
+    assert _route_sort(lib, Kg=0) == -3
+    assert _route_sort(lib, K=0) == -4
+    assert _route_sort(lib, K=33, E=256, G=1, Kg=1) == -4
+    assert _route_sort(lib, K=33) == -4  # more than Kg * g = 32
+    assert _route_sort(lib, B=3) == -5
+    assert _route_sort(lib, B=2048) == -5
+    assert _route_sort(lib, T=-1) == -6
+    assert _route_sort(lib, T=(1 << 31) // 6 + 1) == -7
+    assert _route_sort(lib, R=float("nan")) == -11
+    assert _route_sort(lib, R=float("inf")) == -11
+
+
+def test_route_sort_rejects_bad_buffers(lib):
+    assert _route_sort(lib, logits=0) == -1
+    assert _route_sort(lib, sid=0) == -1
+    assert _route_sort(lib, ws=0) == -10
+    assert _route_sort(lib, ws_bytes=16) == -10
+    assert _route_sort(lib, logits=BASE + 8) == -8  # logits need 16-byte alignment
+    assert _route_sort(lib, ids=BASE + 0x20002) == -8
+    assert _route_sort(lib, ws=BASE + 0x100004) == -8
+    assert _route_sort(lib, sw=BASE + 0x40000) == -9  # sorted weights over sorted ids
+    assert _route_sort(lib, ids=BASE + 0x10) == -9  # topk ids over the logits
+    assert _route_sort(lib, npp=BASE + 0x100010) == -9  # npp inside the workspace
+    assert _route_sort(lib, eid=BASE + 0x10000) == -9  # expert ids over the bias
+
+
+def test_moe_sort_and_topk_validate(lib):
+    P = mrs.moe_sort_max_padded(4, 64, 6, 16)
+    ws = mrs.moe_route_sort_workspace_bytes(4, 64, 6, 16)
+    args = [BASE, BASE + 0x1000, 4, 64, 6, 16, BASE + 0x2000, BASE + 0x2000 + 4 * P,
+            BASE + 0x8000, BASE + 0x9000, BASE + 0x10000, ws, None]
+    bad = list(args)
+    bad[5] = 12
+    assert lib.moe_sort(*bad) == -5
+    bad = list(args)
+    bad[7] = BASE + 0x2000  # sorted weights over sorted ids
+    assert lib.moe_sort(*bad) == -9
+    bad = list(args)
+    bad[11] = 8
+    assert lib.moe_sort(*bad) == -10
+    assert lib.moe_topk(BASE, BASE + 0x1000, 4, 64, 8, 4, 33, 1.0, BASE + 0x2000,
+                        BASE + 0x3000, None) == -4
+    assert lib.moe_topk(BASE + 2, BASE + 0x1000, 4, 64, 8, 4, 6, 1.0, BASE + 0x2000,
+                        BASE + 0x3000, None) == -8
+    # T == 0 needs no buffers for moe_topk and launches nothing
+    assert lib.moe_topk(0, 0, 0, 64, 8, 4, 6, 1.0, 0, 0, None) == 0

@@ -1,0 +1,291 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on a GB300.
+
+Bit-exact: topk_ids, sorted_token_ids[0:npp), expert_ids[0:npp/B), num_tokens_post_pad.
+Weights: within 1e-6 absolute (IEEE expf on both sides, no fast-math), sentinel rows exactly
+0, and sorted_weights exact copies of the GPU's own topk_weights.  Inputs are redrawn where
+the oracle's selection margin is below 1e-6, so ulp-level differences between two correct
+sigmoid evaluations cannot change an id.  The full-size workloads are compared on every
+token, in the launch configuration the benchmark times.
+"""
+import functools
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_expert_routing_sort_gb300 as mrs
+from _support import WEIGHT_ATOL, check_sort_invariants, redraw_callback
+from moe_expert_routing_sort_gb300 import datagen
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mrs.build()
+    oracle.build()
+    mrs.load()
+
+
+def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+@functools.lru_cache(maxsize=None)
+def inputs_for(name: str, T=None, seed=0):
+    kw = {}
+    if T is not None:
+        kw["T"] = T
+    if seed:
+        kw["seed"] = seed
+    w = datagen.workload(name, **kw)
+    inp = datagen.make_inputs(w, needs_redraw=redraw_callback(oracle, w))
+    ref = oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                            w.routed_scale, w.block_m)
+    return w, inp, ref
+
+
+def run_gpu(w, inp, poison=False):
+    logits = to_dev_bf16(inp.logits_bf16)
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    if poison:
+        for t in (out.topk_ids, out.sorted_token_ids, out.expert_ids, out.num_tokens_post_pad):
+            t.fill_(-7)
+        for t in (out.topk_weights, out.sorted_weights):
+            t.fill_(float("nan"))
+        out.workspace.fill_(0xA5)
+    mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale, w.block_m,
+                   out=out)
+    torch.cuda.synchronize()
+    return out
+
+
+def assert_matches(out, ref, w):
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref.num_tokens_post_pad
+    ids = out.topk_ids.cpu().numpy()
+    wt = out.topk_weights.cpu().numpy()
+    bad = np.nonzero(np.any(ids != ref.topk_ids, axis=1))[0]
+    assert bad.size == 0, f"topk_ids differ on tokens {bad[:10]}"
+    assert np.max(np.abs(wt - ref.topk_weights), initial=0.0) <= WEIGHT_ATOL
+    sid = out.sorted_token_ids[:npp].cpu().numpy()
+    sw = out.sorted_weights[:npp].cpu().numpy()
+    eid = out.expert_ids[: npp // w.block_m].cpu().numpy()
+    assert np.array_equal(sid, ref.sorted_token_ids)
+    assert np.array_equal(eid, ref.expert_ids)
+    assert np.max(np.abs(sw - ref.sorted_weights), initial=0.0) <= WEIGHT_ATOL
+    N = w.T * w.topk
+    real = sid != N
+    assert np.all(sw[~real] == 0.0)
+    assert np.array_equal(sw[real], wt.reshape(-1)[sid[real]])
+    assert out.status_word() == 0
+
+
+# ------------------------------------------------------------ the five workloads
+@pytest.mark.parametrize("name", list(datagen.WORKLOADS))
+def test_workload_full_size(name):
+    w, inp, ref = inputs_for(name)
+    out = run_gpu(w, inp)
+    assert_matches(out, ref, w)
+    check_sort_invariants(ref.topk_ids, w.E, w.block_m, out.sorted_token_ids.cpu().numpy(),
+                          out.expert_ids.cpu().numpy(), ref.num_tokens_post_pad)
+
+
+@pytest.mark.parametrize("name", ["decode_T1_E896_G8", "prefill_T512_E896"])
+def test_poisoned_buffers_do_not_matter(name):
+    w, inp, ref = inputs_for(name)
+    assert_matches(run_gpu(w, inp, poison=True), ref, w)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_other_seeds(seed):
+    w, inp, ref = inputs_for("skewed_T8192_E896", T=3000, seed=seed)
+    assert_matches(run_gpu(w, inp), ref, w)
+
+
+# ------------------------------------------------------ ragged sizes, both paths
+@pytest.mark.parametrize("T", [1, 2, 3, 31, 32, 33, 63, 64, 65, 100, 151, 152, 153, 997])
+def test_ragged_token_counts(T):
+    w, inp, ref = inputs_for("prefill_T512_E896", T=T)
+    assert_matches(run_gpu(w, inp), ref, w)
+
+
+SHAPES = [
+    # E, G, Kg, K, B, std
+    (129, 3, 2, 5, 16, 1.0),      # E not a multiple of 8 (unaligned rows)
+    (129, 1, 1, 7, 1, 1.0),
+    (64, 64, 8, 8, 4, 1.0),       # one expert per group, 64 groups
+    (256, 8, 4, 8, 64, 1.0),      # DeepSeek-V3-like
+    (384, 1, 1, 8, 128, 1.0),     # Kimi-K2-like
+    (4096, 16, 16, 32, 1024, 1.0),  # every group kept, K = 32, B = 1024
+    (1, 1, 1, 1, 8, 1.0),         # one expert
+    (96, 6, 6, 1, 2, 2.0),
+    (2048, 32, 5, 12, 32, 1.0),
+]
+
+
+@pytest.mark.parametrize("T", [1, 17, 64, 65, 700])
+@pytest.mark.parametrize("E,G,Kg,K,B,std", SHAPES)
+def test_shapes(E, G, Kg, K, B, std, T):
+    w = datagen.Workload("shape", T=T, E=E, n_group=G, topk_group=Kg, topk=K,
+                         routed_scale=1.5, block_m=B, logit_std=std)
+    inp = datagen.make_inputs(w, needs_redraw=redraw_callback(oracle, w))
+    ref = oracle.route_sort(inp.logits_bf16, inp.bias, G, Kg, K, 1.5, B)
+    assert_matches(run_gpu(w, inp), ref, w)
+
+
+def test_exact_ties_go_to_lower_index():
+    for T in (1, 40, 300):
+        w = datagen.Workload("ties", T=T, E=896, n_group=8, topk_group=4, topk=16,
+                             routed_scale=2.5, block_m=32)
+        logits = np.full((T, 896), datagen.float32_to_bf16_bits(np.float32([0.75]))[0],
+                         np.uint16)
+        bias = np.zeros(896, np.float32)
+        bias[::7] = 0.03125  # a few exact ties at a higher key
+        inp = datagen.RouterInputs(w, logits, bias)
+        ref = oracle.route_sort(logits, bias, 8, 4, 16, 2.5, 32)
+        assert_matches(run_gpu(w, inp), ref, w)
+
+
+def test_empty_call():
+    w = datagen.workload("prefill_T512_E896", T=0)
+    out = mrs.RouteSortBuffers.allocate(0, w.E, w.topk, w.block_m, device=DEV)
+    out.num_tokens_post_pad.fill_(123)
+    out.workspace.fill_(0xFF)
+    logits = torch.empty((0, w.E), dtype=torch.bfloat16, device=DEV)
+    bias = torch.zeros(w.E, dtype=torch.float32, device=DEV)
+    mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale, w.block_m,
+                   out=out)
+    torch.cuda.synchronize()
+    assert int(out.num_tokens_post_pad.item()) == 0
+    assert out.status_word() == 0
+
+
+def test_inputs_unchanged():
+    w, inp, ref = inputs_for("skewed_T8192_E896")
+    logits = to_dev_bf16(inp.logits_bf16)
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    h0 = hashlib.sha256(logits.view(torch.int16).cpu().numpy().tobytes() +
+                        bias.cpu().numpy().tobytes()).hexdigest()
+    mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale, w.block_m)
+    torch.cuda.synchronize()
+    h1 = hashlib.sha256(logits.view(torch.int16).cpu().numpy().tobytes() +
+                        bias.cpu().numpy().tobytes()).hexdigest()
+    assert h0 == h1
+
+
+# ------------------------------------------------------------------ split entry points
+@pytest.mark.parametrize("name", ["decode_T1_E896_G8", "skewed_T8192_E896",
+                                  "wide_T16384_E4096"])
+def test_moe_topk(name):
+    w, inp, ref = inputs_for(name)
+    logits = to_dev_bf16(inp.logits_bf16)
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    ids = torch.full((w.T, w.topk), -5, dtype=torch.int32, device=DEV)
+    wt = torch.full((w.T, w.topk), float("nan"), dtype=torch.float32, device=DEV)
+    mrs.moe_topk(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale, ids, wt)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ref.topk_ids)
+    assert np.max(np.abs(wt.cpu().numpy() - ref.topk_weights)) <= WEIGHT_ATOL
+
+
+def _ids_for(dist, T, K, E, rng):
+    if dist == "uniform":
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+    elif dist == "shared":
+        ids = np.stack([np.concatenate([[0], 1 + rng.permutation(E - 1)[:K - 1]])
+                        for _ in range(T)])
+    elif dist == "one_expert":
+        ids = np.full((T, K), E // 2)
+    elif dist == "every_third_dropped":
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+        ids.reshape(-1)[::3] = -1
+    elif dist == "all_dropped":
+        ids = np.full((T, K), -1)
+    elif dist == "dup_in_token":
+        ids = rng.integers(0, E, (T, K))
+    else:
+        raise ValueError(dist)
+    return ids.astype(np.int32)
+
+
+@pytest.mark.parametrize("dist", ["uniform", "shared", "one_expert", "every_third_dropped",
+                                  "all_dropped", "dup_in_token"])
+@pytest.mark.parametrize("T,K,E,B", [(5, 4, 33, 8), (64, 16, 896, 32), (3001, 8, 256, 64),
+                                     (16384, 8, 4096, 128)])
+def test_moe_sort_distributions(dist, T, K, E, B):
+    rng = np.random.default_rng(T + K + E + B)
+    ids = _ids_for(dist, T, K, E, rng)
+    wts = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
+    ref = oracle.sort(ids, wts, E, B)
+    out = mrs.RouteSortBuffers.allocate(T, E, K, B, device=DEV)
+    out.sorted_token_ids.fill_(-3)
+    out.workspace.fill_(0x5A)
+    d_ids = torch.from_numpy(ids).to(DEV)
+    d_w = torch.from_numpy(wts).to(DEV)
+    mrs.moe_sort(d_ids, d_w, E, B, out.sorted_token_ids, out.sorted_weights, out.expert_ids,
+                 out.num_tokens_post_pad, out.workspace)
+    torch.cuda.synchronize()
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref.num_tokens_post_pad
+    assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)
+    assert np.array_equal(out.sorted_weights[:npp].cpu().numpy(), ref.sorted_weights)
+    assert np.array_equal(out.expert_ids[: npp // B].cpu().numpy(), ref.expert_ids)
+    assert out.status_word() == ref.flags == 0
+
+
+@pytest.mark.parametrize("T", [3, 2000])
+def test_moe_sort_flags_out_of_range_ids(T):
+    rng = np.random.default_rng(T)
+    E, K, B = 64, 4, 16
+    ids = rng.integers(0, E, (T, K)).astype(np.int32)
+    ids[T // 2, 1] = E + 3
+    wts = np.ones((T, K), np.float32)
+    ref = oracle.sort(ids, wts, E, B)
+    assert ref.flags == oracle.FLAG_BAD_EXPERT_ID
+    out = mrs.RouteSortBuffers.allocate(T, E, K, B, device=DEV)
+    mrs.moe_sort(torch.from_numpy(ids).to(DEV), torch.from_numpy(wts).to(DEV), E, B,
+                 out.sorted_token_ids, out.sorted_weights, out.expert_ids,
+                 out.num_tokens_post_pad, out.workspace)
+    torch.cuda.synchronize()
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref.num_tokens_post_pad
+    assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)
+    assert out.status_word() == mrs.DEVICE_BAD_EXPERT_ID
+
+
+# ------------------------------------------------------------------ CUDA graphs
+@pytest.mark.parametrize("name,T", [("decode_T1_E896_G8", None), ("prefill_T512_E896", None),
+                                    ("skewed_T8192_E896", 2048)])
+def test_graph_replay_with_changed_inputs(name, T):
+    w, inp, _ = inputs_for(name, T=T)
+    logits = to_dev_bf16(inp.logits_bf16)
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                       w.block_m, out=out)  # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                       w.block_m, out=out)
+    for seed in range(1, 9):
+        ws = datagen.workload(name, T=w.T, seed=seed)
+        new = datagen.make_inputs(ws, needs_redraw=redraw_callback(oracle, ws))
+        logits.copy_(to_dev_bf16(new.logits_bf16))
+        bias.copy_(torch.from_numpy(new.bias).to(DEV))
+        out.sorted_token_ids.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.route_sort(new.logits_bf16, new.bias, w.n_group, w.topk_group, w.topk,
+                                w.routed_scale, w.block_m)
+        assert_matches(out, ref, w)
