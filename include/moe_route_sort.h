@@ -81,6 +81,8 @@ extern "C" {
 
 /* Device-side status bits, written to the first int32 of the workspace by every call. */
 #define MOE_RS_DEVICE_BAD_EXPERT_ID 0x1   /* moe_sort saw an id >= E; those routes dropped */
+#define MOE_RS_DEVICE_WAIT_TIMEOUT 0x2    /* a bounded device-side wait gave up (an input copy
+                                             did not complete in time); outputs are invalid */
 
 /* ---------------------------------------------------------------- size queries */
 
@@ -125,6 +127,17 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
              int block_m, int32_t* sorted_token_ids, float* sorted_weights,
              int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
              size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Exhaustive check of the bound behind the route kernels' pruning (not an operation of the
+ * path; it has no counterpart in the source pages).  The multi-CTA route kernels discard an
+ * expert only when a cheap score 0.5 * tanh.approx(0.5 x) + 0.5 proves it cannot be
+ * selected; that proof assumes |cheap - exact sigmoid| <= bound for every bf16 x.  Writes
+ * out2[0] = the largest difference over all finite bf16 inputs on this device and
+ * out2[1] = the bound assumed (device memory, 2 floats, caller-owned; valid after the
+ * stream reaches this call).  Selection stays exact only if out2[0] <= out2[1]. */
+int moe_route_sort_proxy_selftest(float* out2, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

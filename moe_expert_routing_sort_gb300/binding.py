@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
         lib.moe_topk.restype = I
         lib.moe_sort.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P]
         lib.moe_sort.restype = I
+        lib.moe_route_sort_proxy_selftest.argtypes = [P, P]
+        lib.moe_route_sort_proxy_selftest.restype = I
         _lib = lib
         return lib
 
@@ -157,6 +159,15 @@ def moe_sort(topk_ids, topk_weights, E, block_m, sorted_token_ids, sorted_weight
                          _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(),
                          _stream_handle(stream))
     _check(rc, "moe_sort")
+
+
+def moe_route_sort_proxy_selftest(out2, stream=None) -> None:
+    """Largest |cheap sigmoid - exact sigmoid| over all bf16 inputs -> out2[0]; bound -> out2[1]."""
+    _need(out2, torch.float32, "out2")
+    if out2.numel() < 2:
+        raise ValueError("out2 needs 2 floats")
+    _check(load().moe_route_sort_proxy_selftest(_ptr(out2), _stream_handle(stream)),
+           "moe_route_sort_proxy_selftest")
 
 
 # ---------------------------------------------------------- convenience buffers

@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/moe_route_sort.h"
+#include "moe_route_sort.h"
 #include "mrs_internal.h"
 
 namespace {
@@ -116,96 +116,110 @@ RouteShape make_shape(int E, int G, int Kg, int K, float R) {
   return sh;
 }
 
+// Segment layout of the route step (see mrs_seg.cuh): groups split into L lanes of equal,
+// 4-expert-aligned segments.  False when the shape does not allow it.
+bool make_seg_shape(int E, int G, int Kg, int K, float R, SegShape& s) {
+  if (G > 32) return false;
+  int L = 1;
+  while (L * 2 * G <= 32) L *= 2;
+  const int g = E / G;
+  if (g % L != 0) return false;
+  const int sl = g / L;
+  if (sl % 4 != 0) return false;
+  s.E = E;
+  s.G = G;
+  s.g = g;
+  s.Kg = Kg;
+  s.K = K;
+  s.L = L;
+  s.log2L = 0;
+  while ((1 << s.log2L) < L) ++s.log2L;
+  s.sl = sl;
+  s.nu = sl / 4;
+  // when segments are a multiple of 128 bytes of keys apart, rotate each lane's unit order
+  // so that lanes of one shared-memory phase hit different banks
+  s.rot = (s.nu % 8 == 0) ? 1 : 0;
+  s.R = R;
+  return true;
+}
+
 int launch_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_RS_OK;
   cudaGetLastError();  // clear a non-sticky launch error
   return MOE_RS_ERR_LAUNCH;
 }
 
-// Warps per CTA of the route kernel that fit in shared memory.
-int route_max_warps(int E, bool hist, const DeviceInfo& d) {
-  int w = 16;
-  while (w > 1 && route_smem_bytes(E, w, hist) > static_cast<size_t>(d.smem_optin)) --w;
-  return w;
-}
-
-// Multi-CTA route step.  Units are contiguous token ranges; one CTA each.
-int run_route(const void* logits, const float* bias, int T, const RouteShape& sh,
-              int32_t* topk_ids, float* topk_w, int32_t* partial, int32_t* unit_flags,
-              int U, const DeviceInfo& d, cudaStream_t st) {
+// Multi-CTA route step.  Units are contiguous token ranges, one CTA each; with `sort`,
+// each CTA also runs phase 1 of the sort step into the workspace.
+int run_route(const void* logits, const float* bias, int T, const RouteShape& sh, bool sort,
+              int32_t* topk_ids, float* topk_w, unsigned char* ws, const WsLayout& l, int U,
+              int nslices, const DeviceInfo& d, cudaStream_t st) {
   RouteArgs a{};
   a.logits = static_cast<const uint16_t*>(logits);
   a.bias = bias;
   a.T = T;
   a.U = U;
-  const bool hist = partial != nullptr;
-  const int maxw = route_max_warps(sh.E, hist, d);
-  const int per_unit = (T + U - 1) / U;
-  a.nwarps = per_unit < maxw ? per_unit : maxw;
+  a.sort = sort;
+  const int tpu = (T + U - 1) / U;
+  a.max_routes = tpu * sh.K;
   a.vec16 = (sh.E % 8) == 0;
+  a.use_seg = a.vec16 && make_seg_shape(sh.E, sh.G, sh.Kg, sh.K, sh.R, a.seg);
+  const int cap = a.use_seg ? kSegThreads / 32 : 16;
+  int nwarps = tpu < cap ? tpu : cap;
+  auto smem_for = [&](int w) {
+    return a.use_seg ? seg_smem_bytes(sh.E, a.seg.nu, w, a.max_routes, sort)
+                     : route_smem_bytes(sh.E, w, a.max_routes, sort);
+  };
+  while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(d.smem_optin)) --nwarps;
+  a.nwarps = nwarps;
+  const size_t smem = smem_for(nwarps);
+  if (smem > static_cast<size_t>(d.smem_optin)) return MOE_RS_ERR_LAUNCH;
   a.sh = sh;
   a.topk_ids = topk_ids;
   a.topk_w = topk_w;
-  a.partial = partial;
-  a.unit_flags = unit_flags;
-  const size_t smem = route_smem_bytes(sh.E, a.nwarps, hist);
-  if (smem > static_cast<size_t>(d.smem_optin)) return MOE_RS_ERR_LAUNCH;
+  if (sort) {
+    a.uo.loc_off = reinterpret_cast<int32_t*>(ws + l.loc_off);
+    a.uo.unit_buf = reinterpret_cast<int2*>(ws + l.unit_buf);
+    a.uo.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
+    a.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
+    a.uo.nslices = nslices;
+  }
   return launch_status(launch_route(a, smem, st));
 }
 
-int units_for(int T, const DeviceInfo& d) {
-  int U = d.sms;
-  if (U > kMaxUnits) U = kMaxUnits;
-  if (U > T) U = T;
-  return U < 1 ? 1 : U;
-}
-
-// Scan + scatter over the partial counts already in the workspace.
-int run_sort_tail(const int32_t* ids, const float* w, int T, int E, int K, int B, int U,
-                  int32_t* sorted_ids, float* sorted_w, int32_t* expert_ids, int32_t* npp,
-                  unsigned char* ws, const WsLayout& l, cudaStream_t st) {
-  ScanArgs s{};
-  s.E = E;
-  s.U = U;
-  s.B = B;
-  s.partial = reinterpret_cast<int32_t*>(ws + l.partial);
-  s.cnt_tot = reinterpret_cast<int32_t*>(ws + l.cnt_tot);
-  s.inchunk_off = reinterpret_cast<int32_t*>(ws + l.inchunk_off);
-  s.chunk_tot = reinterpret_cast<int32_t*>(ws + l.chunk_tot);
-  int rc = launch_status(launch_scan(s, st));
-  if (rc) return rc;
-  ScatterArgs c{};
-  c.ids = ids;
-  c.w = w;
+// Phase 2 of the sort step over the per-unit results in the workspace.
+int run_slices(int T, int E, int K, int B, int U, int nslices, int32_t* sorted_ids,
+               float* sorted_w, int32_t* expert_ids, int32_t* npp, unsigned char* ws,
+               const WsLayout& l, cudaStream_t st) {
+  SliceArgs c{};
   c.T = T;
   c.K = K;
   c.E = E;
   c.U = U;
   c.B = B;
   c.N = T * K;
-  c.nchunk = (E + kChunk - 1) / kChunk;
-  c.partial = s.partial;
-  c.cnt_tot = s.cnt_tot;
-  c.inchunk_off = s.inchunk_off;
-  c.chunk_tot = s.chunk_tot;
+  c.nslices = nslices;
+  c.loc_off = reinterpret_cast<const int32_t*>(ws + l.loc_off);
+  c.unit_buf = reinterpret_cast<const int2*>(ws + l.unit_buf);
+  c.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
   c.unit_flags = reinterpret_cast<const int32_t*>(ws + l.unit_flags);
   c.sorted_ids = sorted_ids;
   c.sorted_w = sorted_w;
   c.expert_ids = expert_ids;
   c.npp = npp;
   c.status = reinterpret_cast<int32_t*>(ws + l.status);
-  return launch_status(launch_scatter(c, st));
+  return launch_status(launch_slices(c, st));
 }
 
 // Single-CTA path: shared-memory layout for the largest wave that fits.
-bool small_plan(int T, int E, int K, int B, bool sort_only, const DeviceInfo& d,
+bool small_plan(int T, int E, int K, int B, bool sort_only, int nu, const DeviceInfo& d,
                 SmallLayout& lay, int& wave, int& nb_max) {
   if (T > kSmallMaxTokens) return false;
   const int N = T * K;
   nb_max = static_cast<int>(max_padded64(T, E, K, B) / B);
-  wave = sort_only ? 0 : (T < 32 ? T : 32);
+  wave = sort_only ? 0 : (T < 16 ? T : 16);
   for (;;) {
-    lay = small_layout(E, N, wave, nb_max, sort_only);
+    lay = small_layout(E, N, wave, nu, sort_only);
     if (lay.total <= d.smem_optin) return true;
     if (sort_only || wave <= 1) return false;
     --wave;
@@ -227,8 +241,10 @@ size_t moe_sort_max_blocks(int T, int E, int topk, int block_m) {
 }
 
 size_t moe_route_sort_workspace_bytes(int T, int E, int topk, int block_m) {
-  if (T < 0 || E < 1 || E > kMaxExperts || topk < 1 || !pow2_block_m(block_m)) return 0;
-  return ws_layout(T, E).total;
+  if (T < 0 || E < 1 || E > kMaxExperts || topk < 1 || topk > kMaxTopk ||
+      !pow2_block_m(block_m))
+    return 0;
+  return ws_layout(T, E, topk).total;
 }
 
 const char* moe_route_sort_strerror(int status) {
@@ -270,8 +286,9 @@ int moe_topk(const void* logits_bf16, const float* bias, int T, int E, int n_gro
   DeviceInfo d;
   if (!device_info(d)) return MOE_RS_ERR_LAUNCH;
   const RouteShape sh = make_shape(E, n_group, topk_group, topk, routed_scale);
-  return run_route(logits_bf16, bias, T, sh, topk_ids, topk_weights, nullptr, nullptr,
-                   units_for(T, d), d, stream);
+  const WsLayout none{};
+  return run_route(logits_bf16, bias, T, sh, false, topk_ids, topk_weights, nullptr, none,
+                   units_for_shape(T, topk, d.sms), 0, d, stream);
 }
 
 int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int n_group,
@@ -289,7 +306,7 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
   if (T > 0 && (!logits_bf16 || !bias || !topk_ids || !topk_weights || !sorted_token_ids ||
                 !sorted_weights || !expert_ids))
     return MOE_RS_ERR_NULL_POINTER;
-  const WsLayout l = ws_layout(T, E);
+  const WsLayout l = ws_layout(T, E, topk);
   if (workspace_bytes < l.total) return MOE_RS_ERR_WORKSPACE;
   if (!aligned(workspace, 16) || !aligned(num_tokens_post_pad, 4)) return MOE_RS_ERR_MISALIGNED;
   if (T > 0 && (!aligned(logits_bf16, 16) || !aligned(bias, 4) || !aligned(topk_ids, 4) ||
@@ -316,8 +333,13 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
 
   SmallLayout lay;
   int wave = 0, nb_max = 0;
-  if (T <= kSmallMaxTokens && small_plan(T, E, topk, block_m, false, d, lay, wave, nb_max)) {
+  SegShape seg{};
+  const bool use_seg = make_seg_shape(E, n_group, topk_group, topk, routed_scale, seg);
+  if (T <= kSmallMaxTokens &&
+      small_plan(T, E, topk, block_m, false, use_seg ? seg.nu : 0, d, lay, wave, nb_max)) {
     SmallArgs a{};
+    a.use_seg = use_seg;
+    a.seg = seg;
     a.logits = static_cast<const uint16_t*>(logits_bf16);
     a.bias = bias;
     a.T = T;
@@ -337,14 +359,13 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
     return launch_status(launch_small(a, false, stream));
   }
 
-  const int U = units_for(T, d);
-  int32_t* partial = reinterpret_cast<int32_t*>(ws + l.partial);
-  int32_t* unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
-  rc = run_route(logits_bf16, bias, T, sh, topk_ids, topk_weights, partial, unit_flags, U, d,
+  const int U = units_for_shape(T, topk, d.sms);
+  const int nslices = slices_for(U, E);
+  rc = run_route(logits_bf16, bias, T, sh, true, topk_ids, topk_weights, ws, l, U, nslices, d,
                  stream);
   if (rc) return rc;
-  return run_sort_tail(topk_ids, topk_weights, T, E, topk, block_m, U, sorted_token_ids,
-                       sorted_weights, expert_ids, num_tokens_post_pad, ws, l, stream);
+  return run_slices(T, E, topk, block_m, U, nslices, sorted_token_ids, sorted_weights,
+                    expert_ids, num_tokens_post_pad, ws, l, stream);
 }
 
 int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, int topk,
@@ -358,7 +379,7 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
   if (T > 0 && (!topk_ids || !topk_weights || !sorted_token_ids || !sorted_weights ||
                 !expert_ids))
     return MOE_RS_ERR_NULL_POINTER;
-  const WsLayout l = ws_layout(T, E);
+  const WsLayout l = ws_layout(T, E, topk);
   if (workspace_bytes < l.total) return MOE_RS_ERR_WORKSPACE;
   if (!aligned(workspace, 16) || !aligned(num_tokens_post_pad, 4)) return MOE_RS_ERR_MISALIGNED;
   if (T > 0 && (!aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
@@ -381,7 +402,7 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
   if (!device_info(d)) return MOE_RS_ERR_LAUNCH;
   SmallLayout lay;
   int wave = 0, nb_max = 0;
-  if (T * topk <= 2048 && small_plan(T, E, topk, block_m, true, d, lay, wave, nb_max)) {
+  if (T * topk <= 2048 && small_plan(T, E, topk, block_m, true, 0, d, lay, wave, nb_max)) {
     SmallArgs a{};
     a.in_ids = topk_ids;
     a.in_w = topk_weights;
@@ -399,19 +420,25 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
     a.status = status;
     return launch_status(launch_small(a, true, stream));
   }
-  const int U = units_for(T, d);
-  CountArgs c{};
+  const int U = units_for_shape(T, topk, d.sms);
+  const int nslices = slices_for(U, E);
+  UnitArgs c{};
   c.ids = topk_ids;
+  c.w = topk_weights;
   c.T = T;
   c.K = topk;
   c.E = E;
   c.U = U;
-  c.partial = reinterpret_cast<int32_t*>(ws + l.partial);
+  c.max_routes = ((T + U - 1) / U) * topk;
+  c.loc_off = reinterpret_cast<int32_t*>(ws + l.loc_off);
+  c.unit_buf = reinterpret_cast<int2*>(ws + l.unit_buf);
+  c.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
   c.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
-  rc = launch_status(launch_count(c, stream));
+  c.nslices = nslices;
+  rc = launch_status(launch_unit(c, stream));
   if (rc) return rc;
-  return run_sort_tail(topk_ids, topk_weights, T, E, topk, block_m, U, sorted_token_ids,
-                       sorted_weights, expert_ids, num_tokens_post_pad, ws, l, stream);
+  return run_slices(T, E, topk, block_m, U, nslices, sorted_token_ids, sorted_weights,
+                    expert_ids, num_tokens_post_pad, ws, l, stream);
 }
 
 }  // extern "C"

@@ -76,6 +76,53 @@ __device__ __forceinline__ float warp_sort_desc(float v, int lane) {
   return v;
 }
 
+// K-th largest of one float per lane (1 <= k <= 32), by counting for each lane how many
+// lanes beat it (larger value, or equal value and lower lane).  32 independent shuffles:
+// short dependency chains, for latency-bound callers.
+__device__ __forceinline__ float warp_kth_largest(float v, int k, int lane) {
+  int rank = 0;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) {
+    const float o = __shfl_sync(kFull, v, m);
+    rank += ((o > v) || (o == v && m < lane)) ? 1 : 0;
+  }
+  const unsigned b = __ballot_sync(kFull, rank == k - 1);
+  return __shfl_sync(kFull, v, __ffs(b) - 1);
+}
+
+// ------------------------------------------------------------------ proxy score
+// Cheap stand-in for the selection key: p = 0.5 * tanh.approx(0.5 x) + (0.5 + bias).
+// 0.5 + 0.5 tanh(x / 2) is the logistic function, so p differs from the exact key
+// s + bias by the hardware tanh approximation (at most kProxyTanhBound over every bf16 x,
+// checked exhaustively on the device by moe_route_sort_proxy_selftest) plus four roundings
+// of values below max|bias| + 1.5 in magnitude; proxy_delta() bounds the total for biases
+// up to kProxyBiasLimit.  The selection only uses p to discard experts that are worse than a
+// proven bound by more than 2 * delta.
+constexpr float kProxyTanhBound = 1.0f / 2048.0f;
+constexpr float kProxyBiasLimit = 1024.0f;
+
+// Bound on |proxy - exact key| for biases of magnitude <= max_abs_bias: the tanh bound
+// plus four half-ulp roundings of values below max_abs_bias + 1.5 (ulp(x) <= x * 2^-23).
+__host__ __device__ inline float proxy_delta(float max_abs_bias) {
+  return kProxyTanhBound + (max_abs_bias + 2.0f) * 2.384185791e-7f;  // 2 * 2^-23
+}
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float proxy_key(float x, float c) {
+  return fmaf(0.5f, tanh_approx(0.5f * x), c);
+}
+
+// Exact key and score of one logit: key = s + bias with s the exact score.
+__device__ __forceinline__ float exact_key(float x, float bias, float& s) {
+  s = exact_score(x);
+  return __fadd_rn(s, bias);
+}
+
 // ------------------------------------------------------------------ route shape
 struct RouteShape {
   int E, G, g, Kg, K;
@@ -93,6 +140,8 @@ struct __align__(16) WarpScratch {
   float gs[kMaxGroups];
   float p2[kMaxGroups];
   int kept[kMaxGroups];
+  unsigned kept_mask[2];  // bit j of group j (groups 0..31, 32..63)
+  int count;              // survivors appended so far
   int sel_id[kMaxTopk];
   float sel_s[kMaxTopk];
 };
@@ -202,8 +251,42 @@ __device__ __forceinline__ bool rank_groups(const RouteShape& sh, WarpScratch& w
   const unsigned b1 = __ballot_sync(kFull, k1);
   if (k0) ws.kept[__popc(b0 & lanemask_lt(lane))] = lane;
   if (k1) ws.kept[__popc(b0) + __popc(b1 & lanemask_lt(lane))] = lane + 32;
+  if (lane == 0) {
+    ws.kept_mask[0] = b0;
+    ws.kept_mask[1] = b1;
+  }
   __syncwarp();
   return certain;
+}
+
+// Slots of the K best of ws.cand[0..total): rank = number of better composites (all
+// composites are distinct, so ranks are 0..total-1).
+__device__ __forceinline__ void rank_candidates(WarpScratch& ws, int total, int K, int lane) {
+  for (int a = lane; a < total; a += 32) {
+    const unsigned long long me = ws.cand[a];
+    int rank = 0;
+#pragma unroll 4
+    for (int b = 0; b < total; ++b) rank += (ws.cand[b] > me) ? 1 : 0;
+    if (rank < K) {
+      ws.sel_id[rank] = composite_expert(me);
+      ws.sel_s[rank] = ws.cand_s[a];
+    }
+  }
+}
+
+// Renormalised weights of the K selected experts: sum of scores in slot order, then
+// (s_k / sum) * R.  Lane k < K returns slot k.
+__device__ __forceinline__ void finish_weights(const WarpScratch& ws, int K, float R, int lane,
+                                               int& id, float& w) {
+  const bool mine = lane < K;
+  const float s = mine ? ws.sel_s[lane] : 0.0f;
+  id = mine ? ws.sel_id[lane] : -1;
+  float sum = 0.0f;
+  if (lane == 0)
+    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, ws.sel_s[k]);  // slot order
+  sum = __shfl_sync(kFull, sum, 0);
+  w = mine ? __fmul_rn(__fdiv_rn(s, sum), R) : 0.0f;
+  __syncwarp();
 }
 
 // --------------------------------------------- step 3: top-K inside the kept groups
@@ -227,7 +310,7 @@ __device__ __forceinline__ void topk_in_kept(const Src& src, const RouteShape& s
     const int base = (all_kept ? i : ws.kept[i]) * g;
     for (int c = lane; c < g; c += 32) M = fmaxf(M, src.proxy(base + c));
   }
-  const float tau = __shfl_sync(kFull, warp_sort_desc(M, lane), sh.K - 1);
+  const float tau = warp_kth_largest(M, sh.K, lane);
   const float theta = (Src::kDelta > 0.0f) ? tau - 2.0f * Src::kDelta : tau;
 
   int cnt = 0;
@@ -253,15 +336,7 @@ __device__ __forceinline__ void topk_in_kept(const Src& src, const RouteShape& s
       }
     }
     __syncwarp();
-    for (int a = lane; a < total; a += 32) {
-      const unsigned long long me = ws.cand[a];
-      int rank = 0;
-      for (int b = 0; b < total; ++b) rank += (ws.cand[b] > me) ? 1 : 0;
-      if (rank < sh.K) {
-        ws.sel_id[rank] = composite_expert(me);
-        ws.sel_s[rank] = ws.cand_s[a];
-      }
-    }
+    rank_candidates(ws, total, sh.K, lane);
   } else {
     // K rounds: the best exact composite strictly below the previous winner.
     unsigned long long prev = ~0ull;
@@ -321,13 +396,7 @@ __device__ __forceinline__ void route_token(const Src& src, const RouteShape& sh
     }
   }
   topk_in_kept(src, sh, ws, lane);
-  const bool mine = lane < sh.K;
-  const float s = mine ? ws.sel_s[lane] : 0.0f;
-  id = mine ? ws.sel_id[lane] : -1;
-  float sum = 0.0f;
-  for (int k = 0; k < sh.K; ++k) sum = __fadd_rn(sum, __shfl_sync(kFull, s, k));
-  w = mine ? __fmul_rn(__fdiv_rn(s, sum), sh.R) : 0.0f;
-  __syncwarp();
+  finish_weights(ws, sh.K, sh.R, lane, id, w);
 }
 
 // Key source over exact keys and scores already in shared memory.
@@ -341,5 +410,71 @@ struct SmemExactSrc {
     return key[e];
   }
 };
+
+// ------------------------------------------------------- TMA bulk copies, mbarriers
+// A device wait gives up after this long (an error bit is raised instead of hanging).
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global memory
+// into shared memory, completing a transaction count of `bytes` on `mbar`.
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
+                                            unsigned long long* mbar) {
+  const uint32_t m = smem_u32(mbar);
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(m), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(m)
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* mbar, uint32_t phase) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(smem_u32(mbar)), "r"(phase)
+      : "memory");
+  return done != 0u;
+}
+
+// Wait for phase `phase` of `mbar` to complete, at most kWaitLimitNs.  Every lane waits
+// (each gets the acquire); the result is made warp-uniform.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* mbar, uint32_t phase) {
+  bool ok = mbar_try_wait(mbar, phase);
+  if (!ok) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (!(ok = mbar_try_wait(mbar, phase))) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  return __all_sync(kFull, ok);
+}
 
 }  // namespace mrs

@@ -6,56 +6,64 @@
 #include <cuda_runtime.h>
 
 #include "mrs_device.cuh"
+#include "mrs_seg.cuh"
 
 namespace mrs {
 
-// Routes per unit-tile in the scatter step: one bit per token in a 64-bit mask.
-constexpr int kTileTokens = 64;
-// Largest number of units (CTAs of the multi-CTA path); sizes the workspace bound.
-constexpr int kMaxUnits = 1024;
 // Largest T that takes the single-CTA path (its ranks use one 64-bit token mask).
 constexpr int kSmallMaxTokens = 64;
-constexpr int kSmallThreads = 1024;
-constexpr int kChunk = 32;  // experts per chunk of the padded scan
-constexpr int kMaxChunks = kMaxExperts / kChunk;
+constexpr int kSmallThreads = 512;
+constexpr int kSegThreads = 512;
+constexpr int kUnitThreads = 512;
+constexpr int kSliceThreads = 512;
+// A unit (one CTA of the route step) holds at most this many routes in shared memory.
+constexpr int kUnitRouteCap = 4096;
 
-// Workspace layout (byte offsets), identical for every call with the same (T, E).
+// Units of the multi-CTA path for T tokens: at least one token and at most kUnitRouteCap
+// routes each; `sms` is the device's SM count (the workspace bound assumes <= 1024).
+inline int units_for_shape(int T, int K, int sms) {
+  const int tpu_cap = kUnitRouteCap / K > 0 ? kUnitRouteCap / K : 1;
+  int U = T < sms ? T : sms;
+  const int need = (T + tpu_cap - 1) / tpu_cap;
+  if (need > U) U = need;
+  return U < 1 ? 1 : U;
+}
+inline int units_bound(int T, int K) { return units_for_shape(T, K, 1024); }
+inline int slices_for(int U, int E) { return U < E ? U : E; }
+
+// Workspace layout (byte offsets), identical for every call with the same (T, E, K).
 struct WsLayout {
   size_t status;       // int32
-  size_t unit_flags;   // int32[kMaxUnits]
-  size_t cnt_tot;      // int32[E]   routes per expert
-  size_t inchunk_off;  // int32[E]   padded offset inside its 32-expert chunk
-  size_t chunk_tot;    // int32[kMaxChunks] padded rows per chunk
-  size_t partial;      // int32[U_bound][E] per-unit counts, then exclusive prefix over units
+  size_t unit_flags;   // int32[U]
+  size_t slice_flags;  // uint64[slices]  look-back words of the slice kernel
+  size_t loc_off;      // int32[U][E + 1] per-unit exclusive offsets of each expert
+  size_t unit_buf;     // int2[T * K]     per-unit routes sorted by expert: (flat index, weight)
   size_t total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-inline int units_bound(int T) { return T < kMaxUnits ? (T > 0 ? T : 1) : kMaxUnits; }
-
-inline WsLayout ws_layout(int T, int E) {
+inline WsLayout ws_layout(int T, int E, int K) {
+  const int U = units_bound(T, K);
   WsLayout l{};
   size_t o = 0;
   l.status = o;
   o = align16(o + 16);
   l.unit_flags = o;
-  o = align16(o + sizeof(int32_t) * kMaxUnits);
-  l.cnt_tot = o;
-  o = align16(o + sizeof(int32_t) * E);
-  l.inchunk_off = o;
-  o = align16(o + sizeof(int32_t) * E);
-  l.chunk_tot = o;
-  o = align16(o + sizeof(int32_t) * kMaxChunks);
-  l.partial = o;
-  o = align16(o + sizeof(int32_t) * (size_t)units_bound(T) * E);
+  o = align16(o + sizeof(int32_t) * U);
+  l.slice_flags = o;
+  o = align16(o + sizeof(unsigned long long) * slices_for(U, E));
+  l.loc_off = o;
+  o = align16(o + sizeof(int32_t) * static_cast<size_t>(U) * (E + 1));
+  l.unit_buf = o;
+  o = align16(o + 8 * static_cast<size_t>(T) * K);
   l.total = o;
   return l;
 }
 
 // ------------------------------------------------------------- single-CTA path
 struct SmallLayout {
-  int bias, keys, svals, scratch, rid, rw, rrank, cnt, off, masks, owner, misc, total;
+  int bias, keys, svals, scratch, umax, rid, rw, rrank, cnt, off, masks, owner, misc, total;
 };
 
 struct SmallArgs {
@@ -65,6 +73,8 @@ struct SmallArgs {
   const float* in_w;
   int T, N, B, wave, nb_max;
   RouteShape sh;
+  bool use_seg;  // route with the segment routine (SegShape valid)
+  SegShape seg;
   SmallLayout lay;
   int32_t* topk_ids;
   float* topk_w;
@@ -76,41 +86,45 @@ struct SmallArgs {
 };
 
 // ------------------------------------------------------------- multi-CTA path
+// Phase-1 outputs of a unit, written at the end of the route (or unit) kernel.
+struct UnitOut {
+  int32_t* loc_off;                 // [U][E + 1]
+  int2* unit_buf;                   // [T * K]
+  unsigned long long* slice_flags;  // [nslices], cleared for the slice kernel
+  int32_t* unit_flags;              // [U]
+  int nslices;
+};
+
 struct RouteArgs {
   const uint16_t* logits;
   const float* bias;
-  int T, U, nwarps;
-  bool vec16;  // rows are 16-byte aligned (E % 8 == 0)
+  int T, U, nwarps, max_routes;
+  bool vec16;    // rows are 16-byte aligned (E % 8 == 0)
+  bool use_seg;  // segment shape valid and rows 16-byte aligned: TMA-staged segment kernel
+  bool sort;     // run phase 1 of the sort step after routing (else route only)
   RouteShape sh;
+  SegShape seg;
   int32_t* topk_ids;
   float* topk_w;
-  int32_t* partial;     // [U][E] or null (route only)
-  int32_t* unit_flags;  // [U] or null
+  UnitOut uo;
 };
 
-struct CountArgs {
-  const int32_t* ids;
-  int T, K, E, U;
-  int32_t* partial;
-  int32_t* unit_flags;
-};
-
-struct ScanArgs {
-  int E, U, B;
-  int32_t* partial;
-  int32_t* cnt_tot;
-  int32_t* inchunk_off;
-  int32_t* chunk_tot;
-};
-
-struct ScatterArgs {
+struct UnitArgs {
   const int32_t* ids;
   const float* w;
-  int T, K, E, U, B, N, nchunk;
-  const int32_t* partial;
-  const int32_t* cnt_tot;
-  const int32_t* inchunk_off;
-  const int32_t* chunk_tot;
+  int T, K, E, U, max_routes;
+  int32_t* loc_off;
+  int2* unit_buf;
+  unsigned long long* slice_flags;
+  int32_t* unit_flags;
+  int nslices;
+};
+
+struct SliceArgs {
+  int T, K, E, U, B, N, nslices;
+  const int32_t* loc_off;
+  const int2* unit_buf;
+  unsigned long long* slice_flags;
   const int32_t* unit_flags;
   int32_t* sorted_ids;
   float* sorted_w;
@@ -122,13 +136,19 @@ struct ScatterArgs {
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st);
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st);
-cudaError_t launch_count(const CountArgs& a, cudaStream_t st);
-cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st);
-cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t st);
+cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st);
+cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st);
 cudaError_t launch_empty(int32_t* npp, int32_t* status, cudaStream_t st);
 
-// Shared memory of the multi-CTA route kernel for a given warp count.
-size_t route_smem_bytes(int E, int nwarps, bool with_hist);
-SmallLayout small_layout(int E, int N, int wave, int nb_max, bool sort_only);
+// Shared memory of the multi-CTA route kernels for a given warp count.
+size_t route_smem_bytes(int E, int nwarps, int max_routes, bool sort);
+size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort);
+SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only);
+
+// Shared memory used by phase 1 of the sort step (mrs_unit.cuh) besides the routes.
+__host__ __device__ inline size_t unit_scratch_bytes(int E) {
+  return align16(sizeof(unsigned long long) * E) + align16(sizeof(int32_t) * E) +
+         align16(sizeof(int32_t) * (E + 1)) + align16(sizeof(int32_t) * E) + 256;
+}
 
 }  // namespace mrs

@@ -1,31 +1,42 @@
 // mrs_route.cu -- route step kernels of MoE route-sort for sm_103a.
 //
-//  * mrs_small_kernel: the whole path (route step + both sort phases) in one CTA, for
-//    decode-sized calls (T <= 64).  Scores of a wave of tokens are computed by the whole
-//    CTA, each warp routes one token, then the CTA counts, scans and scatters in shared
-//    memory.  No global atomics, one launch.
-//  * mrs_route_kernel: the route step of the multi-CTA path.  CTA u owns a contiguous range
-//    of tokens (its "unit"); each warp routes one token at a time and, when asked, the CTA
-//    counts its routes per expert in shared memory and stores the unit's histogram.
+//  * mrs_small_kernel: the whole path (route step + both sort phases) in one CTA for
+//    decode-sized calls (T <= 64): one launch, no global atomics, shared-memory histogram.
+//    The CTA computes the exact scores of a wave of tokens (one DRAM round trip: 16-byte
+//    logit vectors and bias together), each warp routes one token, and the CTA counts,
+//    scans and scatters in shared memory.
+//  * mrs_route_seg_kernel: route step of the multi-CTA path for shapes whose groups split
+//    into equal 4-expert-aligned lane segments (see mrs_seg.cuh).  CTA u owns a contiguous
+//    token range (its "unit"); each warp streams its tokens' rows into shared memory with
+//    double-buffered bulk copies (TMA) and routes them with cheap proxy scores plus exact
+//    refinement; the CTA counts its routes per expert in shared memory for the sort step.
+//  * mrs_route_kernel: the same step for any other shape: exact scores of a row into
+//    shared memory, then the warp-level route step over them.
 //
 // Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary
 // (FP32 logit conversion + correction bias, grouped top-k, both sort phases in one kernel).
 #include "mrs_internal.h"
-#include "../../include/moe_route_sort.h"
+#include "mrs_seg.cuh"
+#include "mrs_unit.cuh"
+#include "moe_route_sort.h"
 
 namespace mrs {
 
-// Exclusive prefix sum of the block_m-padded counts over experts, by a 1024-thread block
-// (4 consecutive experts per thread).  Returns the total; off[e] receives the prefix.
+// Exclusive prefix sum of the block_m-padded counts over experts by the whole block
+// (ept = ceil(E / threads) consecutive experts per thread, at most 8).  off[e] receives the
+// prefix; returns the total.
+template <int kThreads>
 __device__ __forceinline__ int block_scan_padded(const int* cnt, int* off, int E, int B,
                                                  int* wtot) {
+  constexpr int kWarps = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int loc[4];
+  const int ept = (E + kThreads - 1) / kThreads;
+  int loc[8];
   int s = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = tid * 4 + i;
-    const int p = (e < E) ? ((cnt[e] + B - 1) & ~(B - 1)) : 0;
+  for (int i = 0; i < 8; ++i) {
+    const int e = tid * ept + i;
+    const int p = (i < ept && e < E) ? ((cnt[e] + B - 1) & ~(B - 1)) : 0;
     loc[i] = s;
     s += p;
   }
@@ -33,22 +44,90 @@ __device__ __forceinline__ int block_scan_padded(const int* cnt, int* off, int E
   if (lane == 31) wtot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int v = wtot[lane];
+    const int v = (lane < kWarps) ? wtot[lane] : 0;
     const int wi = warp_inclusive_sum(v, lane);
     __syncwarp();
-    wtot[lane] = wi - v;
+    if (lane < kWarps) wtot[lane] = wi - v;
     if (lane == 31) wtot[32] = wi;
   }
   __syncthreads();
   const int base = wtot[warp] + incl - s;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = tid * 4 + i;
-    if (e < E) off[e] = base + loc[i];
+  for (int i = 0; i < 8; ++i) {
+    const int e = tid * ept + i;
+    if (i < ept && e < E) off[e] = base + loc[i];
   }
   const int total = wtot[32];
-  __syncthreads();
+  __syncthreads();  // every off[] is read by other threads next
   return total;
+}
+
+// Exact scores and keys of `nt` rows starting at row t0, by the whole block.
+__device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt, float* keys,
+                                             float* svals) {
+  const int E = a.sh.E;
+  if ((E & 7) == 0) {
+    // 16-byte vectors of 8 logits; the matching 8 biases come from global alongside
+    const int nv = E >> 3;
+    const int total = nt * nv;
+    for (int base = threadIdx.x; base < total; base += kSmallThreads * 4) {
+      uint4 q[4];
+      float bb[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * kSmallThreads;
+        if (idx < total) {
+          const int tl = idx / nv, v = idx - tl * nv;
+          q[u] = reinterpret_cast<const uint4*>(a.logits + static_cast<size_t>(t0 + tl) * E)[v];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) bb[u][j] = a.bias[8 * v + j];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * kSmallThreads;
+        if (idx < total) {
+          const int tl = idx / nv, v = idx - tl * nv;
+          const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+          float* kr = keys + tl * E + 8 * v;
+          float* sr = svals + tl * E + 8 * v;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float s0 = exact_score(__uint_as_float(wd[j] << 16));
+            const float s1 = exact_score(__uint_as_float(wd[j] & 0xffff0000u));
+            sr[2 * j] = s0;
+            sr[2 * j + 1] = s1;
+            kr[2 * j] = __fadd_rn(s0, bb[u][2 * j]);
+            kr[2 * j + 1] = __fadd_rn(s1, bb[u][2 * j + 1]);
+          }
+        }
+      }
+    }
+  } else {
+    const int total = nt * E;
+    for (int base = threadIdx.x; base < total; base += kSmallThreads * 4) {
+      uint16_t x[4];
+      float b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * kSmallThreads;
+        if (idx < total) {
+          const int tl = idx / E, e = idx - tl * E;
+          x[u] = a.logits[static_cast<size_t>(t0 + tl) * E + e];
+          b[u] = a.bias[e];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * kSmallThreads;
+        if (idx < total) {
+          const float s = exact_score(bf16_bits_to_float(x[u]));
+          svals[idx] = s;
+          keys[idx] = __fadd_rn(s, b[u]);
+        }
+      }
+    }
+  }
 }
 
 template <bool kSortOnly>
@@ -61,69 +140,55 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
   float* rw = reinterpret_cast<float*>(smem + a.lay.rw);
   int32_t* cnt = reinterpret_cast<int32_t*>(smem + a.lay.cnt);
   int32_t* off = reinterpret_cast<int32_t*>(smem + a.lay.off);
-  int32_t* owner = reinterpret_cast<int32_t*>(smem + a.lay.owner);
   int32_t* misc = reinterpret_cast<int32_t*>(smem + a.lay.misc);  // [0] flags, [4..37] scan
+  unsigned* masks = reinterpret_cast<unsigned*>(smem + a.lay.masks);  // [2][E]: tokens 0-31, 32-63
 
-  // ------------------------------------------------------------ route step
   if (!kSortOnly) {
-    float* bias_s = reinterpret_cast<float*>(smem + a.lay.bias);
+    // -------------------------------------------------------------- route step
     float* keys = reinterpret_cast<float*>(smem + a.lay.keys);
     float* svals = reinterpret_cast<float*>(smem + a.lay.svals);
     WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem + a.lay.scratch);
-    for (int e = tid; e < E; e += blockDim.x) bias_s[e] = a.bias[e];
-    __syncthreads();
+    for (int e = tid; e < 2 * E; e += kSmallThreads) masks[e] = 0u;
     for (int t0 = 0; t0 < a.T; t0 += a.wave) {
       const int nt = min(a.wave, a.T - t0);
-      for (int tl = 0; tl < nt; ++tl) {
-        const uint16_t* row = a.logits + static_cast<size_t>(t0 + tl) * E;
-        for (int e = tid; e < E; e += blockDim.x) {
-          const float s = exact_score(bf16_bits_to_float(row[e]));
-          svals[tl * E + e] = s;
-          keys[tl * E + e] = __fadd_rn(s, bias_s[e]);
-        }
-      }
+      small_scores(a, t0, nt, keys, svals);
       __syncthreads();
-      if (warp < nt) {
-        const SmemExactSrc src{keys + warp * E, svals + warp * E};
+      for (int tl = warp; tl < nt; tl += kSmallThreads / 32) {
         int id;
         float w;
-        route_token(src, sh, scr[warp], lane, id, w);
+        if (a.use_seg) {
+          float* umax = reinterpret_cast<float*>(smem + a.lay.umax) + warp * 32 * a.seg.nu;
+          route_token_seg(ExactKeyRow{keys + tl * E, svals + tl * E}, a.seg, scr[warp], umax,
+                          lane, 0.0f, id, w);
+        } else {
+          route_token(SmemExactSrc{keys + tl * E, svals + tl * E}, sh, scr[warp], lane, id, w);
+        }
         if (lane < K) {
-          const int r = (t0 + warp) * K + lane;
+          const int t = t0 + tl;
+          const int r = t * K + lane;
           a.topk_ids[r] = id;
           a.topk_w[r] = w;
           rid[r] = id;
           rw[r] = w;
+          // experts are distinct within a token: one bit per token gives count and rank
+          if (id >= 0 && id < E) atomicOr(&masks[(t >> 5) * E + id], 1u << (t & 31));
         }
       }
       __syncthreads();
     }
+    for (int e = tid; e < E; e += kSmallThreads) cnt[e] = __popc(masks[e]) + __popc(masks[E + e]);
+    if (tid == 0) misc[0] = 0;
+    __syncthreads();
   } else {
-    for (int r = tid; r < N; r += blockDim.x) {
+    // ---------------------------------------- sort step only: ranks in flat route order
+    for (int r = tid; r < N; r += kSmallThreads) {
       rid[r] = a.in_ids[r];
       rw[r] = a.in_w[r];
     }
-  }
-
-  // ------------------------------------------------------- sort phase 1: counts, ranks
-  if (tid == 0) misc[0] = 0;
-  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-  if (!kSortOnly) {
-    unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem + a.lay.masks);
-    for (int e = tid; e < E; e += blockDim.x) masks[e] = 0ull;
-    __syncthreads();
-    // experts are distinct within a token: one bit per token gives count and stable rank
-    for (int r = tid; r < N; r += blockDim.x) {
-      const int e = rid[r];
-      if (e >= 0 && e < E) atomicOr(&masks[e], 1ull << (r / K));
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) cnt[e] = __popcll(masks[e]);
-  } else {
-    int32_t* rrank = reinterpret_cast<int32_t*>(smem + a.lay.rrank);
+    for (int e = tid; e < E; e += kSmallThreads) cnt[e] = 0;
     __syncthreads();
     if (warp == 0) {
-      // ids may repeat inside a token: rank routes in flat order, 32 at a time
+      int32_t* rrank = reinterpret_cast<int32_t*>(smem + a.lay.rrank);
       bool bad = false;
       for (int base = 0; base < N; base += 32) {
         const int r = base + lane;
@@ -140,21 +205,22 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
         if (valid && (peers >> lane) == 1u) cnt[e] = c0 + __popc(peers);
         __syncwarp();
       }
-      if (__any_sync(kFull, bad) && lane == 0) misc[0] = MOE_RS_DEVICE_BAD_EXPERT_ID;
+      const bool any_bad = __any_sync(kFull, bad);
+      if (lane == 0) misc[0] = any_bad ? MOE_RS_DEVICE_BAD_EXPERT_ID : 0;
     }
+    __syncthreads();
   }
-  __syncthreads();
 
-  // --------------------------------------------- sort phase 2: padded scan and scatter
-  const int total = block_scan_padded(cnt, off, E, B, misc + 4);
-  for (int r = tid; r < N; r += blockDim.x) {
+  // ------------------------------------------------ padded scan, scatter, padding
+  const int total = block_scan_padded<kSmallThreads>(cnt, off, E, B, misc + 4);
+  for (int r = tid; r < N; r += kSmallThreads) {
     const int e = rid[r];
     if (e < 0 || e >= E) continue;
     int rank;
     if (!kSortOnly) {
-      const unsigned long long* masks =
-          reinterpret_cast<const unsigned long long*>(smem + a.lay.masks);
-      rank = __popcll(masks[e] & ((1ull << (r / K)) - 1ull));
+      const int t = r / K;
+      rank = (t < 32) ? __popc(masks[e] & ((1u << t) - 1u))
+                      : __popc(masks[e]) + __popc(masks[E + e] & ((1u << (t - 32)) - 1u));
     } else {
       rank = reinterpret_cast<const int32_t*>(smem + a.lay.rrank)[r];
     }
@@ -162,28 +228,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
     a.sorted_ids[pos] = r;
     a.sorted_w[pos] = rw[r];
   }
-  for (int e = tid; e < E; e += blockDim.x) {
+  for (int e = tid; e < E; e += kSmallThreads) {
     const int c = cnt[e];
     if (c == 0) continue;
+    const int o = off[e];
     const int p = (c + B - 1) & ~(B - 1);
-    for (int b = off[e] / B; b < (off[e] + p) / B; ++b) owner[b] = e;
-  }
-  __syncthreads();
-  for (int p = tid; p < total; p += blockDim.x) {
-    const int e = owner[p / B];
-    if (p - off[e] >= cnt[e]) {
-      a.sorted_ids[p] = N;
-      a.sorted_w[p] = 0.0f;
+    for (int q = o + c; q < o + p; ++q) {
+      a.sorted_ids[q] = N;
+      a.sorted_w[q] = 0.0f;
     }
+    for (int b = o / B; b < (o + p) / B; ++b) a.expert_ids[b] = e;
   }
-  for (int b = tid; b < total / B; b += blockDim.x) a.expert_ids[b] = owner[b];
   if (tid == 0) {
     *a.npp = total;
     *a.status = misc[0];
   }
 }
 
-SmallLayout small_layout(int E, int N, int wave, int nb_max, bool sort_only) {
+SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only) {
   SmallLayout l{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -191,17 +253,19 @@ SmallLayout small_layout(int E, int N, int wave, int nb_max, bool sort_only) {
     o = align16(o + bytes);
     return at;
   };
-  l.bias = sort_only ? 0 : take(sizeof(float) * E);
+  l.bias = 0;
   l.keys = sort_only ? 0 : take(sizeof(float) * (size_t)wave * E);
   l.svals = sort_only ? 0 : take(sizeof(float) * (size_t)wave * E);
-  l.scratch = sort_only ? 0 : take(sizeof(WarpScratch) * (size_t)wave);
+  const int warps = wave < kSmallThreads / 32 ? wave : kSmallThreads / 32;
+  l.scratch = sort_only ? 0 : take(sizeof(WarpScratch) * (size_t)warps);
+  l.umax = (sort_only || nu == 0) ? 0 : take(sizeof(float) * 32 * (size_t)nu * warps);
   l.rid = take(sizeof(int32_t) * N);
   l.rw = take(sizeof(float) * N);
   l.rrank = sort_only ? take(sizeof(int32_t) * N) : 0;
   l.cnt = take(sizeof(int32_t) * E);
   l.off = take(sizeof(int32_t) * E);
-  l.masks = sort_only ? 0 : take(sizeof(unsigned long long) * E);
-  l.owner = take(sizeof(int32_t) * (nb_max > 0 ? nb_max : 1));
+  l.masks = sort_only ? 0 : take(sizeof(unsigned) * 2 * E);
+  l.owner = 0;
   l.misc = take(sizeof(int32_t) * 40);
   l.total = static_cast<int>(o);
   return l;
@@ -224,25 +288,49 @@ cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ multi-CTA route
-size_t route_smem_bytes(int E, int nwarps, bool with_hist) {
-  const size_t per_warp = align16(sizeof(float) * 2 * (size_t)E) + sizeof(WarpScratch);
-  return align16(sizeof(float) * E) + (with_hist ? align16(sizeof(int32_t) * E) : 0) +
-         per_warp * nwarps;
+// --------------------------------------------------------- multi-CTA route, any shape
+// Shared memory: bias[E], counts[E], the unit's routes (ids, weights), then per warp the
+// exact keys and scores of one row and the route scratch; after routing, the per-warp
+// region is reused by phase 1 of the sort step.
+struct GenCtaLayout {
+  size_t bias, counts, rid, rw, warps, per_warp, total;
+};
+
+__host__ __device__ inline GenCtaLayout gen_cta_layout(int E, int nwarps, int max_routes, bool sort) {
+  GenCtaLayout l{};
+  size_t o = 0;
+  l.bias = o;
+  o = align16(o + sizeof(float) * E);
+  l.counts = o;
+  o = align16(o + sizeof(int32_t) * E);
+  l.rid = o;
+  o = align16(o + (sort ? sizeof(int32_t) * max_routes : 0));
+  l.rw = o;
+  o = align16(o + (sort ? sizeof(float) * max_routes : 0));
+  l.warps = o;
+  l.per_warp = align16(sizeof(float) * 2 * (size_t)E) + sizeof(WarpScratch);
+  size_t region = l.per_warp * nwarps;
+  if (sort && region < unit_scratch_bytes(E)) region = unit_scratch_bytes(E);
+  l.total = o + region;
+  return l;
 }
 
-template <bool kHist>
+size_t route_smem_bytes(int E, int nwarps, int max_routes, bool sort) {
+  return gen_cta_layout(E, nwarps, max_routes, sort).total;
+}
+
+template <bool kSort>
 __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RouteShape sh = a.sh;
   const int E = sh.E, K = sh.K;
-  float* bias_s = reinterpret_cast<float*>(smem);
-  size_t o = align16(sizeof(float) * E);
-  int32_t* counts = reinterpret_cast<int32_t*>(smem + o);
-  if (kHist) o += align16(sizeof(int32_t) * E);
-  const size_t per_warp = align16(sizeof(float) * 2 * (size_t)E) + sizeof(WarpScratch);
-  unsigned char* mine = smem + o + per_warp * warp;
+  const GenCtaLayout lay = gen_cta_layout(E, a.nwarps, a.max_routes, kSort);
+  float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
+  int32_t* counts = reinterpret_cast<int32_t*>(smem + lay.counts);
+  int32_t* rid = reinterpret_cast<int32_t*>(smem + lay.rid);
+  float* rw = reinterpret_cast<float*>(smem + lay.rw);
+  unsigned char* mine = smem + lay.warps + lay.per_warp * warp;
   float* key = reinterpret_cast<float*>(mine);
   float* sv = key + E;
   WarpScratch& scr =
@@ -250,7 +338,7 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
 
   for (int e = tid; e < E; e += blockDim.x) {
     bias_s[e] = a.bias[e];
-    if (kHist) counts[e] = 0;
+    counts[e] = 0;
   }
   __syncthreads();
 
@@ -290,20 +378,199 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
     if (lane < K) {
       a.topk_ids[static_cast<size_t>(t) * K + lane] = id;
       a.topk_w[static_cast<size_t>(t) * K + lane] = w;
-      if (kHist && id >= 0 && id < E) atomicAdd(&counts[id], 1);
+      if (kSort) {
+        rid[(t - t0) * K + lane] = id;
+        rw[(t - t0) * K + lane] = w;
+        if (id >= 0 && id < E) atomicAdd(&counts[id], 1);
+      }
     }
   }
-  if (kHist) {
+  if (kSort) {
     __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) a.partial[static_cast<size_t>(u) * E + e] = counts[e];
-    if (tid == 0) a.unit_flags[u] = 0;
+    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo.loc_off,
+                   a.uo.unit_buf, a.uo.slice_flags, a.uo.nslices, a.U);
+    if (tid == 0) a.uo.unit_flags[u] = 0;
   }
 }
 
+// ------------------------------------------------- multi-CTA route, TMA-staged segments
+// Shared memory: bias[E], c[E] = 0.5 + bias, counts[E], the unit's routes (ids, weights),
+// then per warp: two row buffers of E bf16, two mbarriers, the route scratch and the
+// unit-maximum scratch; after routing, the per-warp region is reused by phase 1.
+struct SegCtaLayout {
+  size_t bias, c, counts, rid, rw, warps, per_warp, rows, mbar, scratch, umax, total;
+};
+
+__host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps,
+                                                       int max_routes, bool sort) {
+  SegCtaLayout l{};
+  size_t o = 0;
+  l.bias = o;
+  o = align16(o + sizeof(float) * E);
+  l.c = o;
+  o = align16(o + sizeof(float) * E);
+  l.counts = o;
+  o = align16(o + sizeof(int32_t) * E);
+  l.rid = o;
+  o = align16(o + (sort ? sizeof(int32_t) * max_routes : 0));
+  l.rw = o;
+  o = align16(o + (sort ? sizeof(float) * max_routes : 0));
+  l.warps = o;
+  size_t w = 0;
+  l.rows = w;
+  w = align16(w + 2 * sizeof(uint16_t) * static_cast<size_t>(E));
+  l.mbar = w;
+  w = align16(w + 2 * sizeof(unsigned long long));
+  l.scratch = w;
+  w = align16(w + sizeof(WarpScratch));
+  l.umax = w;
+  w = align16(w + sizeof(float) * 32 * static_cast<size_t>(nu));
+  l.per_warp = w;
+  size_t region = w * nwarps;
+  const size_t need = align16(sizeof(unsigned long long) * E) + align16(sizeof(int32_t) * E) +
+                      align16(sizeof(int32_t) * (E + 1)) + align16(sizeof(int32_t) * E) + 256;
+  if (sort && region < need) region = need;
+  l.total = o + region;
+  return l;
+}
+
+size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort) {
+  return seg_cta_layout(E, nu, nwarps, max_routes, sort).total;
+}
+
+template <bool kSort>
+__global__ void __launch_bounds__(kSegThreads) mrs_route_seg_kernel(const RouteArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const SegShape sh = a.seg;
+  const int E = sh.E, K = sh.K;
+  const SegCtaLayout lay = seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort);
+  float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
+  float* c_s = reinterpret_cast<float*>(smem + lay.c);
+  int32_t* counts = reinterpret_cast<int32_t*>(smem + lay.counts);
+  int32_t* rid = reinterpret_cast<int32_t*>(smem + lay.rid);
+  float* rw = reinterpret_cast<float*>(smem + lay.rw);
+  unsigned char* mine = smem + lay.warps + lay.per_warp * warp;
+  uint16_t* rows = reinterpret_cast<uint16_t*>(mine + lay.rows);
+  unsigned long long* mbar = reinterpret_cast<unsigned long long*>(mine + lay.mbar);
+  WarpScratch& scr = *reinterpret_cast<WarpScratch*>(mine + lay.scratch);
+  float* umax = reinterpret_cast<float*>(mine + lay.umax);
+  __shared__ int cta_flags;
+  __shared__ unsigned int cta_bmax_bits;
+
+  const int u = blockIdx.x;
+  const int t0 = static_cast<int>(static_cast<long long>(u) * a.T / a.U);
+  const int t1 = static_cast<int>(static_cast<long long>(u + 1) * a.T / a.U);
+  const int n_mine = (t1 - t0 - warp + a.nwarps - 1) / a.nwarps;  // tokens of this warp
+  const uint32_t row_bytes = static_cast<uint32_t>(E) * 2u;
+  auto row_src = [&](int k) {
+    return a.logits + static_cast<size_t>(t0 + warp + k * a.nwarps) * E;
+  };
+
+  // start this warp's first two row copies before anything else
+  if (lane == 0) {
+    mbar_init(&mbar[0], 1);
+    mbar_init(&mbar[1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    if (n_mine > 0) tma_load_1d(rows, row_src(0), row_bytes, &mbar[0]);
+    if (n_mine > 1) tma_load_1d(rows + E, row_src(1), row_bytes, &mbar[1]);
+  }
+  if (tid == 0) {
+    cta_flags = 0;
+    cta_bmax_bits = 0u;
+  }
+  // routes of tokens that never get routed (a timed-out copy) stay dropped
+  if (kSort)
+    for (int i = tid; i < (t1 - t0) * K; i += blockDim.x) rid[i] = -1;
+  __syncthreads();
+  float bmax = 0.0f;  // largest |bias|, NaN-propagating (NaN fails the limit test below)
+  for (int e = tid; e < E; e += blockDim.x) {
+    const float b = a.bias[e];
+    bias_s[e] = b;
+    c_s[e] = __fadd_rn(0.5f, b);
+    const float ab = fabsf(b);
+    bmax = (ab > bmax || ab != ab) ? ab : bmax;
+    counts[e] = 0;
+  }
+  for (int d = 16; d > 0; d >>= 1) {
+    const float o = __shfl_xor_sync(kFull, bmax, d);
+    bmax = (o > bmax || o != o) ? o : bmax;
+  }
+  if (lane == 0) atomicMax(&cta_bmax_bits, (bmax != bmax) ? 0x7fffffffu : __float_as_uint(bmax));
+  __syncthreads();
+  // the proxy bound holds for |bias| <= kProxyBiasLimit; beyond that every step is exact
+  const float bm = __uint_as_float(cta_bmax_bits);
+  const float delta = (bm <= kProxyBiasLimit) ? proxy_delta(bm) : INFINITY;
+
+  uint32_t phase = 0u;  // bit b = parity to wait for on buffer b
+  int issued = n_mine < 2 ? n_mine : 2;
+  int consumed = 0;
+  bool ok = true;
+  for (int k = 0; k < n_mine; ++k) {
+    const int b = k & 1;
+    if (!mbar_wait_bounded(&mbar[b], (phase >> b) & 1u)) {
+      ok = false;
+      break;
+    }
+    consumed = k + 1;
+    phase ^= 1u << b;
+    const int t = t0 + warp + k * a.nwarps;
+    int id;
+    float w;
+    route_token_seg(ProxyRow{rows + b * E, c_s, bias_s}, sh, scr, umax, lane, delta, id, w);
+    if (lane < K) {
+      a.topk_ids[static_cast<size_t>(t) * K + lane] = id;
+      a.topk_w[static_cast<size_t>(t) * K + lane] = w;
+      if (kSort) {
+        rid[(t - t0) * K + lane] = id;
+        rw[(t - t0) * K + lane] = w;
+        if (id >= 0 && id < E) atomicAdd(&counts[id], 1);
+      }
+    }
+    __syncwarp();  // every lane is done with this buffer
+    if (k + 2 < n_mine) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        tma_load_1d(rows + b * E, row_src(k + 2), row_bytes, &mbar[b]);
+      }
+      ++issued;
+    }
+  }
+  if (!ok) {
+    // a copy did not complete in time: report it, then give the copies still in flight a
+    // bounded chance to land before their buffers are reused or the CTA exits
+    if (lane == 0) atomicOr(&cta_flags, MOE_RS_DEVICE_WAIT_TIMEOUT);
+    for (int k = consumed; k < issued; ++k) {
+      const int b = k & 1;
+      mbar_wait_bounded(&mbar[b], (phase >> b) & 1u);
+      phase ^= 1u << b;
+    }
+  }
+  if (kSort) {
+    __syncthreads();
+    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo.loc_off,
+                   a.uo.unit_buf, a.uo.slice_flags, a.uo.nslices, a.U);
+    if (tid == 0) a.uo.unit_flags[u] = cta_flags & MOE_RS_DEVICE_WAIT_TIMEOUT;
+  }
+}
+
+template <bool kSort>
+static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  mrs_route_seg_kernel<kSort><<<a.U, a.nwarps * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {
+  if (a.use_seg) return a.sort ? launch_seg_h<true>(a, smem, st) : launch_seg_h<false>(a, smem, st);
   cudaError_t err;
   const int threads = a.nwarps * 32;
-  if (a.partial) {
+  if (a.sort) {
     err = cudaFuncSetAttribute(mrs_route_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -1,243 +1,254 @@
-// mrs_sort.cu -- sort phases of the multi-CTA MoE route-sort path for sm_103a.
+// mrs_sort.cu -- both sort phases of the multi-CTA MoE route-sort path for sm_103a.
 //
-// Both sort phases ("perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)",
-// Summary) over units: unit u = the routes of a contiguous token range, one CTA each.
-//   count   (moe_sort only) per-unit histogram in shared memory -> partial[u][e]
-//   scan    per 32-expert chunk: exclusive prefix of partial over units (in place), the
-//           expert totals, block_m-padded offsets inside the chunk and the chunk totals
-//   scatter per unit: global offsets = prefix of chunk totals + in-chunk offset + the unit's
-//           prefix; stable ranks inside the unit from 64-token bitmasks; padding rows and
-//           per-block expert ids for a slice of the experts; npp and the status word
-// Order inside each expert segment is token-then-slot, independent of scheduling: no
-// global atomics anywhere.  Dropped routes (negative ids) claim no slot ("Summary --
-// general gfx1250 ordinary-TP route optimization", Dispatch and contracts).
+// Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary
+// ("both sort phases" feeding prepared metadata to GEMM1).  Dropped routes (negative ids)
+// claim no slot: "Summary -- general gfx1250 ordinary-TP route optimization", Dispatch and
+// contracts.
+//
+// Phase 1 runs at the end of the kernel that produced the routes of a unit (a contiguous
+// token range, one CTA): unit_sort_tail() stable-sorts the unit's routes by expert in
+// shared memory and stores, per unit, the exclusive per-expert offsets loc[u][0..E] and
+// the sorted (flat index, weight) list.  It also clears the look-back flags of phase 2.
+//
+// Phase 2 (mrs_slices_kernel) gives every CTA a slice of experts: a prefix over units of
+// the slice's counts, the block_m-padded offsets inside the slice, a decoupled look-back
+// over slices for the slice's base row, then a copy of every (unit, expert) segment to its
+// final rows, the padding rows and the per-block expert ids.  Entries of one expert stay in
+// token-then-slot order by construction; no global atomics are used, and every wait is
+// bounded.
 #include "mrs_internal.h"
-#include "../../include/moe_route_sort.h"
+#include "mrs_unit.cuh"
+#include "moe_route_sort.h"
 
 namespace mrs {
 
-__device__ __forceinline__ void unit_range(int u, int T, int U, int& t0, int& t1) {
-  t0 = static_cast<int>(static_cast<long long>(u) * T / U);
-  t1 = static_cast<int>(static_cast<long long>(u + 1) * T / U);
-}
-
-// ------------------------------------------------------------------------ count
-__global__ void __launch_bounds__(512) mrs_count_kernel(const CountArgs a) {
-  extern __shared__ __align__(16) int32_t cnts[];  // [E] + flag
+// ------------------------------------------------- phase 1 for moe_sort (given routes)
+__global__ void __launch_bounds__(kUnitThreads) mrs_unit_kernel(const UnitArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
-  int32_t* flag = cnts + a.E;
-  for (int e = tid; e < a.E; e += blockDim.x) cnts[e] = 0;
-  if (tid == 0) *flag = 0;
-  __syncthreads();
   int t0, t1;
   unit_range(blockIdx.x, a.T, a.U, t0, t1);
-  const size_t r0 = static_cast<size_t>(t0) * a.K, r1 = static_cast<size_t>(t1) * a.K;
-  for (size_t r = r0 + tid; r < r1; r += blockDim.x) {
-    const int e = a.ids[r];
-    if (e >= a.E) {
-      *flag = MOE_RS_DEVICE_BAD_EXPERT_ID;
-    } else if (e >= 0) {
-      atomicAdd(&cnts[e], 1);
-    }
+  const int nr = (t1 - t0) * a.K;
+  int32_t* rid = reinterpret_cast<int32_t*>(smem);
+  float* rw = reinterpret_cast<float*>(smem + align16(sizeof(int32_t) * a.max_routes));
+  int32_t* cnt = reinterpret_cast<int32_t*>(smem + 2 * align16(sizeof(int32_t) * a.max_routes));
+  unsigned char* scratch = smem + 2 * align16(sizeof(int32_t) * a.max_routes) +
+                           align16(sizeof(int32_t) * (a.E + 1));
+  __shared__ int bad;
+  if (tid == 0) bad = 0;
+  for (int e = tid; e < a.E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const size_t r0 = static_cast<size_t>(t0) * a.K;
+  for (int i = tid; i < nr; i += blockDim.x) {
+    const int e = a.ids[r0 + i];
+    rid[i] = e;
+    rw[i] = a.w[r0 + i];
+    if (e >= a.E) bad = MOE_RS_DEVICE_BAD_EXPERT_ID;
+    else if (e >= 0) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
-  for (int e = tid; e < a.E; e += blockDim.x)
-    a.partial[static_cast<size_t>(blockIdx.x) * a.E + e] = cnts[e];
-  if (tid == 0) a.unit_flags[blockIdx.x] = *flag;
+  unit_sort_tail(rid, rw, cnt, a.E, a.K, blockIdx.x, t0, t1, scratch, a.loc_off, a.unit_buf,
+                 a.slice_flags, a.nslices, a.U);
+  if (tid == 0) a.unit_flags[blockIdx.x] = bad;
 }
 
-cudaError_t launch_count(const CountArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(int32_t) * (a.E + 1);
-  mrs_count_kernel<<<a.U, 512, smem, st>>>(a);
+size_t unit_kernel_smem(int E, int max_routes) {
+  return 2 * align16(sizeof(int32_t) * max_routes) + align16(sizeof(int32_t) * (E + 1)) +
+         unit_scratch_bytes(E);
+}
+
+cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st) {
+  const size_t smem = unit_kernel_smem(a.E, a.max_routes);
+  cudaError_t err = cudaFuncSetAttribute(mrs_unit_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  mrs_unit_kernel<<<a.U, kUnitThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------------- scan
-// Block of 32 warps; lane = expert inside the chunk, warp w = a contiguous run of units.
-__global__ void __launch_bounds__(1024) mrs_scan_kernel(const ScanArgs a) {
-  __shared__ int32_t part[32][33];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int e = blockIdx.x * kChunk + lane;
-  const bool valid = e < a.E;
-  const int u0 = static_cast<int>(static_cast<long long>(warp) * a.U / 32);
-  const int u1 = static_cast<int>(static_cast<long long>(warp + 1) * a.U / 32);
-  int sum = 0;
-  if (valid)
-    for (int u = u0; u < u1; ++u) sum += a.partial[static_cast<size_t>(u) * a.E + e];
-  part[warp][lane] = sum;
-  __syncthreads();
-  if (warp == 0) {
-    int run = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int v = part[w][lane];
-      part[w][lane] = run;
-      run += v;
-    }
-    const int pad = valid ? ((run + a.B - 1) & ~(a.B - 1)) : 0;
-    const int incl = warp_inclusive_sum(pad, lane);
-    if (valid) {
-      a.cnt_tot[e] = run;
-      a.inchunk_off[e] = incl - pad;
-    }
-    if (lane == 31) a.chunk_tot[blockIdx.x] = incl;
-  }
-  __syncthreads();
-  if (valid) {
-    int run = part[warp][lane];
-    for (int u = u0; u < u1; ++u) {
-      const size_t i = static_cast<size_t>(u) * a.E + e;
-      const int v = a.partial[i];
-      a.partial[i] = run;
-      run += v;
-    }
-  }
+// ------------------------------------------------------------------ phase 2: slices
+constexpr unsigned long long kFlagAgg = 1ull << 32;  // value = the slice's padded rows
+constexpr unsigned long long kFlagInc = 2ull << 32;  // value = rows up to and including it
+constexpr unsigned long long kFlagErr = 1ull << 40;  // a wait before this slice gave up
+constexpr unsigned long long kFlagState = 3ull << 32;
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
-cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st) {
-  const int nchunk = (a.E + kChunk - 1) / kChunk;
-  mrs_scan_kernel<<<nchunk, 1024, 0, st>>>(a);
-  return cudaGetLastError();
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// ---------------------------------------------------------------------- scatter
-__global__ void __launch_bounds__(512) mrs_scatter_kernel(const ScatterArgs a) {
+__global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  const int E = a.E, K = a.K, B = a.B;
-  unsigned long long* masks = reinterpret_cast<unsigned long long*>(smem);  // [E]
-  int32_t* base = reinterpret_cast<int32_t*>(smem + align16(sizeof(unsigned long long) * E));
-  int32_t* cpre = base + E;              // [kMaxChunks + 1]
-  int32_t* flag = cpre + kMaxChunks + 1;  // [1]
+  const int c = blockIdx.x;
+  const int e0 = static_cast<int>(static_cast<long long>(c) * a.E / a.nslices);
+  const int e1 = static_cast<int>(static_cast<long long>(c + 1) * a.E / a.nslices);
+  const int ns = e1 - e0;
+  const int U = a.U, K = a.K, B = a.B;
+  int32_t* locs = reinterpret_cast<int32_t*>(smem);                      // [U][ns + 1]
+  int32_t* ex = locs + static_cast<size_t>(U) * (ns + 1);                 // [U][ns]
+  int32_t* tot = ex + static_cast<size_t>(U) * ns;                        // [ns]
+  int32_t* soff = tot + ns;                                               // [ns + 1]
+  __shared__ int32_t base_s, flags_s;
 
-  // global chunk offsets: exclusive prefix of the chunk totals (<= 128 chunks)
-  if (warp == 0) {
-    int v[4];
+  // everything below reads what the previous kernel wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  for (int idx = tid; idx < U * (ns + 1); idx += blockDim.x) {
+    const int u = idx / (ns + 1), i = idx - u * (ns + 1);
+    locs[idx] = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + e0 + i];
+  }
+  if (tid == 0) flags_s = 0;
+  __syncthreads();
+  // prefix over units of each expert's counts: warp per expert, lanes over runs of units
+  for (int i = warp; i < ns; i += nwarps) {
+    const int per = (U + 31) / 32;
+    const int ulo = min(U, lane * per), uhi = min(U, ulo + per);
     int s = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = lane * 4 + i;
-      v[i] = (c < a.nchunk) ? a.chunk_tot[c] : 0;
-      s += v[i];
-    }
+    for (int u = ulo; u < uhi; ++u) s += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
     const int incl = warp_inclusive_sum(s, lane);
-    int run = incl - s;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      cpre[lane * 4 + i] = run;
-      run += v[i];
+    int r = incl - s;
+    for (int u = ulo; u < uhi; ++u) {
+      ex[u * ns + i] = r;
+      r += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
     }
-    if (lane == 31) cpre[kMaxChunks] = incl;
-  }
-  if (tid == 0) *flag = 0;
-  __syncthreads();
-  const int u = blockIdx.x;
-  for (int e = tid; e < E; e += blockDim.x) {
-    base[e] = cpre[e / kChunk] + a.inchunk_off[e] + a.partial[static_cast<size_t>(u) * E + e];
-    masks[e] = 0ull;
+    if (lane == 31) tot[i] = incl;
   }
   __syncthreads();
-
-  int t0, t1;
-  unit_range(u, a.T, a.U, t0, t1);
-  for (int tt = t0; tt < t1; tt += kTileTokens) {
-    const int nt = min(kTileTokens, t1 - tt);
-    const int nr = nt * K;
-    const size_t r0 = static_cast<size_t>(tt) * K;
-    for (int i = tid; i < nr; i += blockDim.x) {
-      const int e = a.ids[r0 + i];
-      if (e < 0 || e >= E) continue;
-      const unsigned long long bit = 1ull << (i / K);
-      const unsigned long long old = atomicOr(&masks[e], bit);
-      if (old & bit) *flag = 1;  // the same expert twice in one token
+  // padded offsets inside the slice (one warp; slices hold few experts)
+  if (warp == 0) {
+    int run = 0;
+    for (int i0 = 0; i0 < ns; i0 += 32) {
+      const int i = i0 + lane;
+      const int p = (i < ns) ? ((tot[i] + B - 1) & ~(B - 1)) : 0;
+      const int incl = warp_inclusive_sum(p, lane);
+      if (i < ns) soff[i] = run + incl - p;
+      run += __shfl_sync(kFull, incl, 31);
     }
-    __syncthreads();
-    if (*flag == 0) {
-      for (int i = tid; i < nr; i += blockDim.x) {
-        const size_t r = r0 + i;
-        const int e = a.ids[r];
-        if (e < 0 || e >= E) continue;
-        const int tl = i / K;
-        const int pos = base[e] + __popcll(masks[e] & ((1ull << tl) - 1ull));
-        a.sorted_ids[pos] = static_cast<int32_t>(r);
-        a.sorted_w[pos] = a.w[r];
-      }
-      __syncthreads();
-      for (int i = tid; i < nr; i += blockDim.x) {
-        const int e = a.ids[r0 + i];
-        if (e < 0 || e >= E) continue;
-        const unsigned long long m = masks[e];
-        if ((m >> (i / K)) == 1ull) {  // last token of the tile routed to e
-          base[e] += __popcll(m);
-          masks[e] = 0ull;
-        }
-      }
-      __syncthreads();
+    if (lane == 0) soff[ns] = run;
+  }
+  __syncthreads();
+  // decoupled look-back over slices for this slice's first row, one warp reading 32
+  // predecessor flags per round: the nearest inclusive prefix ends the walk, aggregates in
+  // front of it are added.  A timed-out wait marks the flag this slice publishes, so the
+  // error reaches the last slice (the status word's writer).
+  if (warp == 0) {
+    const uint32_t mine = static_cast<uint32_t>(soff[ns]);
+    int base = 0;
+    unsigned long long err = 0ull;
+    if (c == 0) {
+      if (lane == 0) st_release_u64(&a.slice_flags[0], kFlagInc | mine);
     } else {
-      // repeated ids inside a token: rank this tile's routes in flat order, 32 at a time
-      for (int i = tid; i < nr; i += blockDim.x) {
-        const int e = a.ids[r0 + i];
-        if (e >= 0 && e < E) masks[e] = 0ull;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        for (int b0 = 0; b0 < nr; b0 += 32) {
-          const int i = b0 + lane;
-          const size_t r = r0 + i;
-          const int e = (i < nr) ? a.ids[r] : -1;
-          const bool valid = (e >= 0) && (e < E);
-          const unsigned peers = __match_any_sync(kFull, valid ? e : -1 - lane);
-          int p0 = 0;
-          if (valid) {
-            p0 = base[e];
-            const int pos = p0 + __popc(peers & lanemask_lt(lane));
-            a.sorted_ids[pos] = static_cast<int32_t>(r);
-            a.sorted_w[pos] = a.w[r];
+      if (lane == 0) st_release_u64(&a.slice_flags[c], kFlagAgg | mine);
+      const unsigned long long t_start = globaltimer_ns();
+      int hi = c - 1;  // next predecessor to read
+      while (hi >= 0) {
+        const int p = hi - lane;
+        const unsigned long long f = (p >= 0) ? ld_acquire_u64(&a.slice_flags[p]) : kFlagAgg;
+        const unsigned long long state = f & kFlagState;
+        const unsigned inc = __ballot_sync(kFull, p >= 0 && state == kFlagInc);
+        const unsigned none = __ballot_sync(kFull, p >= 0 && state == 0ull);
+        // lanes up to the nearest inclusive flag are the ones that count this round
+        const int stop = inc ? __ffs(inc) - 1 : 31;
+        const unsigned upto = (stop == 31) ? kFull : ((2u << stop) - 1u);
+        if ((none & upto) != 0u) {  // a needed predecessor has not published yet
+          if (globaltimer_ns() - t_start > kWaitLimitNs) {
+            err = kFlagErr;
+            break;
           }
-          __syncwarp();
-          if (valid && (peers >> lane) == 1u) base[e] = p0 + __popc(peers);
-          __syncwarp();
+          continue;
         }
+        const bool take = p >= 0 && lane <= stop;
+        int v = take ? static_cast<int>(f & 0xffffffffull) : 0;
+        unsigned long long ev = take ? (f & kFlagErr) : 0ull;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+          v += __shfl_xor_sync(kFull, v, d);
+          ev |= __shfl_xor_sync(kFull, ev, d);
+        }
+        base += v;
+        err |= ev;
+        if (inc) break;
+        hi -= 32;
       }
-      __syncthreads();
-      if (tid == 0) *flag = 0;
-      __syncthreads();
+      if (lane == 0)
+        st_release_u64(&a.slice_flags[c], kFlagInc | err | static_cast<uint32_t>(base + mine));
+    }
+    if (lane == 0) {
+      base_s = base;
+      flags_s = err ? MOE_RS_DEVICE_WAIT_TIMEOUT : 0;
     }
   }
-
-  // padding rows and block owners for this unit's slice of the experts
-  const int e0 = static_cast<int>(static_cast<long long>(u) * E / a.U);
-  const int e1 = static_cast<int>(static_cast<long long>(u + 1) * E / a.U);
-  for (int e = e0 + warp; e < e1; e += nwarps) {
-    const int c = a.cnt_tot[e];
-    if (c == 0) continue;
-    const int off = cpre[e / kChunk] + a.inchunk_off[e];
-    const int pad = (c + B - 1) & ~(B - 1);
-    for (int p = off + c + lane; p < off + pad; p += 32) {
+  __syncthreads();
+  const int base = base_s;
+  // copy every (unit, expert) segment to its rows
+  for (int idx = tid; idx < U * ns; idx += blockDim.x) {
+    const int u = idx / ns, i = idx - u * ns;
+    const int lo = locs[u * (ns + 1) + i], n = locs[u * (ns + 1) + i + 1] - lo;
+    if (n == 0) continue;
+    int t0, t1;
+    unit_range(u, a.T, U, t0, t1);
+    const int2* __restrict__ src = a.unit_buf + static_cast<size_t>(t0) * K + lo;
+    int32_t* __restrict__ dids = a.sorted_ids + base + soff[i] + ex[idx];
+    float* __restrict__ dw = a.sorted_w + base + soff[i] + ex[idx];
+#pragma unroll 4
+    for (int k = 0; k < n; ++k) {
+      const int2 v = src[k];
+      dids[k] = v.x;
+      dw[k] = __int_as_float(v.y);
+    }
+  }
+  // padding rows and block owners
+  for (int i = warp; i < ns; i += nwarps) {
+    const int cnt = tot[i];
+    if (cnt == 0) continue;
+    const int off = base + soff[i];
+    const int pad = (cnt + B - 1) & ~(B - 1);
+    for (int p = off + cnt + lane; p < off + pad; p += 32) {
       a.sorted_ids[p] = a.N;
       a.sorted_w[p] = 0.0f;
     }
-    for (int b = off / B + lane; b < (off + pad) / B; b += 32) a.expert_ids[b] = e;
+    for (int b = off / B + lane; b < (off + pad) / B; b += 32) a.expert_ids[b] = e0 + i;
   }
-  if (u == 0 && warp == 0) {
+  if (c == a.nslices - 1 && warp == 0) {
     int f = 0;
-    for (int v = lane; v < a.U; v += 32) f |= a.unit_flags[v];
-    f = __reduce_or_sync(kFull, f);
+    for (int v = lane; v < U; v += 32) f |= a.unit_flags[v];
+    f = __reduce_or_sync(kFull, f) | flags_s;
     if (lane == 0) {
-      *a.npp = cpre[kMaxChunks];
+      *a.npp = base + soff[ns];
       *a.status = f;
     }
   }
 }
 
-cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t st) {
-  const size_t smem = align16(sizeof(unsigned long long) * a.E) +
-                      sizeof(int32_t) * (a.E + kMaxChunks + 2);
-  cudaError_t err = cudaFuncSetAttribute(
-      mrs_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+size_t slices_smem_bytes(int U, int E, int nslices) {
+  const int ns = (E + nslices - 1) / nslices;
+  return sizeof(int32_t) * (static_cast<size_t>(U) * (ns + 1) + static_cast<size_t>(U) * ns +
+                            2 * static_cast<size_t>(ns) + 1);
+}
+
+cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st) {
+  const size_t smem = slices_smem_bytes(a.U, a.E, a.nslices);
+  cudaError_t err = cudaFuncSetAttribute(mrs_slices_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  mrs_scatter_kernel<<<a.U, 512, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.nslices);
+  cfg.blockDim = dim3(kSliceThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mrs_slices_kernel, a);
 }
 
 // ------------------------------------------------------------------ empty call

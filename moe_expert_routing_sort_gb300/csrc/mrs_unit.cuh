@@ -1,0 +1,148 @@
+// mrs_unit.cuh -- phase 1 of the sort step for one unit (a contiguous token range): the
+// unit's routes stable-sorted by expert in shared memory, with per-unit expert offsets.
+// Shared by the route kernels (which run it after routing) and the moe_sort unit kernel.
+// Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary
+// ("both sort phases").
+#pragma once
+
+#include "mrs_internal.h"
+
+namespace mrs {
+
+__device__ __forceinline__ void unit_range(int u, int T, int U, int& t0, int& t1) {
+  t0 = static_cast<int>(static_cast<long long>(u) * T / U);
+  t1 = static_cast<int>(static_cast<long long>(u + 1) * T / U);
+}
+
+// Exclusive prefix sum of v[0..n) by the whole block into out[0..n], out[n] = total.
+// scan_tmp: 33 ints.  Ends with a block barrier.
+__device__ __forceinline__ void block_exclusive_scan(const int32_t* v, int32_t* out, int n,
+                                                     int32_t* scan_tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int per = (n + nthreads - 1) / nthreads;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int s = 0;
+  for (int i = lo; i < hi; ++i) s += v[i];
+  const int incl = warp_inclusive_sum(s, lane);
+  if (lane == 31) scan_tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = (lane < nwarps) ? scan_tmp[lane] : 0;
+    const int xi = warp_inclusive_sum(x, lane);
+    __syncwarp();
+    if (lane < nwarps) scan_tmp[lane] = xi - x;
+    if (lane == 31) scan_tmp[32] = xi;
+  }
+  __syncthreads();
+  int run = scan_tmp[warp] + incl - s;
+  for (int i = lo; i < hi; ++i) {
+    const int x = v[i];
+    out[i] = run;
+    run += x;
+  }
+  if (tid == 0) out[n] = scan_tmp[32];
+  __syncthreads();
+}
+
+
+// Phase 1 for unit u (see the file comment).  rid/rw: the unit's routes in shared memory,
+// index (t - t0) * K + k; an id outside [0, E) is not placed.  cnt: the unit's per-expert
+// counts of placed routes (shared memory, may be overwritten).  scratch: shared memory of
+// unit_scratch_bytes(E), free for use.  All threads of the CTA call this.
+__device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* rw, int32_t* cnt, int E, int K,
+                               int u, int t0, int t1, unsigned char* scratch,
+                               int32_t* loc_off_g, int2* unit_buf_g,
+                               unsigned long long* slice_flags, int nslices, int U) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  unsigned* masks = reinterpret_cast<unsigned*>(scratch);  // one bit per token of a 32-token tile
+  size_t o = align16(sizeof(unsigned long long) * E);
+  int32_t* run = reinterpret_cast<int32_t*>(scratch + o);
+  o += align16(sizeof(int32_t) * E);
+  int32_t* loc = reinterpret_cast<int32_t*>(scratch + o);
+  o += align16(sizeof(int32_t) * (E + 1));
+  o += align16(sizeof(int32_t) * E);
+  int32_t* misc = reinterpret_cast<int32_t*>(scratch + o);  // [0..32] scan, [40] dup flag
+
+  // clear the look-back flags of the slice kernel that follows
+  for (int c = u + tid * U; c < nslices; c += blockDim.x * U) slice_flags[c] = 0ull;
+
+  block_exclusive_scan(cnt, loc, E, misc);
+  int32_t* loc_g = loc_off_g + static_cast<size_t>(u) * (E + 1);
+  for (int e = tid; e <= E; e += blockDim.x) loc_g[e] = loc[e];
+  for (int e = tid; e < E; e += blockDim.x) {
+    run[e] = loc[e];
+    masks[e] = 0u;
+  }
+  if (tid == 0) misc[40] = 0;
+  __syncthreads();
+
+  // tiles of 32 tokens: warp w takes tokens w, w + nwarps, ... of the tile, lane k slot k
+  int2* out = unit_buf_g + static_cast<size_t>(t0) * K;
+  const int nt_all = t1 - t0;
+  for (int tb = 0; tb < nt_all; tb += 32) {
+    const int nt = min(32, nt_all - tb);
+    for (int tl = warp; tl < nt; tl += nwarps) {
+      const int e = (lane < K) ? rid[(tb + tl) * K + lane] : -1;
+      if (e >= 0 && e < E) {
+        const unsigned bit = 1u << tl;
+        if (atomicOr(&masks[e], bit) & bit) misc[40] = 1;  // an expert twice in one token
+      }
+    }
+    __syncthreads();
+    if (misc[40] == 0) {
+      for (int tl = warp; tl < nt; tl += nwarps) {
+        const int r = (tb + tl) * K + lane;
+        const int e = (lane < K) ? rid[r] : -1;
+        if (e >= 0 && e < E) {
+          const int pos = run[e] + __popc(masks[e] & ((1u << tl) - 1u));
+          out[pos] = make_int2(t0 * K + r, __float_as_int(rw[r]));
+        }
+      }
+      __syncthreads();
+      for (int tl = warp; tl < nt; tl += nwarps) {
+        const int e = (lane < K) ? rid[(tb + tl) * K + lane] : -1;
+        if (e >= 0 && e < E) {
+          const unsigned m = masks[e];
+          if ((m >> tl) == 1u) {  // the tile's last token routed to e
+            run[e] += __popc(m);
+            masks[e] = 0u;
+          }
+        }
+      }
+      __syncthreads();
+    } else {
+      // repeated ids inside a token: place this tile's routes in flat order, 32 at a time
+      const int nr = nt * K;
+      const int r0 = tb * K;
+      for (int i = tid; i < nr; i += blockDim.x) {
+        const int e = rid[r0 + i];
+        if (e >= 0 && e < E) masks[e] = 0u;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        for (int b0 = 0; b0 < nr; b0 += 32) {
+          const int i = b0 + lane;
+          const int e = (i < nr) ? rid[r0 + i] : -1;
+          const bool valid = (e >= 0) && (e < E);
+          const unsigned peers = __match_any_sync(kFull, valid ? e : -1 - lane);
+          int p0 = 0;
+          if (valid) {
+            p0 = run[e];
+            out[p0 + __popc(peers & lanemask_lt(lane))] =
+                make_int2(t0 * K + r0 + i, __float_as_int(rw[r0 + i]));
+          }
+          __syncwarp();
+          if (valid && (peers >> lane) == 1u) run[e] = p0 + __popc(peers);
+          __syncwarp();
+        }
+      }
+      __syncthreads();
+      if (tid == 0) misc[40] = 0;
+      __syncthreads();
+    }
+  }
+}
+
+}  // namespace mrs

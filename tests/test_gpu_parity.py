@@ -154,6 +154,33 @@ def test_exact_ties_go_to_lower_index():
         assert_matches(run_gpu(w, inp), ref, w)
 
 
+def test_proxy_bound_holds_for_every_bf16_input():
+    out = torch.zeros(2, dtype=torch.float32, device=DEV)
+    mrs.moe_route_sort_proxy_selftest(out)
+    torch.cuda.synchronize()
+    max_err, bound = out.cpu().tolist()
+    assert 0.0 < max_err <= bound, (max_err, bound)
+
+
+@pytest.mark.parametrize("T", [300, 2000])
+def test_huge_bias_takes_the_exact_route(T):
+    # |bias| above the proxy's rounding limit makes every step exact.  Keys near 1100 are
+    # spaced 1.2e-4 apart, so tokens are redrawn at a correspondingly wider margin.
+    w = datagen.Workload("bigbias", T=T, E=896, n_group=8, topk_group=4, topk=16,
+                         routed_scale=2.5, block_m=32)
+    bias = datagen.make_inputs(datagen.workload("prefill_T512_E896", T=1)).bias.copy()
+    bias[::45] += np.float32(1100.0)
+
+    def needs(logits, _):
+        m = oracle.margins(logits, bias, 8, 4, 16)
+        return np.nonzero(m < 5e-4)[0]
+
+    logits = datagen.make_inputs(w, needs_redraw=needs).logits_bf16
+    inp = datagen.RouterInputs(w, logits, bias)
+    ref = oracle.route_sort(logits, bias, 8, 4, 16, 2.5, 32)
+    assert_matches(run_gpu(w, inp), ref, w)
+
+
 def test_empty_call():
     w = datagen.workload("prefill_T512_E896", T=0)
     out = mrs.RouteSortBuffers.allocate(0, w.E, w.topk, w.block_m, device=DEV)
