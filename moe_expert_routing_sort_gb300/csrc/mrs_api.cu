@@ -327,6 +327,26 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
   int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
   if (T == 0) return launch_status(launch_empty(num_tokens_post_pad, status, stream));
 
+  if (T == 1) {
+    DecodeArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.bias = bias;
+    a.E = E;
+    a.G = n_group;
+    a.g = E / n_group;
+    a.Kg = topk_group;
+    a.K = topk;
+    a.B = block_m;
+    a.R = routed_scale;
+    a.topk_ids = topk_ids;
+    a.topk_w = topk_weights;
+    a.sorted_ids = sorted_token_ids;
+    a.sorted_w = sorted_weights;
+    a.expert_ids = expert_ids;
+    a.npp = num_tokens_post_pad;
+    a.status = status;
+    return launch_status(launch_decode(a, stream));
+  }
   DeviceInfo d;
   if (!device_info(d)) return MOE_RS_ERR_LAUNCH;
   const RouteShape sh = make_shape(E, n_group, topk_group, topk, routed_scale);

@@ -85,6 +85,21 @@ struct SmallArgs {
   int32_t* status;
 };
 
+// ------------------------------------------------------------- one token (decode)
+struct DecodeArgs {
+  const uint16_t* logits;
+  const float* bias;
+  int E, G, g, Kg, K, B;
+  float R;
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* sorted_ids;
+  float* sorted_w;
+  int32_t* expert_ids;
+  int32_t* npp;
+  int32_t* status;
+};
+
 // ------------------------------------------------------------- multi-CTA path
 // Phase-1 outputs of a unit, written at the end of the route (or unit) kernel.
 struct UnitOut {
@@ -135,6 +150,7 @@ struct SliceArgs {
 
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st);
 cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st);
 cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st);

@@ -194,41 +194,38 @@ __device__ __forceinline__ void route_token_seg(const Row& row, const SegShape& 
   }
   const float theta = tau - 2.0f * delta;
 
-  // ---- survivors: my units whose best reaches theta; up to 4 per lane are kept in
-  // registers and compacted with a warp scan (more than 4 sends the warp to the exact path)
+  // ---- survivors: my units whose best reaches theta, compacted without atomics: count,
+  // warp scan for each lane's first slot, then write (the few surviving units are read twice)
   if (lane < sh.K) {
     ws.sel_id[lane] = -1;
     ws.sel_s[lane] = 0.0f;
   }
+  const bool scan_mine = kept && m1 >= theta;
   int found = 0;
-  int se0 = 0, se1 = 0, se2 = 0, se3 = 0;
-  if (kept && m1 >= theta) {
+  if (scan_mine) {
+    for (int u = 0; u < sh.nu; ++u) {
+      if (my_umax[u * 32] >= theta) {
+        float v[4];
+        row.unit(seg0 + 4 * u, v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) found += (v[t] >= theta) ? 1 : 0;
+      }
+    }
+  }
+  const int incl = warp_inclusive_sum(found, lane);
+  const int total = __shfl_sync(kFull, incl, 31);
+  if (total <= kCandCap && found > 0) {
+    int pos = incl - found;
     for (int u = 0; u < sh.nu; ++u) {
       if (my_umax[u * 32] >= theta) {
         float v[4];
         row.unit(seg0 + 4 * u, v);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          if (v[t] >= theta) {
-            const int e = seg0 + 4 * u + t;
-            se3 = (found == 3) ? e : se3;
-            se2 = (found == 2) ? e : se2;
-            se1 = (found == 1) ? e : se1;
-            se0 = (found == 0) ? e : se0;
-            ++found;
-          }
+          if (v[t] >= theta) ws.cand[pos++] = static_cast<unsigned long long>(seg0 + 4 * u + t);
         }
       }
     }
-  }
-  const int before = warp_inclusive_sum(found, lane) - found;
-  int total = __shfl_sync(kFull, before + found, 31);
-  if (__any_sync(kFull, found > 4)) total = kCandCap + 1;  // take the exact K-round path
-  if (total <= kCandCap) {
-    if (found > 0) ws.cand[before] = static_cast<unsigned long long>(se0);
-    if (found > 1) ws.cand[before + 1] = static_cast<unsigned long long>(se1);
-    if (found > 2) ws.cand[before + 2] = static_cast<unsigned long long>(se2);
-    if (found > 3) ws.cand[before + 3] = static_cast<unsigned long long>(se3);
   }
   __syncwarp();
   if (total <= kCandCap) {
@@ -247,7 +244,7 @@ __device__ __forceinline__ void route_token_seg(const Row& row, const SegShape& 
     for (int k = 0; k < sh.K; ++k) {
       unsigned long long best = 0ull;
       float best_s = 0.0f;
-      if (kept && m1 >= theta) {
+      if (scan_mine) {
         for (int u = 0; u < sh.nu; ++u) {
           if (my_umax[u * 32] >= theta) {
             float v[4];

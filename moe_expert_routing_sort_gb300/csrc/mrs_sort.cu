@@ -12,8 +12,9 @@
 //
 // Phase 2 (mrs_slices_kernel) gives every CTA a slice of experts: a prefix over units of
 // the slice's counts, the block_m-padded offsets inside the slice, a decoupled look-back
-// over slices for the slice's base row, then a copy of every (unit, expert) segment to its
-// final rows, the padding rows and the per-block expert ids.  Entries of one expert stay in
+// for the slice's base row (every slice publishes its padded size and sums those of the
+// slices before it), then a copy of every route to its final row, the padding rows and the
+// per-block expert ids.  Entries of one expert stay in
 // token-then-slot order by construction; no global atomics are used, and every wait is
 // bounded.
 #include "mrs_internal.h"
@@ -67,10 +68,7 @@ cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------ phase 2: slices
-constexpr unsigned long long kFlagAgg = 1ull << 32;  // value = the slice's padded rows
-constexpr unsigned long long kFlagInc = 2ull << 32;  // value = rows up to and including it
-constexpr unsigned long long kFlagErr = 1ull << 40;  // a wait before this slice gave up
-constexpr unsigned long long kFlagState = 3ull << 32;
+constexpr unsigned long long kFlagReady = 1ull << 32;  // low word = the slice's padded rows
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
@@ -91,10 +89,10 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   const int e1 = static_cast<int>(static_cast<long long>(c + 1) * a.E / a.nslices);
   const int ns = e1 - e0;
   const int U = a.U, K = a.K, B = a.B;
-  int32_t* locs = reinterpret_cast<int32_t*>(smem);                      // [U][ns + 1]
-  int32_t* ex = locs + static_cast<size_t>(U) * (ns + 1);                 // [U][ns]
-  int32_t* tot = ex + static_cast<size_t>(U) * ns;                        // [ns]
-  int32_t* soff = tot + ns;                                               // [ns + 1]
+  int32_t* locs = reinterpret_cast<int32_t*>(smem);                  // [U][ns + 1]
+  int32_t* seg = locs + static_cast<size_t>(U) * (ns + 1);            // [ns][U + 1] starts
+  int32_t* tot = seg + static_cast<size_t>(ns) * (U + 1);             // [ns + 1] unpadded prefix
+  int32_t* soff = tot + ns + 1;                                       // [ns + 1] padded prefix
   __shared__ int32_t base_s, flags_s;
 
   // everything below reads what the previous kernel wrote
@@ -104,109 +102,105 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
     const int u = idx / (ns + 1), i = idx - u * (ns + 1);
     locs[idx] = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + e0 + i];
   }
-  if (tid == 0) flags_s = 0;
   __syncthreads();
-  // prefix over units of each expert's counts: warp per expert, lanes over runs of units
+  // per expert of the slice: exclusive prefix over units of its counts (warp per expert)
   for (int i = warp; i < ns; i += nwarps) {
     const int per = (U + 31) / 32;
     const int ulo = min(U, lane * per), uhi = min(U, ulo + per);
-    int s = 0;
-    for (int u = ulo; u < uhi; ++u) s += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
-    const int incl = warp_inclusive_sum(s, lane);
-    int r = incl - s;
+    int sum = 0;
+    for (int u = ulo; u < uhi; ++u) sum += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
+    const int incl = warp_inclusive_sum(sum, lane);
+    int r = incl - sum;
     for (int u = ulo; u < uhi; ++u) {
-      ex[u * ns + i] = r;
+      seg[i * (U + 1) + u] = r;
       r += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
     }
-    if (lane == 31) tot[i] = incl;
+    if (lane == 31) seg[i * (U + 1) + U] = incl;
   }
   __syncthreads();
-  // padded offsets inside the slice (one warp; slices hold few experts)
+  // unpadded and padded prefixes over the slice's experts (one warp)
   if (warp == 0) {
-    int run = 0;
+    int run = 0, prun = 0;
     for (int i0 = 0; i0 < ns; i0 += 32) {
       const int i = i0 + lane;
-      const int p = (i < ns) ? ((tot[i] + B - 1) & ~(B - 1)) : 0;
-      const int incl = warp_inclusive_sum(p, lane);
-      if (i < ns) soff[i] = run + incl - p;
-      run += __shfl_sync(kFull, incl, 31);
+      const int cnt = (i < ns) ? seg[i * (U + 1) + U] : 0;
+      const int pad = (cnt + B - 1) & ~(B - 1);
+      const int ci = warp_inclusive_sum(cnt, lane);
+      const int pi = warp_inclusive_sum(pad, lane);
+      if (i < ns) {
+        tot[i] = run + ci - cnt;
+        soff[i] = prun + pi - pad;
+      }
+      run += __shfl_sync(kFull, ci, 31);
+      prun += __shfl_sync(kFull, pi, 31);
     }
-    if (lane == 0) soff[ns] = run;
+    if (lane == 0) {
+      tot[ns] = run;
+      soff[ns] = prun;
+      flags_s = 0;
+    }
   }
   __syncthreads();
-  // decoupled look-back over slices for this slice's first row, one warp reading 32
-  // predecessor flags per round: the nearest inclusive prefix ends the walk, aggregates in
-  // front of it are added.  A timed-out wait marks the flag this slice publishes, so the
-  // error reaches the last slice (the status word's writer).
+  // this slice's first row = sum of the padded sizes of all earlier slices: publish mine,
+  // then read every earlier slice's word in parallel (one warp; bounded wait)
   if (warp == 0) {
-    const uint32_t mine = static_cast<uint32_t>(soff[ns]);
+    if (lane == 0) st_release_u64(&a.slice_flags[c], kFlagReady | static_cast<uint32_t>(soff[ns]));
     int base = 0;
-    unsigned long long err = 0ull;
-    if (c == 0) {
-      if (lane == 0) st_release_u64(&a.slice_flags[0], kFlagInc | mine);
-    } else {
-      if (lane == 0) st_release_u64(&a.slice_flags[c], kFlagAgg | mine);
-      const unsigned long long t_start = globaltimer_ns();
-      int hi = c - 1;  // next predecessor to read
-      while (hi >= 0) {
-        const int p = hi - lane;
-        const unsigned long long f = (p >= 0) ? ld_acquire_u64(&a.slice_flags[p]) : kFlagAgg;
-        const unsigned long long state = f & kFlagState;
-        const unsigned inc = __ballot_sync(kFull, p >= 0 && state == kFlagInc);
-        const unsigned none = __ballot_sync(kFull, p >= 0 && state == 0ull);
-        // lanes up to the nearest inclusive flag are the ones that count this round
-        const int stop = inc ? __ffs(inc) - 1 : 31;
-        const unsigned upto = (stop == 31) ? kFull : ((2u << stop) - 1u);
-        if ((none & upto) != 0u) {  // a needed predecessor has not published yet
-          if (globaltimer_ns() - t_start > kWaitLimitNs) {
-            err = kFlagErr;
-            break;
-          }
-          continue;
+    bool ok = true;
+    const unsigned long long t_start = globaltimer_ns();
+    for (int p0 = 0; p0 < c; p0 += 32) {
+      const int p = p0 + lane;
+      unsigned long long f = 0ull;
+      for (;;) {
+        f = (p < c) ? ld_acquire_u64(&a.slice_flags[p]) : kFlagReady;
+        const bool missing = (f & kFlagReady) == 0ull;
+        if (!__any_sync(kFull, missing)) break;
+        if (globaltimer_ns() - t_start > kWaitLimitNs) {
+          ok = false;
+          break;
         }
-        const bool take = p >= 0 && lane <= stop;
-        int v = take ? static_cast<int>(f & 0xffffffffull) : 0;
-        unsigned long long ev = take ? (f & kFlagErr) : 0ull;
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-          v += __shfl_xor_sync(kFull, v, d);
-          ev |= __shfl_xor_sync(kFull, ev, d);
-        }
-        base += v;
-        err |= ev;
-        if (inc) break;
-        hi -= 32;
       }
-      if (lane == 0)
-        st_release_u64(&a.slice_flags[c], kFlagInc | err | static_cast<uint32_t>(base + mine));
+      if (!ok) break;
+      int v = (p < c) ? static_cast<int>(f & 0xffffffffull) : 0;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+      base += v;
     }
     if (lane == 0) {
       base_s = base;
-      flags_s = err ? MOE_RS_DEVICE_WAIT_TIMEOUT : 0;
+      flags_s = ok ? 0 : MOE_RS_DEVICE_WAIT_TIMEOUT;
     }
   }
   __syncthreads();
   const int base = base_s;
-  // copy every (unit, expert) segment to its rows
-  for (int idx = tid; idx < U * ns; idx += blockDim.x) {
-    const int u = idx / ns, i = idx - u * ns;
-    const int lo = locs[u * (ns + 1) + i], n = locs[u * (ns + 1) + i + 1] - lo;
-    if (n == 0) continue;
+  // copy: route q of the slice (expert-major, then unit, then rank) goes to
+  // base + soff[i] + (q - tot[i]); its (expert, unit) segment is found by binary search
+  const int nroutes = tot[ns];
+  for (int q = tid; q < nroutes; q += blockDim.x) {
+    int lo = 0, hi = ns - 1;  // expert: last i with tot[i] <= q
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tot[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    const int i = lo;
+    const int qi = q - tot[i];
+    const int32_t* si = seg + i * (U + 1);
+    int ul = 0, uh = U - 1;  // unit: last u with si[u] <= qi
+    while (ul < uh) {
+      const int mid = (ul + uh + 1) >> 1;
+      if (si[mid] <= qi) ul = mid; else uh = mid - 1;
+    }
+    const int u = ul;
     int t0, t1;
     unit_range(u, a.T, U, t0, t1);
-    const int2* __restrict__ src = a.unit_buf + static_cast<size_t>(t0) * K + lo;
-    int32_t* __restrict__ dids = a.sorted_ids + base + soff[i] + ex[idx];
-    float* __restrict__ dw = a.sorted_w + base + soff[i] + ex[idx];
-#pragma unroll 4
-    for (int k = 0; k < n; ++k) {
-      const int2 v = src[k];
-      dids[k] = v.x;
-      dw[k] = __int_as_float(v.y);
-    }
+    const int2 v = a.unit_buf[static_cast<size_t>(t0) * K + locs[u * (ns + 1) + i] + (qi - si[u])];
+    const int dst = base + soff[i] + qi;
+    a.sorted_ids[dst] = v.x;
+    a.sorted_w[dst] = __int_as_float(v.y);
   }
   // padding rows and block owners
   for (int i = warp; i < ns; i += nwarps) {
-    const int cnt = tot[i];
+    const int cnt = tot[i + 1] - tot[i];
     if (cnt == 0) continue;
     const int off = base + soff[i];
     const int pad = (cnt + B - 1) & ~(B - 1);
@@ -229,8 +223,8 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
 
 size_t slices_smem_bytes(int U, int E, int nslices) {
   const int ns = (E + nslices - 1) / nslices;
-  return sizeof(int32_t) * (static_cast<size_t>(U) * (ns + 1) + static_cast<size_t>(U) * ns +
-                            2 * static_cast<size_t>(ns) + 1);
+  return sizeof(int32_t) * (static_cast<size_t>(U) * (ns + 1) +
+                            static_cast<size_t>(ns) * (U + 1) + 2 * static_cast<size_t>(ns) + 2);
 }
 
 cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st) {
