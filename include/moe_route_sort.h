@@ -78,6 +78,8 @@ extern "C" {
 #define MOE_RS_ERR_WORKSPACE (-10)        /* workspace NULL or smaller than required       */
 #define MOE_RS_ERR_BAD_SCALE (-11)        /* routed_scale not finite                       */
 #define MOE_RS_ERR_LAUNCH (-12)           /* the CUDA runtime rejected a kernel launch     */
+#define MOE_RS_ERR_TOO_LARGE (-13)        /* shape needs more than the static scratch of
+                                             moe_route_sort_noalloc                        */
 
 /* Device-side status bits, written to the first int32 of the workspace by every call. */
 #define MOE_RS_DEVICE_BAD_EXPERT_ID 0x1   /* moe_sort saw an id >= E; those routes dropped */
@@ -127,6 +129,39 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
              int block_m, int32_t* sorted_token_ids, float* sorted_weights,
              int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
              size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------- allocation-free variant */
+
+/* Bytes of the scratch array that moe_route_sort_noalloc keeps in the library itself. */
+#define MOE_RS_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* moe_route_sort without a workspace argument.  (This entry point has no counterpart in the
+ * source pages; it exists for callers, not for the method.)
+ *
+ * Some callers cannot hand the library scratch memory: a plugin invoked by an inference
+ * runtime that passes it only its input and output pointers and owns all device memory
+ * itself; code that must not call cudaMalloc on the serving path because it synchronises
+ * the device and is not stream-ordered; or an engine whose memory budget is fully reserved
+ * up front.  For them the scratch lives in a fixed 32 MiB array compiled into the library
+ * (MOE_RS_NOALLOC_SCRATCH_BYTES), so this call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  Every GPU that loads the library holds those
+ * 32 MiB until the process exits.
+ *
+ * Arguments, outputs, results and errors are those of moe_route_sort, plus
+ * MOE_RS_ERR_TOO_LARGE when moe_route_sort_workspace_bytes(T, E, topk, block_m) exceeds
+ * MOE_RS_NOALLOC_SCRATCH_BYTES (for example 16384 tokens x 4096 experts x top-8 needs about
+ * 18 MiB and is accepted).  The first call on each device looks up the array's device
+ * address with that device current; make that first call before any stream capture.
+ * All calls on a device share the one array and it keeps whatever the previous call left in
+ * it (the path needs no zeroed scratch); two calls that can run on the GPU at the same time
+ * (different streams, or graphs replayed concurrently) race on it and give wrong results.
+ * The status word of moe_route_sort is written into that shared array and is not exposed. */
+int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, int E,
+                           int n_group, int topk_group, int topk, float routed_scale,
+                           int block_m, int32_t* topk_ids, float* topk_weights,
+                           int32_t* sorted_token_ids, float* sorted_weights,
+                           int32_t* expert_ids, int32_t* num_tokens_post_pad,
+                           cudaStream_t stream);
 
 /* ------------------------------------------------------------------ diagnostics */
 

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     library_path,
     load,
     moe_route_sort,
+    moe_route_sort_noalloc,
     moe_route_sort_proxy_selftest,
     moe_route_sort_workspace_bytes,
     moe_sort,

@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
         lib.moe_topk.restype = I
         lib.moe_sort.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P]
         lib.moe_sort.restype = I
+        lib.moe_route_sort_noalloc.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P]
+        lib.moe_route_sort_noalloc.restype = I
         lib.moe_route_sort_proxy_selftest.argtypes = [P, P]
         lib.moe_route_sort_proxy_selftest.restype = I
         _lib = lib
@@ -129,6 +131,31 @@ def moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_
         _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
         workspace.numel(), _stream_handle(stream))
     _check(rc, "moe_route_sort")
+
+
+def moe_route_sort_noalloc(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
+                           topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
+                           num_tokens_post_pad, stream=None) -> None:
+    """moe_route_sort with the library's own static scratch (no workspace, no allocation).
+
+    For callers that cannot provide or allocate scratch memory; see include/moe_route_sort.h.
+    Calls that may overlap on the GPU share that scratch and must not be issued.
+    """
+    T, E = logits.shape
+    _need(logits, torch.bfloat16, "logits")
+    _need(bias, torch.float32, "bias")
+    for t, dt, n in [(topk_ids, torch.int32, "topk_ids"), (topk_weights, torch.float32,
+                     "topk_weights"), (sorted_token_ids, torch.int32, "sorted_token_ids"),
+                     (sorted_weights, torch.float32, "sorted_weights"),
+                     (expert_ids, torch.int32, "expert_ids"),
+                     (num_tokens_post_pad, torch.int32, "num_tokens_post_pad")]:
+        _need(t, dt, n)
+    rc = load().moe_route_sort_noalloc(
+        _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
+        block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
+        _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad),
+        _stream_handle(stream))
+    _check(rc, "moe_route_sort_noalloc")
 
 
 def moe_topk(logits, bias, n_group, topk_group, topk, routed_scale, topk_ids, topk_weights,

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "moe_route_sort.h"
 #include "mrs_internal.h"
@@ -265,6 +266,8 @@ const char* moe_route_sort_strerror(int status) {
     case MOE_RS_ERR_WORKSPACE: return "workspace is NULL or smaller than required";
     case MOE_RS_ERR_BAD_SCALE: return "routed_scale must be finite";
     case MOE_RS_ERR_LAUNCH: return "the CUDA runtime rejected a kernel launch";
+    case MOE_RS_ERR_TOO_LARGE:
+      return "the shape needs more scratch than moe_route_sort_noalloc's static 32 MiB";
     default: return "unknown status";
   }
 }
@@ -459,6 +462,47 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
   if (rc) return rc;
   return run_slices(T, E, topk, block_m, U, nslices, sorted_token_ids, sorted_weights,
                     expert_ids, num_tokens_post_pad, ws, l, stream);
+}
+
+// ------------------------------------------------- allocation-free variant
+// Scratch for moe_route_sort_noalloc: a fixed array in the library's device image, so the
+// call itself allocates nothing.  Every GPU that loads the library keeps these bytes until
+// the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_RS_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the array on the current device, looked up once per device (with that
+// device current) and cached; nullptr if the lookup fails.
+static void* noalloc_scratch_ptr() {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, int E,
+                           int n_group, int topk_group, int topk, float routed_scale,
+                           int block_m, int32_t* topk_ids, float* topk_weights,
+                           int32_t* sorted_token_ids, float* sorted_weights,
+                           int32_t* expert_ids, int32_t* num_tokens_post_pad,
+                           cudaStream_t stream) {
+  const size_t need = moe_route_sort_workspace_bytes(T, E, topk, block_m);
+  if (need > MOE_RS_NOALLOC_SCRATCH_BYTES) return MOE_RS_ERR_TOO_LARGE;
+  void* scratch = noalloc_scratch_ptr();
+  if (scratch == nullptr) return MOE_RS_ERR_LAUNCH;
+  return moe_route_sort(logits_bf16, bias, T, E, n_group, topk_group, topk, routed_scale,
+                        block_m, topk_ids, topk_weights, sorted_token_ids, sorted_weights,
+                        expert_ids, num_tokens_post_pad, scratch, MOE_RS_NOALLOC_SCRATCH_BYTES,
+                        stream);
 }
 
 }  // extern "C"
