@@ -117,16 +117,17 @@ RouteShape make_shape(int E, int G, int Kg, int K, float R) {
   return sh;
 }
 
-// Segment layout of the route step (see mrs_seg.cuh): groups split into L lanes of equal,
-// 4-expert-aligned segments.  False when the shape does not allow it.
-bool make_seg_shape(int E, int G, int Kg, int K, float R, SegShape& s) {
-  if (G > 32) return false;
+// Segment layout of the route step (see mrs_seg.cuh) for `lanes` lanes per token: groups
+// split into L lanes of equal, 4-expert-aligned segments.  False when the shape does not
+// allow it.
+bool make_seg_shape(int E, int G, int Kg, int K, float R, int lanes, SegShape& s) {
+  if (G > lanes) return false;
   int L = 1;
-  while (L * 2 * G <= 32) L *= 2;
+  while (L * 2 * G <= lanes) L *= 2;
   const int g = E / G;
   if (g % L != 0) return false;
   const int sl = g / L;
-  if (sl % 4 != 0) return false;
+  if (sl % 4 != 0 || sl > 256) return false;  // units per lane fit a 64-bit mask
   s.E = E;
   s.G = G;
   s.g = g;
@@ -164,16 +165,65 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   const int tpu = (T + U - 1) / U;
   a.max_routes = tpu * sh.K;
   a.vec16 = (sh.E % 8) == 0;
-  a.use_seg = a.vec16 && make_seg_shape(sh.E, sh.G, sh.Kg, sh.K, sh.R, a.seg);
-  const int cap = a.use_seg ? kSegThreads / 32 : 16;
-  int nwarps = tpu < cap ? tpu : cap;
-  auto smem_for = [&](int w) {
-    return a.use_seg ? seg_smem_bytes(sh.E, a.seg.nu, w, a.max_routes, sort)
-                     : route_smem_bytes(sh.E, w, a.max_routes, sort);
+  // Launch plan of the segment kernel for `lanes` lanes per token and a release mode: the
+  // most warps (up to one per step of the unit) whose shared memory fits, with the largest
+  // number of row buffers (<= max_nbuf) that costs no warps.
+  struct Plan {
+    bool seg;
+    SegShape shape;
+    int lanes, nbuf, nwarps, want;
+    bool early;
+    size_t smem;
   };
-  while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(d.smem_optin)) --nwarps;
-  a.nwarps = nwarps;
-  const size_t smem = smem_for(nwarps);
+  auto plan_for = [&](int lanes, bool early, int max_nbuf) {
+    Plan p{};
+    p.lanes = lanes;
+    p.early = early;
+    p.seg = a.vec16 && make_seg_shape(sh.E, sh.G, sh.Kg, sh.K, sh.R, lanes, p.shape);
+    if (!p.seg) return p;
+    const int tpw = 32 / lanes;
+    const int steps = (tpu + tpw - 1) / tpw;
+    const int cap = kSegThreads / 32;
+    p.want = steps < cap ? steps : cap;
+    for (int nbuf = max_nbuf; nbuf >= 1; --nbuf) {
+      int w = p.want;
+      auto bytes = [&](int ww) {
+        return seg_smem_bytes(sh.E, p.shape.nu, ww, a.max_routes, sort, tpw, nbuf, early);
+      };
+      while (w > 1 && bytes(w) > static_cast<size_t>(d.smem_optin)) --w;
+      if (w > p.nwarps) {
+        p.nwarps = w;
+        p.nbuf = nbuf;
+        p.smem = bytes(w);
+      }
+    }
+    return p;
+  };
+  // Preference: two tokens per warp (16 lanes each; the per-token shuffle and scan work of
+  // the route step is shared by two tokens) with rows kept in shared memory until the
+  // selection is done, when K <= 16 and all warps fit with two buffers each; the same with
+  // one token per warp; else one token per warp, buffers handed back after pass 1.
+  Plan p{};
+  if (sh.K <= 16) p = plan_for(16, false, 2);
+  if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32, false, 2);
+  if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32, true, 2);
+  a.use_seg = p.seg;
+  size_t smem;
+  if (p.seg) {
+    a.seg = p.shape;
+    a.lanes = p.lanes;
+    a.nbuf = p.nbuf;
+    a.early = p.early;
+    a.nwarps = p.nwarps;
+    smem = p.smem;
+  } else {
+    int w = tpu < 16 ? tpu : 16;
+    while (w > 1 && route_smem_bytes(sh.E, w, a.max_routes, sort) >
+                        static_cast<size_t>(d.smem_optin))
+      --w;
+    a.nwarps = w;
+    smem = route_smem_bytes(sh.E, w, a.max_routes, sort);
+  }
   if (smem > static_cast<size_t>(d.smem_optin)) return MOE_RS_ERR_LAUNCH;
   a.sh = sh;
   a.topk_ids = topk_ids;
@@ -357,7 +407,7 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
   SmallLayout lay;
   int wave = 0, nb_max = 0;
   SegShape seg{};
-  const bool use_seg = make_seg_shape(E, n_group, topk_group, topk, routed_scale, seg);
+  const bool use_seg = make_seg_shape(E, n_group, topk_group, topk, routed_scale, 32, seg);
   if (T <= kSmallMaxTokens &&
       small_plan(T, E, topk, block_m, false, use_seg ? seg.nu : 0, d, lay, wave, nb_max)) {
     SmallArgs a{};

@@ -8,8 +8,8 @@
 //  * mrs_route_seg_kernel: route step of the multi-CTA path for shapes whose groups split
 //    into equal 4-expert-aligned lane segments (see mrs_seg.cuh).  CTA u owns a contiguous
 //    token range (its "unit"); each warp streams its tokens' rows into shared memory with
-//    double-buffered bulk copies (TMA) and routes them with cheap proxy scores plus exact
-//    refinement; the CTA counts its routes per expert in shared memory for the sort step.
+//    bulk copies (TMA) and routes them with cheap proxy scores plus exact refinement, one
+//    or two tokens per warp; the CTA counts its routes per expert for the sort step.
 //  * mrs_route_kernel: the same step for any other shape: exact scores of a row into
 //    shared memory, then the warp-level route step over them.
 //
@@ -130,6 +130,8 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
   }
 }
 
+static_assert(sizeof(SegScratch) <= sizeof(WarpScratch), "segment scratch reuses WarpScratch");
+
 template <bool kSortOnly>
 __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const SmallArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -149,6 +151,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
     float* svals = reinterpret_cast<float*>(smem + a.lay.svals);
     WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem + a.lay.scratch);
     for (int e = tid; e < 2 * E; e += kSmallThreads) masks[e] = 0u;
+    if (a.use_seg && warp < a.wave)
+      ub_init_pads(reinterpret_cast<unsigned short*>(smem + a.lay.umax + ub_bytes(a.seg.nu) * warp),
+                   lane, a.seg.nu);
     for (int t0 = 0; t0 < a.T; t0 += a.wave) {
       const int nt = min(a.wave, a.T - t0);
       small_scores(a, t0, nt, keys, svals);
@@ -157,9 +162,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
         int id;
         float w;
         if (a.use_seg) {
-          float* umax = reinterpret_cast<float*>(smem + a.lay.umax) + warp * 32 * a.seg.nu;
-          route_token_seg(ExactKeyRow{keys + tl * E, svals + tl * E}, a.seg, scr[warp], umax,
-                          lane, 0.0f, id, w);
+          unsigned short* umax = reinterpret_cast<unsigned short*>(
+              smem + a.lay.umax + ub_bytes(a.seg.nu) * warp);
+          const ExactKeyRow row{keys + tl * E, svals + tl * E};
+          const LaneTop top = seg_pass1<32, 1>(row, a.seg, umax, lane, true);
+          seg_select<32, 1>(row, a.seg, *reinterpret_cast<SegScratch*>(&scr[warp]), umax, lane,
+                            0.0f, true, top, id, w);
         } else {
           route_token(SmemExactSrc{keys + tl * E, svals + tl * E}, sh, scr[warp], lane, id, w);
         }
@@ -258,7 +266,7 @@ SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only) {
   l.svals = sort_only ? 0 : take(sizeof(float) * (size_t)wave * E);
   const int warps = wave < kSmallThreads / 32 ? wave : kSmallThreads / 32;
   l.scratch = sort_only ? 0 : take(sizeof(WarpScratch) * (size_t)warps);
-  l.umax = (sort_only || nu == 0) ? 0 : take(sizeof(float) * 32 * (size_t)nu * warps);
+  l.umax = (sort_only || nu == 0) ? 0 : take(ub_bytes(nu) * warps);
   l.rid = take(sizeof(int32_t) * N);
   l.rw = take(sizeof(float) * N);
   l.rrank = sort_only ? take(sizeof(int32_t) * N) : 0;
@@ -393,22 +401,25 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
   }
 }
 
+
 // ------------------------------------------------- multi-CTA route, TMA-staged segments
-// Shared memory: bias[E], c[E] = 0.5 + bias, counts[E], the unit's routes (ids, weights),
-// then per warp: two row buffers of E bf16, two mbarriers, the route scratch and the
-// unit-maximum scratch; after routing, the per-warp region is reused by phase 1.
+// Shared memory: c[E] = 0.5 + bias, bias[E] (unless the selection reads it from global
+// memory), counts[E], the unit's routes (ids, weights), then per warp: nbuf row buffers of
+// tpw rows each, two mbarriers, one route scratch per token of a step and the unit bounds;
+// after routing, the per-warp region is reused by phase 1.
 struct SegCtaLayout {
-  size_t bias, c, counts, rid, rw, warps, per_warp, rows, mbar, scratch, umax, total;
+  size_t c, bias, counts, rid, rw, warps, per_warp, rows, mbar, scratch, umax, total;
 };
 
 __host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps,
-                                                       int max_routes, bool sort) {
+                                                       int max_routes, bool sort, int tpw,
+                                                       int nbuf, bool early) {
   SegCtaLayout l{};
   size_t o = 0;
-  l.bias = o;
-  o = align16(o + sizeof(float) * E);
   l.c = o;
   o = align16(o + sizeof(float) * E);
+  l.bias = o;
+  o = align16(o + (early ? 0 : sizeof(float) * E));
   l.counts = o;
   o = align16(o + sizeof(int32_t) * E);
   l.rid = o;
@@ -418,66 +429,78 @@ __host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps
   l.warps = o;
   size_t w = 0;
   l.rows = w;
-  w = align16(w + 2 * sizeof(uint16_t) * static_cast<size_t>(E));
+  w = align16(w + static_cast<size_t>(nbuf) * tpw * sizeof(uint16_t) * E);
   l.mbar = w;
   w = align16(w + 2 * sizeof(unsigned long long));
   l.scratch = w;
-  w = align16(w + sizeof(WarpScratch));
+  w = align16(w + static_cast<size_t>(tpw) * sizeof(SegScratch));
   l.umax = w;
-  w = align16(w + sizeof(float) * 32 * static_cast<size_t>(nu));
+  w = align16(w + ub_bytes(nu));
   l.per_warp = w;
   size_t region = w * nwarps;
-  const size_t need = align16(sizeof(unsigned long long) * E) + align16(sizeof(int32_t) * E) +
-                      align16(sizeof(int32_t) * (E + 1)) + align16(sizeof(int32_t) * E) + 256;
-  if (sort && region < need) region = need;
+  if (sort && region < unit_scratch_bytes(E)) region = unit_scratch_bytes(E);
   l.total = o + region;
   return l;
 }
 
-size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort) {
-  return seg_cta_layout(E, nu, nwarps, max_routes, sort).total;
+size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw,
+                      int nbuf, bool early) {
+  return seg_cta_layout(E, nu, nwarps, max_routes, sort, tpw, nbuf, early).total;
 }
 
-template <bool kSort>
-__global__ void __launch_bounds__(kSegThreads) mrs_route_seg_kernel(const RouteArgs a) {
+// Warp w of unit u takes steps w, w + nwarps, ...; step i covers the 32 / LT consecutive
+// tokens t0 + i * (32 / LT) + h, token h routed by lanes [h * LT, (h + 1) * LT).  The rows
+// of a step are contiguous, so one bulk copy brings them in.  With kEarly a buffer is handed
+// back to the copy engine as soon as pass 1 is done with it (the selection then reads the
+// few row parts it needs from global memory); otherwise after the selection.
+template <bool kSort, int LT, bool kEarly>
+__global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const RouteArgs a) {
+  constexpr int kTpw = 32 / LT;
+  constexpr int kParts = (LT == 16) ? 2 : 1;
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = lane / LT, ll = lane & (LT - 1);
   const SegShape sh = a.seg;
-  const int E = sh.E, K = sh.K;
-  const SegCtaLayout lay = seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort);
-  float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
+  const int E = sh.E, K = sh.K, nbuf = a.nbuf;
+  const SegCtaLayout lay =
+      seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort, kTpw, nbuf, kEarly);
   float* c_s = reinterpret_cast<float*>(smem + lay.c);
+  float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
   int32_t* counts = reinterpret_cast<int32_t*>(smem + lay.counts);
   int32_t* rid = reinterpret_cast<int32_t*>(smem + lay.rid);
   float* rw = reinterpret_cast<float*>(smem + lay.rw);
   unsigned char* mine = smem + lay.warps + lay.per_warp * warp;
   uint16_t* rows = reinterpret_cast<uint16_t*>(mine + lay.rows);
   unsigned long long* mbar = reinterpret_cast<unsigned long long*>(mine + lay.mbar);
-  WarpScratch& scr = *reinterpret_cast<WarpScratch*>(mine + lay.scratch);
-  float* umax = reinterpret_cast<float*>(mine + lay.umax);
+  SegScratch* scr = reinterpret_cast<SegScratch*>(mine + lay.scratch);
+  unsigned short* umax = reinterpret_cast<unsigned short*>(mine + lay.umax);
   __shared__ int cta_flags;
   __shared__ unsigned int cta_bmax_bits;
 
   const int u = blockIdx.x;
   const int t0 = static_cast<int>(static_cast<long long>(u) * a.T / a.U);
   const int t1 = static_cast<int>(static_cast<long long>(u + 1) * a.T / a.U);
-  const int n_mine = (t1 - t0 - warp + a.nwarps - 1) / a.nwarps;  // tokens of this warp
-  const uint32_t row_bytes = static_cast<uint32_t>(E) * 2u;
-  auto row_src = [&](int k) {
-    return a.logits + static_cast<size_t>(t0 + warp + k * a.nwarps) * E;
+  const int n_steps = (t1 - t0 + kTpw - 1) / kTpw;
+  const int n_mine = (n_steps - warp + a.nwarps - 1) / a.nwarps;  // steps of this warp
+  auto step_t = [&](int k) { return t0 + (warp + k * a.nwarps) * kTpw; };
+  auto issue = [&](int k, int b) {
+    const int ts = step_t(k);
+    const int n = min(kTpw, t1 - ts);
+    tma_load_1d(rows + static_cast<size_t>(b) * kTpw * E,
+                a.logits + static_cast<size_t>(ts) * E,
+                static_cast<uint32_t>(n) * static_cast<uint32_t>(E) * 2u, &mbar[b]);
   };
 
-  // start this warp's first two row copies before anything else
+  // start this warp's first copies before anything else
   if (lane == 0) {
     mbar_init(&mbar[0], 1);
     mbar_init(&mbar[1], 1);
     fence_mbar_init();
   }
   __syncwarp();
-  if (lane == 0) {
-    if (n_mine > 0) tma_load_1d(rows, row_src(0), row_bytes, &mbar[0]);
-    if (n_mine > 1) tma_load_1d(rows + E, row_src(1), row_bytes, &mbar[1]);
-  }
+  if (lane == 0)
+    for (int k = 0; k < nbuf && k < n_mine; ++k) issue(k, k);
+  ub_init_pads(umax, lane, sh.nu);
   if (tid == 0) {
     cta_flags = 0;
     cta_bmax_bits = 0u;
@@ -489,8 +512,8 @@ __global__ void __launch_bounds__(kSegThreads) mrs_route_seg_kernel(const RouteA
   float bmax = 0.0f;  // largest |bias|, NaN-propagating (NaN fails the limit test below)
   for (int e = tid; e < E; e += blockDim.x) {
     const float b = a.bias[e];
-    bias_s[e] = b;
     c_s[e] = __fadd_rn(0.5f, b);
+    if (!kEarly) bias_s[e] = b;
     const float ab = fabsf(b);
     bmax = (ab > bmax || ab != ab) ? ab : bmax;
     counts[e] = 0;
@@ -506,37 +529,54 @@ __global__ void __launch_bounds__(kSegThreads) mrs_route_seg_kernel(const RouteA
   const float delta = (bm <= kProxyBiasLimit) ? proxy_delta(bm) : INFINITY;
 
   uint32_t phase = 0u;  // bit b = parity to wait for on buffer b
-  int issued = n_mine < 2 ? n_mine : 2;
+  int issued = n_mine < nbuf ? n_mine : nbuf;
   int consumed = 0;
   bool ok = true;
   for (int k = 0; k < n_mine; ++k) {
-    const int b = k & 1;
+    const int b = (nbuf == 2) ? (k & 1) : 0;
     if (!mbar_wait_bounded(&mbar[b], (phase >> b) & 1u)) {
       ok = false;
       break;
     }
     consumed = k + 1;
     phase ^= 1u << b;
-    const int t = t0 + warp + k * a.nwarps;
-    int id;
-    float w;
-    route_token_seg(ProxyRow{rows + b * E, c_s, bias_s}, sh, scr, umax, lane, delta, id, w);
-    if (lane < K) {
-      a.topk_ids[static_cast<size_t>(t) * K + lane] = id;
-      a.topk_w[static_cast<size_t>(t) * K + lane] = w;
-      if (kSort) {
-        rid[(t - t0) * K + lane] = id;
-        rw[(t - t0) * K + lane] = w;
-        if (id >= 0 && id < E) atomicAdd(&counts[id], 1);
+    const int t = step_t(k) + h;
+    const bool valid = t < t1;
+    const ProxyRow<kEarly> row{rows + static_cast<size_t>(b * kTpw + h) * E,
+                               a.logits + static_cast<size_t>(valid ? t : t0) * E, c_s,
+                               kEarly ? a.bias : bias_s};
+    const LaneTop top = seg_pass1<LT, kParts>(row, sh, umax, lane, valid);
+    if (kEarly) {
+      __syncwarp();  // every lane is done with the buffer
+      if (k + nbuf < n_mine) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(k + nbuf, b);
+        }
+        ++issued;
       }
     }
-    __syncwarp();  // every lane is done with this buffer
-    if (k + 2 < n_mine) {
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        tma_load_1d(rows + b * E, row_src(k + 2), row_bytes, &mbar[b]);
+    int id;
+    float w;
+    seg_select<LT, kParts>(row, sh, scr[h], umax, lane, delta, valid, top, id, w);
+    if (!kEarly) {
+      __syncwarp();  // every lane is done with the buffer
+      if (k + nbuf < n_mine) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(k + nbuf, b);
+        }
+        ++issued;
       }
-      ++issued;
+    }
+    if (valid && ll < K) {
+      a.topk_ids[static_cast<size_t>(t) * K + ll] = id;
+      a.topk_w[static_cast<size_t>(t) * K + ll] = w;
+      if (kSort) {
+        rid[(t - t0) * K + ll] = id;
+        rw[(t - t0) * K + ll] = w;
+        if (id >= 0 && id < E) atomicAdd(&counts[id], 1);
+      }
     }
   }
   if (!ok) {
@@ -544,7 +584,7 @@ __global__ void __launch_bounds__(kSegThreads) mrs_route_seg_kernel(const RouteA
     // bounded chance to land before their buffers are reused or the CTA exits
     if (lane == 0) atomicOr(&cta_flags, MOE_RS_DEVICE_WAIT_TIMEOUT);
     for (int k = consumed; k < issued; ++k) {
-      const int b = k & 1;
+      const int b = (nbuf == 2) ? (k & 1) : 0;
       mbar_wait_bounded(&mbar[b], (phase >> b) & 1u);
       phase ^= 1u << b;
     }
@@ -557,17 +597,26 @@ __global__ void __launch_bounds__(kSegThreads) mrs_route_seg_kernel(const RouteA
   }
 }
 
-template <bool kSort>
+template <bool kSort, int LT, bool kEarly>
 static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort>,
+  cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort, LT, kEarly>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  mrs_route_seg_kernel<kSort><<<a.U, a.nwarps * 32, smem, st>>>(a);
+  mrs_route_seg_kernel<kSort, LT, kEarly><<<a.U, a.nwarps * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
 
+template <bool kSort>
+static cudaError_t launch_seg(const RouteArgs& a, size_t smem, cudaStream_t st) {
+  if (a.lanes == 16)
+    return a.early ? launch_seg_h<kSort, 16, true>(a, smem, st)
+                   : launch_seg_h<kSort, 16, false>(a, smem, st);
+  return a.early ? launch_seg_h<kSort, 32, true>(a, smem, st)
+                 : launch_seg_h<kSort, 32, false>(a, smem, st);
+}
+
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  if (a.use_seg) return a.sort ? launch_seg_h<true>(a, smem, st) : launch_seg_h<false>(a, smem, st);
+  if (a.use_seg) return a.sort ? launch_seg<true>(a, smem, st) : launch_seg<false>(a, smem, st);
   cudaError_t err;
   const int threads = a.nwarps * 32;
   if (a.sort) {

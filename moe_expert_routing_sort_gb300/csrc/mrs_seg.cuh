@@ -1,19 +1,27 @@
 // mrs_seg.cuh -- warp-level route step over contiguous per-lane segments of a group.
 //
-// Lane l of the warp owns group j = l / L and, inside it, the contiguous segment
-// [j*g + q*sl, j*g + (q+1)*sl) with q = l % L and sl = g / L, read as units of 4 experts.
-// One pass over the segment gives the lane's top-2 (and the best of every unit); the group
-// score is a shuffle merge over the L lanes of the group; the K-th-best threshold comes from
-// the lanes' own top-2; survivors are found by rescanning only units whose best can reach
-// the threshold.  Source of the step: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE
-// handoff (stack)", Summary (correction bias, grouped top-k).
+// A token is routed by LT consecutive lanes of a warp (LT = 32, or 16 for two tokens per
+// warp).  Inside those, lane ll owns group j = ll / L and the contiguous segment
+// [j*g + q*sl, j*g + (q+1)*sl) of it (q = ll % L, sl = g / L), read as units of 4 experts.
+//   seg_pass1   the only step that reads the whole row: the lane's top-2 (in V interleaved
+//               parts) and an upper bound of the best value of every unit (fp16, rounded up)
+//   seg_select  the rest, from those summaries: group scores are a shuffle merge over the
+//               L lanes of a group, the K-th-best threshold comes from the parts' top-2, and
+//               only units whose bound reaches the threshold are read again
+// so the row buffer can take the next token's row as soon as pass 1 is done.
+// Source of the step: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff
+// (stack)", Summary (correction bias, grouped top-k).
 //
-// The row is read through a source with
-//   unit(e0, v[4])   the 4 selection values (proxies, or exact keys) of experts e0..e0+3
-//   exact(e, s)      the exact key of expert e, and its exact score through s
+// A row source provides
+//   unit(e0, v[4])          selection values (proxies or exact keys) of e0..e0+3
+//   late_words(e0)          the raw bf16 words of e0..e0+3 after pass 1
+//   values(e0, words, v[4]) the selection values from those words
+//   exact(e, bits, s)       exact key of expert e (logit bits `bits`), score through s
 // and `delta` bounds |value - exact key| (0 for exact sources).  Decisions are exact:
-// proxies only discard experts proven worse than a bound by more than 2 * delta.
+// values only discard experts proven worse than a bound by more than 2 * delta.
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include "mrs_device.cuh"
 
@@ -21,11 +29,19 @@ namespace mrs {
 
 struct SegShape {
   int E, G, g, Kg, K;
-  int L, log2L;  // lanes per group (power of two); G * L <= 32
-  int sl;        // experts per lane segment (multiple of 4)
-  int nu;        // units of 4 experts per segment
+  int L, log2L;  // lanes per group (power of two); G * L <= lanes per token
+  int sl;        // experts per lane segment (multiple of 4, at most 256)
+  int nu;        // units of 4 experts per segment (at most 64)
   int rot;       // unit order of lane l starts at (l * rot) % nu (spreads smem banks)
   float R;
+};
+
+// Route scratch of one token (shared memory).
+struct __align__(16) SegScratch {
+  unsigned long long cand[kCandCap];
+  float cand_s[kCandCap];
+  int sel_id[kMaxTopk];
+  float sel_s[kMaxTopk];
 };
 
 __device__ __forceinline__ void top2_insert(float& m1, float& m2, float v) {
@@ -33,24 +49,35 @@ __device__ __forceinline__ void top2_insert(float& m1, float& m2, float v) {
   m1 = fmaxf(m1, v);
 }
 
-// Best of 4 values and the running top-2 after them.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Best of 4 values; the running top-2 absorbs them.
 __device__ __forceinline__ float top2_unit(const float (&v)[4], float& m1, float& m2) {
   const float h0 = fmaxf(v[0], v[1]), l0 = fminf(v[0], v[1]);
   const float h1 = fmaxf(v[2], v[3]), l1 = fminf(v[2], v[3]);
   const float a1 = fmaxf(h0, h1);
-  float a2;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(a2) : "f"(fminf(h0, h1)), "f"(l0), "f"(l1));
-  // merge (a1, a2) into (m1, m2)
-  float n2;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(n2) : "f"(m2), "f"(fminf(m1, a1)), "f"(a2));
-  m2 = n2;
+  const float a2 = max3f(fminf(h0, h1), l0, l1);
+  m2 = max3f(m2, fminf(m1, a1), a2);
   m1 = fmaxf(m1, a1);
   return a1;
+}
+
+// Unit bounds are kept as fp16 rounded towards +inf: still upper bounds, half the space.
+__device__ __forceinline__ unsigned short ub_half(float v) {
+  return __half_as_ushort(__float2half_ru(v));
+}
+__device__ __forceinline__ float ub_float(unsigned short h) {
+  return __half2float(__ushort_as_half(h));
 }
 
 // ------------------------------------------------------------------ row sources
 // Exact keys and scores already in shared memory (single-CTA path).
 struct ExactKeyRow {
+  static constexpr bool kLateGlobal = false;
   const float* key;
   const float* s;
   __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
@@ -60,102 +87,245 @@ struct ExactKeyRow {
     v[2] = q.z;
     v[3] = q.w;
   }
-  __device__ __forceinline__ float exact(int e, float& se) const {
+  __device__ __forceinline__ uint2 late_words(int) const { return make_uint2(0u, 0u); }
+  __device__ __forceinline__ void values(int e0, uint2, float (&v)[4]) const { unit(e0, v); }
+  __device__ __forceinline__ float exact(int e, uint32_t, float& se) const {
     se = s[e];
     return key[e];
   }
 };
 
-// A bf16 logit row in shared memory; values are proxies (multi-CTA path).
+// A bf16 logit row staged in shared memory; values are proxies.  With kLateGlobal the
+// buffer is handed back after pass 1 and later reads go to the row in global memory (just
+// copied, so they hit L2); otherwise they read the staged row.
+template <bool kLateGlobalReads>
 struct ProxyRow {
-  const uint16_t* row;  // [E] bf16 bit patterns
-  const float* c;       // [E] 0.5 + bias
-  const float* bias;    // [E]
-  __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
-    const uint2 w = *reinterpret_cast<const uint2*>(row + e0);
+  static constexpr bool kLateGlobal = kLateGlobalReads;
+  const uint16_t* row;   // [E] bf16 bit patterns, shared memory
+  const uint16_t* grow;  // the same row, global memory (used with kLateGlobal)
+  const float* c;        // [E] 0.5 + bias, shared memory
+  const float* bias;     // [E] bias (shared memory, or global with kLateGlobal)
+  __device__ __forceinline__ void values(int e0, uint2 w, float (&v)[4]) const {
     const float4 cc = *reinterpret_cast<const float4*>(c + e0);
     v[0] = proxy_key(__uint_as_float(w.x << 16), cc.x);
     v[1] = proxy_key(__uint_as_float(w.x & 0xffff0000u), cc.y);
     v[2] = proxy_key(__uint_as_float(w.y << 16), cc.z);
     v[3] = proxy_key(__uint_as_float(w.y & 0xffff0000u), cc.w);
   }
-  __device__ __forceinline__ float exact(int e, float& se) const {
-    return exact_key(bf16_bits_to_float(row[e]), bias[e], se);
+  __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
+    values(e0, *reinterpret_cast<const uint2*>(row + e0), v);
+  }
+  __device__ __forceinline__ uint2 late_words(int e0) const {
+    return kLateGlobal ? __ldg(reinterpret_cast<const uint2*>(grow + e0))
+                       : *reinterpret_cast<const uint2*>(row + e0);
+  }
+  __device__ __forceinline__ float exact(int e, uint32_t bits, float& se) const {
+    const float b = kLateGlobal ? __ldg(bias + e) : bias[e];
+    return exact_key(bf16_bits_to_float(static_cast<uint16_t>(bits)), b, se);
   }
 };
 
-// --------------------------------------------------------------- the route step
-// umax: this warp's scratch of 32 * nu floats, unit-major (umax[u * 32 + lane]), holding the
-// best value of every unit of the lane's segment.  Lane k < K returns slot k in (id, w).
-template <class Row>
-__device__ __forceinline__ void route_token_seg(const Row& row, const SegShape& sh,
-                                                WarpScratch& ws, float* umax, int lane,
-                                                float delta, int& id, float& w) {
-  const int j = lane >> sh.log2L;          // my group
-  const int q = lane & (sh.L - 1);
-  const bool active = j < sh.G;
-  const int seg0 = j * sh.g + q * sh.sl;   // first expert of my segment
-  float* my_umax = umax + lane;  // unit u of my segment at my_umax[u * 32]
+// bf16 bits of expert e0 + t from the two words of a unit.
+__device__ __forceinline__ uint32_t unit_bits(uint2 w, int t) {
+  const uint32_t word = (t < 2) ? w.x : w.y;
+  return (t & 1) ? (word >> 16) : (word & 0xffffu);
+}
 
-  // ---- pass 1: top-2 of my segment, best of each unit
-  float m1 = -INFINITY, m2 = -INFINITY;
-  if (active) {
-    int u = (lane * sh.rot) % sh.nu;
-#pragma unroll 4
-    for (int k = 0; k < sh.nu; ++k) {
+// ------------------------------------------------------------------ unit bounds
+// A warp's unit bounds live in shared memory as fp16 quads: the bound of unit u of lane l
+// is half (u & 3) of the 8-byte word (u >> 2) * 32 + l; slots of units >= nu hold -inf.
+__device__ __forceinline__ int ub_index(int lane, int u) {
+  return ((((u >> 2) << 5) + lane) << 2) + (u & 3);
+}
+
+__device__ __forceinline__ float unit_ub(const unsigned short* umax, int lane, int u) {
+  return ub_float(umax[ub_index(lane, u)]);
+}
+
+// Bytes of a warp's unit bounds.
+__host__ __device__ inline size_t ub_bytes(int nu) {
+  return static_cast<size_t>((nu + 3) >> 2) * 32 * 8;
+}
+
+// The pad slots of a lane's last quad; once per kernel (pass 1 never writes them).
+__device__ __forceinline__ void ub_init_pads(unsigned short* umax, int lane, int nu) {
+  for (int u = nu; u < ((nu + 3) & ~3); ++u) umax[ub_index(lane, u)] = 0xfc00u;  // -inf
+}
+
+// Bit u set for each unit (u < nu <= 64) whose bound may reach theta: bounds are compared
+// in fp16 against theta rounded down, which can only add units.
+__device__ __forceinline__ unsigned long long hot_units(const unsigned short* umax, int lane,
+                                                        int nu, float theta) {
+  const __half th = __float2half_rd(theta);
+  const __half2 th2 = __halves2half2(th, th);
+  const uint2* q = reinterpret_cast<const uint2*>(umax) + lane;
+  unsigned long long hot = 0ull;
+  const int nq = (nu + 3) >> 2;
+  for (int i = 0; i < nq; ++i) {
+    const uint2 x = q[i * 32];
+    const unsigned ma = __hge2_mask(*reinterpret_cast<const __half2*>(&x.x), th2);
+    const unsigned mb = __hge2_mask(*reinterpret_cast<const __half2*>(&x.y), th2);
+    const unsigned nib = (ma & 1u) | ((ma >> 15) & 2u) | ((mb & 1u) << 2) | ((mb >> 13) & 8u);
+    hot |= static_cast<unsigned long long>(nib) << (4 * i);
+  }
+  return hot;
+}
+
+// ------------------------------------------------------- helpers over LT-lane segments
+template <int LT>
+__device__ __forceinline__ unsigned seg_lanes(int lane) {
+  return (LT == 32) ? kFull : (((1u << LT) - 1u) << (lane & ~(LT - 1)));
+}
+
+// Value of rank k (0-based, descending) among the values of my LT-lane segment: bitonic
+// sort inside each segment.
+template <int LT>
+__device__ __forceinline__ float seg_kth_desc(float v, int ll, int k) {
+#pragma unroll
+  for (int kk = 2; kk <= LT; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(kFull, v, j);
+      const bool desc = (ll & kk) == 0;
+      const bool lower = (ll & j) == 0;
+      v = (desc == lower) ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return __shfl_sync(kFull, v, k, LT);
+}
+
+// Descending rank k (0-based) among two values per lane of my LT-lane segment (2 * LT
+// values; element 2 * ll + r is register r of lane ll): bitonic sort over the segment.
+template <int LT>
+__device__ __forceinline__ float seg_kth_desc2(float v0, float v1, int ll, int k) {
+#pragma unroll
+  for (int kk = 2; kk <= 2 * LT; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      const bool desc = ((2 * ll) & kk) == 0;
+      if (j == 1) {  // partners are the lane's own two registers
+        const float hi = fmaxf(v0, v1), lo = fminf(v0, v1);
+        v0 = desc ? hi : lo;
+        v1 = desc ? lo : hi;
+      } else {
+        const int d = j >> 1;
+        const bool lower = (ll & d) == 0;
+        const float o0 = __shfl_xor_sync(kFull, v0, d);
+        const float o1 = __shfl_xor_sync(kFull, v1, d);
+        v0 = (desc == lower) ? fmaxf(v0, o0) : fminf(v0, o0);
+        v1 = (desc == lower) ? fmaxf(v1, o1) : fminf(v1, o1);
+      }
+    }
+  }
+  const float a0 = __shfl_sync(kFull, v0, k >> 1, LT);
+  const float a1 = __shfl_sync(kFull, v1, k >> 1, LT);
+  return (k & 1) ? a1 : a0;
+}
+
+// Pass-1 summary of a lane: top-2 over its segment in V interleaved parts (part = unit
+// step modulo V).  The parts cover disjoint experts, so V parts give the threshold of the
+// selection as many samples as V times the lanes.
+struct LaneTop {
+  float a1, a2;  // part 0
+  float b1, b2;  // part 1 (-inf when V == 1)
+  __device__ __forceinline__ float m1() const { return fmaxf(a1, b1); }
+  __device__ __forceinline__ float m2() const { return max3f(fminf(a1, b1), a2, b2); }
+};
+
+// ------------------------------------------------------------------------ pass 1
+// umax: the warp's unit bounds.  Lanes of an invalid token (or beyond the groups) return
+// -inf and write nothing.
+template <int LT, int V, class Row>
+__device__ __forceinline__ LaneTop seg_pass1(const Row& row, const SegShape& sh,
+                                             unsigned short* umax, int lane, bool token_valid) {
+  static_assert(V == 1 || V == 2, "one or two parts per lane");
+  const int ll = lane & (LT - 1);
+  const int j = ll >> sh.log2L;
+  LaneTop r{-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (!token_valid || j >= sh.G) return r;
+  const int seg0 = j * sh.g + (ll & (sh.L - 1)) * sh.sl;
+  int u = (lane * sh.rot) % sh.nu;
+  int k = 0;
+#pragma unroll (4 / V)
+  for (; k + V <= sh.nu; k += V) {
+#pragma unroll
+    for (int p = 0; p < V; ++p) {
       float v[4];
       row.unit(seg0 + 4 * u, v);
-      my_umax[u * 32] = top2_unit(v, m1, m2);
+      umax[ub_index(lane, u)] =
+          ub_half(p == 0 ? top2_unit(v, r.a1, r.a2) : top2_unit(v, r.b1, r.b2));
       u = (u + 1 == sh.nu) ? 0 : u + 1;
     }
   }
+  if (k < sh.nu) {  // odd unit count with two parts
+    float v[4];
+    row.unit(seg0 + 4 * u, v);
+    umax[ub_index(lane, u)] = ub_half(top2_unit(v, r.a1, r.a2));
+  }
+  return r;
+}
+
+// --------------------------------------------------------------------- selection
+// Everything after pass 1 for the token of my segment; ws is that token's scratch.
+// Every branch that holds a shuffle is uniform over the warp.  Lane ll < K of the segment
+// returns slot ll in (id, w).
+template <int LT, int V, class Row>
+__device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, SegScratch& ws,
+                                           const unsigned short* umax, int lane, float delta,
+                                           bool token_valid, const LaneTop& top, int& id,
+                                           float& w) {
+  const float m1 = top.m1(), m2 = top.m2();
+  const int ll = lane & (LT - 1);
+  const int j = ll >> sh.log2L;  // my group
+  const int q = ll & (sh.L - 1);
+  const bool active = token_valid && j < sh.G;
+  const int seg0 = j * sh.g + q * sh.sl;
+  const unsigned lanes = seg_lanes<LT>(lane);
+
   // ---- group score: merge the L lanes of the group
   float g1 = m1, g2 = m2;
   for (int d = 1; d < sh.L; d <<= 1) {
     const float o1 = __shfl_xor_sync(kFull, g1, d);
     const float o2 = __shfl_xor_sync(kFull, g2, d);
-    float n2;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(n2) : "f"(g2), "f"(o2), "f"(fminf(g1, o1)));
-    g2 = n2;
+    g2 = max3f(g2, o2, fminf(g1, o1));
     g1 = fmaxf(g1, o1);
   }
   bool kept = active;
   if (sh.Kg < sh.G) {
-    float gs = active ? __fadd_rn(g1, g2) : -INFINITY;
-    // rank of my group among the G groups (leaders are lanes i * L)
-    int rank = 0;
+    const float gs = active ? __fadd_rn(g1, g2) : -INFINITY;
+    int rank = 0;  // groups that beat mine (group i's first lane is lane i * L)
     for (int i = 0; i < sh.G; ++i) {
-      const float o = __shfl_sync(kFull, gs, i << sh.log2L);
+      const float o = __shfl_sync(kFull, gs, i << sh.log2L, LT);
       rank += (o > gs || (o == gs && i < j)) ? 1 : 0;
     }
+    kept = active && rank < sh.Kg;
     const float eta = 2.0f * delta + 1e-6f;  // |approximate - exact group score| bound
     bool certain = true;
     float A = 0.0f, B = 0.0f;
     if (delta > 0.0f) {
-      const unsigned ha = __ballot_sync(kFull, active && rank == sh.Kg - 1);
-      const unsigned hb = __ballot_sync(kFull, active && rank == sh.Kg);
-      A = __shfl_sync(kFull, gs, __ffs(ha) - 1);
-      B = __shfl_sync(kFull, gs, __ffs(hb) - 1);
-      certain = (A - B) > 2.0f * eta;
+      const unsigned ha = __ballot_sync(kFull, active && rank == sh.Kg - 1) & lanes;
+      const unsigned hb = __ballot_sync(kFull, active && rank == sh.Kg) & lanes;
+      A = __shfl_sync(kFull, gs, ha ? __ffs(ha) - 1 : 0);
+      B = __shfl_sync(kFull, gs, hb ? __ffs(hb) - 1 : 0);
+      certain = !(ha && hb) || (A - B) > 2.0f * eta;
     }
-    if (certain) {
-      kept = active && rank < sh.Kg;
-    } else {
+    if (__any_sync(kFull, !certain)) {
       // groups within 2*eta of the boundary get exact scores; the others keep their side
-      const bool surely_in = active && gs > B + 2.0f * eta;
-      const bool unsure = active && !surely_in && gs >= A - 2.0f * eta;
+      const bool surely_in = certain ? kept : (active && gs > B + 2.0f * eta);
+      const bool unsure = !certain && active && !surely_in && gs >= A - 2.0f * eta;
       float x1 = -INFINITY, x2 = -INFINITY;
       if (unsure) {
-        const float lo = g2 - 2.0f * delta;  // exact top-2 of the group lie in this window
+        const float lo = g2 - 2.0f * delta;  // the exact top-2 of the group lie above this
         for (int u = 0; u < sh.nu; ++u) {
-          if (my_umax[u * 32] >= lo) {
+          if (unit_ub(umax, lane, u) >= lo) {
+            const uint2 wd = row.late_words(seg0 + 4 * u);
             float v[4];
-            row.unit(seg0 + 4 * u, v);
+            row.values(seg0 + 4 * u, wd, v);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               if (v[t] >= lo) {
                 float s;
-                top2_insert(x1, x2, row.exact(seg0 + 4 * u + t, s));
+                top2_insert(x1, x2, row.exact(seg0 + 4 * u + t, unit_bits(wd, t), s));
               }
             }
           }
@@ -164,96 +334,142 @@ __device__ __forceinline__ void route_token_seg(const Row& row, const SegShape& 
       for (int d = 1; d < sh.L; d <<= 1) {
         const float o1 = __shfl_xor_sync(kFull, x1, d);
         const float o2 = __shfl_xor_sync(kFull, x2, d);
-        float n2;
-        asm("max.f32 %0, %1, %2, %3;" : "=f"(n2) : "f"(x2), "f"(o2), "f"(fminf(x1, o1)));
-        x2 = n2;
+        x2 = max3f(x2, o2, fminf(x1, o1));
         x1 = fmaxf(x1, o1);
       }
       const float xs = unsure ? __fadd_rn(x1, x2) : -INFINITY;
-      const unsigned in_mask = __ballot_sync(kFull, surely_in && q == 0);
+      const unsigned in_mask = __ballot_sync(kFull, surely_in && q == 0) & lanes;
       const int slots = sh.Kg - __popc(in_mask);
       int xr = 0;
       for (int i = 0; i < sh.G; ++i) {
         const int src = i << sh.log2L;
-        const float o = __shfl_sync(kFull, xs, src);
-        const bool ou = __shfl_sync(kFull, unsure ? 1 : 0, src) != 0;
+        const float o = __shfl_sync(kFull, xs, src, LT);
+        const bool ou = __shfl_sync(kFull, unsure ? 1 : 0, src, LT) != 0;
         xr += (ou && (o > xs || (o == xs && i < j))) ? 1 : 0;
       }
-      kept = surely_in || (unsure && xr < slots);
+      if (!certain) kept = surely_in || (unsure && xr < slots);
     }
   }
 
-  // ---- top-K threshold from the lanes' own top-2 (lanes of kept groups only): at least
-  // ceil(K/2) lanes hold two values >= t2, so at least K values are >= t2; when fewer lanes
-  // are kept, t1 = the K-th best lane maximum is the bound
-  const float k2 = kept ? m2 : -INFINITY;
-  float tau = __shfl_sync(kFull, warp_sort_desc(k2, lane), (sh.K - 1) >> 1);
-  if (tau == -INFINITY) {
-    const float k1 = kept ? m1 : -INFINITY;
-    tau = __shfl_sync(kFull, warp_sort_desc(k1, lane), sh.K - 1);
+  // ---- top-K threshold from the pass-1 samples of kept groups: at least ceil(K/2) parts
+  // hold two values >= t2, so at least K values are >= t2; t1 = the K-th best part maximum
+  // is also such a bound.  -inf when too few parts are kept.
+  float tau;
+  const float ninf = -INFINITY;
+  if (V == 1) {
+    tau = seg_kth_desc<LT>(kept ? m2 : ninf, ll, (sh.K - 1) >> 1);
+    if (sh.K <= LT && __any_sync(kFull, tau == -INFINITY))
+      tau = fmaxf(tau, seg_kth_desc<LT>(kept ? m1 : ninf, ll, sh.K - 1));
+  } else {
+    tau = seg_kth_desc2<LT>(kept ? top.a2 : ninf, kept ? top.b2 : ninf, ll, (sh.K - 1) >> 1);
+    if (sh.K <= 2 * LT && __any_sync(kFull, tau == -INFINITY))
+      tau = fmaxf(tau, seg_kth_desc2<LT>(kept ? top.a1 : ninf, kept ? top.b1 : ninf, ll,
+                                         sh.K - 1));
   }
   const float theta = tau - 2.0f * delta;
 
-  // ---- survivors: my units whose best reaches theta, compacted without atomics: count,
-  // warp scan for each lane's first slot, then write (the few surviving units are read twice)
-  if (lane < sh.K) {
-    ws.sel_id[lane] = -1;
-    ws.sel_s[lane] = 0.0f;
+  // ---- survivors: values >= theta in units whose bound may reach theta.  The lanes walk
+  // their hot units in step (one unit per lane per round, the next one's words already in
+  // flight) and append records (bf16 bits << 16) | expert at a segment-wide running count.
+  if (ll < sh.K) {
+    ws.sel_id[ll] = -1;
+    ws.sel_s[ll] = 0.0f;
   }
   const bool scan_mine = kept && m1 >= theta;
-  int found = 0;
-  if (scan_mine) {
-    for (int u = 0; u < sh.nu; ++u) {
-      if (my_umax[u * 32] >= theta) {
-        float v[4];
-        row.unit(seg0 + 4 * u, v);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) found += (v[t] >= theta) ? 1 : 0;
-      }
-    }
+  unsigned long long hot = scan_mine ? hot_units(umax, lane, sh.nu, theta) : 0ull;
+  const unsigned lt = lanemask_lt(lane) & lanes;
+  int total = 0;
+  bool have = hot != 0ull;
+  int u = 0;
+  uint2 wd = make_uint2(0u, 0u);
+  if (have) {
+    u = __ffsll(static_cast<long long>(hot)) - 1;
+    hot &= hot - 1ull;
+    wd = row.late_words(seg0 + 4 * u);
   }
-  const int incl = warp_inclusive_sum(found, lane);
-  const int total = __shfl_sync(kFull, incl, 31);
-  if (total <= kCandCap && found > 0) {
-    int pos = incl - found;
-    for (int u = 0; u < sh.nu; ++u) {
-      if (my_umax[u * 32] >= theta) {
-        float v[4];
-        row.unit(seg0 + 4 * u, v);
+  while (__any_sync(kFull, have)) {
+    const bool have_n = hot != 0ull;
+    int u_n = 0;
+    uint2 wd_n = make_uint2(0u, 0u);
+    if (have_n) {
+      u_n = __ffsll(static_cast<long long>(hot)) - 1;
+      hot &= hot - 1ull;
+      wd_n = row.late_words(seg0 + 4 * u_n);
+    }
+    unsigned hits = 0u;
+    if (have) {
+      float v[4];
+      row.values(seg0 + 4 * u, wd, v);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (v[t] >= theta) ws.cand[pos++] = static_cast<unsigned long long>(seg0 + 4 * u + t);
-        }
+      for (int t = 0; t < 4; ++t) hits |= (v[t] >= theta) ? (1u << t) : 0u;
+    }
+    const int n = __popc(hits);
+    const unsigned b0 = __ballot_sync(kFull, n & 1) & lanes;
+    const unsigned b1 = __ballot_sync(kFull, n & 2) & lanes;
+    const unsigned b2 = __ballot_sync(kFull, n & 4) & lanes;
+    int pos = total + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+    total += __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if ((hits >> t) & 1u) {
+        if (pos < kCandCap)
+          ws.cand[pos] = (unit_bits(wd, t) << 16) | static_cast<uint32_t>(seg0 + 4 * u + t);
+        ++pos;
       }
     }
+    have = have_n;
+    u = u_n;
+    wd = wd_n;
   }
   __syncwarp();
-  if (total <= kCandCap) {
-    for (int a = lane; a < total; a += 32) {
-      const int e = static_cast<int>(ws.cand[a]);
+  if (__all_sync(kFull, total <= kCandCap)) {
+    for (int a = ll; a < total; a += LT) {
+      const uint32_t r = static_cast<uint32_t>(ws.cand[a]);
+      const int e = static_cast<int>(r & 0xffffu);
       float s;
-      const float k = row.exact(e, s);
+      const float k = row.exact(e, r >> 16, s);
       ws.cand[a] = composite(k, e);
       ws.cand_s[a] = s;
     }
     __syncwarp();
-    rank_candidates(ws, total, sh.K, lane);
+    // slot = number of better composites (composites are distinct); two per lane at once
+    for (int a0 = ll; a0 < total; a0 += 2 * LT) {
+      const int a1 = a0 + LT;
+      const unsigned long long me0 = ws.cand[a0];
+      const unsigned long long me1 = (a1 < total) ? ws.cand[a1] : ~0ull;
+      int r0 = 0, r1 = 0;
+#pragma unroll 4
+      for (int b = 0; b < total; ++b) {
+        const unsigned long long c = ws.cand[b];
+        r0 += (c > me0) ? 1 : 0;
+        r1 += (c > me1) ? 1 : 0;
+      }
+      if (r0 < sh.K) {
+        ws.sel_id[r0] = composite_expert(me0);
+        ws.sel_s[r0] = ws.cand_s[a0];
+      }
+      if (a1 < total && r1 < sh.K) {
+        ws.sel_id[r1] = composite_expert(me1);
+        ws.sel_s[r1] = ws.cand_s[a1];
+      }
+    }
   } else {
-    // many survivors (wide ties): K rounds of the best exact composite below the last one
+    // very many survivors (wide ties): K rounds of the best exact composite below the last
     unsigned long long prev = ~0ull;
     for (int k = 0; k < sh.K; ++k) {
       unsigned long long best = 0ull;
       float best_s = 0.0f;
       if (scan_mine) {
-        for (int u = 0; u < sh.nu; ++u) {
-          if (my_umax[u * 32] >= theta) {
+        for (int uu = 0; uu < sh.nu; ++uu) {
+          if (unit_ub(umax, lane, uu) >= theta) {
+            const uint2 w2 = row.late_words(seg0 + 4 * uu);
             float v[4];
-            row.unit(seg0 + 4 * u, v);
+            row.values(seg0 + 4 * uu, w2, v);
             for (int t = 0; t < 4; ++t) {
               if (v[t] >= theta) {
-                const int e = seg0 + 4 * u + t;
+                const int e = seg0 + 4 * uu + t;
                 float s;
-                const unsigned long long c = composite(row.exact(e, s), e);
+                const unsigned long long c = composite(row.exact(e, unit_bits(w2, t), s), e);
                 if (c < prev && c > best) {
                   best = c;
                   best_s = s;
@@ -263,23 +479,44 @@ __device__ __forceinline__ void route_token_seg(const Row& row, const SegShape& 
           }
         }
       }
-      unsigned long long wb = best;
+      unsigned long long wbest = best;
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(kFull, wb, d);
-        wb = (o > wb) ? o : wb;
+      for (int d = LT >> 1; d > 0; d >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(kFull, wbest, d);
+        wbest = (o > wbest) ? o : wbest;
       }
-      const unsigned owner = __ballot_sync(kFull, best == wb && wb != 0ull);
-      const float ws_s = __shfl_sync(kFull, best_s, owner ? __ffs(owner) - 1 : 0);
-      if (lane == 0 && wb != 0ull) {
-        ws.sel_id[k] = composite_expert(wb);
-        ws.sel_s[k] = ws_s;
+      const unsigned owner = __ballot_sync(kFull, best == wbest && wbest != 0ull) & lanes;
+      const float owner_s = __shfl_sync(kFull, best_s, owner ? __ffs(owner) - 1 : 0);
+      if (ll == 0 && wbest != 0ull) {
+        ws.sel_id[k] = composite_expert(wbest);
+        ws.sel_s[k] = owner_s;
       }
-      prev = wb;
+      prev = wbest;
     }
   }
   __syncwarp();
-  finish_weights(ws, sh.K, sh.R, lane, id, w);
+  // ---- renormalised weights: sum of the scores in slot order, then (s_k / sum) * R
+  const bool mine = ll < sh.K;
+  const float s = mine ? ws.sel_s[ll] : 0.0f;
+  id = mine ? ws.sel_id[ll] : -1;
+  float sum = 0.0f;
+  if (ll == 0) {
+    float4 q4[kMaxTopk / 4];
+    const float4* s4 = reinterpret_cast<const float4*>(ws.sel_s);
+#pragma unroll
+    for (int i = 0; i < kMaxTopk / 4; ++i)
+      q4[i] = (4 * i < sh.K) ? s4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < kMaxTopk / 4; ++i) {
+      if (4 * i < sh.K) sum = __fadd_rn(sum, q4[i].x);
+      if (4 * i + 1 < sh.K) sum = __fadd_rn(sum, q4[i].y);
+      if (4 * i + 2 < sh.K) sum = __fadd_rn(sum, q4[i].z);
+      if (4 * i + 3 < sh.K) sum = __fadd_rn(sum, q4[i].w);
+    }
+  }
+  sum = __shfl_sync(kFull, sum, 0, LT);
+  w = mine ? __fmul_rn(__fdiv_rn(s, sum), sh.R) : 0.0f;
+  __syncwarp();
 }
 
 }  // namespace mrs
