@@ -165,30 +165,28 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   const int tpu = (T + U - 1) / U;
   a.max_routes = tpu * sh.K;
   a.vec16 = (sh.E % 8) == 0;
-  // Launch plan of the segment kernel for `lanes` lanes per token and a release mode: the
-  // most warps (up to one per step of the unit) whose shared memory fits, with the largest
-  // number of row buffers (<= max_nbuf) that costs no warps.
+  // Launch plan of the segment kernel for `lanes` lanes per token: the most warps (up to
+  // one per step of the unit) whose shared memory fits, with the largest number of row
+  // buffers (<= 2) that costs no warps.
   struct Plan {
     bool seg;
     SegShape shape;
     int lanes, nbuf, nwarps, want;
-    bool early;
     size_t smem;
   };
-  auto plan_for = [&](int lanes, bool early, int max_nbuf) {
+  auto plan_for = [&](int lanes) {
     Plan p{};
     p.lanes = lanes;
-    p.early = early;
     p.seg = a.vec16 && make_seg_shape(sh.E, sh.G, sh.Kg, sh.K, sh.R, lanes, p.shape);
     if (!p.seg) return p;
     const int tpw = 32 / lanes;
     const int steps = (tpu + tpw - 1) / tpw;
     const int cap = kSegThreads / 32;
     p.want = steps < cap ? steps : cap;
-    for (int nbuf = max_nbuf; nbuf >= 1; --nbuf) {
+    for (int nbuf = 2; nbuf >= 1; --nbuf) {
       int w = p.want;
       auto bytes = [&](int ww) {
-        return seg_smem_bytes(sh.E, p.shape.nu, ww, a.max_routes, sort, tpw, nbuf, early);
+        return seg_smem_bytes(sh.E, p.shape.nu, ww, a.max_routes, sort, tpw, nbuf);
       };
       while (w > 1 && bytes(w) > static_cast<size_t>(d.smem_optin)) --w;
       if (w > p.nwarps) {
@@ -199,21 +197,18 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
     }
     return p;
   };
-  // Preference: two tokens per warp (16 lanes each; the per-token shuffle and scan work of
-  // the route step is shared by two tokens) with rows kept in shared memory until the
-  // selection is done, when K <= 16 and all warps fit with two buffers each; the same with
-  // one token per warp; else one token per warp, buffers handed back after pass 1.
+  // Two tokens per warp (16 lanes each) share the per-token shuffle and scan work of the
+  // route step: taken when K <= 16, the unit has tokens for every warp and all warps fit
+  // with two row buffers each.  Otherwise one token per warp.
   Plan p{};
-  if (sh.K <= 16) p = plan_for(16, false, 2);
-  if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32, false, 2);
-  if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32, true, 2);
+  if (sh.K <= 16 && tpu >= 2 * (kSegThreads / 32)) p = plan_for(16);
+  if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32);
   a.use_seg = p.seg;
   size_t smem;
   if (p.seg) {
     a.seg = p.shape;
     a.lanes = p.lanes;
     a.nbuf = p.nbuf;
-    a.early = p.early;
     a.nwarps = p.nwarps;
     smem = p.smem;
   } else {

@@ -91,18 +91,19 @@ __device__ __forceinline__ float warp_kth_largest(float v, int k, int lane) {
 }
 
 // ------------------------------------------------------------------ proxy score
-// Cheap stand-in for the selection key: p = 0.5 * tanh.approx(0.5 x) + (0.5 + bias).
-// 0.5 + 0.5 tanh(x / 2) is the logistic function, so p differs from the exact key
-// s + bias by the hardware tanh approximation (at most kProxyTanhBound over every bf16 x,
-// checked exhaustively on the device by moe_route_sort_proxy_selftest) plus four roundings
-// of values below max|bias| + 1.5 in magnitude; proxy_delta() bounds the total for biases
-// up to kProxyBiasLimit.  The selection only uses p to discard experts that are worse than a
-// proven bound by more than 2 * delta.
+// Cheap stand-in for the selection key, shifted by the constant -0.5 that every expert
+// shares: p = 0.5 * tanh.approx(0.5 x) + bias.  0.5 + 0.5 tanh(x / 2) is the logistic
+// function, so p + 0.5 differs from the exact key s + bias by the hardware tanh
+// approximation (at most kProxyTanhBound over every bf16 x, checked exhaustively on the
+// device by moe_route_sort_proxy_selftest) plus the roundings of p and of the exact key
+// (values below max|bias| + 1 in magnitude); proxy_delta() bounds the total for biases up
+// to kProxyBiasLimit.  The selection only compares proxies with each other and uses them
+// to discard experts that are worse than a proven bound by more than 2 * delta.
 constexpr float kProxyTanhBound = 1.0f / 2048.0f;
 constexpr float kProxyBiasLimit = 1024.0f;
 
-// Bound on |proxy - exact key| for biases of magnitude <= max_abs_bias: the tanh bound
-// plus four half-ulp roundings of values below max_abs_bias + 1.5 (ulp(x) <= x * 2^-23).
+// Bound on |proxy + 0.5 - exact key| for biases of magnitude <= max_abs_bias: the tanh
+// bound plus four half-ulp roundings of values below max_abs_bias + 1.5 (two are needed).
 __host__ __device__ inline float proxy_delta(float max_abs_bias) {
   return kProxyTanhBound + (max_abs_bias + 2.0f) * 2.384185791e-7f;  // 2 * 2^-23
 }
@@ -113,8 +114,8 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ float proxy_key(float x, float c) {
-  return fmaf(0.5f, tanh_approx(0.5f * x), c);
+__device__ __forceinline__ float proxy_key(float x, float bias) {
+  return fmaf(0.5f, tanh_approx(0.5f * x), bias);
 }
 
 // Exact key and score of one logit: key = s + bias with s the exact score.

@@ -119,7 +119,6 @@ struct RouteArgs {
   bool sort;     // run phase 1 of the sort step after routing (else route only)
   int lanes;     // segment kernel: lanes per token (32, or 16 for two tokens per warp)
   int nbuf;      // segment kernel: row buffers per warp (1 or 2)
-  bool early;    // segment kernel: hand a row buffer back after pass 1 (late reads global)
   RouteShape sh;
   SegShape seg;
   int32_t* topk_ids;
@@ -161,8 +160,7 @@ cudaError_t launch_empty(int32_t* npp, int32_t* status, cudaStream_t st);
 
 // Shared memory of the multi-CTA route kernels for a given warp count.
 size_t route_smem_bytes(int E, int nwarps, int max_routes, bool sort);
-size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw, int nbuf,
-                      bool early);
+size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw, int nbuf);
 SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only);
 
 // Shared memory used by phase 1 of the sort step (mrs_unit.cuh) besides the routes.

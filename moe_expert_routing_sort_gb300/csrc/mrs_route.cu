@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
           const ExactKeyRow row{keys + tl * E, svals + tl * E};
           const LaneTop top = seg_pass1<32, 1>(row, a.seg, umax, lane, true);
           seg_select<32, 1>(row, a.seg, *reinterpret_cast<SegScratch*>(&scr[warp]), umax, lane,
-                            0.0f, true, top, id, w);
+                            0.0f, true, top, [] {}, id, w);
         } else {
           route_token(SmemExactSrc{keys + tl * E, svals + tl * E}, sh, scr[warp], lane, id, w);
         }
@@ -403,23 +403,20 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
 
 
 // ------------------------------------------------- multi-CTA route, TMA-staged segments
-// Shared memory: c[E] = 0.5 + bias, bias[E] (unless the selection reads it from global
-// memory), counts[E], the unit's routes (ids, weights), then per warp: nbuf row buffers of
-// tpw rows each, two mbarriers, one route scratch per token of a step and the unit bounds;
-// after routing, the per-warp region is reused by phase 1.
+// Shared memory: bias[E], counts[E], the unit's routes (ids, weights), then per warp: nbuf
+// row buffers of tpw rows each, two mbarriers, one route scratch per token of a step and the
+// unit bounds; after routing, the per-warp region is reused by phase 1.
 struct SegCtaLayout {
-  size_t c, bias, counts, rid, rw, warps, per_warp, rows, mbar, scratch, umax, total;
+  size_t bias, counts, rid, rw, warps, per_warp, rows, mbar, scratch, umax, total;
 };
 
 __host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps,
                                                        int max_routes, bool sort, int tpw,
-                                                       int nbuf, bool early) {
+                                                       int nbuf) {
   SegCtaLayout l{};
   size_t o = 0;
-  l.c = o;
-  o = align16(o + sizeof(float) * E);
   l.bias = o;
-  o = align16(o + (early ? 0 : sizeof(float) * E));
+  o = align16(o + sizeof(float) * E);
   l.counts = o;
   o = align16(o + sizeof(int32_t) * E);
   l.rid = o;
@@ -444,16 +441,15 @@ __host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps
 }
 
 size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw,
-                      int nbuf, bool early) {
-  return seg_cta_layout(E, nu, nwarps, max_routes, sort, tpw, nbuf, early).total;
+                      int nbuf) {
+  return seg_cta_layout(E, nu, nwarps, max_routes, sort, tpw, nbuf).total;
 }
 
 // Warp w of unit u takes steps w, w + nwarps, ...; step i covers the 32 / LT consecutive
 // tokens t0 + i * (32 / LT) + h, token h routed by lanes [h * LT, (h + 1) * LT).  The rows
-// of a step are contiguous, so one bulk copy brings them in.  With kEarly a buffer is handed
-// back to the copy engine as soon as pass 1 is done with it (the selection then reads the
-// few row parts it needs from global memory); otherwise after the selection.
-template <bool kSort, int LT, bool kEarly>
+// of a step are contiguous, so one bulk copy brings them in.  A buffer goes back to the copy
+// engine (for the warp's step nbuf further on) as soon as the selection stops reading it.
+template <bool kSort, int LT>
 __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const RouteArgs a) {
   constexpr int kTpw = 32 / LT;
   constexpr int kParts = (LT == 16) ? 2 : 1;
@@ -462,9 +458,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   const int h = lane / LT, ll = lane & (LT - 1);
   const SegShape sh = a.seg;
   const int E = sh.E, K = sh.K, nbuf = a.nbuf;
-  const SegCtaLayout lay =
-      seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort, kTpw, nbuf, kEarly);
-  float* c_s = reinterpret_cast<float*>(smem + lay.c);
+  const SegCtaLayout lay = seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort, kTpw, nbuf);
   float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
   int32_t* counts = reinterpret_cast<int32_t*>(smem + lay.counts);
   int32_t* rid = reinterpret_cast<int32_t*>(smem + lay.rid);
@@ -512,8 +506,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   float bmax = 0.0f;  // largest |bias|, NaN-propagating (NaN fails the limit test below)
   for (int e = tid; e < E; e += blockDim.x) {
     const float b = a.bias[e];
-    c_s[e] = __fadd_rn(0.5f, b);
-    if (!kEarly) bias_s[e] = b;
+    bias_s[e] = b;
     const float ab = fabsf(b);
     bmax = (ab > bmax || ab != ab) ? ab : bmax;
     counts[e] = 0;
@@ -542,11 +535,9 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
     phase ^= 1u << b;
     const int t = step_t(k) + h;
     const bool valid = t < t1;
-    const ProxyRow<kEarly> row{rows + static_cast<size_t>(b * kTpw + h) * E,
-                               a.logits + static_cast<size_t>(valid ? t : t0) * E, c_s,
-                               kEarly ? a.bias : bias_s};
+    const ProxyRow row{rows + static_cast<size_t>(b * kTpw + h) * E, bias_s};
     const LaneTop top = seg_pass1<LT, kParts>(row, sh, umax, lane, valid);
-    if (kEarly) {
+    auto release = [&] {
       __syncwarp();  // every lane is done with the buffer
       if (k + nbuf < n_mine) {
         if (lane == 0) {
@@ -555,20 +546,10 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
         }
         ++issued;
       }
-    }
+    };
     int id;
     float w;
-    seg_select<LT, kParts>(row, sh, scr[h], umax, lane, delta, valid, top, id, w);
-    if (!kEarly) {
-      __syncwarp();  // every lane is done with the buffer
-      if (k + nbuf < n_mine) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue(k + nbuf, b);
-        }
-        ++issued;
-      }
-    }
+    seg_select<LT, kParts>(row, sh, scr[h], umax, lane, delta, valid, top, release, id, w);
     if (valid && ll < K) {
       a.topk_ids[static_cast<size_t>(t) * K + ll] = id;
       a.topk_w[static_cast<size_t>(t) * K + ll] = w;
@@ -597,22 +578,18 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   }
 }
 
-template <bool kSort, int LT, bool kEarly>
+template <bool kSort, int LT>
 static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort, LT, kEarly>,
+  cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort, LT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  mrs_route_seg_kernel<kSort, LT, kEarly><<<a.U, a.nwarps * 32, smem, st>>>(a);
+  mrs_route_seg_kernel<kSort, LT><<<a.U, a.nwarps * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 template <bool kSort>
 static cudaError_t launch_seg(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  if (a.lanes == 16)
-    return a.early ? launch_seg_h<kSort, 16, true>(a, smem, st)
-                   : launch_seg_h<kSort, 16, false>(a, smem, st);
-  return a.early ? launch_seg_h<kSort, 32, true>(a, smem, st)
-                 : launch_seg_h<kSort, 32, false>(a, smem, st);
+  return a.lanes == 16 ? launch_seg_h<kSort, 16>(a, smem, st) : launch_seg_h<kSort, 32>(a, smem, st);
 }
 
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {

@@ -8,17 +8,19 @@
 //   seg_select  the rest, from those summaries: group scores are a shuffle merge over the
 //               L lanes of a group, the K-th-best threshold comes from the parts' top-2, and
 //               only units whose bound reaches the threshold are read again
-// so the row buffer can take the next token's row as soon as pass 1 is done.
+// The selection reads the row only up to the survivor step; after that it calls the
+// caller's release(), so the row buffer can take the next row while the token finishes.
 // Source of the step: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff
 // (stack)", Summary (correction bias, grouped top-k).
 //
 // A row source provides
 //   unit(e0, v[4])          selection values (proxies or exact keys) of e0..e0+3
-//   late_words(e0)          the raw bf16 words of e0..e0+3 after pass 1
+//   late_words(e0)          the raw bf16 words of e0..e0+3
 //   values(e0, words, v[4]) the selection values from those words
 //   exact(e, bits, s)       exact key of expert e (logit bits `bits`), score through s
-// and `delta` bounds |value - exact key| (0 for exact sources).  Decisions are exact:
-// values only discard experts proven worse than a bound by more than 2 * delta.
+// Selection values are the exact keys minus a constant shift common to all experts, up to
+// `delta` (0 for exact sources).  Decisions are exact: values only discard experts proven
+// worse than a bound by more than 2 * delta, and only differences of values are used.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -77,7 +79,6 @@ __device__ __forceinline__ float ub_float(unsigned short h) {
 // ------------------------------------------------------------------ row sources
 // Exact keys and scores already in shared memory (single-CTA path).
 struct ExactKeyRow {
-  static constexpr bool kLateGlobal = false;
   const float* key;
   const float* s;
   __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
@@ -95,33 +96,26 @@ struct ExactKeyRow {
   }
 };
 
-// A bf16 logit row staged in shared memory; values are proxies.  With kLateGlobal the
-// buffer is handed back after pass 1 and later reads go to the row in global memory (just
-// copied, so they hit L2); otherwise they read the staged row.
-template <bool kLateGlobalReads>
+// A bf16 logit row staged in shared memory; values are the shifted proxies
+// 0.5 * tanh.approx(0.5 x) + bias (the exact key minus 0.5, up to delta).
 struct ProxyRow {
-  static constexpr bool kLateGlobal = kLateGlobalReads;
-  const uint16_t* row;   // [E] bf16 bit patterns, shared memory
-  const uint16_t* grow;  // the same row, global memory (used with kLateGlobal)
-  const float* c;        // [E] 0.5 + bias, shared memory
-  const float* bias;     // [E] bias (shared memory, or global with kLateGlobal)
+  const uint16_t* row;  // [E] bf16 bit patterns, shared memory
+  const float* bias;    // [E] shared memory
   __device__ __forceinline__ void values(int e0, uint2 w, float (&v)[4]) const {
-    const float4 cc = *reinterpret_cast<const float4*>(c + e0);
-    v[0] = proxy_key(__uint_as_float(w.x << 16), cc.x);
-    v[1] = proxy_key(__uint_as_float(w.x & 0xffff0000u), cc.y);
-    v[2] = proxy_key(__uint_as_float(w.y << 16), cc.z);
-    v[3] = proxy_key(__uint_as_float(w.y & 0xffff0000u), cc.w);
-  }
-  __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
-    values(e0, *reinterpret_cast<const uint2*>(row + e0), v);
+    const float4 bb = *reinterpret_cast<const float4*>(bias + e0);
+    v[0] = proxy_key(__uint_as_float(w.x << 16), bb.x);
+    v[1] = proxy_key(__uint_as_float(w.x & 0xffff0000u), bb.y);
+    v[2] = proxy_key(__uint_as_float(w.y << 16), bb.z);
+    v[3] = proxy_key(__uint_as_float(w.y & 0xffff0000u), bb.w);
   }
   __device__ __forceinline__ uint2 late_words(int e0) const {
-    return kLateGlobal ? __ldg(reinterpret_cast<const uint2*>(grow + e0))
-                       : *reinterpret_cast<const uint2*>(row + e0);
+    return *reinterpret_cast<const uint2*>(row + e0);
+  }
+  __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
+    values(e0, late_words(e0), v);
   }
   __device__ __forceinline__ float exact(int e, uint32_t bits, float& se) const {
-    const float b = kLateGlobal ? __ldg(bias + e) : bias[e];
-    return exact_key(bf16_bits_to_float(static_cast<uint16_t>(bits)), b, se);
+    return exact_key(bf16_bits_to_float(static_cast<uint16_t>(bits)), bias[e], se);
   }
 };
 
@@ -267,13 +261,14 @@ __device__ __forceinline__ LaneTop seg_pass1(const Row& row, const SegShape& sh,
 
 // --------------------------------------------------------------------- selection
 // Everything after pass 1 for the token of my segment; ws is that token's scratch.
-// Every branch that holds a shuffle is uniform over the warp.  Lane ll < K of the segment
-// returns slot ll in (id, w).
-template <int LT, int V, class Row>
+// Every branch that holds a shuffle is uniform over the warp; release() is called once, by
+// the whole warp, as soon as the row is no longer read.  Lane ll < K of the segment returns
+// slot ll in (id, w).
+template <int LT, int V, class Row, class Release>
 __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, SegScratch& ws,
                                            const unsigned short* umax, int lane, float delta,
-                                           bool token_valid, const LaneTop& top, int& id,
-                                           float& w) {
+                                           bool token_valid, const LaneTop& top,
+                                           const Release& release, int& id, float& w) {
   const float m1 = top.m1(), m2 = top.m2();
   const int ll = lane & (LT - 1);
   const int j = ll >> sh.log2L;  // my group
@@ -369,8 +364,8 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
   const float theta = tau - 2.0f * delta;
 
   // ---- survivors: values >= theta in units whose bound may reach theta.  The lanes walk
-  // their hot units in step (one unit per lane per round, the next one's words already in
-  // flight) and append records (bf16 bits << 16) | expert at a segment-wide running count.
+  // their hot units in step (one unit per lane per round, the next one's words loaded
+  // ahead) and append records (bf16 bits << 16) | expert at a segment-wide running count.
   if (ll < sh.K) {
     ws.sel_id[ll] = -1;
     ws.sel_s[ll] = 0.0f;
@@ -421,8 +416,10 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
     u = u_n;
     wd = wd_n;
   }
+  const bool fits = __all_sync(kFull, total <= kCandCap);
+  if (fits) release();  // the records hold the logit bits; the row is not read again
   __syncwarp();
-  if (__all_sync(kFull, total <= kCandCap)) {
+  if (fits) {
     for (int a = ll; a < total; a += LT) {
       const uint32_t r = static_cast<uint32_t>(ws.cand[a]);
       const int e = static_cast<int>(r & 0xffffu);
@@ -493,6 +490,7 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
       }
       prev = wbest;
     }
+    release();
   }
   __syncwarp();
   // ---- renormalised weights: sum of the scores in slot order, then (s_k / sum) * R
