@@ -226,6 +226,7 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   if (sort) {
     a.uo.loc_off = reinterpret_cast<int32_t*>(ws + l.loc_off);
     a.uo.unit_buf = reinterpret_cast<int2*>(ws + l.unit_buf);
+    a.uo.unit_e = reinterpret_cast<uint16_t*>(ws + l.unit_e);
     a.uo.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
     a.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
     a.uo.nslices = nslices;
@@ -247,6 +248,8 @@ int run_slices(int T, int E, int K, int B, int U, int nslices, int32_t* sorted_i
   c.nslices = nslices;
   c.loc_off = reinterpret_cast<const int32_t*>(ws + l.loc_off);
   c.unit_buf = reinterpret_cast<const int2*>(ws + l.unit_buf);
+  c.unit_e = reinterpret_cast<const uint16_t*>(ws + l.unit_e);
+  c.adj = reinterpret_cast<int32_t*>(ws + l.adj);
   c.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
   c.unit_flags = reinterpret_cast<const int32_t*>(ws + l.unit_flags);
   c.sorted_ids = sorted_ids;
@@ -254,7 +257,9 @@ int run_slices(int T, int E, int K, int B, int U, int nslices, int32_t* sorted_i
   c.expert_ids = expert_ids;
   c.npp = npp;
   c.status = reinterpret_cast<int32_t*>(ws + l.status);
-  return launch_status(launch_slices(c, st));
+  int rc = launch_status(launch_slices(c, st));
+  if (rc) return rc;
+  return launch_status(launch_scatter(c, st));
 }
 
 // Single-CTA path: shared-memory layout for the largest wave that fits.
@@ -498,11 +503,12 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
   c.E = E;
   c.U = U;
   c.max_routes = ((T + U - 1) / U) * topk;
-  c.loc_off = reinterpret_cast<int32_t*>(ws + l.loc_off);
-  c.unit_buf = reinterpret_cast<int2*>(ws + l.unit_buf);
-  c.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
-  c.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
-  c.nslices = nslices;
+  c.uo.loc_off = reinterpret_cast<int32_t*>(ws + l.loc_off);
+  c.uo.unit_buf = reinterpret_cast<int2*>(ws + l.unit_buf);
+  c.uo.unit_e = reinterpret_cast<uint16_t*>(ws + l.unit_e);
+  c.uo.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
+  c.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
+  c.uo.nslices = nslices;
   rc = launch_status(launch_unit(c, stream));
   if (rc) return rc;
   return run_slices(T, E, topk, block_m, U, nslices, sorted_token_ids, sorted_weights,

@@ -19,16 +19,19 @@ constexpr int kSliceThreads = 512;
 // A unit (one CTA of the route step) holds at most this many routes in shared memory.
 constexpr int kUnitRouteCap = 4096;
 
-// Units of the multi-CTA path for T tokens: at least one token and at most kUnitRouteCap
-// routes each; `sms` is the device's SM count (the workspace bound assumes <= 1024).
+// Units of the multi-CTA path for T tokens: one per SM (counting at most kMaxUnitSms SMs),
+// at least one token and at most kUnitRouteCap routes each; `sms` is the device's SM count.
+constexpr int kMaxUnitSms = 256;
 inline int units_for_shape(int T, int K, int sms) {
   const int tpu_cap = kUnitRouteCap / K > 0 ? kUnitRouteCap / K : 1;
-  int U = T < sms ? T : sms;
+  const int s = sms < kMaxUnitSms ? sms : kMaxUnitSms;
+  int U = T < s ? T : s;
   const int need = (T + tpu_cap - 1) / tpu_cap;
   if (need > U) U = need;
   return U < 1 ? 1 : U;
 }
-inline int units_bound(int T, int K) { return units_for_shape(T, K, 1024); }
+// The largest unit count of any device: the workspace is sized for it.
+inline int units_bound(int T, int K) { return units_for_shape(T, K, kMaxUnitSms); }
 inline int slices_for(int U, int E) { return U < E ? U : E; }
 
 // Workspace layout (byte offsets), identical for every call with the same (T, E, K).
@@ -38,6 +41,9 @@ struct WsLayout {
   size_t slice_flags;  // uint64[slices]  look-back words of the slice kernel
   size_t loc_off;      // int32[U][E + 1] per-unit exclusive offsets of each expert
   size_t unit_buf;     // int2[T * K]     per-unit routes sorted by expert: (flat index, weight)
+  size_t unit_e;       // uint16[T * K]   the expert of each unit_buf entry
+  size_t adj;          // int32[U][E]     final row of unit u's first route of expert e, minus
+                       //                 that route's position in the unit's list
   size_t total;
 };
 
@@ -57,6 +63,10 @@ inline WsLayout ws_layout(int T, int E, int K) {
   o = align16(o + sizeof(int32_t) * static_cast<size_t>(U) * (E + 1));
   l.unit_buf = o;
   o = align16(o + 8 * static_cast<size_t>(T) * K);
+  l.unit_e = o;
+  o = align16(o + 2 * static_cast<size_t>(T) * K);
+  l.adj = o;
+  o = align16(o + sizeof(int32_t) * static_cast<size_t>(U) * E);
   l.total = o;
   return l;
 }
@@ -105,6 +115,7 @@ struct DecodeArgs {
 struct UnitOut {
   int32_t* loc_off;                 // [U][E + 1]
   int2* unit_buf;                   // [T * K]
+  uint16_t* unit_e;                 // [T * K]
   unsigned long long* slice_flags;  // [nslices], cleared for the slice kernel
   int32_t* unit_flags;              // [U]
   int nslices;
@@ -130,17 +141,15 @@ struct UnitArgs {
   const int32_t* ids;
   const float* w;
   int T, K, E, U, max_routes;
-  int32_t* loc_off;
-  int2* unit_buf;
-  unsigned long long* slice_flags;
-  int32_t* unit_flags;
-  int nslices;
+  UnitOut uo;
 };
 
 struct SliceArgs {
   int T, K, E, U, B, N, nslices;
   const int32_t* loc_off;
   const int2* unit_buf;
+  const uint16_t* unit_e;
+  int32_t* adj;
   unsigned long long* slice_flags;
   const int32_t* unit_flags;
   int32_t* sorted_ids;
@@ -156,6 +165,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st);
 cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st);
 cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st);
+cudaError_t launch_scatter(const SliceArgs& a, cudaStream_t st);
 cudaError_t launch_empty(int32_t* npp, int32_t* status, cudaStream_t st);
 
 // Shared memory of the multi-CTA route kernels for a given warp count.

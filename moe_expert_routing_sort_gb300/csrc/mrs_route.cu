@@ -395,8 +395,7 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
   }
   if (kSort) {
     __syncthreads();
-    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo.loc_off,
-                   a.uo.unit_buf, a.uo.slice_flags, a.uo.nslices, a.U);
+    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo, a.U);
     if (tid == 0) a.uo.unit_flags[u] = 0;
   }
 }
@@ -572,8 +571,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   }
   if (kSort) {
     __syncthreads();
-    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo.loc_off,
-                   a.uo.unit_buf, a.uo.slice_flags, a.uo.nslices, a.U);
+    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo, a.U);
     if (tid == 0) a.uo.unit_flags[u] = cta_flags & MOE_RS_DEVICE_WAIT_TIMEOUT;
   }
 }

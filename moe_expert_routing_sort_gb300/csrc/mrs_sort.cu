@@ -8,15 +8,19 @@
 // Phase 1 runs at the end of the kernel that produced the routes of a unit (a contiguous
 // token range, one CTA): unit_sort_tail() stable-sorts the unit's routes by expert in
 // shared memory and stores, per unit, the exclusive per-expert offsets loc[u][0..E] and
-// the sorted (flat index, weight) list.  It also clears the look-back flags of phase 2.
+// the sorted (flat index, weight, expert) list.  It also clears the look-back flags of
+// phase 2.
 //
-// Phase 2 (mrs_slices_kernel) gives every CTA a slice of experts: a prefix over units of
-// the slice's counts, the block_m-padded offsets inside the slice, a decoupled look-back
-// for the slice's base row (every slice publishes its padded size and sums those of the
-// slices before it), then a copy of every route to its final row, the padding rows and the
-// per-block expert ids.  Entries of one expert stay in
-// token-then-slot order by construction; no global atomics are used, and every wait is
-// bounded.
+// Phase 2a (mrs_slices_kernel) gives every CTA a slice of experts: a prefix over units of
+// the slice's counts, the block_m-padded offsets inside the slice and a decoupled
+// look-back for the slice's base row (every slice publishes its padded size and sums those
+// of the slices before it).  It stores, for every (unit, expert) pair with routes, the
+// final row of the pair's first route minus that route's position in the unit's list,
+// and writes the padding rows and the per-block expert ids.
+// Phase 2b (mrs_scatter_kernel), one CTA per unit, moves each route of the unit's list to
+// its final row: work is proportional to the unit's routes, however skewed the experts.
+// Entries of one expert stay in token-then-slot order by construction; no global atomics
+// are used, and every wait is bounded.
 #include "mrs_internal.h"
 #include "mrs_unit.cuh"
 #include "moe_route_sort.h"
@@ -48,9 +52,8 @@ __global__ void __launch_bounds__(kUnitThreads) mrs_unit_kernel(const UnitArgs a
     else if (e >= 0) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
-  unit_sort_tail(rid, rw, cnt, a.E, a.K, blockIdx.x, t0, t1, scratch, a.loc_off, a.unit_buf,
-                 a.slice_flags, a.nslices, a.U);
-  if (tid == 0) a.unit_flags[blockIdx.x] = bad;
+  unit_sort_tail(rid, rw, cnt, a.E, a.K, blockIdx.x, t0, t1, scratch, a.uo, a.U);
+  if (tid == 0) a.uo.unit_flags[blockIdx.x] = bad;
 }
 
 size_t unit_kernel_smem(int E, int max_routes) {
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   const int e0 = static_cast<int>(static_cast<long long>(c) * a.E / a.nslices);
   const int e1 = static_cast<int>(static_cast<long long>(c + 1) * a.E / a.nslices);
   const int ns = e1 - e0;
-  const int U = a.U, K = a.K, B = a.B;
+  const int U = a.U, B = a.B;
   int32_t* locs = reinterpret_cast<int32_t*>(smem);                  // [U][ns + 1]
   int32_t* seg = locs + static_cast<size_t>(U) * (ns + 1);            // [ns][U + 1] starts
   int32_t* tot = seg + static_cast<size_t>(ns) * (U + 1);             // [ns + 1] unpadded prefix
@@ -173,30 +176,12 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   }
   __syncthreads();
   const int base = base_s;
-  // copy: route q of the slice (expert-major, then unit, then rank) goes to
-  // base + soff[i] + (q - tot[i]); its (expert, unit) segment is found by binary search
-  const int nroutes = tot[ns];
-  for (int q = tid; q < nroutes; q += blockDim.x) {
-    int lo = 0, hi = ns - 1;  // expert: last i with tot[i] <= q
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (tot[mid] <= q) lo = mid; else hi = mid - 1;
-    }
-    const int i = lo;
-    const int qi = q - tot[i];
-    const int32_t* si = seg + i * (U + 1);
-    int ul = 0, uh = U - 1;  // unit: last u with si[u] <= qi
-    while (ul < uh) {
-      const int mid = (ul + uh + 1) >> 1;
-      if (si[mid] <= qi) ul = mid; else uh = mid - 1;
-    }
-    const int u = ul;
-    int t0, t1;
-    unit_range(u, a.T, U, t0, t1);
-    const int2 v = a.unit_buf[static_cast<size_t>(t0) * K + locs[u * (ns + 1) + i] + (qi - si[u])];
-    const int dst = base + soff[i] + qi;
-    a.sorted_ids[dst] = v.x;
-    a.sorted_w[dst] = __int_as_float(v.y);
+  // (unit, expert) pairs with routes: final row of the first one, minus its list position
+  for (int idx = tid; idx < U * ns; idx += blockDim.x) {
+    const int u = idx / ns, i = idx - u * ns;
+    const int l0 = locs[u * (ns + 1) + i];
+    if (locs[u * (ns + 1) + i + 1] > l0)
+      a.adj[static_cast<size_t>(u) * a.E + e0 + i] = base + soff[i] + seg[i * (U + 1) + u] - l0;
   }
   // padding rows and block owners
   for (int i = warp; i < ns; i += nwarps) {
@@ -218,6 +203,23 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
       *a.npp = base + soff[ns];
       *a.status = f;
     }
+  }
+}
+
+// ------------------------------------------------------------------ phase 2b: scatter
+__global__ void __launch_bounds__(kSliceThreads) mrs_scatter_kernel(const SliceArgs a) {
+  const int u = blockIdx.x;
+  int t0, t1;
+  unit_range(u, a.T, a.U, t0, t1);
+  const size_t r0 = static_cast<size_t>(t0) * a.K;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int n = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + a.E];  // routes placed
+  const int32_t* adj = a.adj + static_cast<size_t>(u) * a.E;
+  for (int p = threadIdx.x; p < n; p += blockDim.x) {
+    const int2 v = a.unit_buf[r0 + p];
+    const int dst = adj[a.unit_e[r0 + p]] + p;
+    a.sorted_ids[dst] = v.x;
+    a.sorted_w[dst] = __int_as_float(v.y);
   }
 }
 
@@ -243,6 +245,20 @@ cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, mrs_slices_kernel, a);
+}
+
+cudaError_t launch_scatter(const SliceArgs& a, cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.U);
+  cfg.blockDim = dim3(kSliceThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mrs_scatter_kernel, a);
 }
 
 // ------------------------------------------------------------------ empty call

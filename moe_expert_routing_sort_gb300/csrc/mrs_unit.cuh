@@ -49,11 +49,14 @@ __device__ __forceinline__ void block_exclusive_scan(const int32_t* v, int32_t* 
 // Phase 1 for unit u (see the file comment).  rid/rw: the unit's routes in shared memory,
 // index (t - t0) * K + k; an id outside [0, E) is not placed.  cnt: the unit's per-expert
 // counts of placed routes (shared memory, may be overwritten).  scratch: shared memory of
-// unit_scratch_bytes(E), free for use.  All threads of the CTA call this.
-__device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* rw, int32_t* cnt, int E, int K,
-                               int u, int t0, int t1, unsigned char* scratch,
-                               int32_t* loc_off_g, int2* unit_buf_g,
-                               unsigned long long* slice_flags, int nslices, int U) {
+// unit_scratch_bytes(E), free for use.  Writes the unit's offsets, its sorted routes and
+// their experts to uo.  All threads of the CTA call this.
+__device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* rw, int32_t* cnt,
+                                               int E, int K, int u, int t0, int t1,
+                                               unsigned char* scratch, const UnitOut& uo,
+                                               int U) {
+  unsigned long long* slice_flags = uo.slice_flags;
+  const int nslices = uo.nslices;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   unsigned* masks = reinterpret_cast<unsigned*>(scratch);  // one bit per token of a 32-token tile
@@ -69,7 +72,7 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
   for (int c = u + tid * U; c < nslices; c += blockDim.x * U) slice_flags[c] = 0ull;
 
   block_exclusive_scan(cnt, loc, E, misc);
-  int32_t* loc_g = loc_off_g + static_cast<size_t>(u) * (E + 1);
+  int32_t* loc_g = uo.loc_off + static_cast<size_t>(u) * (E + 1);
   for (int e = tid; e <= E; e += blockDim.x) loc_g[e] = loc[e];
   for (int e = tid; e < E; e += blockDim.x) {
     run[e] = loc[e];
@@ -79,7 +82,8 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
   __syncthreads();
 
   // tiles of 32 tokens: warp w takes tokens w, w + nwarps, ... of the tile, lane k slot k
-  int2* out = unit_buf_g + static_cast<size_t>(t0) * K;
+  int2* out = uo.unit_buf + static_cast<size_t>(t0) * K;
+  uint16_t* out_e = uo.unit_e + static_cast<size_t>(t0) * K;
   const int nt_all = t1 - t0;
   for (int tb = 0; tb < nt_all; tb += 32) {
     const int nt = min(32, nt_all - tb);
@@ -98,6 +102,7 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
         if (e >= 0 && e < E) {
           const int pos = run[e] + __popc(masks[e] & ((1u << tl) - 1u));
           out[pos] = make_int2(t0 * K + r, __float_as_int(rw[r]));
+          out_e[pos] = static_cast<uint16_t>(e);
         }
       }
       __syncthreads();
@@ -130,8 +135,9 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
           int p0 = 0;
           if (valid) {
             p0 = run[e];
-            out[p0 + __popc(peers & lanemask_lt(lane))] =
-                make_int2(t0 * K + r0 + i, __float_as_int(rw[r0 + i]));
+            const int pos = p0 + __popc(peers & lanemask_lt(lane));
+            out[pos] = make_int2(t0 * K + r0 + i, __float_as_int(rw[r0 + i]));
+            out_e[pos] = static_cast<uint16_t>(e);
           }
           __syncwarp();
           if (valid && (peers >> lane) == 1u) run[e] = p0 + __popc(peers);
