@@ -431,6 +431,12 @@ __device__ __forceinline__ void mbar_init(unsigned long long* mbar, uint32_t cou
                : "memory");
 }
 
+// Ends the life of an mbarrier (no arrivals or copies pending on it) so that its shared
+// memory can be used for something else.
+__device__ __forceinline__ void mbar_inval(unsigned long long* mbar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(mbar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

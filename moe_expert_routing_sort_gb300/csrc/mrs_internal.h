@@ -32,7 +32,12 @@ inline int units_for_shape(int T, int K, int sms) {
 }
 // The largest unit count of any device: the workspace is sized for it.
 inline int units_bound(int T, int K) { return units_for_shape(T, K, kMaxUnitSms); }
-inline int slices_for(int U, int E) { return U < E ? U : E; }
+// Expert slices of the sort step: one per unit, at most one per expert and kMaxSlices.
+constexpr int kMaxSlices = 256;
+inline int slices_for(int U, int E) {
+  const int n = U < E ? U : E;
+  return n < kMaxSlices ? n : kMaxSlices;
+}
 
 // Workspace layout (byte offsets), identical for every call with the same (T, E, K).
 struct WsLayout {
@@ -42,7 +47,7 @@ struct WsLayout {
   size_t loc_off;      // int32[U][E + 1] per-unit exclusive offsets of each expert
   size_t unit_buf;     // int2[T * K]     per-unit routes sorted by expert: (flat index, weight)
   size_t unit_e;       // uint16[T * K]   the expert of each unit_buf entry
-  size_t adj;          // int32[U][E]     final row of unit u's first route of expert e, minus
+  size_t adj;          // int32[E][U]     final row of unit u's first route of expert e, minus
                        //                 that route's position in the unit's list
   size_t total;
 };

@@ -484,6 +484,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
                 static_cast<uint32_t>(n) * static_cast<uint32_t>(E) * 2u, &mbar[b]);
   };
 
+  // the sort kernel that follows may take SMs as this grid's blocks exit (it waits for all)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // start this warp's first copies before anything else
   if (lane == 0) {
     mbar_init(&mbar[0], 1);
@@ -559,15 +561,21 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
       }
     }
   }
+  bool drained = true;
   if (!ok) {
     // a copy did not complete in time: report it, then give the copies still in flight a
     // bounded chance to land before their buffers are reused or the CTA exits
     if (lane == 0) atomicOr(&cta_flags, MOE_RS_DEVICE_WAIT_TIMEOUT);
     for (int k = consumed; k < issued; ++k) {
       const int b = (nbuf == 2) ? (k & 1) : 0;
-      mbar_wait_bounded(&mbar[b], (phase >> b) & 1u);
+      drained &= mbar_wait_bounded(&mbar[b], (phase >> b) & 1u);
       phase ^= 1u << b;
     }
+  }
+  // the barriers' memory is reused by the sort step below
+  if (drained && lane == 0) {
+    mbar_inval(&mbar[0]);
+    mbar_inval(&mbar[1]);
   }
   if (kSort) {
     __syncthreads();

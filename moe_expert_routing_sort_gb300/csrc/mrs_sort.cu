@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kUnitThreads) mrs_unit_kernel(const UnitArgs a
   unsigned char* scratch = smem + 2 * align16(sizeof(int32_t) * a.max_routes) +
                            align16(sizeof(int32_t) * (a.E + 1));
   __shared__ int bad;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) bad = 0;
   for (int e = tid; e < a.E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -73,14 +74,14 @@ cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st) {
 // ------------------------------------------------------------------ phase 2: slices
 constexpr unsigned long long kFlagReady = 1ull << 32;  // low word = the slice's padded rows
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceArgs a) {
@@ -92,33 +93,43 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   const int e1 = static_cast<int>(static_cast<long long>(c + 1) * a.E / a.nslices);
   const int ns = e1 - e0;
   const int U = a.U, B = a.B;
-  int32_t* locs = reinterpret_cast<int32_t*>(smem);                  // [U][ns + 1]
-  int32_t* seg = locs + static_cast<size_t>(U) * (ns + 1);            // [ns][U + 1] starts
-  int32_t* tot = seg + static_cast<size_t>(ns) * (U + 1);             // [ns + 1] unpadded prefix
+  int32_t* locs = reinterpret_cast<int32_t*>(smem);                  // [ns + 1][U] (by expert)
+  int32_t* seg = locs + static_cast<size_t>(ns + 1) * U;             // [ns][U] starts
+  int32_t* tot = seg + static_cast<size_t>(ns) * U;                  // [ns + 1] unpadded prefix
   int32_t* soff = tot + ns + 1;                                       // [ns + 1] padded prefix
   __shared__ int32_t base_s, flags_s;
 
   // everything below reads what the previous kernel wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  for (int idx = tid; idx < U * (ns + 1); idx += blockDim.x) {
-    const int u = idx / (ns + 1), i = idx - u * (ns + 1);
-    locs[idx] = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + e0 + i];
+  if (tid == 0) {
+    base_s = 0;
+    flags_s = 0;
+  }
+  // the slice's columns of the per-unit offsets (a warp reads 4 units' pieces at a time),
+  // stored by expert
+  for (int u0 = 4 * warp; u0 < U; u0 += 4 * nwarps) {
+    for (int i = lane; i <= ns; i += 32) {
+      int v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (u0 + k < U) v[k] = a.loc_off[static_cast<size_t>(u0 + k) * (a.E + 1) + e0 + i];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (u0 + k < U) locs[i * U + u0 + k] = v[k];
+    }
   }
   __syncthreads();
-  // per expert of the slice: exclusive prefix over units of its counts (warp per expert)
+  // per expert of the slice (warp per expert): exclusive prefix over units of its counts
   for (int i = warp; i < ns; i += nwarps) {
-    const int per = (U + 31) / 32;
-    const int ulo = min(U, lane * per), uhi = min(U, ulo + per);
-    int sum = 0;
-    for (int u = ulo; u < uhi; ++u) sum += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
-    const int incl = warp_inclusive_sum(sum, lane);
-    int r = incl - sum;
-    for (int u = ulo; u < uhi; ++u) {
-      seg[i * (U + 1) + u] = r;
-      r += locs[u * (ns + 1) + i + 1] - locs[u * (ns + 1) + i];
+    int run = 0;
+    for (int u0 = 0; u0 < U; u0 += 32) {
+      const int u = u0 + lane;
+      const int cnt = (u < U) ? locs[(i + 1) * U + u] - locs[i * U + u] : 0;
+      const int incl = warp_inclusive_sum(cnt, lane);
+      if (u < U) seg[i * U + u] = run + incl - cnt;
+      run += __shfl_sync(kFull, incl, 31);
     }
-    if (lane == 31) seg[i * (U + 1) + U] = incl;
+    if (lane == 0) tot[i] = run;  // the expert's count, for now
   }
   __syncthreads();
   // unpadded and padded prefixes over the slice's experts (one warp)
@@ -126,10 +137,11 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
     int run = 0, prun = 0;
     for (int i0 = 0; i0 < ns; i0 += 32) {
       const int i = i0 + lane;
-      const int cnt = (i < ns) ? seg[i * (U + 1) + U] : 0;
+      const int cnt = (i < ns) ? tot[i] : 0;
       const int pad = (cnt + B - 1) & ~(B - 1);
       const int ci = warp_inclusive_sum(cnt, lane);
       const int pi = warp_inclusive_sum(pad, lane);
+      __syncwarp();
       if (i < ns) {
         tot[i] = run + ci - cnt;
         soff[i] = prun + pi - pad;
@@ -140,48 +152,52 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
     if (lane == 0) {
       tot[ns] = run;
       soff[ns] = prun;
-      flags_s = 0;
+      // publish this slice's padded size for the slices after it (the word is all they
+      // read from this slice, so no ordering with other memory is needed)
+      st_relaxed_u64(&a.slice_flags[c], kFlagReady | static_cast<uint32_t>(prun));
     }
   }
-  __syncthreads();
-  // this slice's first row = sum of the padded sizes of all earlier slices: publish mine,
-  // then read every earlier slice's word in parallel (one warp; bounded wait)
+  // this slice's first row = sum of the padded sizes of all earlier slices: warp 0 polls
+  // all their words at once (lane l holds slices l, l + 32, ...; bounded wait)
   if (warp == 0) {
-    if (lane == 0) st_release_u64(&a.slice_flags[c], kFlagReady | static_cast<uint32_t>(soff[ns]));
-    int base = 0;
-    bool ok = true;
     const unsigned long long t_start = globaltimer_ns();
-    for (int p0 = 0; p0 < c; p0 += 32) {
-      const int p = p0 + lane;
-      unsigned long long f = 0ull;
-      for (;;) {
-        f = (p < c) ? ld_acquire_u64(&a.slice_flags[p]) : kFlagReady;
-        const bool missing = (f & kFlagReady) == 0ull;
-        if (!__any_sync(kFull, missing)) break;
-        if (globaltimer_ns() - t_start > kWaitLimitNs) {
-          ok = false;
-          break;
-        }
-      }
-      if (!ok) break;
-      int v = (p < c) ? static_cast<int>(f & 0xffffffffull) : 0;
+    unsigned long long f[kMaxSlices / 32];
+    bool ok = true;
+    for (;;) {
+      bool missing = false;
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
-      base += v;
+      for (int k = 0; k < kMaxSlices / 32; ++k) {
+        const int p = lane + 32 * k;
+        f[k] = (p < c) ? ld_relaxed_u64(&a.slice_flags[p]) : kFlagReady;
+        missing |= (f[k] & kFlagReady) == 0ull;
+      }
+      if (!__any_sync(kFull, missing)) break;
+      if (globaltimer_ns() - t_start > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
     }
+    int v = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxSlices / 32; ++k)
+      v += (lane + 32 * k < c) ? static_cast<int>(f[k] & 0xffffffffull) : 0;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
     if (lane == 0) {
-      base_s = base;
+      base_s = v;
       flags_s = ok ? 0 : MOE_RS_DEVICE_WAIT_TIMEOUT;
     }
   }
   __syncthreads();
   const int base = base_s;
-  // (unit, expert) pairs with routes: final row of the first one, minus its list position
-  for (int idx = tid; idx < U * ns; idx += blockDim.x) {
-    const int u = idx / ns, i = idx - u * ns;
-    const int l0 = locs[u * (ns + 1) + i];
-    if (locs[u * (ns + 1) + i + 1] > l0)
-      a.adj[static_cast<size_t>(u) * a.E + e0 + i] = base + soff[i] + seg[i * (U + 1) + u] - l0;
+  // (expert, unit) pairs with routes: final row of the first one, minus its list position
+  for (int i = warp; i < ns; i += nwarps) {
+    int32_t* adj = a.adj + static_cast<size_t>(e0 + i) * U;
+    const int b_i = base + soff[i];
+    for (int u = lane; u < U; u += 32) {
+      const int l0 = locs[i * U + u];
+      if (locs[(i + 1) * U + u] > l0) adj[u] = b_i + seg[i * U + u] - l0;
+    }
   }
   // padding rows and block owners
   for (int i = warp; i < ns; i += nwarps) {
@@ -214,10 +230,9 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_scatter_kernel(const SliceA
   const size_t r0 = static_cast<size_t>(t0) * a.K;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + a.E];  // routes placed
-  const int32_t* adj = a.adj + static_cast<size_t>(u) * a.E;
   for (int p = threadIdx.x; p < n; p += blockDim.x) {
     const int2 v = a.unit_buf[r0 + p];
-    const int dst = adj[a.unit_e[r0 + p]] + p;
+    const int dst = a.adj[static_cast<size_t>(a.unit_e[r0 + p]) * a.U + u] + p;
     a.sorted_ids[dst] = v.x;
     a.sorted_w[dst] = __int_as_float(v.y);
   }
@@ -225,8 +240,8 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_scatter_kernel(const SliceA
 
 size_t slices_smem_bytes(int U, int E, int nslices) {
   const int ns = (E + nslices - 1) / nslices;
-  return sizeof(int32_t) * (static_cast<size_t>(U) * (ns + 1) +
-                            static_cast<size_t>(ns) * (U + 1) + 2 * static_cast<size_t>(ns) + 2);
+  return sizeof(int32_t) * (static_cast<size_t>(ns + 1) * U + static_cast<size_t>(ns) * U +
+                            2 * static_cast<size_t>(ns) + 2);
 }
 
 cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st) {
