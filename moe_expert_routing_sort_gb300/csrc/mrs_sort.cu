@@ -80,9 +80,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 
 __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -153,8 +150,9 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
       tot[ns] = run;
       soff[ns] = prun;
       // publish this slice's padded size for the slices after it (the word is all they
-      // read from this slice, so no ordering with other memory is needed)
-      st_relaxed_u64(&a.slice_flags[c], kFlagReady | static_cast<uint32_t>(prun));
+      // read from this slice, so no ordering with other memory is needed); an atomic
+      // exchange is performed at L2 at once, where the polls look
+      atomicExch(&a.slice_flags[c], kFlagReady | static_cast<uint32_t>(prun));
     }
   }
   // this slice's first row = sum of the padded sizes of all earlier slices: warp 0 polls
