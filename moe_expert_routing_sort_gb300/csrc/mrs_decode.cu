@@ -50,6 +50,8 @@ __device__ __forceinline__ void warp_top2_merge(float& m1, float& m2) {
 __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
   __shared__ DecodeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();
   const int E = a.E, G = a.G, g = a.g, Kg = a.Kg, K = a.K, B = a.B;
   const bool grouped = Kg < G;
 
@@ -270,8 +272,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  mrs_decode_kernel<<<1, kDecodeThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(mrs_decode_kernel, dim3(1), dim3(kDecodeThreads), 0, st, a);
 }
 
 }  // namespace mrs

@@ -90,6 +90,14 @@ __device__ __forceinline__ float warp_kth_largest(float v, int k, int lane) {
   return __shfl_sync(kFull, v, __ffs(b) - 1);
 }
 
+// Programmatic dependent launch: wait until the previous kernel of the stream has completed
+// and its memory is visible (returns at once when there is none), and let the next kernel
+// of the stream be scheduled early (it waits the same way).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ proxy score
 // Cheap stand-in for the selection key, shifted by the constant -0.5 that every expert
 // shares: p = 0.5 * tanh.approx(0.5 x) + bias.  0.5 + 0.5 tanh(x / 2) is the logistic

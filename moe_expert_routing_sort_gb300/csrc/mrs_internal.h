@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "mrs_device.cuh"
 #include "mrs_seg.cuh"
@@ -163,6 +164,25 @@ struct SliceArgs {
   int32_t* npp;
   int32_t* status;
 };
+
+// Launch with programmatic dependent launch allowed: the kernel may be scheduled while the
+// previous kernel of the stream is finishing; every kernel launched this way executes
+// griddepcontrol.wait (pdl_wait) before it touches global memory, so stream order holds.
+template <class... Params, class... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st);

@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
   int32_t* off = reinterpret_cast<int32_t*>(smem + a.lay.off);
   int32_t* misc = reinterpret_cast<int32_t*>(smem + a.lay.misc);  // [0] flags, [4..37] scan
   unsigned* masks = reinterpret_cast<unsigned*>(smem + a.lay.masks);  // [2][E]: tokens 0-31, 32-63
+  pdl_trigger();
+  pdl_wait();
 
   if (!kSortOnly) {
     // -------------------------------------------------------------- route step
@@ -286,14 +288,14 @@ cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st) {
     err = cudaFuncSetAttribute(mrs_small_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    mrs_small_kernel<true><<<1, kSmallThreads, smem, st>>>(a);
+    err = launch_pdl(mrs_small_kernel<true>, dim3(1), dim3(kSmallThreads), smem, st, a);
   } else {
     err = cudaFuncSetAttribute(mrs_small_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    mrs_small_kernel<false><<<1, kSmallThreads, smem, st>>>(a);
+    err = launch_pdl(mrs_small_kernel<false>, dim3(1), dim3(kSmallThreads), smem, st, a);
   }
-  return cudaGetLastError();
+  return err;
 }
 
 // --------------------------------------------------------- multi-CTA route, any shape
@@ -343,6 +345,8 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
   float* sv = key + E;
   WarpScratch& scr =
       *reinterpret_cast<WarpScratch*>(mine + align16(sizeof(float) * 2 * (size_t)E));
+  pdl_trigger();
+  pdl_wait();
 
   for (int e = tid; e < E; e += blockDim.x) {
     bias_s[e] = a.bias[e];
@@ -485,7 +489,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   };
 
   // the sort kernel that follows may take SMs as this grid's blocks exit (it waits for all)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();
   // start this warp's first copies before anything else
   if (lane == 0) {
     mbar_init(&mbar[0], 1);
@@ -589,8 +594,8 @@ static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st
   cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort, LT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  mrs_route_seg_kernel<kSort, LT><<<a.U, a.nwarps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(mrs_route_seg_kernel<kSort, LT>, dim3(a.U), dim3(a.nwarps * 32), smem, st,
+                    a);
 }
 
 template <bool kSort>
@@ -606,14 +611,14 @@ cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {
     err = cudaFuncSetAttribute(mrs_route_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    mrs_route_kernel<true><<<a.U, threads, smem, st>>>(a);
+    err = launch_pdl(mrs_route_kernel<true>, dim3(a.U), dim3(threads), smem, st, a);
   } else {
     err = cudaFuncSetAttribute(mrs_route_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    mrs_route_kernel<false><<<a.U, threads, smem, st>>>(a);
+    err = launch_pdl(mrs_route_kernel<false>, dim3(a.U), dim3(threads), smem, st, a);
   }
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace mrs

@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(kUnitThreads) mrs_unit_kernel(const UnitArgs a
   unsigned char* scratch = smem + 2 * align16(sizeof(int32_t) * a.max_routes) +
                            align16(sizeof(int32_t) * (a.E + 1));
   __shared__ int bad;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();
   if (tid == 0) bad = 0;
   for (int e = tid; e < a.E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -67,8 +68,7 @@ cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st) {
   cudaError_t err = cudaFuncSetAttribute(mrs_unit_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  mrs_unit_kernel<<<a.U, kUnitThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(mrs_unit_kernel, dim3(a.U), dim3(kUnitThreads), smem, st, a);
 }
 
 // ------------------------------------------------------------------ phase 2: slices
@@ -276,13 +276,13 @@ cudaError_t launch_scatter(const SliceArgs& a, cudaStream_t st) {
 
 // ------------------------------------------------------------------ empty call
 __global__ void mrs_empty_kernel(int32_t* npp, int32_t* status) {
+  pdl_wait();
   *npp = 0;
   if (status) *status = 0;
 }
 
 cudaError_t launch_empty(int32_t* npp, int32_t* status, cudaStream_t st) {
-  mrs_empty_kernel<<<1, 1, 0, st>>>(npp, status);
-  return cudaGetLastError();
+  return launch_pdl(mrs_empty_kernel, dim3(1), dim3(1), 0, st, npp, status);
 }
 
 }  // namespace mrs
