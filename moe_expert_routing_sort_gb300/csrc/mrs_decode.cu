@@ -1,15 +1,22 @@
 // mrs_decode.cu -- the whole route-sort path for one token (decode), one CTA, one launch.
 //
-// Latency-oriented: every step uses the whole CTA and the sort needs no scan over experts.
-//   scores    thread t owns experts t, t + 512, ...; one DRAM round trip (logits and bias)
-//   groups    warp j scores group j (sum of its two best keys) from shared memory
-//   kept      every warp ranks the G group scores itself (no barrier needed)
-//   threshold each warp's two best candidates are samples; the K-th best sample is a lower
-//             bound on the K-th best candidate key
-//   survivors candidates at or above it are compacted and ranked in parallel by counting
+// Latency-oriented: three block barriers from the logits to the outputs.
+//   rows      group j is held by TPG consecutive threads (TPG = the largest power of two
+//             with TPG * G <= 512): thread i of the group owns experts j*g + i + TPG*r;
+//             one DRAM round trip brings logits and bias, exact scores stay in registers
+//   groups    a shuffle tree over each group's threads gives, at the 8-thread level, the
+//             top-2 of every 8-thread segment (threshold samples) and, at the top, the
+//             group's top-2 (one partial per warp when a group spans several warps)
+//   ---- barrier
+//   kept      every warp merges the partials and ranks the G group scores itself
+//   threshold at least ceil(K/2) kept segments hold two keys >= t2, so at least K kept keys
+//             are >= t2 (and the K-th best segment maximum is also such a bound)
+//   survivors kept keys at or above it are compacted (warp-aggregated slots)
+//   ---- barrier
+//   rank      warp 0 ranks the survivors by counting and writes the K slots
 //   sort      one token: each selected expert gets one route, so expert id_k owns block
 //             (number of selected ids below id_k), its row 0 is route k and rows 1..B-1 are
-//             padding; npp = K * B
+//             padding (written at the start, as they depend on nothing); npp = K * B
 // Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary --
 // the B1 (batch-one) route-sort: FP32 logits, correction bias, grouped top-k, both sort
 // phases, in one kernel.
@@ -20,179 +27,186 @@ namespace mrs {
 
 constexpr int kDecodeThreads = 512;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
-constexpr int kDecodeEpt = kMaxExperts / kDecodeThreads;  // experts per thread, at most
-constexpr int kDecodeCap = 128;                            // survivors kept for ranking
+constexpr int kDecodeEpt = 16;   // experts per thread, at most (g <= TPG * kDecodeEpt)
+constexpr int kDecodeCap = 128;  // survivors kept for ranking
+constexpr int kDecodeSamples = kDecodeThreads / 8;
 
 struct DecodeSmem {
-  float key[kMaxExperts];
-  float s[kMaxExperts];
-  float gs[kMaxGroups];
-  float samples[2 * kDecodeWarps];
+  float samp1[kDecodeSamples], samp2[kDecodeSamples];  // 8-thread segments' top-2
+  float part1[64], part2[64];                          // per-group partial top-2
   unsigned long long cand[kDecodeCap];
   float cand_s[kDecodeCap];
   unsigned long long wbest[kDecodeWarps];
   float wbest_s[kDecodeWarps];
-  int sel_id[kMaxTopk];
-  float sel_s[kMaxTopk];
+  alignas(16) int sel_id[kMaxTopk];
+  alignas(16) float sel_s[kMaxTopk];
   int count;
 };
 
-__device__ __forceinline__ void warp_top2_merge(float& m1, float& m2) {
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) {
-    const float o1 = __shfl_xor_sync(kFull, m1, d);
-    const float o2 = __shfl_xor_sync(kFull, m2, d);
-    m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
-    m1 = fmaxf(m1, o1);
-  }
+__device__ __forceinline__ void top2_merge_xor(float& m1, float& m2, int d) {
+  const float o1 = __shfl_xor_sync(kFull, m1, d);
+  const float o2 = __shfl_xor_sync(kFull, m2, d);
+  m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+  m1 = fmaxf(m1, o1);
+}
+
+// Threads per group for G groups: the largest power of two with TPG * G <= 512 (>= 8).
+__host__ __device__ inline int decode_tpg(int G) {
+  int t = 512;
+  while (t * G > kDecodeThreads) t >>= 1;
+  return t;
 }
 
 __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
   __shared__ DecodeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.G, g = a.g, Kg = a.Kg, K = a.K, B = a.B;
+  const int TPG = decode_tpg(G);
+  const int P = TPG > 32 ? TPG / 32 : 1;  // partials per group
+  const int j = tid / TPG, i = tid - j * TPG;
+  const bool in_group = j < G;
+  // experts per thread: 2 * 256 / G < TPG, so g = E / G <= 4096 / G < 16 * TPG
+  const int R = (g + TPG - 1) / TPG;
   pdl_trigger();
   pdl_wait();
-  const int E = a.E, G = a.G, g = a.g, Kg = a.Kg, K = a.K, B = a.B;
-  const bool grouped = Kg < G;
 
-  // ---- exact scores and keys (one DRAM round trip)
+  // ---- loads (one DRAM round trip); rows that depend on nothing meanwhile
   float key[kDecodeEpt], sv[kDecodeEpt];
   {
     uint16_t x[kDecodeEpt];
     float b[kDecodeEpt];
 #pragma unroll
-    for (int i = 0; i < kDecodeEpt; ++i) {
-      const int e = tid + kDecodeThreads * i;
-      if (e < E) {
-        x[i] = a.logits[e];
-        b[i] = a.bias[e];
+    for (int r = 0; r < kDecodeEpt; ++r) {
+      if (r >= R) break;
+      const int li = i + TPG * r;
+      if (in_group && li < g) {
+        x[r] = a.logits[j * g + li];
+        b[r] = a.bias[j * g + li];
       }
     }
-#pragma unroll
-    for (int i = 0; i < kDecodeEpt; ++i) {
-      const int e = tid + kDecodeThreads * i;
-      key[i] = -INFINITY;
-      sv[i] = 0.0f;
-      if (e < E) {
-        sv[i] = exact_score(bf16_bits_to_float(x[i]));
-        key[i] = __fadd_rn(sv[i], b[i]);
-        sm.key[e] = key[i];
-        sm.s[e] = sv[i];
+    for (int p = tid; p < K * B; p += kDecodeThreads) {
+      if ((p & (B - 1)) != 0) {
+        a.sorted_ids[p] = K;  // sentinel T * K with T = 1
+        a.sorted_w[p] = 0.0f;
       }
+    }
+    if (tid == 0) {
+      *a.npp = K * B;
+      *a.status = 0;
+      sm.count = 0;
+    }
+    float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kDecodeEpt; ++r) {
+      const int li = i + TPG * r;
+      key[r] = -INFINITY;
+      sv[r] = 0.0f;
+      if (r < R && in_group && li < g) {
+        sv[r] = exact_score(bf16_bits_to_float(x[r]));
+        key[r] = __fadd_rn(sv[r], b[r]);
+        t2 = fmaxf(t2, fminf(t1, key[r]));
+        t1 = fmaxf(t1, key[r]);
+      }
+    }
+    // ---- shuffle tree: 8-thread segments (samples), then the group (partials)
+    top2_merge_xor(t1, t2, 1);
+    top2_merge_xor(t1, t2, 2);
+    top2_merge_xor(t1, t2, 4);
+    if ((tid & 7) == 0) {
+      sm.samp1[tid >> 3] = t1;
+      sm.samp2[tid >> 3] = t2;
+    }
+    for (int d = 8; d < 32 && d < TPG; d <<= 1) top2_merge_xor(t1, t2, d);
+    if (in_group && (i & 31 & (TPG - 1)) == 0) {
+      const int p = (TPG > 32) ? (i >> 5) : 0;
+      sm.part1[j * P + p] = t1;
+      sm.part2[j * P + p] = t2;
     }
   }
-  if (tid == 0) sm.count = 0;
   __syncthreads();
 
-  // ---- group scores (warp per group), then every warp ranks the groups itself
-  if (grouped) {
-    for (int j = warp; j < G; j += kDecodeWarps) {
-      float m1 = -INFINITY, m2 = -INFINITY;
-      for (int i = lane; i < g; i += 32) {
-        const float v = sm.key[j * g + i];
-        m2 = fmaxf(m2, fminf(m1, v));
-        m1 = fmaxf(m1, v);
-      }
-      warp_top2_merge(m1, m2);
-      if (lane == 0) sm.gs[j] = (g >= 2) ? __fadd_rn(m1, m2) : m1;
-    }
-    __syncthreads();
-  }
+  // ---- group scores and kept groups, by every warp (lane l holds groups l and l + 32)
   unsigned km0 = 0xffffffffu, km1 = 0xffffffffu;
-  if (grouped) {
-    bool k0 = false, k1 = false;
-    if (lane < G) {
-      const float v = sm.gs[lane];
-      int r = 0;
-      for (int jj = 0; jj < G; ++jj) {
-        const float o = sm.gs[jj];
-        r += (o > v || (o == v && jj < lane)) ? 1 : 0;
-      }
-      k0 = r < Kg;
-    }
-    if (lane + 32 < G) {
-      const float v = sm.gs[lane + 32];
-      int r = 0;
-      for (int jj = 0; jj < G; ++jj) {
-        const float o = sm.gs[jj];
-        r += (o > v || (o == v && jj < lane + 32)) ? 1 : 0;
-      }
-      k1 = r < Kg;
-    }
-    km0 = __ballot_sync(kFull, k0);
-    km1 = __ballot_sync(kFull, k1);
-  }
-
-  // ---- candidates; each warp's two best are threshold samples
-  bool cand[kDecodeEpt];
-  float t1 = -INFINITY, t2 = -INFINITY;
+  if (Kg < G) {
+    float gs[2];
 #pragma unroll
-  for (int i = 0; i < kDecodeEpt; ++i) {
-    const int e = tid + kDecodeThreads * i;
-    bool c = e < E;
-    if (c && grouped) {
-      const int j = e / g;
-      c = ((j < 32 ? (km0 >> j) : (km1 >> (j - 32))) & 1u) != 0u;
+    for (int h = 0; h < 2; ++h) {
+      const int l = lane + 32 * h;
+      gs[h] = -INFINITY;
+      if (l < G) {
+        float m1 = -INFINITY, m2 = -INFINITY;
+        for (int p = 0; p < P; ++p) {
+          const float o1 = sm.part1[l * P + p], o2 = sm.part2[l * P + p];
+          m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+          m1 = fmaxf(m1, o1);
+        }
+        gs[h] = (g >= 2) ? __fadd_rn(m1, m2) : m1;
+      }
     }
-    cand[i] = c;
-    if (c) {
-      t2 = fmaxf(t2, fminf(t1, key[i]));
-      t1 = fmaxf(t1, key[i]);
+    int rk0 = 0, rk1 = 0;
+    for (int m = 0; m < G; ++m) {
+      const float o = __shfl_sync(kFull, (m < 32) ? gs[0] : gs[1], m & 31);
+      rk0 += (o > gs[0] || (o == gs[0] && m < lane)) ? 1 : 0;
+      rk1 += (o > gs[1] || (o == gs[1] && m < lane + 32)) ? 1 : 0;
     }
+    km0 = __ballot_sync(kFull, lane < G && rk0 < Kg);
+    km1 = __ballot_sync(kFull, lane + 32 < G && rk1 < Kg);
   }
-  warp_top2_merge(t1, t2);
-  if (lane == 0) {
-    sm.samples[2 * warp] = t1;
-    sm.samples[2 * warp + 1] = t2;
-  }
-  __syncthreads();
-  // every warp: the K-th best of the 32 samples (distinct candidates); -inf if fewer
+  auto kept_group = [&](int grp) {
+    return ((grp < 32 ? (km0 >> grp) : (km1 >> (grp - 32))) & 1u) != 0u;
+  };
+
+  // ---- threshold from the kept segments' samples (segment q covers threads 8q .. 8q+7)
   float tau;
   {
-    const float v = sm.samples[lane];
-    int r = 0;
-#pragma unroll
-    for (int m = 0; m < 2 * kDecodeWarps; ++m) {
-      const float o = sm.samples[m];
-      r += (o > v || (o == v && m < lane)) ? 1 : 0;
-    }
-    const unsigned hit = __ballot_sync(kFull, r == K - 1);
-    tau = __shfl_sync(kFull, v, __ffs(hit) - 1);
-    if (!(tau > -INFINITY)) tau = -INFINITY;
+    const int q0 = lane, q1 = lane + 32;
+    const int g0 = (8 * q0) / TPG, g1 = (8 * q1) / TPG;
+    const bool k0 = g0 < G && kept_group(g0), k1 = g1 < G && kept_group(g1);
+    const float ninf = -INFINITY;
+    tau = seg_kth_desc2<32>(k0 ? sm.samp2[q0] : ninf, k1 ? sm.samp2[q1] : ninf, lane,
+                            (K - 1) >> 1);
+    if (__any_sync(kFull, tau == -INFINITY))
+      tau = fmaxf(tau, seg_kth_desc2<32>(k0 ? sm.samp1[q0] : ninf, k1 ? sm.samp1[q1] : ninf,
+                                         lane, K - 1));
   }
 
-  // ---- survivors: candidates with key >= tau, compacted (warp-aggregated slots)
+  // ---- survivors: kept keys >= tau, compacted (warp-aggregated slots)
+  const bool mine_kept = in_group && kept_group(j);
 #pragma unroll
-  for (int i = 0; i < kDecodeEpt; ++i) {
-    const bool sv_ok = cand[i] && key[i] >= tau;
-    const unsigned b = __ballot_sync(kFull, sv_ok);
-    if (b) {
+  for (int r = 0; r < kDecodeEpt; ++r) {
+    if (r >= R) break;
+    const bool s_ok = mine_kept && key[r] >= tau;
+    const unsigned bl = __ballot_sync(kFull, s_ok);
+    if (bl) {
       int base = 0;
-      if (lane == 0) base = atomicAdd(&sm.count, __popc(b));
+      if (lane == 0) base = atomicAdd(&sm.count, __popc(bl));
       base = __shfl_sync(kFull, base, 0);
-      if (sv_ok) {
-        const int pos = base + __popc(b & lanemask_lt(lane));
+      if (s_ok) {
+        const int pos = base + __popc(bl & lanemask_lt(lane));
         if (pos < kDecodeCap) {
-          const int e = tid + kDecodeThreads * i;
-          sm.cand[pos] = composite(key[i], e);
-          sm.cand_s[pos] = sv[i];
+          sm.cand[pos] = composite(key[r], j * g + i + TPG * r);
+          sm.cand_s[pos] = sv[r];
         }
       }
     }
   }
   __syncthreads();
   const int total = sm.count;
+
   if (total <= kDecodeCap) {
-    for (int q = tid; q < total; q += kDecodeThreads) {
-      const unsigned long long me = sm.cand[q];
-      int r = 0;
+    if (warp != 0) return;
+    // ---- warp 0: rank by counting (composites are distinct)
+    for (int c0 = lane; c0 < total; c0 += 32) {
+      const unsigned long long me = sm.cand[c0];
+      int rk = 0;
 #pragma unroll 8
-      for (int p = 0; p < total; ++p) r += (sm.cand[p] > me) ? 1 : 0;
-      if (r < K) {
-        sm.sel_id[r] = composite_expert(me);
-        sm.sel_s[r] = sm.cand_s[q];
+      for (int p = 0; p < total; ++p) rk += (sm.cand[p] > me) ? 1 : 0;
+      if (rk < K) {
+        sm.sel_id[rk] = composite_expert(me);
+        sm.sel_s[rk] = sm.cand_s[c0];
       }
     }
+    __syncwarp();
   } else {
     // very many survivors (wide exact ties): K rounds of a block-wide maximum
     unsigned long long prev = ~0ull;
@@ -200,12 +214,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       unsigned long long best = 0ull;
       float best_s = 0.0f;
 #pragma unroll
-      for (int i = 0; i < kDecodeEpt; ++i) {
-        if (cand[i] && key[i] >= tau) {
-          const unsigned long long c = composite(key[i], tid + kDecodeThreads * i);
+      for (int r = 0; r < kDecodeEpt; ++r) {
+        if (mine_kept && key[r] >= tau) {
+          const unsigned long long c = composite(key[r], j * g + i + TPG * r);
           if (c < prev && c > best) {
             best = c;
-            best_s = sv[i];
+            best_s = sv[r];
           }
         }
       }
@@ -237,37 +251,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       prev = all;
       __syncthreads();
     }
+    if (warp != 0) return;
   }
-  __syncthreads();
 
-  // ---- weights, outputs and the one-token sort (warp 0)
-  if (warp == 0) {
-    const bool mine = lane < K;
-    const int id = mine ? sm.sel_id[lane] : 0x7fffffff;
-    const float s = mine ? sm.sel_s[lane] : 0.0f;
-    float sum = 0.0f;
-    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, sm.sel_s[k]);  // slot order
-    const float w = __fmul_rn(__fdiv_rn(s, sum), a.R);
-    int blk = 0;  // number of selected ids below mine
+  // ---- warp 0: weights, outputs and the one-token sort
+  const bool mine = lane < K;
+  const int id = mine ? sm.sel_id[lane] : 0x7fffffff;
+  const float s = mine ? sm.sel_s[lane] : 0.0f;
+  float sum = 0.0f;
+  if (lane == 0) {  // slot order
+    float4 q4[kMaxTopk / 4];
+    const float4* s4 = reinterpret_cast<const float4*>(sm.sel_s);
 #pragma unroll
-    for (int m = 0; m < 32; ++m) blk += (__shfl_sync(kFull, id, m) < id) ? 1 : 0;
-    if (mine) {
-      a.topk_ids[lane] = id;
-      a.topk_w[lane] = w;
-      a.sorted_ids[blk * B] = lane;
-      a.sorted_w[blk * B] = w;
-      a.expert_ids[blk] = id;
+    for (int h = 0; h < kMaxTopk / 4; ++h)
+      q4[h] = (4 * h < K) ? s4[h] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int h = 0; h < kMaxTopk / 4; ++h) {
+      if (4 * h < K) sum = __fadd_rn(sum, q4[h].x);
+      if (4 * h + 1 < K) sum = __fadd_rn(sum, q4[h].y);
+      if (4 * h + 2 < K) sum = __fadd_rn(sum, q4[h].z);
+      if (4 * h + 3 < K) sum = __fadd_rn(sum, q4[h].w);
     }
-    for (int p = lane; p < K * B; p += 32) {
-      if ((p & (B - 1)) != 0) {
-        a.sorted_ids[p] = K;  // sentinel T * K with T = 1
-        a.sorted_w[p] = 0.0f;
-      }
-    }
-    if (lane == 0) {
-      *a.npp = K * B;
-      *a.status = 0;
-    }
+  }
+  sum = __shfl_sync(kFull, sum, 0);
+  const float w = __fmul_rn(__fdiv_rn(s, sum), a.R);
+  int blk = 0;  // number of selected ids below mine
+#pragma unroll
+  for (int m = 0; m < 32; ++m) blk += (__shfl_sync(kFull, id, m) < id) ? 1 : 0;
+  if (mine) {
+    a.topk_ids[lane] = id;
+    a.topk_w[lane] = w;
+    a.sorted_ids[blk * B] = lane;
+    a.sorted_w[blk * B] = w;
+    a.expert_ids[blk] = id;
   }
 }
 
