@@ -41,6 +41,10 @@ SECONDARY = ["prefill_T512_E896", "skewed_T8192_E896", "wide_T16384_E4096"]
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024
 METRIC = "route-sort µs/call at T=1 E=896; routed tokens/s and % HBM roofline at T≥512"
+# DRAM bytes (read + write) of one decode-kernel launch on the headline workload, from the
+# ncu capture summarised in profiles/decode_kernel_decode_T1_E896_G8.md (caches flushed
+# before the launch, so it includes the kernel's code and parameters).
+DECODE_TRAFFIC_BYTES = 64512
 
 
 def parse_args():
@@ -439,10 +443,12 @@ def main():
                    "routed_scale": w.routed_scale, "calls_per_step": head["calls_per_step"],
                    "l2": "flushed (256 MiB write) before every step; rotating input sets",
                    "parallelism": "replicas" if world > 1 else "single"},
-        "roofline": {"bound": "hbm", "kernel": "moe_route_sort (whole call)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "mrs_decode_kernel (the whole call at T=1)" if w.T == 1 else
+                               "moe_route_sort (whole call)",
                      "achieved": head["achieved_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": head["roofline_frac"], "peak_kind": peak_kind,
-                     "traffic": None},
+                     "traffic": DECODE_TRAFFIC_BYTES if w.name == HEADLINE else None},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
