@@ -229,6 +229,7 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
     a.uo.unit_e = reinterpret_cast<uint16_t*>(ws + l.unit_e);
     a.uo.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
     a.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
+    a.uo.status = reinterpret_cast<int32_t*>(ws + l.status);
     a.uo.nslices = nslices;
   }
   return launch_status(launch_route(a, smem, st));
@@ -508,6 +509,7 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
   c.uo.unit_e = reinterpret_cast<uint16_t*>(ws + l.unit_e);
   c.uo.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
   c.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
+  c.uo.status = reinterpret_cast<int32_t*>(ws + l.status);
   c.uo.nslices = nslices;
   rc = launch_status(launch_unit(c, stream));
   if (rc) return rc;

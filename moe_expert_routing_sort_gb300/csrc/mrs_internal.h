@@ -124,6 +124,7 @@ struct UnitOut {
   uint16_t* unit_e;                 // [T * K]
   unsigned long long* slice_flags;  // [nslices], cleared for the slice kernel
   int32_t* unit_flags;              // [U]
+  int32_t* status;                  // cleared for the slice kernel
   int nslices;
 };
 

@@ -81,6 +81,22 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 }
 
 
+// Moves each placed route of unit u's sorted list to row = offset(expert, unit) + position.
+__device__ __forceinline__ void scatter_unit(const SliceArgs& a, int u, int tid, int nthreads) {
+  int t0, t1;
+  unit_range(u, a.T, a.U, t0, t1);
+  const size_t r0 = static_cast<size_t>(t0) * a.K;
+  const int n = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + a.E];  // routes placed
+  for (int p = tid; p < n; p += nthreads) {
+    const int2 v = a.unit_buf[r0 + p];
+    const int dst = a.adj[static_cast<size_t>(a.unit_e[r0 + p]) * a.U + u] + p;
+    a.sorted_ids[dst] = v.x;
+    a.sorted_w[dst] = __int_as_float(v.y);
+  }
+}
+
+size_t slices_smem_bytes(int U, int E, int nslices);
+
 __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -212,29 +228,22 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   if (c == a.nslices - 1 && warp == 0) {
     int f = 0;
     for (int v = lane; v < U; v += 32) f |= a.unit_flags[v];
-    f = __reduce_or_sync(kFull, f) | flags_s;
+    f = __reduce_or_sync(kFull, f);
     if (lane == 0) {
       *a.npp = base + soff[ns];
-      *a.status = f;
+      if (f) atomicOr(a.status, f);
     }
   }
+  if (flags_s != 0 && tid == 0) atomicOr(a.status, flags_s);
 }
 
 // ------------------------------------------------------------------ phase 2b: scatter
 __global__ void __launch_bounds__(kSliceThreads) mrs_scatter_kernel(const SliceArgs a) {
-  const int u = blockIdx.x;
-  int t0, t1;
-  unit_range(u, a.T, a.U, t0, t1);
-  const size_t r0 = static_cast<size_t>(t0) * a.K;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int n = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + a.E];  // routes placed
-  for (int p = threadIdx.x; p < n; p += blockDim.x) {
-    const int2 v = a.unit_buf[r0 + p];
-    const int dst = a.adj[static_cast<size_t>(a.unit_e[r0 + p]) * a.U + u] + p;
-    a.sorted_ids[dst] = v.x;
-    a.sorted_w[dst] = __int_as_float(v.y);
-  }
+  scatter_unit(a, blockIdx.x, threadIdx.x, blockDim.x);
 }
+
+
 
 size_t slices_smem_bytes(int U, int E, int nslices) {
   const int ns = (E + nslices - 1) / nslices;

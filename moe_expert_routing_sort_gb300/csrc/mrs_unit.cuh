@@ -68,8 +68,9 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
   o += align16(sizeof(int32_t) * E);
   int32_t* misc = reinterpret_cast<int32_t*>(scratch + o);  // [0..32] scan, [40] dup flag
 
-  // clear the look-back flags of the slice kernel that follows
+  // clear the look-back words and the status word for the slice kernel
   for (int c = u + tid * U; c < nslices; c += blockDim.x * U) slice_flags[c] = 0ull;
+  if (u == 0 && tid == 0) *uo.status = 0;
 
   block_exclusive_scan(cnt, loc, E, misc);
   int32_t* loc_g = uo.loc_off + static_cast<size_t>(u) * (E + 1);
