@@ -17,6 +17,7 @@ constexpr int kSmallThreads = 512;
 constexpr int kSegThreads = 512;
 constexpr int kUnitThreads = 512;
 constexpr int kSliceThreads = 512;
+constexpr int kSliceWarps = kSliceThreads / 32;
 // A unit (one CTA of the route step) holds at most this many routes in shared memory.
 constexpr int kUnitRouteCap = 4096;
 

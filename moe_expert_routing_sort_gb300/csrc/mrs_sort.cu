@@ -106,9 +106,10 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   const int e1 = static_cast<int>(static_cast<long long>(c + 1) * a.E / a.nslices);
   const int ns = e1 - e0;
   const int U = a.U, B = a.B;
-  int32_t* locs = reinterpret_cast<int32_t*>(smem);                  // [ns + 1][U] (by expert)
-  int32_t* seg = locs + static_cast<size_t>(ns + 1) * U;             // [ns][U] starts
-  int32_t* tot = seg + static_cast<size_t>(ns) * U;                  // [ns + 1] unpadded prefix
+  const int SU = U | 1;  // row stride of locs and seg (odd: conflict-free columns)
+  int32_t* locs = reinterpret_cast<int32_t*>(smem);                  // [ns + 1][SU] (by expert)
+  int32_t* seg = locs + static_cast<size_t>(ns + 1) * SU;            // [ns][SU] starts
+  int32_t* tot = seg + static_cast<size_t>(ns) * SU;                 // [ns + 1] unpadded prefix
   int32_t* soff = tot + ns + 1;                                       // [ns + 1] padded prefix
   __shared__ int32_t base_s, flags_s;
 
@@ -118,31 +119,43 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
     base_s = 0;
     flags_s = 0;
   }
-  // the slice's columns of the per-unit offsets (a warp reads 4 units' pieces at a time),
-  // stored by expert
-  for (int u0 = 4 * warp; u0 < U; u0 += 4 * nwarps) {
-    for (int i = lane; i <= ns; i += 32) {
-      int v[4];
+  // the slice's columns of the per-unit offsets, stored by expert: lane i reads column
+  // e0 + i of units warp, warp + 16, ... with all its loads in flight at once
+  for (int i0 = 0; i0 <= ns; i0 += 32) {
+    const int i = i0 + lane;
+    for (int ub = 0; ub < U; ub += 16 * kSliceWarps) {
+      int v[16];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (u0 + k < U) v[k] = a.loc_off[static_cast<size_t>(u0 + k) * (a.E + 1) + e0 + i];
+      for (int k = 0; k < 16; ++k) {
+        const int u = ub + warp + k * kSliceWarps;
+        if (i <= ns && u < U) v[k] = a.loc_off[static_cast<size_t>(u) * (a.E + 1) + e0 + i];
+      }
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (u0 + k < U) locs[i * U + u0 + k] = v[k];
+      for (int k = 0; k < 16; ++k) {
+        const int u = ub + warp + k * kSliceWarps;
+        if (i <= ns && u < U) locs[i * SU + u] = v[k];
+      }
     }
   }
   __syncthreads();
-  // per expert of the slice (warp per expert): exclusive prefix over units of its counts
-  for (int i = warp; i < ns; i += nwarps) {
-    int run = 0;
-    for (int u0 = 0; u0 < U; u0 += 32) {
-      const int u = u0 + lane;
-      const int cnt = (u < U) ? locs[(i + 1) * U + u] - locs[i * U + u] : 0;
-      const int incl = warp_inclusive_sum(cnt, lane);
-      if (u < U) seg[i * U + u] = run + incl - cnt;
-      run += __shfl_sync(kFull, incl, 31);
+  // per expert of the slice (warp per expert): exclusive prefix over units of its counts;
+  // lane l sums a run of consecutive units, one warp scan joins the runs
+  {
+    const int per = (U + 31) / 32;
+    const int ulo = min(U, lane * per), uhi = min(U, ulo + per);
+    for (int i = warp; i < ns; i += nwarps) {
+      const int* lo = locs + i * SU;
+      const int* hi = locs + (i + 1) * SU;
+      int sum = 0;
+      for (int u = ulo; u < uhi; ++u) sum += hi[u] - lo[u];
+      const int incl = warp_inclusive_sum(sum, lane);
+      int r = incl - sum;
+      for (int u = ulo; u < uhi; ++u) {
+        seg[i * SU + u] = r;
+        r += hi[u] - lo[u];
+      }
+      if (lane == 31) tot[i] = incl;  // the expert's count, for now
     }
-    if (lane == 0) tot[i] = run;  // the expert's count, for now
   }
   __syncthreads();
   // unpadded and padded prefixes over the slice's experts (one warp)
@@ -209,8 +222,8 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
     int32_t* adj = a.adj + static_cast<size_t>(e0 + i) * U;
     const int b_i = base + soff[i];
     for (int u = lane; u < U; u += 32) {
-      const int l0 = locs[i * U + u];
-      if (locs[(i + 1) * U + u] > l0) adj[u] = b_i + seg[i * U + u] - l0;
+      const int l0 = locs[i * SU + u];
+      if (locs[(i + 1) * SU + u] > l0) adj[u] = b_i + seg[i * SU + u] - l0;
     }
   }
   // padding rows and block owners
@@ -247,8 +260,8 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_scatter_kernel(const SliceA
 
 size_t slices_smem_bytes(int U, int E, int nslices) {
   const int ns = (E + nslices - 1) / nslices;
-  return sizeof(int32_t) * (static_cast<size_t>(ns + 1) * U + static_cast<size_t>(ns) * U +
-                            2 * static_cast<size_t>(ns) + 2);
+  const size_t SU = static_cast<size_t>(U | 1);
+  return sizeof(int32_t) * ((ns + 1) * SU + ns * SU + 2 * static_cast<size_t>(ns) + 2);
 }
 
 cudaError_t launch_slices(const SliceArgs& a, cudaStream_t st) {
