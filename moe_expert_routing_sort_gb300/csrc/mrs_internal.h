@@ -34,10 +34,13 @@ inline int units_for_shape(int T, int K, int sms) {
 }
 // The largest unit count of any device: the workspace is sized for it.
 inline int units_bound(int T, int K) { return units_for_shape(T, K, kMaxUnitSms); }
-// Expert slices of the sort step: one per unit, at most one per expert and kMaxSlices.
+// Expert slices of the sort step: one per unit, or more so that a slice holds at most 16
+// experts; at most one per expert and kMaxSlices.
 constexpr int kMaxSlices = 256;
 inline int slices_for(int U, int E) {
-  const int n = U < E ? U : E;
+  int n = (E + 15) / 16;
+  if (n < U) n = U;
+  if (n > E) n = E;
   return n < kMaxSlices ? n : kMaxSlices;
 }
 
