@@ -22,12 +22,16 @@ constexpr int kSliceWarps = kSliceThreads / 32;
 constexpr int kUnitRouteCap = 4096;
 
 // Units of the multi-CTA path for T tokens: one per SM (counting at most kMaxUnitSms SMs),
-// at least one token and at most kUnitRouteCap routes each; `sms` is the device's SM count.
+// but no fewer than kUnitMinTokens tokens each (a unit's warps have a token each before the
+// sort step has more units to join), and at most kUnitRouteCap routes each; `sms` is the
+// device's SM count.
 constexpr int kMaxUnitSms = 256;
+constexpr int kUnitMinTokens = 16;
 inline int units_for_shape(int T, int K, int sms) {
   const int tpu_cap = kUnitRouteCap / K > 0 ? kUnitRouteCap / K : 1;
   const int s = sms < kMaxUnitSms ? sms : kMaxUnitSms;
-  int U = T < s ? T : s;
+  const int by_tokens = (T + kUnitMinTokens - 1) / kUnitMinTokens;
+  int U = by_tokens < s ? by_tokens : s;
   const int need = (T + tpu_cap - 1) / tpu_cap;
   if (need > U) U = need;
   return U < 1 ? 1 : U;
