@@ -234,7 +234,8 @@ def time_graph_steps(rep: Replica, steps: int, warmup: int, world: int, clocks=N
 
 def e2e_time(w, steps: int, warmup: int, world: int):
     """Whole calls through the public API with host buffers: pinned H2D of the logits, the
-    route-sort call, D2H of every output (full buffers), timed with events on the stream."""
+    route-sort call, D2H of every output (full buffers, one copy of the block that holds
+    them), timed with events on the stream."""
     import torch
 
     import moe_expert_routing_sort_gb300 as mrs
@@ -244,18 +245,14 @@ def e2e_time(w, steps: int, warmup: int, world: int):
     bias = torch.from_numpy(inp.bias).cuda()  # router parameter, resident
     d_logits = torch.empty_like(h_logits, device="cuda")
     out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
-    outs = [out.topk_ids, out.topk_weights, out.sorted_token_ids, out.sorted_weights,
-            out.expert_ids, out.num_tokens_post_pad]
+    outs = [out.outputs]  # all six outputs, one contiguous block
     h_outs = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
     s = torch.cuda.Stream()
 
     def one():
-        with torch.cuda.stream(s):
-            d_logits.copy_(h_logits, non_blocking=True)
-            mrs.route_sort(d_logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
-                           w.block_m, out=out)
-            for h, d in zip(h_outs, outs):
-                h.copy_(d, non_blocking=True)
+        # one library call: H2D of the logits, the route-sort, D2H of the output block
+        mrs.route_sort_from_host(h_logits, d_logits, bias, w.n_group, w.topk_group, w.topk,
+                                 w.routed_scale, w.block_m, out, h_outs[0], stream=s)
 
     for _ in range(warmup):
         one()

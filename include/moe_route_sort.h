@@ -130,6 +130,23 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
              int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
              size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_route_sort for callers whose logits live in host memory, as one enqueued sequence on
+ * `stream`: copy the T x E bf16 logits from `logits_host` (pinned host memory, for an
+ * asynchronous copy) into `logits_dev`, run moe_route_sort on them with the other device
+ * arguments, then copy `result_bytes` bytes from `result_dev` (device memory holding the
+ * outputs the caller wants back, for example one block containing all of them) to
+ * `result_host`.  Returns MOE_RS_ERR_NULL_POINTER for a missing copy pointer, the codes of
+ * moe_route_sort, or MOE_RS_ERR_LAUNCH if a copy cannot be enqueued.  Nothing waits: the
+ * host results are valid once the stream has reached the end of this sequence. */
+int moe_route_sort_from_host(const void* logits_host, void* logits_dev, const float* bias,
+                             int T, int E, int n_group, int topk_group, int topk,
+                             float routed_scale, int block_m, int32_t* topk_ids,
+                             float* topk_weights, int32_t* sorted_token_ids,
+                             float* sorted_weights, int32_t* expert_ids,
+                             int32_t* num_tokens_post_pad, void* workspace,
+                             size_t workspace_bytes, const void* result_dev, void* result_host,
+                             size_t result_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------- allocation-free variant */
 
 /* Bytes of the scratch array that moe_route_sort_noalloc keeps in the library itself. */
@@ -150,7 +167,7 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
  * Arguments, outputs, results and errors are those of moe_route_sort, plus
  * MOE_RS_ERR_TOO_LARGE when moe_route_sort_workspace_bytes(T, E, topk, block_m) exceeds
  * MOE_RS_NOALLOC_SCRATCH_BYTES (for example 16384 tokens x 4096 experts x top-8 needs about
- * 18 MiB and is accepted).  The first call on each device looks up the array's device
+ * 9.3 MiB and is accepted).  The first call on each device looks up the array's device
  * address with that device current; make that first call before any stream capture.
  * All calls on a device share the one array and it keeps whatever the previous call left in
  * it (the path needs no zeroed scratch); two calls that can run on the GPU at the same time

@@ -21,5 +21,6 @@ from .binding import (  # noqa: F401
     moe_sort_max_padded,
     moe_topk,
     route_sort,
+    route_sort_from_host,
     strerror,
 )

@@ -36,6 +36,8 @@ def library_path() -> str:
 def load() -> ctypes.CDLL:
     """Load ``libmoe_route_sort.so``; raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -62,6 +64,9 @@ def load() -> ctypes.CDLL:
         lib.moe_sort.restype = I
         lib.moe_route_sort_noalloc.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P]
         lib.moe_route_sort_noalloc.restype = I
+        lib.moe_route_sort_from_host.argtypes = [P, P, P, I, I, I, I, I, F, I, P, P, P, P, P, P,
+                                                 P, S, P, P, S, P]
+        lib.moe_route_sort_from_host.restype = I
         lib.moe_route_sort_proxy_selftest.argtypes = [P, P]
         lib.moe_route_sort_proxy_selftest.restype = I
         _lib = lib
@@ -200,7 +205,10 @@ def moe_route_sort_proxy_selftest(out2, stream=None) -> None:
 # ---------------------------------------------------------- convenience buffers
 @dataclass
 class RouteSortBuffers:
-    """Caller-owned output buffers plus workspace for one (T, E, topk, block_m) shape."""
+    """Caller-owned output buffers plus workspace for one (T, E, topk, block_m) shape.
+
+    ``allocate`` places the six outputs in one contiguous device block (``outputs``, bytes),
+    so a caller can bring every result to the host with a single copy."""
 
     topk_ids: torch.Tensor
     topk_weights: torch.Tensor
@@ -209,6 +217,7 @@ class RouteSortBuffers:
     expert_ids: torch.Tensor
     num_tokens_post_pad: torch.Tensor
     workspace: torch.Tensor
+    outputs: Optional[torch.Tensor] = None
 
     @classmethod
     def allocate(cls, T, E, topk, block_m, device="cuda") -> "RouteSortBuffers":
@@ -217,20 +226,56 @@ class RouteSortBuffers:
         ws = moe_route_sort_workspace_bytes(T, E, topk, block_m)
         if ws == 0:
             raise ValueError("invalid shape for route-sort buffers")
-        kw = dict(device=device)
-        return cls(
-            topk_ids=torch.empty((T, topk), dtype=torch.int32, **kw),
-            topk_weights=torch.empty((T, topk), dtype=torch.float32, **kw),
-            sorted_token_ids=torch.empty(P, dtype=torch.int32, **kw),
-            sorted_weights=torch.empty(P, dtype=torch.float32, **kw),
-            expert_ids=torch.empty(NB, dtype=torch.int32, **kw),
-            num_tokens_post_pad=torch.empty(1, dtype=torch.int32, **kw),
-            workspace=torch.empty(ws, dtype=torch.uint8, **kw),
-        )
+        parts = [("topk_ids", torch.int32, (T, topk)), ("topk_weights", torch.float32, (T, topk)),
+                 ("sorted_token_ids", torch.int32, (P,)), ("sorted_weights", torch.float32, (P,)),
+                 ("expert_ids", torch.int32, (NB,)), ("num_tokens_post_pad", torch.int32, (1,))]
+        offs, total = [], 0
+        for _, _, shape in parts:
+            n = 4
+            for d in shape:
+                n *= d
+            offs.append((total, n))
+            total += (n + 15) // 16 * 16
+        block = torch.empty(max(total, 16), dtype=torch.uint8, device=device)
+        views = {name: block[o:o + n].view(dt).view(shape)
+                 for (name, dt, shape), (o, n) in zip(parts, offs)}
+        return cls(workspace=torch.empty(ws, dtype=torch.uint8, device=device), outputs=block,
+                   **views)
 
     def status_word(self) -> int:
         """Device status bits of the last completed call (synchronises the device)."""
         return int(self.workspace[:4].view(torch.int32).item())
+
+
+def route_sort_from_host(logits_host, logits_dev, bias, n_group, topk_group, topk,
+                         routed_scale, block_m, out: RouteSortBuffers, result_host,
+                         stream=None) -> RouteSortBuffers:
+    """moe_route_sort_from_host: copy the host logits in, run, copy every output back.
+
+    ``logits_host`` is a pinned CPU bf16 tensor [T, E]; ``logits_dev`` a device tensor of the
+    same shape that receives it; ``out`` buffers from ``RouteSortBuffers.allocate``, whose
+    ``outputs`` block is copied into ``result_host`` (pinned CPU uint8, same size).  All of
+    it is enqueued on the stream; the host copy is valid once the stream reaches its end."""
+    T, E = logits_host.shape
+    if logits_host.is_cuda or logits_host.dtype != torch.bfloat16:
+        raise ValueError("logits_host must be a CPU bf16 tensor")
+    if not logits_host.is_contiguous() or tuple(logits_dev.shape) != (T, E):
+        raise ValueError("logits_host must be contiguous and match logits_dev")
+    _need(logits_dev, torch.bfloat16, "logits_dev")
+    _need(bias, torch.float32, "bias")
+    if out.outputs is None or result_host.is_cuda or result_host.numel() != out.outputs.numel():
+        raise ValueError("out must come from RouteSortBuffers.allocate; result_host must be a "
+                         "CPU tensor of out.outputs' size")
+    rc = load().moe_route_sort_from_host(
+        logits_host.data_ptr(), logits_dev.data_ptr(), bias.data_ptr(), T, E, n_group,
+        topk_group, topk, float(routed_scale), block_m, out.topk_ids.data_ptr(),
+        out.topk_weights.data_ptr(), out.sorted_token_ids.data_ptr(),
+        out.sorted_weights.data_ptr(), out.expert_ids.data_ptr(),
+        out.num_tokens_post_pad.data_ptr(), out.workspace.data_ptr(), out.workspace.numel(),
+        out.outputs.data_ptr(), result_host.data_ptr(), out.outputs.numel(),
+        _stream_handle(stream))
+    _check(rc, "moe_route_sort_from_host")
+    return out
 
 
 def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
@@ -239,7 +284,19 @@ def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
     T, E = logits.shape
     if out is None:
         out = RouteSortBuffers.allocate(T, E, topk, block_m, device=logits.device)
-    moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
-                   out.topk_ids, out.topk_weights, out.sorted_token_ids, out.sorted_weights,
-                   out.expert_ids, out.num_tokens_post_pad, out.workspace, stream=stream)
+    if out.outputs is None:
+        moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
+                       out.topk_ids, out.topk_weights, out.sorted_token_ids, out.sorted_weights,
+                       out.expert_ids, out.num_tokens_post_pad, out.workspace, stream=stream)
+        return out
+    # buffers from allocate() have the right types and layout: check the inputs only
+    _need(logits, torch.bfloat16, "logits")
+    _need(bias, torch.float32, "bias")
+    rc = load().moe_route_sort(
+        logits.data_ptr(), bias.data_ptr(), T, E, n_group, topk_group, topk,
+        float(routed_scale), block_m, out.topk_ids.data_ptr(), out.topk_weights.data_ptr(),
+        out.sorted_token_ids.data_ptr(), out.sorted_weights.data_ptr(),
+        out.expert_ids.data_ptr(), out.num_tokens_post_pad.data_ptr(), out.workspace.data_ptr(),
+        out.workspace.numel(), _stream_handle(stream))
+    _check(rc, "moe_route_sort")
     return out

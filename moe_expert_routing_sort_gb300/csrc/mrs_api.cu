@@ -517,6 +517,34 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
                     expert_ids, num_tokens_post_pad, ws, l, stream);
 }
 
+int moe_route_sort_from_host(const void* logits_host, void* logits_dev, const float* bias,
+                             int T, int E, int n_group, int topk_group, int topk,
+                             float routed_scale, int block_m, int32_t* topk_ids,
+                             float* topk_weights, int32_t* sorted_token_ids,
+                             float* sorted_weights, int32_t* expert_ids,
+                             int32_t* num_tokens_post_pad, void* workspace,
+                             size_t workspace_bytes, const void* result_dev, void* result_host,
+                             size_t result_bytes, cudaStream_t stream) {
+  if (T > 0 && (!logits_host || !logits_dev)) return MOE_RS_ERR_NULL_POINTER;
+  if (result_bytes > 0 && (!result_dev || !result_host)) return MOE_RS_ERR_NULL_POINTER;
+  int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
+  if (rc) return rc;
+  const size_t in_bytes = 2 * static_cast<size_t>(T) * static_cast<size_t>(E);
+  if (in_bytes > 0 &&
+      cudaMemcpyAsync(logits_dev, logits_host, in_bytes, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess)
+    return launch_status(cudaErrorInvalidValue);
+  rc = moe_route_sort(logits_dev, bias, T, E, n_group, topk_group, topk, routed_scale, block_m,
+                      topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
+                      num_tokens_post_pad, workspace, workspace_bytes, stream);
+  if (rc) return rc;
+  if (result_bytes > 0 &&
+      cudaMemcpyAsync(result_host, result_dev, result_bytes, cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess)
+    return launch_status(cudaErrorInvalidValue);
+  return MOE_RS_OK;
+}
+
 // ------------------------------------------------- allocation-free variant
 // Scratch for moe_route_sort_noalloc: a fixed array in the library's device image, so the
 // call itself allocates nothing.  Every GPU that loads the library keeps these bytes until

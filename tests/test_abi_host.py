@@ -119,3 +119,20 @@ def test_moe_sort_and_topk_validate(lib):
                         BASE + 0x3000, None) == -8
     # T == 0 needs no buffers for moe_topk and launches nothing
     assert lib.moe_topk(0, 0, 0, 64, 8, 4, 6, 1.0, 0, 0, None) == 0
+
+
+def _from_host(lib, logits_host=BASE + 0x200000, logits_dev=BASE, result_dev=BASE + 0x300000,
+               result_host=BASE + 0x400000, result_bytes=64):
+    ws_bytes = mrs.moe_route_sort_workspace_bytes(4, 64, 6, 16)
+    return lib.moe_route_sort_from_host(
+        logits_host, logits_dev, BASE + 0x10000, 4, 64, 8, 4, 6, 2.5, 16, BASE + 0x20000,
+        BASE + 0x30000, BASE + 0x40000, BASE + 0x80000, BASE + 0xC0000, BASE + 0xD0000,
+        BASE + 0x100000, ws_bytes, result_dev, result_host, result_bytes, None)
+
+
+def test_from_host_rejects_missing_copy_pointers(lib):
+    # checked before anything is enqueued: no pointer is dereferenced
+    assert _from_host(lib, logits_host=None) == -1
+    assert _from_host(lib, logits_dev=None) == -1
+    assert _from_host(lib, result_dev=None) == -1
+    assert _from_host(lib, result_host=None) == -1

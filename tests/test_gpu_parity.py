@@ -316,3 +316,27 @@ def test_graph_replay_with_changed_inputs(name, T):
         ref = oracle.route_sort(new.logits_bf16, new.bias, w.n_group, w.topk_group, w.topk,
                                 w.routed_scale, w.block_m)
         assert_matches(out, ref, w)
+
+
+@pytest.mark.parametrize("name", ["decode_T1_E896_G8", "prefill_T512_E896"])
+def test_from_host_matches_device_call(name):
+    # copy in, route-sort, copy the whole output block back: same bytes as the device call
+    w, inp, ref = inputs_for(name)
+    h_logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    d_logits = torch.empty_like(h_logits, device=DEV)
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    out.outputs.fill_(0)
+    h_res = torch.empty(out.outputs.numel(), dtype=torch.uint8).pin_memory()
+    mrs.route_sort_from_host(h_logits, d_logits, bias, w.n_group, w.topk_group, w.topk,
+                             w.routed_scale, w.block_m, out, h_res)
+    torch.cuda.synchronize()
+    dev = run_gpu(w, inp)
+    npp = int(dev.num_tokens_post_pad.item())
+    assert torch.equal(h_res, out.outputs.cpu())  # the copy-out is the device block
+    assert torch.equal(out.topk_ids.cpu(), dev.topk_ids.cpu())
+    assert torch.equal(out.num_tokens_post_pad.cpu(), dev.num_tokens_post_pad.cpu())
+    assert torch.equal(out.sorted_token_ids[:npp].cpu(), dev.sorted_token_ids[:npp].cpu())
+    assert torch.equal(out.expert_ids[: npp // w.block_m].cpu(),
+                       dev.expert_ids[: npp // w.block_m].cpu())
+    assert torch.equal(out.topk_weights.cpu(), dev.topk_weights.cpu())
