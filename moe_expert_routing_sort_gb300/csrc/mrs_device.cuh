@@ -61,21 +61,6 @@ __device__ __forceinline__ int warp_inclusive_sum(int v, int lane) {
   return v;
 }
 
-// Bitonic sort of one float per lane into descending order across the warp.
-__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(kFull, v, j);
-      const bool desc = (lane & k) == 0;
-      const bool lower = (lane & j) == 0;
-      v = (desc == lower) ? fmaxf(v, o) : fminf(v, o);
-    }
-  }
-  return v;
-}
-
 // K-th largest of one float per lane (1 <= k <= 32), by counting for each lane how many
 // lanes beat it (larger value, or equal value and lower lane).  32 independent shuffles:
 // short dependency chains, for latency-bound callers.
