@@ -130,6 +130,19 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
              int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
              size_t workspace_bytes, cudaStream_t stream);
 
+/* Sort step with atomic slot reservation: the arguments, contracts, npp, expert_ids and
+ * padding rows of moe_sort, but the rows of one expert's segment hold its routes in an order
+ * that depends on how the device's atomics happen to run (no token-then-slot guarantee; two
+ * calls may differ).  Per-block shared-memory counts, one global atomic interval reservation
+ * per nonempty (expert, block), block-local atomic ranks: the scheme of "Summary -- general
+ * gfx1250 ordinary-TP route optimization", Capacity and dispatch.  It exists to measure what
+ * moe_sort's deterministic order costs.  Uses the workspace of moe_route_sort_workspace_bytes;
+ * zeroes part of it with one cudaMemsetAsync on `stream`. */
+int moe_sort_atomic(const int32_t* topk_ids, const float* topk_weights, int T, int E, int topk,
+                    int block_m, int32_t* sorted_token_ids, float* sorted_weights,
+                    int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
 /* moe_route_sort for callers whose logits live in host memory, as one enqueued sequence on
  * `stream`: copy the T x E bf16 logits from `logits_host` (pinned host memory, for an
  * asynchronous copy) into `logits_dev`, run moe_route_sort on them with the other device

@@ -61,6 +61,8 @@ def load() -> ctypes.CDLL:
         lib.moe_topk.argtypes = [P, P, I, I, I, I, I, F, P, P, P]
         lib.moe_topk.restype = I
         lib.moe_sort.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P]
+        lib.moe_sort_atomic.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P]
+        lib.moe_sort_atomic.restype = I
         lib.moe_sort.restype = I
         lib.moe_route_sort_noalloc.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P]
         lib.moe_route_sort_noalloc.restype = I
@@ -177,7 +179,9 @@ def moe_topk(logits, bias, n_group, topk_group, topk, routed_scale, topk_ids, to
 
 
 def moe_sort(topk_ids, topk_weights, E, block_m, sorted_token_ids, sorted_weights, expert_ids,
-             num_tokens_post_pad, workspace, stream=None) -> None:
+             num_tokens_post_pad, workspace, stream=None, atomic=False) -> None:
+    """Sort step only.  ``atomic=True`` calls moe_sort_atomic (order inside each expert's
+    segment unspecified; see include/moe_route_sort.h)."""
     T, K = topk_ids.shape
     _need(topk_ids, torch.int32, "topk_ids")
     _need(topk_weights, torch.float32, "topk_weights")
@@ -186,11 +190,11 @@ def moe_sort(topk_ids, topk_weights, E, block_m, sorted_token_ids, sorted_weight
     _need(expert_ids, torch.int32, "expert_ids")
     _need(num_tokens_post_pad, torch.int32, "num_tokens_post_pad")
     _need(workspace, torch.uint8, "workspace")
-    rc = load().moe_sort(_ptr(topk_ids), _ptr(topk_weights), T, E, K, block_m,
-                         _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
-                         _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(),
-                         _stream_handle(stream))
-    _check(rc, "moe_sort")
+    fn = load().moe_sort_atomic if atomic else load().moe_sort
+    rc = fn(_ptr(topk_ids), _ptr(topk_weights), T, E, K, block_m, _ptr(sorted_token_ids),
+            _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
+            workspace.numel(), _stream_handle(stream))
+    _check(rc, "moe_sort_atomic" if atomic else "moe_sort")
 
 
 def moe_route_sort_proxy_selftest(out2, stream=None) -> None:

@@ -545,6 +545,61 @@ int moe_route_sort_from_host(const void* logits_host, void* logits_dev, const fl
   return MOE_RS_OK;
 }
 
+int moe_sort_atomic(const int32_t* topk_ids, const float* topk_weights, int T, int E, int topk,
+                    int block_m, int32_t* sorted_token_ids, float* sorted_weights,
+                    int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_sort_shape(T, E, topk, block_m);
+  if (rc) return rc;
+  if (!num_tokens_post_pad || !workspace) return workspace ? MOE_RS_ERR_NULL_POINTER
+                                                           : MOE_RS_ERR_WORKSPACE;
+  if (T > 0 && (!topk_ids || !topk_weights || !sorted_token_ids || !sorted_weights ||
+                !expert_ids))
+    return MOE_RS_ERR_NULL_POINTER;
+  const WsLayout l = ws_layout(T, E, topk);
+  if (workspace_bytes < l.total) return MOE_RS_ERR_WORKSPACE;
+  if (!aligned(workspace, 16) || !aligned(num_tokens_post_pad, 4)) return MOE_RS_ERR_MISALIGNED;
+  if (T > 0 && (!aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+                !aligned(sorted_token_ids, 4) || !aligned(sorted_weights, 4) ||
+                !aligned(expert_ids, 4)))
+    return MOE_RS_ERR_MISALIGNED;
+  const size_t NK = static_cast<size_t>(T) * topk;
+  const size_t P = static_cast<size_t>(max_padded64(T, E, topk, block_m));
+  const size_t NB = P / block_m;
+  const Span outs[] = {span(sorted_token_ids, 4 * P), span(sorted_weights, 4 * P),
+                       span(expert_ids, 4 * NB), span(num_tokens_post_pad, 4),
+                       span(workspace, workspace_bytes)};
+  const Span ins[] = {span(topk_ids, 4 * NK), span(topk_weights, 4 * NK)};
+  if (any_alias(outs, 5, ins, 2)) return MOE_RS_ERR_ALIAS;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
+  if (T == 0) return launch_status(launch_empty(num_tokens_post_pad, status, stream));
+  DeviceInfo d;
+  if (!device_info(d)) return MOE_RS_ERR_LAUNCH;
+  const size_t arr = align16(sizeof(int32_t) * static_cast<size_t>(E));
+  AtomicSortArgs a{};
+  a.ids = topk_ids;
+  a.w = topk_weights;
+  a.N = T * topk;
+  a.E = E;
+  a.B = block_m;
+  a.cnt = reinterpret_cast<int32_t*>(ws + 16);
+  a.cursor = reinterpret_cast<int32_t*>(ws + 16 + arr);
+  a.offs = reinterpret_cast<int32_t*>(ws + 16 + 2 * arr);
+  a.status = status;
+  a.sorted_ids = sorted_token_ids;
+  a.sorted_w = sorted_weights;
+  a.expert_ids = expert_ids;
+  a.npp = num_tokens_post_pad;
+  const int nblk = atomic_sort_blocks(a.N, d.sms);
+  a.chunk = (a.N + nblk - 1) / nblk;
+  // the status word and the counts start at zero
+  if (cudaMemsetAsync(ws, 0, 16 + sizeof(int32_t) * static_cast<size_t>(E), stream) !=
+      cudaSuccess)
+    return launch_status(cudaErrorInvalidValue);
+  return launch_status(launch_atomic_sort(a, nblk, stream));
+}
+
 // ------------------------------------------------- allocation-free variant
 // Scratch for moe_route_sort_noalloc: a fixed array in the library's device image, so the
 // call itself allocates nothing.  Every GPU that loads the library keeps these bytes until

@@ -81,6 +81,9 @@ inline WsLayout ws_layout(int T, int E, int K) {
   o = align16(o + 2 * static_cast<size_t>(T) * K);
   l.adj = o;
   o = align16(o + sizeof(int32_t) * static_cast<size_t>(U) * E);
+  // moe_sort_atomic uses the same workspace as status + three [E] arrays from offset 16
+  const size_t atomic_need = 16 + 3 * align16(sizeof(int32_t) * static_cast<size_t>(E));
+  if (o < atomic_need) o = atomic_need;
   l.total = o;
   return l;
 }
@@ -192,6 +195,23 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// ------------------------------------------------------- atomic-order sort step
+struct AtomicSortArgs {
+  const int32_t* ids;
+  const float* w;
+  int N, E, B, chunk;
+  int32_t* cnt;     // [E] global counts (zeroed before the launch)
+  int32_t* cursor;  // [E] reservation cursors
+  int32_t* offs;    // [E] padded exclusive offsets
+  int32_t* status;
+  int32_t* sorted_ids;
+  float* sorted_w;
+  int32_t* expert_ids;
+  int32_t* npp;
+};
+int atomic_sort_blocks(int N, int sms);
+cudaError_t launch_atomic_sort(const AtomicSortArgs& a, int nblk, cudaStream_t st);
 
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st);

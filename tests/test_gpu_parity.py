@@ -268,6 +268,43 @@ def test_moe_sort_distributions(dist, T, K, E, B):
     assert out.status_word() == ref.flags == 0
 
 
+@pytest.mark.parametrize("dist", ["uniform", "shared", "one_expert", "every_third_dropped",
+                                  "all_dropped", "dup_in_token"])
+@pytest.mark.parametrize("T,K,E,B", [(5, 4, 33, 8), (3001, 8, 256, 64), (16384, 8, 4096, 128)])
+def test_moe_sort_atomic_places_the_same_routes(dist, T, K, E, B):
+    # order inside an expert's segment is unspecified: compare each segment as a set, and
+    # everything else exactly
+    rng = np.random.default_rng(T + K + E + B)
+    ids = _ids_for(dist, T, K, E, rng)
+    wts = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
+    ref = oracle.sort(ids, wts, E, B)
+    out = mrs.RouteSortBuffers.allocate(T, E, K, B, device=DEV)
+    out.sorted_token_ids.fill_(-3)
+    out.workspace.fill_(0x5A)
+    mrs.moe_sort(torch.from_numpy(ids).to(DEV), torch.from_numpy(wts).to(DEV), E, B,
+                 out.sorted_token_ids, out.sorted_weights, out.expert_ids,
+                 out.num_tokens_post_pad, out.workspace, atomic=True)
+    torch.cuda.synchronize()
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref.num_tokens_post_pad
+    eids = out.expert_ids[: npp // B].cpu().numpy()
+    assert np.array_equal(eids, ref.expert_ids)
+    sid = out.sorted_token_ids[:npp].cpu().numpy()
+    sw = out.sorted_weights[:npp].cpu().numpy()
+    flat_w = wts.reshape(-1)
+    # padding rows exactly where the oracle has them (each segment's tail)
+    assert np.array_equal(sid == T * K, ref.sorted_token_ids == T * K)
+    # per expert segment: same set of flat indices, weights travel with their route
+    starts = np.flatnonzero(np.r_[True, eids[1:] != eids[:-1]]) * B
+    ends = np.r_[starts[1:], npp]
+    for s0, s1 in zip(starts, ends):
+        assert np.array_equal(np.sort(sid[s0:s1]), np.sort(ref.sorted_token_ids[s0:s1]))
+    real = sid < T * K
+    assert np.array_equal(sw[real], flat_w[sid[real]])
+    assert np.all(sw[~real] == 0.0)
+    assert out.status_word() == ref.flags == 0
+
+
 @pytest.mark.parametrize("T", [3, 2000])
 def test_moe_sort_flags_out_of_range_ids(T):
     rng = np.random.default_rng(T)
