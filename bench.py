@@ -308,6 +308,55 @@ def measure_workload(w, steps, warmup, world, peak_gbs, clocks=None):
     }
 
 
+def measure_sort_only(w, steps, warmup, world, atomic: bool, calls: int = 16):
+    """moe_sort (deterministic) or moe_sort_atomic alone, on the routes route_sort gives for
+    workload w: per-call time of a graph of `calls` calls, L2 flushed before each step."""
+    import torch
+
+    import moe_expert_routing_sort_gb300 as mrs
+
+    inp = datagen.make_inputs(w)
+    logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).cuda()
+    bias = torch.from_numpy(inp.bias).cuda()
+    routed = mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                            w.block_m)
+    ids, wts = routed.topk_ids.clone(), routed.topk_weights.clone()
+    outs = [mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m) for _ in range(calls)]
+    s = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def run():
+        for o in outs:
+            mrs.moe_sort(ids, wts, w.E, w.block_m, o.sorted_token_ids, o.sorted_weights,
+                         o.expert_ids, o.num_tokens_post_pad, o.workspace, stream=s,
+                         atomic=atomic)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            flush.fill_(1)
+            g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    with torch.cuda.stream(s):
+        for k, (a, b) in enumerate(ev):
+            flush.fill_(k & 0xFF)
+            a.record(s)
+            g.replay()
+            b.record(s)
+    torch.cuda.synchronize()
+    ms = dist_max(sum(a.elapsed_time(b) for a, b in ev), world)
+    return ms * 1e3 / (steps * calls)
+
+
 # ----------------------------------------------------------------- CPU oracle
 def cpu_oracle_rate(w, budget_s: float):
     """Time the oracle on a bounded sample of workload w: (seconds per token, sample text)."""
@@ -413,6 +462,11 @@ def main():
             configs[name] = {k: r[k] for k in ("us_per_call", "tokens_per_s", "routes_per_s",
                                                  "achieved_gbs", "roofline_frac",
                                                  "algorithmic_bytes_per_call", "calls_per_step")}
+            if ws.T > 1024:  # the sort step alone: deterministic order vs atomic slot order
+                n = max(3, min(args.steps, 10))
+                configs[name]["sort_only_us"] = {
+                    "deterministic": measure_sort_only(ws, n, args.warmup, world, False),
+                    "atomic_order": measure_sort_only(ws, n, args.warmup, world, True)}
 
     cpu = None
     if rank == 0:
