@@ -77,6 +77,8 @@ def _load():
         lib.oracle_weights_row.restype = None
         lib.oracle_route.argtypes = [P, P, i32, i32, i32, i32, i32, f32, P, P]
         lib.oracle_route.restype = i32
+        lib.oracle_route_softmax.argtypes = [P, i32, i32, i32, f32, P, P]
+        lib.oracle_route_softmax.restype = i32
         lib.oracle_max_padded.argtypes = [i32, i32, i32, i32]
         lib.oracle_max_padded.restype = ctypes.c_int64
         lib.oracle_sort.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P, P]
@@ -199,6 +201,26 @@ def route(logits, bias, n_group, topk_group, topk, routed_scale):
         "route",
     )
     return ids, w
+
+
+def route_softmax(logits, topk, routed_scale):
+    """Softmax variant (R9, no bias, no groups): topk_ids [T,K], topk_weights [T,K]."""
+    lib = _load()
+    lg = _u16(logits)
+    T, E = lg.shape
+    ids = np.empty((T, topk), np.int32)
+    w = np.empty((T, topk), np.float32)
+    _check(lib.oracle_route_softmax(_ptr(lg), T, E, topk, float(routed_scale), _ptr(ids),
+                                    _ptr(w)), "route_softmax")
+    return ids, w
+
+
+def route_sort_softmax(logits, topk, routed_scale, block_m):
+    ids, w = route_softmax(logits, topk, routed_scale)
+    res = sort(ids, w, np.shape(logits)[1], block_m)
+    res["topk_ids"] = ids
+    res["topk_weights"] = w
+    return res
 
 
 def max_padded(T: int, E: int, topk: int, block_m: int) -> int:

@@ -31,6 +31,11 @@
  *                 expert_ids[b] = owner of block b of size B
  *   R8 ids        in the sort step, id < 0 is a dropped route (no slot, not counted);
  *                 id >= E is invalid: flagged and dropped
+ *   R9 softmax    the softmax variant (no bias, no groups): key = x; the K largest keys,
+ *                 ties to the lower index; m = x of slot 0; s_k = expf(x_k - m) in slot
+ *                 order; w_k = (s_k / (s_0 + ... + s_{K-1})) * R -- the softmax over all E
+ *                 experts restricted to the selected ones and renormalised (the normaliser
+ *                 over all E cancels), so selection and weights need no full-row sum
  *
  * Parity pins: every function here is pinned by the tests in tests/test_oracle_pins.py
  * (bf16 decoding against a library conversion over all 65536 patterns, sigmoid against a
@@ -282,6 +287,44 @@ int oracle_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E
   free(off);
   free(fill);
   return ORACLE_OK;
+}
+
+/* R9: route step of the softmax variant for all tokens: topk_ids [T,K], topk_weights [T,K].
+ * Selection is a full sort of the row's logits on (x desc, index asc). */
+int oracle_route_softmax(const uint16_t* logits, int T, int E, int K, float routed_scale,
+                         int32_t* topk_ids, float* topk_weights) {
+  if (T < 0 || E < 1 || K < 1 || K > E) return ORACLE_ERR_ARGS;
+  float* x = (float*)malloc(sizeof(float) * (size_t)E);
+  int32_t kept_all = 1;
+  int rc = ORACLE_OK;
+  if (!x) return ORACLE_ERR_NOMEM;
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) x[e] = oracle_bf16_to_float(logits[(size_t)t * E + e]);
+    int32_t* ids = topk_ids + (size_t)t * K;
+    rc = oracle_topk_row(x, E, 1, &kept_all, K, ids);
+    if (rc) break;
+    float m = x[ids[0]];
+    float sum = 0.0f;
+    for (int k = 0; k < K; ++k) sum = sum + expf(x[ids[k]] - m);
+    for (int k = 0; k < K; ++k) {
+      float q = expf(x[ids[k]] - m) / sum;
+      topk_weights[(size_t)t * K + k] = q * routed_scale;
+    }
+  }
+  free(x);
+  return rc;
+}
+
+/* The softmax variant's whole path: route step (R9) then the sort step. */
+int oracle_route_sort_softmax(const uint16_t* logits, int T, int E, int K, float routed_scale,
+                              int B, int32_t* topk_ids, float* topk_weights,
+                              int32_t* sorted_token_ids, float* sorted_weights,
+                              int32_t* expert_ids, int32_t* num_tokens_post_pad) {
+  int rc = oracle_route_softmax(logits, T, E, K, routed_scale, topk_ids, topk_weights);
+  if (rc) return rc;
+  int32_t flags = 0;
+  return oracle_sort(topk_ids, topk_weights, T, E, K, B, sorted_token_ids, sorted_weights,
+                     expert_ids, num_tokens_post_pad, &flags);
 }
 
 /* The whole path: route step then sort step. */

@@ -319,3 +319,46 @@ def test_margins_detect_planted_ties(oracle_mod):
     bias[10] = bias[11] = 0.0
     m2 = oracle_mod.margins(logits, bias, 1, 1, 16)
     assert m2[0] == 0.0
+
+
+# ------------------------------------------------------ softmax variant (reading R9)
+def test_softmax_topk_is_argsort_of_logits(oracle_mod):
+    # selection is on the logits themselves: a textbook stable argsort of -x (ties -> lower
+    # index), on coarse values so that exact ties are frequent
+    rng = np.random.default_rng(5)
+    T, E, K = 40, 96, 7
+    x = np.round(rng.standard_normal((T, E)) * 4) / 4
+    logits = datagen.float32_to_bf16_bits(x.astype(np.float32))
+    ids, _ = oracle_mod.route_softmax(logits, K, 1.0)
+    for t in range(T):
+        want = np.argsort(-x[t], kind="stable")[:K]
+        assert np.array_equal(ids[t], want)
+
+
+def test_softmax_weights_are_renormalised_softmax(oracle_mod):
+    rng = np.random.default_rng(6)
+    T, E, K, R = 64, 200, 8, 2.5
+    logits = datagen.float32_to_bf16_bits(rng.standard_normal((T, E)).astype(np.float32) * 3)
+    ids, w = oracle_mod.route_softmax(logits, K, R)
+    x = (logits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for t in range(T):
+        p = np.exp(x[t] - x[t].max())
+        p = p / p.sum()                       # softmax over all E experts
+        sel = p[ids[t]]
+        ref = sel / sel.sum() * R             # restricted to the top-K, renormalised
+        assert np.allclose(w[t], ref, rtol=0, atol=2e-7 * R)
+        assert np.all(np.diff(w[t]) <= 0)     # slots in descending order
+        assert abs(w[t].astype(np.float64).sum() - R) < 1e-5
+
+
+def test_softmax_two_experts_closed_form(oracle_mod):
+    # K = 2: w_0 = R * sigmoid(x_0 - x_1) exactly in real arithmetic; x = [2, 0, 1, 0]
+    logits = datagen.float32_to_bf16_bits(np.float32([[2.0, 0.0, 1.0, 0.0]]))
+    ids, w = oracle_mod.route_softmax(logits, 2, 1.0)
+    assert ids.tolist() == [[0, 2]]
+    assert abs(w[0, 0] - 1 / (1 + math.exp(-1))) < 1e-7
+    assert abs(w[0, 1] - 1 / (1 + math.exp(1))) < 1e-7
+    # ties: [1, 3, 3, 0] -> slots 1 then 2 (lower index first), equal weights
+    logits = datagen.float32_to_bf16_bits(np.float32([[1.0, 3.0, 3.0, 0.0]]))
+    ids, w = oracle_mod.route_softmax(logits, 2, 4.0)
+    assert ids.tolist() == [[1, 2]] and w.tolist() == [[2.0, 2.0]]
