@@ -377,3 +377,30 @@ def test_from_host_matches_device_call(name):
     assert torch.equal(out.expert_ids[: npp // w.block_m].cpu(),
                        dev.expert_ids[: npp // w.block_m].cpu())
     assert torch.equal(out.topk_weights.cpu(), dev.topk_weights.cpu())
+
+
+# ---------------------------------------------- the metadata drives a grouped GEMM
+@pytest.mark.parametrize("name", ["prefill_T512_E896", "skewed_T8192_E896"])
+def test_metadata_drives_a_block_grouped_gemm(name):
+    # A consumer in the shape of GEMM1: for each block_m block, the rows named by
+    # sorted_token_ids (token = row // K, sentinel rows skipped) times the block's expert
+    # weight, scaled by sorted_weights, summed back per token.  It must equal the dense
+    # per-token sum over the token's top-k experts.  Synthetic activations and weights.
+    w, inp, _ = inputs_for(name, T=1024 if name.startswith("skewed") else None)
+    out = run_gpu(w, inp)
+    T, K, B, E = w.T, w.topk, w.block_m, w.E
+    H, N = 64, 32
+    g = torch.Generator(device=DEV).manual_seed(7)
+    X = torch.randn(T, H, device=DEV, generator=g)
+    W = torch.randn(E, H, N, device=DEV, generator=g) / H ** 0.5
+    npp = int(out.num_tokens_post_pad.item())
+    nb = npp // B
+    rows = out.sorted_token_ids[:npp].long().view(nb, B)
+    valid = rows < T * K
+    tok = torch.where(valid, rows // K, torch.zeros_like(rows))
+    rw = torch.where(valid, out.sorted_weights[:npp].view(nb, B), torch.zeros(nb, B, device=DEV))
+    Y = torch.bmm(X[tok], W[out.expert_ids[:nb].long()]) * rw.unsqueeze(-1)  # [nb, B, N]
+    got = torch.zeros(T, N, device=DEV).index_add_(0, tok.view(-1), Y.view(-1, N))
+    ids = out.topk_ids.long()
+    ref = torch.einsum("th,tkhn,tk->tn", X, W[ids], out.topk_weights)
+    assert torch.allclose(got, ref, rtol=1e-4, atol=1e-4), (got - ref).abs().max().item()
