@@ -115,6 +115,24 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
                    int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream);
 
+/* The whole path with softmax scoring, for MoE families that route on a softmax without a
+ * correction bias or expert groups.  The source pages define only the sigmoid + bias scoring
+ * above; this is its plain generalisation to the other scoring, over the expert counts and
+ * top-k widths that "Summary -- general gfx1250 ordinary-TP route optimization" (ROCm/aiter
+ * pull 7095), Generality and negative results, sweeps.  Per token t:
+ *   x_e = float(bf16 logit); topk_ids[t,0..K) = the K largest x_e, best first (equal logits:
+ *   lower expert index first; -0 and +0 are equal);
+ *   m = x of slot 0; q_k = expf(x_{id_k} - m); topk_weights[t,k] = (q_k / (q_0 + ... +
+ *   q_{K-1})) * R (sum in slot order) -- the softmax over all E experts restricted to the
+ *   selected ones and renormalised, whose normaliser over all E cancels.
+ * The sort step, outputs, layouts, workspace, limits (with n_group = topk_group = 1, so
+ * 1 <= K <= min(32, E)) and errors are those of moe_route_sort; there is no bias argument. */
+int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, float routed_scale,
+                           int block_m, int32_t* topk_ids, float* topk_weights,
+                           int32_t* sorted_token_ids, float* sorted_weights,
+                           int32_t* expert_ids, int32_t* num_tokens_post_pad,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Route step only ("grouped top-k" of the same Summary): topk_ids/topk_weights [T,K]. */
 int moe_topk(const void* logits_bf16, const float* bias, int T, int E, int n_group,
              int topk_group, int topk, float routed_scale, int32_t* topk_ids,

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     moe_route_sort,
     moe_route_sort_noalloc,
     moe_route_sort_proxy_selftest,
+    moe_route_sort_softmax,
     moe_route_sort_workspace_bytes,
     moe_sort,
     moe_sort_max_blocks,
@@ -22,5 +23,6 @@ from .binding import (  # noqa: F401
     moe_topk,
     route_sort,
     route_sort_from_host,
+    route_sort_softmax,
     strerror,
 )

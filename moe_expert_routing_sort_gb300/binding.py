@@ -58,6 +58,8 @@ def load() -> ctypes.CDLL:
         lib.moe_route_sort_strerror.restype = ctypes.c_char_p
         lib.moe_route_sort.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P, S, P]
         lib.moe_route_sort.restype = I
+        lib.moe_route_sort_softmax.argtypes = [P, I, I, I, F, I, P, P, P, P, P, P, P, S, P]
+        lib.moe_route_sort_softmax.restype = I
         lib.moe_topk.argtypes = [P, P, I, I, I, I, I, F, P, P, P]
         lib.moe_topk.restype = I
         lib.moe_sort.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P]
@@ -138,6 +140,38 @@ def moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_
         _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
         workspace.numel(), _stream_handle(stream))
     _check(rc, "moe_route_sort")
+
+
+def moe_route_sort_softmax(logits, topk, routed_scale, block_m, topk_ids, topk_weights,
+                           sorted_token_ids, sorted_weights, expert_ids, num_tokens_post_pad,
+                           workspace, stream=None) -> None:
+    """Whole path with softmax scoring (no bias, no groups) into caller-owned buffers."""
+    T, E = logits.shape
+    _need(logits, torch.bfloat16, "logits")
+    for t, dt, n in [(topk_ids, torch.int32, "topk_ids"), (topk_weights, torch.float32,
+                     "topk_weights"), (sorted_token_ids, torch.int32, "sorted_token_ids"),
+                     (sorted_weights, torch.float32, "sorted_weights"),
+                     (expert_ids, torch.int32, "expert_ids"),
+                     (num_tokens_post_pad, torch.int32, "num_tokens_post_pad"),
+                     (workspace, torch.uint8, "workspace")]:
+        _need(t, dt, n)
+    rc = load().moe_route_sort_softmax(
+        _ptr(logits), T, E, topk, float(routed_scale), block_m, _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
+        _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "moe_route_sort_softmax")
+
+
+def route_sort_softmax(logits, topk, routed_scale, block_m,
+                       out: Optional[RouteSortBuffers] = None, stream=None) -> RouteSortBuffers:
+    """Allocate (unless ``out`` is given) and run moe_route_sort_softmax."""
+    T, E = logits.shape
+    if out is None:
+        out = RouteSortBuffers.allocate(T, E, topk, block_m, device=logits.device)
+    moe_route_sort_softmax(logits, topk, routed_scale, block_m, out.topk_ids, out.topk_weights,
+                           out.sorted_token_ids, out.sorted_weights, out.expert_ids,
+                           out.num_tokens_post_pad, out.workspace, stream=stream)
+    return out
 
 
 def moe_route_sort_noalloc(logits, bias, n_group, topk_group, topk, routed_scale, block_m,

@@ -207,6 +207,7 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   size_t smem;
   if (p.seg) {
     a.seg = p.shape;
+    a.seg.softmax = sh.softmax;
     a.lanes = p.lanes;
     a.nbuf = p.nbuf;
     a.nwarps = p.nwarps;
@@ -345,20 +346,27 @@ int moe_topk(const void* logits_bf16, const float* bias, int T, int E, int n_gro
                    units_for_shape(T, topk, d.sms), 0, d, stream);
 }
 
-int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int n_group,
-                   int topk_group, int topk, float routed_scale, int block_m,
-                   int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
-                   float* sorted_weights, int32_t* expert_ids,
-                   int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
-                   cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The whole path for both scorings: sigmoid + bias with grouped top-k (softmax == false), or
+// softmax over the logits with plain top-k (softmax == true: n_group = topk_group = 1 and
+// bias unused, may be NULL).
+int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, int n_group,
+                    int topk_group, int topk, float routed_scale, int block_m, bool softmax,
+                    int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
+                    float* sorted_weights, int32_t* expert_ids, int32_t* num_tokens_post_pad,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
   if (rc) return rc;
   rc = check_sort_shape(T, E, topk, block_m);
   if (rc) return rc;
   if (!num_tokens_post_pad || !workspace) return workspace ? MOE_RS_ERR_NULL_POINTER
                                                            : MOE_RS_ERR_WORKSPACE;
-  if (T > 0 && (!logits_bf16 || !bias || !topk_ids || !topk_weights || !sorted_token_ids ||
-                !sorted_weights || !expert_ids))
+  if (softmax) bias = nullptr;
+  if (T > 0 && (!logits_bf16 || (!bias && !softmax) || !topk_ids || !topk_weights ||
+                !sorted_token_ids || !sorted_weights || !expert_ids))
     return MOE_RS_ERR_NULL_POINTER;
   const WsLayout l = ws_layout(T, E, topk);
   if (workspace_bytes < l.total) return MOE_RS_ERR_WORKSPACE;
@@ -375,7 +383,7 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
                        span(expert_ids, 4 * NB),       span(num_tokens_post_pad, 4),
                        span(workspace, workspace_bytes)};
   const Span ins[] = {span(logits_bf16, 2 * static_cast<size_t>(T) * E),
-                      span(bias, T > 0 ? 4 * static_cast<size_t>(E) : 0)};
+                      span(bias, (T > 0 && bias) ? 4 * static_cast<size_t>(E) : 0)};
   if (any_alias(outs, 7, ins, 2)) return MOE_RS_ERR_ALIAS;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
@@ -392,6 +400,7 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
     a.K = topk;
     a.B = block_m;
     a.R = routed_scale;
+    a.softmax = softmax ? 1 : 0;
     a.topk_ids = topk_ids;
     a.topk_w = topk_weights;
     a.sorted_ids = sorted_token_ids;
@@ -403,12 +412,14 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
   }
   DeviceInfo d;
   if (!device_info(d)) return MOE_RS_ERR_LAUNCH;
-  const RouteShape sh = make_shape(E, n_group, topk_group, topk, routed_scale);
+  RouteShape sh = make_shape(E, n_group, topk_group, topk, routed_scale);
+  sh.softmax = softmax ? 1 : 0;
 
   SmallLayout lay;
   int wave = 0, nb_max = 0;
   SegShape seg{};
   const bool use_seg = make_seg_shape(E, n_group, topk_group, topk, routed_scale, 32, seg);
+  seg.softmax = sh.softmax;
   if (T <= kSmallMaxTokens &&
       small_plan(T, E, topk, block_m, false, use_seg ? seg.nu : 0, d, lay, wave, nb_max)) {
     SmallArgs a{};
@@ -440,6 +451,32 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
   if (rc) return rc;
   return run_slices(T, E, topk, block_m, U, nslices, sorted_token_ids, sorted_weights,
                     expert_ids, num_tokens_post_pad, ws, l, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int n_group,
+                   int topk_group, int topk, float routed_scale, int block_m,
+                   int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
+                   float* sorted_weights, int32_t* expert_ids,
+                   int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  return route_sort_impl(logits_bf16, bias, T, E, n_group, topk_group, topk, routed_scale,
+                         block_m, false, topk_ids, topk_weights, sorted_token_ids,
+                         sorted_weights, expert_ids, num_tokens_post_pad, workspace,
+                         workspace_bytes, stream);
+}
+
+int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, float routed_scale,
+                           int block_m, int32_t* topk_ids, float* topk_weights,
+                           int32_t* sorted_token_ids, float* sorted_weights,
+                           int32_t* expert_ids, int32_t* num_tokens_post_pad,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return route_sort_impl(logits_bf16, nullptr, T, E, 1, 1, topk, routed_scale, block_m, true,
+                         topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
+                         num_tokens_post_pad, workspace, workspace_bytes, stream);
 }
 
 int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, int topk,

@@ -17,6 +17,8 @@
 //   sort      one token: each selected expert gets one route, so expert id_k owns block
 //             (number of selected ids below id_k), its row 0 is route k and rows 1..B-1 are
 //             padding (written at the start, as they depend on nothing); npp = K * B
+// With softmax scoring (G = 1, no bias) the keys are the logits and the weight step turns the
+// selected logits into softmax terms.
 // Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary --
 // the B1 (batch-one) route-sort: FP32 logits, correction bias, grouped top-k, both sort
 // phases, in one kernel.
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       const int li = i + TPG * r;
       if (in_group && li < g) {
         x[r] = a.logits[j * g + li];
-        b[r] = a.bias[j * g + li];
+        b[r] = a.softmax ? 0.0f : a.bias[j * g + li];
       }
     }
     for (int p = tid; p < K * B; p += kDecodeThreads) {
@@ -102,8 +104,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       key[r] = -INFINITY;
       sv[r] = 0.0f;
       if (r < R && in_group && li < g) {
-        sv[r] = exact_score(bf16_bits_to_float(x[r]));
-        key[r] = __fadd_rn(sv[r], b[r]);
+        key[r] = score_key(bf16_bits_to_float(x[r]), b[r], a.softmax != 0, sv[r]);
         t2 = fmaxf(t2, fminf(t1, key[r]));
         t1 = fmaxf(t1, key[r]);
       }
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   }
 
   // ---- warp 0: weights, outputs and the one-token sort
+  if (a.softmax) softmax_terms(sm.sel_s, lane, K);
   const bool mine = lane < K;
   const int id = mine ? sm.sel_id[lane] : 0x7fffffff;
   const float s = mine ? sm.sel_s[lane] : 0.0f;

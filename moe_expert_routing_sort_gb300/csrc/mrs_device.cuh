@@ -122,6 +122,32 @@ __device__ __forceinline__ float exact_key(float x, float bias, float& s) {
   return __fadd_rn(s, bias);
 }
 
+// Softmax-scored routing selects on the logit itself.  Adding +0 turns a -0 logit into +0,
+// so that the two zeros, equal as floats, also tie in the composite order (lower index wins).
+__device__ __forceinline__ float logit_key(float x) { return __fadd_rn(x, 0.0f); }
+
+// Score and selection key of one logit: the sigmoid score and score + bias, or with softmax
+// scoring the logit for both (the weight step turns it into a softmax term).
+__device__ __forceinline__ float score_key(float x, float bias, bool softmax, float& s) {
+  if (softmax) {
+    s = x;
+    return logit_key(x);
+  }
+  return exact_key(x, bias, s);
+}
+
+// Softmax-scored routing: the logits x_k of the K selected slots (sel_s[0..K), slot 0 the
+// largest) become the terms exp(x_k - x_0).  Renormalising them gives the softmax over all
+// experts restricted to the selection (the common factor cancels), and no term exceeds 1.
+// Called by every lane of the warp; lane slot `k` (< K) converts its own slot.
+__device__ __forceinline__ void softmax_terms(float* sel_s, int k, int K) {
+  const float x0 = sel_s[0];
+  const float t = (k < K) ? expf(__fsub_rn(sel_s[k], x0)) : 0.0f;
+  __syncwarp();
+  if (k < K) sel_s[k] = t;
+  __syncwarp();
+}
+
 // ------------------------------------------------------------------ route shape
 struct RouteShape {
   int E, G, g, Kg, K;
@@ -130,6 +156,7 @@ struct RouteShape {
   int gpr;     // groups per round = 32 / L
   int rounds;  // ceil(G / gpr)
   float R;     // routed_scale
+  int softmax; // 1: keys are the logits, weights the renormalised softmax (no bias)
 };
 
 // Per-warp shared scratch of the route step.
@@ -274,9 +301,11 @@ __device__ __forceinline__ void rank_candidates(WarpScratch& ws, int total, int 
 }
 
 // Renormalised weights of the K selected experts: sum of scores in slot order, then
-// (s_k / sum) * R.  Lane k < K returns slot k.
-__device__ __forceinline__ void finish_weights(const WarpScratch& ws, int K, float R, int lane,
-                                               int& id, float& w) {
+// (s_k / sum) * R; with `softmax` the scores are first the terms of softmax_terms.  Lane
+// k < K returns slot k.
+__device__ __forceinline__ void finish_weights(WarpScratch& ws, int K, float R, bool softmax,
+                                               int lane, int& id, float& w) {
+  if (softmax) softmax_terms(ws.sel_s, lane, K);
   const bool mine = lane < K;
   const float s = mine ? ws.sel_s[lane] : 0.0f;
   id = mine ? ws.sel_id[lane] : -1;
@@ -395,7 +424,7 @@ __device__ __forceinline__ void route_token(const Src& src, const RouteShape& sh
     }
   }
   topk_in_kept(src, sh, ws, lane);
-  finish_weights(ws, sh.K, sh.R, lane, id, w);
+  finish_weights(ws, sh.K, sh.R, sh.softmax != 0, lane, id, w);
 }
 
 // Key source over exact keys and scores already in shared memory.

@@ -118,6 +118,7 @@ struct DecodeArgs {
   const float* bias;
   int E, G, g, Kg, K, B;
   float R;
+  int softmax;  // 1: softmax scoring (G == 1, bias unused)
   int32_t* topk_ids;
   float* topk_w;
   int32_t* sorted_ids;

@@ -66,6 +66,7 @@ __device__ __forceinline__ int block_scan_padded(const int* cnt, int* off, int E
 __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt, float* keys,
                                              float* svals) {
   const int E = a.sh.E;
+  const bool sm = a.sh.softmax != 0;  // no bias with softmax scoring
   if ((E & 7) == 0) {
     // 16-byte vectors of 8 logits; the matching 8 biases come from global alongside
     const int nv = E >> 3;
@@ -80,7 +81,7 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
           const int tl = idx / nv, v = idx - tl * nv;
           q[u] = reinterpret_cast<const uint4*>(a.logits + static_cast<size_t>(t0 + tl) * E)[v];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) bb[u][j] = a.bias[8 * v + j];
+          for (int j = 0; j < 8; ++j) bb[u][j] = sm ? 0.0f : a.bias[8 * v + j];
         }
       }
 #pragma unroll
@@ -93,12 +94,9 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
           float* sr = svals + tl * E + 8 * v;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float s0 = exact_score(__uint_as_float(wd[j] << 16));
-            const float s1 = exact_score(__uint_as_float(wd[j] & 0xffff0000u));
-            sr[2 * j] = s0;
-            sr[2 * j + 1] = s1;
-            kr[2 * j] = __fadd_rn(s0, bb[u][2 * j]);
-            kr[2 * j + 1] = __fadd_rn(s1, bb[u][2 * j + 1]);
+            kr[2 * j] = score_key(__uint_as_float(wd[j] << 16), bb[u][2 * j], sm, sr[2 * j]);
+            kr[2 * j + 1] = score_key(__uint_as_float(wd[j] & 0xffff0000u), bb[u][2 * j + 1],
+                                      sm, sr[2 * j + 1]);
           }
         }
       }
@@ -114,16 +112,14 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
         if (idx < total) {
           const int tl = idx / E, e = idx - tl * E;
           x[u] = a.logits[static_cast<size_t>(t0 + tl) * E + e];
-          b[u] = a.bias[e];
+          b[u] = sm ? 0.0f : a.bias[e];
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int idx = base + u * kSmallThreads;
         if (idx < total) {
-          const float s = exact_score(bf16_bits_to_float(x[u]));
-          svals[idx] = s;
-          keys[idx] = __fadd_rn(s, b[u]);
+          keys[idx] = score_key(bf16_bits_to_float(x[u]), b[u], sm, svals[idx]);
         }
       }
     }
@@ -348,8 +344,9 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
   pdl_trigger();
   pdl_wait();
 
+  const bool sm = sh.softmax != 0;  // no bias with softmax scoring
   for (int e = tid; e < E; e += blockDim.x) {
-    bias_s[e] = a.bias[e];
+    bias_s[e] = sm ? 0.0f : a.bias[e];
     counts[e] = 0;
   }
   __syncthreads();
@@ -368,19 +365,14 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int e = v * 8 + 2 * j;
-          const float s0 = exact_score(__uint_as_float(wd[j] << 16));
-          const float s1 = exact_score(__uint_as_float(wd[j] & 0xffff0000u));
-          sv[e] = s0;
-          sv[e + 1] = s1;
-          key[e] = __fadd_rn(s0, bias_s[e]);
-          key[e + 1] = __fadd_rn(s1, bias_s[e + 1]);
+          key[e] = score_key(__uint_as_float(wd[j] << 16), bias_s[e], sm, sv[e]);
+          key[e + 1] =
+              score_key(__uint_as_float(wd[j] & 0xffff0000u), bias_s[e + 1], sm, sv[e + 1]);
         }
       }
     } else {
       for (int e = lane; e < E; e += 32) {
-        const float s = exact_score(bf16_bits_to_float(row[e]));
-        sv[e] = s;
-        key[e] = __fadd_rn(s, bias_s[e]);
+        key[e] = score_key(bf16_bits_to_float(row[e]), bias_s[e], sm, sv[e]);
       }
     }
     __syncwarp();
@@ -452,7 +444,8 @@ size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int 
 // tokens t0 + i * (32 / LT) + h, token h routed by lanes [h * LT, (h + 1) * LT).  The rows
 // of a step are contiguous, so one bulk copy brings them in.  A buffer goes back to the copy
 // engine (for the warp's step nbuf further on) as soon as the selection stops reading it.
-template <bool kSort, int LT>
+// kSoftmax: softmax scoring, selection on the logits themselves (LogitRow, no bias, exact).
+template <bool kSort, int LT, bool kSoftmax>
 __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const RouteArgs a) {
   constexpr int kTpw = 32 / LT;
   constexpr int kParts = (LT == 16) ? 2 : 1;
@@ -511,10 +504,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   __syncthreads();
   float bmax = 0.0f;  // largest |bias|, NaN-propagating (NaN fails the limit test below)
   for (int e = tid; e < E; e += blockDim.x) {
-    const float b = a.bias[e];
-    bias_s[e] = b;
-    const float ab = fabsf(b);
-    bmax = (ab > bmax || ab != ab) ? ab : bmax;
+    if (!kSoftmax) {
+      const float b = a.bias[e];
+      bias_s[e] = b;
+      const float ab = fabsf(b);
+      bmax = (ab > bmax || ab != ab) ? ab : bmax;
+    }
     counts[e] = 0;
   }
   for (int d = 16; d > 0; d >>= 1) {
@@ -525,7 +520,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   __syncthreads();
   // the proxy bound holds for |bias| <= kProxyBiasLimit; beyond that every step is exact
   const float bm = __uint_as_float(cta_bmax_bits);
-  const float delta = (bm <= kProxyBiasLimit) ? proxy_delta(bm) : INFINITY;
+  const float delta = kSoftmax ? 0.0f : (bm <= kProxyBiasLimit) ? proxy_delta(bm) : INFINITY;
 
   uint32_t phase = 0u;  // bit b = parity to wait for on buffer b
   int issued = n_mine < nbuf ? n_mine : nbuf;
@@ -541,7 +536,11 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
     phase ^= 1u << b;
     const int t = step_t(k) + h;
     const bool valid = t < t1;
-    const ProxyRow row{rows + static_cast<size_t>(b * kTpw + h) * E, bias_s};
+    const uint16_t* row_s = rows + static_cast<size_t>(b * kTpw + h) * E;
+    const auto row = [&] {
+      if constexpr (kSoftmax) return LogitRow{row_s};
+      else return ProxyRow{row_s, bias_s};
+    }();
     const LaneTop top = seg_pass1<LT, kParts>(row, sh, umax, lane, valid);
     auto release = [&] {
       __syncwarp();  // every lane is done with the buffer
@@ -589,22 +588,27 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   }
 }
 
-template <bool kSort, int LT>
+template <bool kSort, int LT, bool kSoftmax>
 static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(mrs_route_seg_kernel<kSort, LT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto* kern = mrs_route_seg_kernel<kSort, LT, kSoftmax>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(mrs_route_seg_kernel<kSort, LT>, dim3(a.U), dim3(a.nwarps * 32), smem, st,
-                    a);
+  return launch_pdl(kern, dim3(a.U), dim3(a.nwarps * 32), smem, st, a);
 }
 
-template <bool kSort>
+template <bool kSort, bool kSoftmax>
 static cudaError_t launch_seg(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  return a.lanes == 16 ? launch_seg_h<kSort, 16>(a, smem, st) : launch_seg_h<kSort, 32>(a, smem, st);
+  return a.lanes == 16 ? launch_seg_h<kSort, 16, kSoftmax>(a, smem, st)
+                       : launch_seg_h<kSort, 32, kSoftmax>(a, smem, st);
 }
 
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  if (a.use_seg) return a.sort ? launch_seg<true>(a, smem, st) : launch_seg<false>(a, smem, st);
+  if (a.use_seg) {
+    // softmax scoring only comes with the sort step (moe_route_sort_softmax)
+    if (a.seg.softmax) return a.sort ? launch_seg<true, true>(a, smem, st) : cudaErrorInvalidValue;
+    return a.sort ? launch_seg<true, false>(a, smem, st) : launch_seg<false, false>(a, smem, st);
+  }
   cudaError_t err;
   const int threads = a.nwarps * 32;
   if (a.sort) {

@@ -18,6 +18,7 @@
 //   late_words(e0)          the raw bf16 words of e0..e0+3
 //   values(e0, words, v[4]) the selection values from those words
 //   exact(e, bits, s)       exact key of expert e (logit bits `bits`), score through s
+//                           (for softmax scoring the logit, converted at the weight step)
 // Selection values are the exact keys minus a constant shift common to all experts, up to
 // `delta` (0 for exact sources).  Decisions are exact: values only discard experts proven
 // worse than a bound by more than 2 * delta, and only differences of values are used.
@@ -36,6 +37,7 @@ struct SegShape {
   int nu;        // units of 4 experts per segment (at most 64)
   int rot;       // unit order of lane l starts at (l * rot) % nu (spreads smem banks)
   float R;
+  int softmax;   // 1: values are the logits (LogitRow), weights the renormalised softmax
 };
 
 // Route scratch of one token (shared memory).
@@ -116,6 +118,29 @@ struct ProxyRow {
   }
   __device__ __forceinline__ float exact(int e, uint32_t bits, float& se) const {
     return exact_key(bf16_bits_to_float(static_cast<uint16_t>(bits)), bias[e], se);
+  }
+};
+
+// A bf16 logit row staged in shared memory, selected on the logits themselves (softmax
+// scoring): values are exact, so delta = 0; the score handed on is the logit, turned into a
+// softmax term by the weight step.
+struct LogitRow {
+  const uint16_t* row;  // [E] bf16 bit patterns, shared memory
+  __device__ __forceinline__ void values(int, uint2 w, float (&v)[4]) const {
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xffff0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xffff0000u);
+  }
+  __device__ __forceinline__ uint2 late_words(int e0) const {
+    return *reinterpret_cast<const uint2*>(row + e0);
+  }
+  __device__ __forceinline__ void unit(int e0, float (&v)[4]) const {
+    values(e0, late_words(e0), v);
+  }
+  __device__ __forceinline__ float exact(int, uint32_t bits, float& se) const {
+    se = bf16_bits_to_float(bits);
+    return logit_key(se);
   }
 };
 
@@ -494,6 +519,7 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
   }
   __syncwarp();
   // ---- renormalised weights: sum of the scores in slot order, then (s_k / sum) * R
+  if (sh.softmax) softmax_terms(ws.sel_s, ll, sh.K);
   const bool mine = ll < sh.K;
   const float s = mine ? ws.sel_s[ll] : 0.0f;
   id = mine ? ws.sel_id[ll] : -1;

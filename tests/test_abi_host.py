@@ -136,3 +136,27 @@ def test_from_host_rejects_missing_copy_pointers(lib):
     assert _from_host(lib, logits_dev=None) == -1
     assert _from_host(lib, result_dev=None) == -1
     assert _from_host(lib, result_host=None) == -1
+
+
+def _softmax(lib, T=4, E=64, K=6, R=1.0, B=16, logits=BASE, ids=BASE + 0x20000,
+             ws=BASE + 0x100000, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = mrs.moe_route_sort_workspace_bytes(max(T, 0), E, K, B) if E > 0 else 1 << 20
+    return lib.moe_route_sort_softmax(logits, T, E, K, R, B, ids, BASE + 0x30000,
+                                      BASE + 0x40000, BASE + 0x80000, BASE + 0xC0000,
+                                      BASE + 0xD0000, ws, ws_bytes, None)
+
+
+def test_softmax_variant_validates(lib):
+    # no groups: K is bounded by E itself (and by 32)
+    assert _softmax(lib, E=0) == -2
+    assert _softmax(lib, E=5, K=6) == -4
+    assert _softmax(lib, E=256, K=33) == -4
+    assert _softmax(lib, K=0) == -4
+    assert _softmax(lib, B=24) == -5
+    assert _softmax(lib, T=-3) == -6
+    assert _softmax(lib, R=float("nan")) == -11
+    assert _softmax(lib, logits=0) == -1
+    assert _softmax(lib, logits=BASE + 4) == -8
+    assert _softmax(lib, ws_bytes=16) == -10
+    assert _softmax(lib, ids=BASE + 0x30000) == -9  # topk ids over topk weights
