@@ -78,6 +78,9 @@ def _load():
         lib.oracle_route.argtypes = [P, P, i32, i32, i32, i32, i32, f32, P, P]
         lib.oracle_route.restype = i32
         lib.oracle_route_softmax.argtypes = [P, i32, i32, i32, f32, P, P]
+        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_gate_logits.argtypes = [P, P, i32, i32, i32, P]
         lib.oracle_route_softmax.restype = i32
         lib.oracle_max_padded.argtypes = [i32, i32, i32, i32]
         lib.oracle_max_padded.restype = ctypes.c_int64
@@ -265,6 +268,32 @@ def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m):
     res = sort(ids, w, E, block_m)
     res["topk_ids"] = ids
     res["topk_weights"] = w
+    return res
+
+
+def double_to_bf16(v: float) -> int:
+    """R14: the bf16 bit pattern nearest to v (ties to even), one rounding."""
+    return int(_load().oracle_double_to_bf16(float(v)))
+
+
+def gate_logits(hidden, w_gate) -> np.ndarray:
+    """R14: bf16 logits [T,E] of bf16 hidden [T,H] and bf16 gate rows [E,H]."""
+    hs = _u16(hidden)
+    ws = _u16(w_gate)
+    T, H = hs.shape
+    E, H2 = ws.shape
+    if H != H2:
+        raise ValueError("hidden and gate rows differ in length")
+    out = np.empty((T, E), np.uint16)
+    _check(_load().oracle_gate_logits(_ptr(hs), _ptr(ws), T, E, H, _ptr(out)), "gate_logits")
+    return out
+
+
+def gate_route_sort(hidden, w_gate, bias, n_group, topk_group, topk, routed_scale, block_m):
+    """Gate projection (R14) then the whole path; the result also holds the logits."""
+    logits = gate_logits(hidden, w_gate)
+    res = route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m)
+    res["logits"] = logits
     return res
 
 

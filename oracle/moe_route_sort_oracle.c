@@ -31,11 +31,15 @@
  *                 expert_ids[b] = owner of block b of size B
  *   R8 ids        in the sort step, id < 0 is a dropped route (no slot, not counted);
  *                 id >= E is invalid: flagged and dropped
- *   R9 softmax    the softmax variant (no bias, no groups): key = x; the K largest keys,
+ *   R13 softmax   the softmax variant (no bias, no groups): key = x; the K largest keys,
  *                 ties to the lower index; m = x of slot 0; s_k = expf(x_k - m) in slot
  *                 order; w_k = (s_k / (s_0 + ... + s_{K-1})) * R -- the softmax over all E
  *                 experts restricted to the selected ones and renormalised (the normaliser
  *                 over all E cancels), so selection and weights need no full-row sum
+ *   R14 gate      the router gate projection ahead of the path: logits[t,e] = the bf16
+ *                 nearest (ties to even) to the dot product of hidden row t and gate row e,
+ *                 both bf16; one rounding of the exact sum (formed here in double, whose
+ *                 products of two bf16 values are exact)
  *
  * Parity pins: every function here is pinned by the tests in tests/test_oracle_pins.py
  * (bf16 decoding against a library conversion over all 65536 patterns, sigmoid against a
@@ -289,7 +293,7 @@ int oracle_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E
   return ORACLE_OK;
 }
 
-/* R9: route step of the softmax variant for all tokens: topk_ids [T,K], topk_weights [T,K].
+/* R13: route step of the softmax variant for all tokens: topk_ids [T,K], topk_weights [T,K].
  * Selection is a full sort of the row's logits on (x desc, index asc). */
 int oracle_route_softmax(const uint16_t* logits, int T, int E, int K, float routed_scale,
                          int32_t* topk_ids, float* topk_weights) {
@@ -315,7 +319,7 @@ int oracle_route_softmax(const uint16_t* logits, int T, int E, int K, float rout
   return rc;
 }
 
-/* The softmax variant's whole path: route step (R9) then the sort step. */
+/* The softmax variant's whole path: route step (R13) then the sort step. */
 int oracle_route_sort_softmax(const uint16_t* logits, int T, int E, int K, float routed_scale,
                               int B, int32_t* topk_ids, float* topk_weights,
                               int32_t* sorted_token_ids, float* sorted_weights,
@@ -325,6 +329,46 @@ int oracle_route_sort_softmax(const uint16_t* logits, int T, int E, int K, float
   int32_t flags = 0;
   return oracle_sort(topk_ids, topk_weights, T, E, K, B, sorted_token_ids, sorted_weights,
                      expert_ids, num_tokens_post_pad, &flags);
+}
+
+/* ------------------------------------------------------------ gate projection */
+
+/* R14: the bf16 nearest to v, ties to even, in one rounding.  The bf16 spacing at v is
+ * 2^(e-8) for |v| in [2^(e-1), 2^e) and 2^-133 below the normal range; scaling by it turns the
+ * rounding into rint (round-half-even in the default rounding mode) on an exact double. */
+uint16_t oracle_double_to_bf16(double v) {
+  if (v != v) return 0x7fc0;
+  if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+  int e = 0;
+  (void)frexp(fabs(v), &e);
+  int q = e - 8;
+  if (q < -133) q = -133;
+  double r = ldexp(rint(ldexp(fabs(v), -q)), q);
+  float f = (r >= 0x1p128) ? INFINITY : (float)r; /* r has at most 8 significant bits */
+  uint32_t bits;
+  memcpy(&bits, &f, sizeof bits);
+  bits >>= 16;
+  if (v < 0) bits |= 0x8000u;
+  return (uint16_t)bits;
+}
+
+/* R14: logits [T,E] (bf16) of hidden [T,H] (bf16) times gate weights [E,H] (bf16, one row per
+ * expert): each entry one dot product in h order, in double, rounded once to bf16. */
+int oracle_gate_logits(const uint16_t* hidden, const uint16_t* w, int T, int E, int H,
+                       uint16_t* logits) {
+  if (T < 0 || E < 1 || H < 1) return ORACLE_ERR_ARGS;
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double sum = 0.0;
+      for (int h = 0; h < H; ++h) {
+        double a = (double)oracle_bf16_to_float(hidden[(size_t)t * H + h]);
+        double b = (double)oracle_bf16_to_float(w[(size_t)e * H + h]);
+        sum = sum + a * b;
+      }
+      logits[(size_t)t * E + e] = oracle_double_to_bf16(sum);
+    }
+  }
+  return ORACLE_OK;
 }
 
 /* The whole path: route step then sort step. */

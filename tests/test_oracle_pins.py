@@ -362,3 +362,81 @@ def test_softmax_two_experts_closed_form(oracle_mod):
     logits = datagen.float32_to_bf16_bits(np.float32([[1.0, 3.0, 3.0, 0.0]]))
     ids, w = oracle_mod.route_softmax(logits, 2, 4.0)
     assert ids.tolist() == [[1, 2]] and w.tolist() == [[2.0, 2.0]]
+
+
+# -------------------------------------------- gate projection (reading R14)
+def _bf16_neighbours_rne(v: float) -> int:
+    # independent rounding: exact rational comparison against the two bracketing finite
+    # bf16 values from the full table, ties to the even pattern
+    # (on |v| over the non-negative patterns 0x0000..0x7f80; the sign is put back after)
+    from fractions import Fraction
+    sign = 0x8000 if math.copysign(1.0, v) < 0 else 0
+    a = abs(v)
+    bits = np.arange(0x7F81, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32).astype(np.float64)  # ascending, ends at +inf
+    i = int(np.searchsorted(vals, a, side="left"))
+    if vals[i] == a:
+        return int(bits[i]) | sign
+    lo, hi = i - 1, i
+    dl = Fraction(a) - Fraction(float(vals[lo]))
+    dh = (Fraction(float(vals[hi])) - Fraction(a)) if np.isfinite(vals[hi]) else None
+    if dh is None or dl < dh:
+        pick = lo
+    elif dh < dl:
+        pick = hi
+    else:
+        pick = lo if (int(bits[lo]) & 1) == 0 else hi
+    return int(bits[pick]) | sign
+
+
+def test_double_to_bf16_rounds_once_to_nearest_even(oracle_mod):
+    # ties: 1 + 2^-8 lies halfway between 1 (0x3f80) and 1 + 2^-7 (0x3f81): even is 0x3f80;
+    # 1 + 3 * 2^-8 lies halfway between 0x3f81 and 0x3f82: even is 0x3f82
+    assert oracle_mod.double_to_bf16(1 + 2 ** -8) == 0x3F80
+    assert oracle_mod.double_to_bf16(1 + 3 * 2 ** -8) == 0x3F82
+    assert oracle_mod.double_to_bf16(-(1 + 3 * 2 ** -8)) == 0xBF82
+    # just above a tie rounds up (a double rounding through float32 would lose this)
+    assert oracle_mod.double_to_bf16(1 + 2 ** -8 + 2 ** -40) == 0x3F81
+    assert oracle_mod.double_to_bf16(0.0) == 0x0000
+    assert oracle_mod.double_to_bf16(-0.0) == 0x8000
+    assert oracle_mod.double_to_bf16(1e39) == 0x7F80
+    rng = np.random.default_rng(21)
+    vals = np.concatenate([rng.standard_normal(300) * 10.0 ** rng.integers(-30, 30, 300),
+                           rng.standard_normal(100) * 1e-39])  # subnormal range too
+    for v in vals:
+        assert oracle_mod.double_to_bf16(float(v)) == _bf16_neighbours_rne(float(v)), v
+
+
+def test_gate_logits_exact_on_a_coarse_grid(oracle_mod):
+    # hidden = i/16, w = j/64 with small integers: every partial sum is a multiple of 2^-10
+    # below 2^9, so the dot products are exact in float32; torch's float32 -> bf16
+    # conversion (one rounding, nearest-even) must then give the same bits
+    rng = np.random.default_rng(22)
+    T, E, H = 5, 48, 1024
+    h = rng.integers(-16, 17, (T, H)) / 16.0
+    w = rng.integers(-3, 4, (E, H)) / 64.0
+    hb = datagen.float32_to_bf16_bits(h.astype(np.float32))
+    wb = datagen.float32_to_bf16_bits(w.astype(np.float32))
+    got = oracle_mod.gate_logits(hb, wb)
+    exact = (h @ w.T).astype(np.float32)
+    assert np.array_equal((h @ w.T), exact.astype(np.float64))  # representable exactly
+    want = torch.from_numpy(exact).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_gate_logits_within_half_ulp_of_float64(oracle_mod):
+    rng = np.random.default_rng(23)
+    T, E, H = 3, 40, 777
+    hb = datagen.float32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wb = datagen.float32_to_bf16_bits((rng.standard_normal((E, H)) * 0.03).astype(np.float32))
+    got = oracle_mod.gate_logits(hb, wb)
+    hx = (hb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wx = (wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = hx @ wx.T
+    g = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # the bf16 spacing at |ref| is 2^(floor(log2|ref|) - 7)
+    spacing = 2.0 ** (np.floor(np.log2(np.abs(ref))) - 7)
+    assert np.all(np.abs(g - ref) <= 0.5 * spacing * (1 + 1e-12))
+    for t in range(T):  # and the row/column roles are not swapped
+        for e in (0, 17, 39):
+            assert got[t, e] == _bf16_neighbours_rne(float(np.dot(hx[t], wx[e])))
