@@ -70,7 +70,7 @@ extern "C" {
 #define MOE_RS_ERR_BAD_GROUPS (-3)        /* G outside [1, 64], E % G != 0, Kg outside [1,G] */
 #define MOE_RS_ERR_BAD_TOPK (-4)          /* K outside [1, 32] or K > Kg * g               */
 #define MOE_RS_ERR_BAD_BLOCK_M (-5)       /* B not a power of two in [1, 1024]             */
-#define MOE_RS_ERR_BAD_TOKENS (-6)        /* T < 0                                         */
+#define MOE_RS_ERR_BAD_TOKENS (-6)        /* T < 0 (or T > 8 for moe_gate_route_sort)      */
 #define MOE_RS_ERR_OVERFLOW (-7)          /* N or the padded length does not fit in int32  */
 #define MOE_RS_ERR_MISALIGNED (-8)        /* logits not 16-byte aligned, or another buffer
                                              not aligned to its element size (workspace: 16) */
@@ -80,6 +80,7 @@ extern "C" {
 #define MOE_RS_ERR_LAUNCH (-12)           /* the CUDA runtime rejected a kernel launch     */
 #define MOE_RS_ERR_TOO_LARGE (-13)        /* shape needs more than the static scratch of
                                              moe_route_sort_noalloc                        */
+#define MOE_RS_ERR_BAD_HIDDEN (-14)       /* H not a multiple of 8 in [8, 8192]            */
 
 /* Device-side status bits, written to the first int32 of the workspace by every call. */
 #define MOE_RS_DEVICE_BAD_EXPERT_ID 0x1   /* moe_sort saw an id >= E; those routes dropped */
@@ -132,6 +133,31 @@ int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, floa
                            int32_t* sorted_token_ids, float* sorted_weights,
                            int32_t* expert_ids, int32_t* num_tokens_post_pad,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The router gate projection fused ahead of the whole path, for batch-one decode and other
+ * calls of up to 8 tokens ("perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff
+ * (stack)", Summary: the stack specialises the Kimi-K3 B1 gate projection whose logits the
+ * route-sort consumes).  First
+ *   logits[t,e] = bf16 nearest (ties to even) to sum over h of hidden[t,h] * w_gate[e,h],
+ * with the sum accumulated in fp32 in a fixed order (so the same inputs always give the same
+ * logits; the rounding is exactly that of the true dot product whenever the fp32 partial
+ * sums are exact, for example on coarse value grids), then moe_route_sort on those logits.
+ * hidden_bf16: [T,H] bf16, w_gate_bf16: [E,H] bf16 (one row per expert, the layout of a
+ * linear layer's weight), both 16-byte aligned device memory, read only; logits_bf16: [T,E]
+ * bf16 device output owned by the caller (16-byte aligned), also the path's input.  The
+ * projection reads the gate matrix once (E*H*2 bytes) with CUDA-core FMAs: at T <= 8 it is a
+ * matrix-vector product bound by that read.  The route kernels start while it runs and wait
+ * for its results on the device, so the call is one stream-ordered sequence.
+ * Limits: those of moe_route_sort, plus 0 <= T <= 8 and H a multiple of 8 in [8, 8192].
+ * Errors: those of moe_route_sort, plus MOE_RS_ERR_BAD_HIDDEN, MOE_RS_ERR_BAD_TOKENS for
+ * T > 8, MOE_RS_ERR_NULL_POINTER / MOE_RS_ERR_MISALIGNED for hidden, w_gate or logits, and
+ * MOE_RS_ERR_ALIAS if hidden or w_gate overlaps any output or the workspace. */
+int moe_gate_route_sort(const void* hidden_bf16, const void* w_gate_bf16, const float* bias,
+                        int T, int E, int H, int n_group, int topk_group, int topk,
+                        float routed_scale, int block_m, void* logits_bf16, int32_t* topk_ids,
+                        float* topk_weights, int32_t* sorted_token_ids, float* sorted_weights,
+                        int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
 
 /* Route step only ("grouped top-k" of the same Summary): topk_ids/topk_weights [T,K]. */
 int moe_topk(const void* logits_bf16, const float* bias, int T, int E, int n_group,

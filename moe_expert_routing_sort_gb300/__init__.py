@@ -11,7 +11,9 @@ from .binding import (  # noqa: F401
     RouteSortBuffers,
     RouteSortError,
     library_path,
+    gate_route_sort,
     load,
+    moe_gate_route_sort,
     moe_route_sort,
     moe_route_sort_noalloc,
     moe_route_sort_proxy_selftest,

@@ -58,6 +58,9 @@ def load() -> ctypes.CDLL:
         lib.moe_route_sort_strerror.restype = ctypes.c_char_p
         lib.moe_route_sort.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P, S, P]
         lib.moe_route_sort.restype = I
+        lib.moe_gate_route_sort.argtypes = [P, P, P, I, I, I, I, I, I, F, I, P, P, P, P, P, P,
+                                            P, P, S, P]
+        lib.moe_gate_route_sort.restype = I
         lib.moe_route_sort_softmax.argtypes = [P, I, I, I, F, I, P, P, P, P, P, P, P, S, P]
         lib.moe_route_sort_softmax.restype = I
         lib.moe_topk.argtypes = [P, P, I, I, I, I, I, F, P, P, P]
@@ -172,6 +175,51 @@ def route_sort_softmax(logits, topk, routed_scale, block_m,
                            out.sorted_token_ids, out.sorted_weights, out.expert_ids,
                            out.num_tokens_post_pad, out.workspace, stream=stream)
     return out
+
+
+def moe_gate_route_sort(hidden, w_gate, bias, n_group, topk_group, topk, routed_scale,
+                        block_m, logits, topk_ids, topk_weights, sorted_token_ids,
+                        sorted_weights, expert_ids, num_tokens_post_pad, workspace,
+                        stream=None) -> None:
+    """Gate projection (hidden [T,H] x w_gate [E,H]) into ``logits`` [T,E], then the whole
+    path, into caller-owned buffers (see include/moe_route_sort.h)."""
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(w_gate, torch.bfloat16, "w_gate")
+    _need(bias, torch.float32, "bias")
+    _need(logits, torch.bfloat16, "logits")
+    if tuple(w_gate.shape) != (E, H) or tuple(logits.shape) != (T, E):
+        raise ValueError("w_gate must be [E, H] and logits [T, E] for hidden [T, H]")
+    for t, dt, n in [(topk_ids, torch.int32, "topk_ids"), (topk_weights, torch.float32,
+                     "topk_weights"), (sorted_token_ids, torch.int32, "sorted_token_ids"),
+                     (sorted_weights, torch.float32, "sorted_weights"),
+                     (expert_ids, torch.int32, "expert_ids"),
+                     (num_tokens_post_pad, torch.int32, "num_tokens_post_pad"),
+                     (workspace, torch.uint8, "workspace")]:
+        _need(t, dt, n)
+    rc = load().moe_gate_route_sort(
+        _ptr(hidden), _ptr(w_gate), _ptr(bias), T, E, H, n_group, topk_group, topk,
+        float(routed_scale), block_m, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
+        _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
+        _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "moe_gate_route_sort")
+
+
+def gate_route_sort(hidden, w_gate, bias, n_group, topk_group, topk, routed_scale, block_m,
+                    out: Optional[RouteSortBuffers] = None, logits=None, stream=None):
+    """Allocate (unless given) and run moe_gate_route_sort; returns (logits, buffers)."""
+    T = hidden.shape[0]
+    E = w_gate.shape[0]
+    if out is None:
+        out = RouteSortBuffers.allocate(T, E, topk, block_m, device=hidden.device)
+    if logits is None:
+        logits = torch.empty(T, E, dtype=torch.bfloat16, device=hidden.device)
+    moe_gate_route_sort(hidden, w_gate, bias, n_group, topk_group, topk, routed_scale, block_m,
+                        logits, out.topk_ids, out.topk_weights, out.sorted_token_ids,
+                        out.sorted_weights, out.expert_ids, out.num_tokens_post_pad,
+                        out.workspace, stream=stream)
+    return logits, out
 
 
 def moe_route_sort_noalloc(logits, bias, n_group, topk_group, topk, routed_scale, block_m,

@@ -310,7 +310,8 @@ const char* moe_route_sort_strerror(int status) {
     case MOE_RS_ERR_BAD_TOPK:
       return "topk must be in [1, 32] and at most topk_group * (E / n_group)";
     case MOE_RS_ERR_BAD_BLOCK_M: return "block_m must be a power of two in [1, 1024]";
-    case MOE_RS_ERR_BAD_TOKENS: return "number of tokens T must be >= 0";
+    case MOE_RS_ERR_BAD_TOKENS:
+      return "number of tokens T must be >= 0 (and at most 8 for moe_gate_route_sort)";
     case MOE_RS_ERR_OVERFLOW: return "T*topk or the padded length does not fit in int32";
     case MOE_RS_ERR_MISALIGNED:
       return "logits/workspace must be 16-byte aligned, other buffers 4-byte aligned";
@@ -320,6 +321,8 @@ const char* moe_route_sort_strerror(int status) {
     case MOE_RS_ERR_LAUNCH: return "the CUDA runtime rejected a kernel launch";
     case MOE_RS_ERR_TOO_LARGE:
       return "the shape needs more scratch than moe_route_sort_noalloc's static 32 MiB";
+    case MOE_RS_ERR_BAD_HIDDEN:
+      return "hidden size H must be a multiple of 8 in [8, 8192]";
     default: return "unknown status";
   }
 }
@@ -350,14 +353,24 @@ int moe_topk(const void* logits_bf16, const float* bias, int T, int E, int n_gro
 
 namespace {
 
+// Gate projection run ahead of the path (moe_gate_route_sort): it writes the logits the
+// path then reads.  Checked by the caller except for what route_sort_impl checks itself.
+struct GatePre {
+  const void* hidden;
+  const void* w_gate;
+  int H;
+};
+
 // The whole path for both scorings: sigmoid + bias with grouped top-k (softmax == false), or
 // softmax over the logits with plain top-k (softmax == true: n_group = topk_group = 1 and
-// bias unused, may be NULL).
+// bias unused, may be NULL).  With `gate`, the gate projection producing logits_bf16 is
+// launched first, once every argument has been accepted.
 int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, int n_group,
                     int topk_group, int topk, float routed_scale, int block_m, bool softmax,
-                    int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
-                    float* sorted_weights, int32_t* expert_ids, int32_t* num_tokens_post_pad,
-                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                    const GatePre* gate, int32_t* topk_ids, float* topk_weights,
+                    int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
+                    int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
   int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
   if (rc) return rc;
   rc = check_sort_shape(T, E, topk, block_m);
@@ -388,6 +401,23 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
   if (T == 0) return launch_status(launch_empty(num_tokens_post_pad, status, stream));
+  if (gate) {
+    DeviceInfo gd;
+    if (!device_info(gd)) return MOE_RS_ERR_LAUNCH;
+    const GatePlan gp = gate_plan(T, E, gate->H, gd.sms);
+    if (gp.smem > static_cast<size_t>(gd.smem_optin)) return MOE_RS_ERR_LAUNCH;
+    GateArgs ga{};
+    ga.hidden = static_cast<const uint16_t*>(gate->hidden);
+    ga.w = static_cast<const uint16_t*>(gate->w_gate);
+    ga.logits = static_cast<uint16_t*>(const_cast<void*>(logits_bf16));
+    ga.T = T;
+    ga.E = E;
+    ga.H = gate->H;
+    ga.rpc = gp.rpc;
+    ga.nch = gp.nch;
+    rc = launch_status(launch_gate(ga, gp, stream));
+    if (rc) return rc;
+  }
 
   if (T == 1) {
     DecodeArgs a{};
@@ -464,7 +494,47 @@ int moe_route_sort(const void* logits_bf16, const float* bias, int T, int E, int
                    int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream) {
   return route_sort_impl(logits_bf16, bias, T, E, n_group, topk_group, topk, routed_scale,
-                         block_m, false, topk_ids, topk_weights, sorted_token_ids,
+                         block_m, false, nullptr, topk_ids, topk_weights, sorted_token_ids,
+                         sorted_weights, expert_ids, num_tokens_post_pad, workspace,
+                         workspace_bytes, stream);
+}
+
+int moe_gate_route_sort(const void* hidden_bf16, const void* w_gate_bf16, const float* bias,
+                        int T, int E, int H, int n_group, int topk_group, int topk,
+                        float routed_scale, int block_m, void* logits_bf16, int32_t* topk_ids,
+                        float* topk_weights, int32_t* sorted_token_ids, float* sorted_weights,
+                        int32_t* expert_ids, int32_t* num_tokens_post_pad, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  if (T > kGateMaxTokens) return MOE_RS_ERR_BAD_TOKENS;
+  if (H < 8 || H > kGateMaxHidden || H % 8 != 0) return MOE_RS_ERR_BAD_HIDDEN;
+  int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
+  if (rc) return rc;
+  if (T > 0) {
+    if (!hidden_bf16 || !w_gate_bf16 || !logits_bf16) return MOE_RS_ERR_NULL_POINTER;
+    if (!aligned(hidden_bf16, 16) || !aligned(w_gate_bf16, 16)) return MOE_RS_ERR_MISALIGNED;
+    // the gate's inputs must not overlap anything the call writes
+    const size_t NK = static_cast<size_t>(T) * topk;
+    const size_t P = block_m >= 1 && (block_m & (block_m - 1)) == 0
+                         ? static_cast<size_t>(max_padded64(T, E, topk, block_m))
+                         : 0;
+    const size_t NB = block_m >= 1 ? P / static_cast<size_t>(block_m) : 0;
+    const Span outs[] = {span(logits_bf16, 2 * static_cast<size_t>(T) * E),
+                         span(topk_ids, topk_ids ? 4 * NK : 0),
+                         span(topk_weights, topk_weights ? 4 * NK : 0),
+                         span(sorted_token_ids, sorted_token_ids ? 4 * P : 0),
+                         span(sorted_weights, sorted_weights ? 4 * P : 0),
+                         span(expert_ids, expert_ids ? 4 * NB : 0),
+                         span(num_tokens_post_pad, num_tokens_post_pad ? 4 : 0),
+                         span(workspace, workspace ? workspace_bytes : 0)};
+    const Span ins[] = {span(hidden_bf16, 2 * static_cast<size_t>(T) * H),
+                        span(w_gate_bf16, 2 * static_cast<size_t>(E) * H)};
+    for (const Span& o : outs)
+      for (const Span& i : ins)
+        if (overlap(o, i)) return MOE_RS_ERR_ALIAS;
+  }
+  const GatePre gate{hidden_bf16, w_gate_bf16, H};
+  return route_sort_impl(logits_bf16, bias, T, E, n_group, topk_group, topk, routed_scale,
+                         block_m, false, &gate, topk_ids, topk_weights, sorted_token_ids,
                          sorted_weights, expert_ids, num_tokens_post_pad, workspace,
                          workspace_bytes, stream);
 }
@@ -475,7 +545,7 @@ int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, floa
                            int32_t* expert_ids, int32_t* num_tokens_post_pad,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return route_sort_impl(logits_bf16, nullptr, T, E, 1, 1, topk, routed_scale, block_m, true,
-                         topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
+                         nullptr, topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
                          num_tokens_post_pad, workspace, workspace_bytes, stream);
 }
 

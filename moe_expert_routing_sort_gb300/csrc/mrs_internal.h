@@ -214,6 +214,25 @@ struct AtomicSortArgs {
 int atomic_sort_blocks(int N, int sms);
 cudaError_t launch_atomic_sort(const AtomicSortArgs& a, int nblk, cudaStream_t st);
 
+// ------------------------------------------------------ gate projection (GEMV)
+constexpr int kGateMaxTokens = 8;     // tokens per call of the gate path
+constexpr int kGateMaxHidden = 8192;  // hidden size limit (a multiple of 8)
+struct GateArgs {
+  const uint16_t* hidden;  // [T, H] bf16
+  const uint16_t* w;       // [E, H] bf16, one gate row per expert
+  uint16_t* logits;        // [T, E] bf16
+  int T, E, H;
+  int rpc;  // gate rows per CTA
+  int nch;  // chunks per row
+};
+// Launch plan: rows per CTA, grid, chunks per row and shared memory for `sms` SMs.
+struct GatePlan {
+  int rpc, grid, nch;
+  size_t smem;
+};
+GatePlan gate_plan(int T, int E, int H, int sms);
+cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
+
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);

@@ -15,6 +15,16 @@ Recipe (numpy ``default_rng(seed)``, PCG64), in draw order:
   4. redraws: for each row the callback names (ascending), ``E`` new normals from the same
      stream with the same recipe; repeated until the callback names no row (at most
      ``max_rounds`` rounds, else an error).
+
+Gate-projection inputs (``make_gate_inputs``: hidden states and gate rows that produce the
+logits), numpy ``default_rng(seed)``, in draw order:
+  1. bias as in step 2 above;
+  2. gate rows ``rng.integers(-3, 4, (E, H)) / 64``;
+  3. hidden rows ``rng.integers(-16, 17, (T, H)) / 16``;
+  4. redraws of hidden rows as in step 4 above.
+Both grids are exact in bf16, and every partial sum of a dot product is a multiple of 2^-10
+below 2^9 (H <= 8192), so a float32 accumulation of it is exact in any order.  With H = 7168
+the logits have a standard deviation of about 1.6.
 """
 from __future__ import annotations
 
@@ -133,3 +143,44 @@ def make_inputs(
             sub = needs_redraw(logits[rows], bias)
             rows = sorted(rows[int(i)] for i in sub)
     return RouterInputs(w, logits, bias, redrawn)
+
+
+@dataclass
+class GateInputs:
+    hidden_bf16: np.ndarray  # uint16 [T, H], bf16 bit patterns
+    w_gate_bf16: np.ndarray  # uint16 [E, H], one gate row per expert
+    bias: np.ndarray  # float32 [E]
+    redrawn_rows: int = 0
+
+
+def make_gate_inputs(
+    T: int,
+    E: int,
+    H: int,
+    bias_half_range: float = 0.1,
+    seed: int = 0,
+    needs_redraw: Optional[Callable[[np.ndarray, np.ndarray, np.ndarray], Iterable[int]]] = None,
+    max_rounds: int = 64,
+) -> GateInputs:
+    """Draw hidden states and gate rows on the coarse grids of the recipe above."""
+    rng = np.random.default_rng(seed)
+    bias = rng.uniform(-bias_half_range, bias_half_range, E).astype(np.float32)
+    w = float32_to_bf16_bits((rng.integers(-3, 4, (E, H)) / 64.0).astype(np.float32))
+
+    def rows(n):
+        return float32_to_bf16_bits((rng.integers(-16, 17, (n, H)) / 16.0).astype(np.float32))
+
+    hidden = rows(T)
+    redrawn = 0
+    if needs_redraw is not None and T > 0:
+        todo = sorted(set(int(r) for r in needs_redraw(hidden, w, bias)))
+        rounds = 0
+        while todo:
+            rounds += 1
+            if rounds > max_rounds:
+                raise RuntimeError(f"near-tie hidden rows remain after {max_rounds} rounds")
+            hidden[todo] = rows(len(todo))
+            redrawn += len(todo)
+            sub = needs_redraw(hidden[todo], w, bias)
+            todo = sorted(todo[int(i)] for i in sub)
+    return GateInputs(hidden, w, bias, redrawn)

@@ -59,6 +59,18 @@ def redraw_callback(oracle_mod, w):
     return needs
 
 
+def gate_redraw_callback(oracle_mod, n_group, topk_group, topk):
+    """needs_redraw(hidden, w_gate, bias) -> hidden rows whose logits (from the oracle's gate
+    projection) have an oracle selection margin below NEAR_TIE."""
+
+    def needs(hidden, w_gate, bias):
+        logits = oracle_mod.gate_logits(hidden, w_gate)
+        m = oracle_mod.margins(logits, bias, n_group, topk_group, topk)
+        return np.nonzero(m < NEAR_TIE)[0]
+
+    return needs
+
+
 def check_sort_invariants(topk_ids, E, block_m, sorted_token_ids, expert_ids, npp,
                           sorted_weights=None, topk_weights=None):
     """Properties the sort output must have for any valid input (dropped ids allowed).

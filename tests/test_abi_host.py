@@ -48,7 +48,7 @@ def test_size_queries():
 
 
 def test_strerror_covers_codes():
-    for code in range(-12, 1):
+    for code in range(-14, 1):
         assert mrs.strerror(code) != "unknown status"
     assert mrs.strerror(-99) == "unknown status"
 
@@ -160,3 +160,28 @@ def test_softmax_variant_validates(lib):
     assert _softmax(lib, logits=BASE + 4) == -8
     assert _softmax(lib, ws_bytes=16) == -10
     assert _softmax(lib, ids=BASE + 0x30000) == -9  # topk ids over topk weights
+
+
+def _gate(lib, T=2, E=64, H=256, hidden=BASE + 0x200000, w_gate=BASE + 0x210000,
+          logits=BASE + 0x300000, ids=BASE + 0x20000, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = mrs.moe_route_sort_workspace_bytes(max(T, 0), E, 6, 16)
+    return lib.moe_gate_route_sort(hidden, w_gate, BASE + 0x10000, T, E, H, 8, 4, 6, 2.5, 16,
+                                   logits, ids, BASE + 0x30000, BASE + 0x40000, BASE + 0x80000,
+                                   BASE + 0xC0000, BASE + 0xD0000, BASE + 0x100000, ws_bytes,
+                                   None)
+
+
+def test_gate_variant_validates(lib):
+    assert _gate(lib, T=9) == -6       # at most 8 tokens
+    assert _gate(lib, H=7) == -14
+    assert _gate(lib, H=0) == -14
+    assert _gate(lib, H=8200) == -14
+    assert _gate(lib, hidden=0) == -1
+    assert _gate(lib, logits=0) == -1
+    assert _gate(lib, w_gate=BASE + 0x210008) == -8
+    assert _gate(lib, logits=BASE + 0x300002) == -8
+    assert _gate(lib, hidden=BASE + 0x300000) == -9  # hidden over the logits output
+    assert _gate(lib, w_gate=BASE + 0x100000) == -9  # gate rows over the workspace
+    assert _gate(lib, ids=BASE + 0x300010) == -9     # topk ids over the logits
+    assert _gate(lib, ws_bytes=16) == -10
