@@ -357,6 +357,79 @@ def measure_sort_only(w, steps, warmup, world, atomic: bool, calls: int = 16):
     return ms * 1e3 / (steps * calls)
 
 
+def measure_gate(T, E, H, steps, warmup, world, peak_gbs, unfused=True):
+    """moe_gate_route_sort (gate GEMV + the whole path) on the decode shape: per-call time of a
+    graph over rotating sets (each its own gate matrix, more than twice the L2 in total, so
+    every call reads its matrix from HBM), L2 flushed before each step.  With `unfused`, the
+    same calls with the gate as a cuBLAS matmul followed by route_sort, for comparison."""
+    import torch
+
+    import moe_expert_routing_sort_gb300 as mrs
+
+    w = datagen.workload(HEADLINE)
+    n_sets = int(min(48, max(2, math.ceil(2 * L2_BYTES / (2 * E * H)))))
+    sets = []
+    for i in range(n_sets):
+        inp = datagen.make_gate_inputs(T, E, H, seed=100 + i)
+        hid = torch.from_numpy(inp.hidden_bf16.view(np.int16)).view(torch.bfloat16).cuda()
+        wg = torch.from_numpy(inp.w_gate_bf16.view(np.int16)).view(torch.bfloat16).cuda()
+        bias = torch.from_numpy(inp.bias).cuda()
+        out = mrs.RouteSortBuffers.allocate(T, E, w.topk, w.block_m, device="cuda")
+        logits = torch.empty(T, E, dtype=torch.bfloat16, device="cuda")
+        sets.append((hid, wg, bias, out, logits))
+    s = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def fused():
+        for hid, wg, bias, out, logits in sets:
+            mrs.gate_route_sort(hid, wg, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                                w.block_m, out=out, logits=logits, stream=s)
+
+    def split():
+        for hid, wg, bias, out, logits in sets:
+            torch.matmul(hid, wg.t(), out=logits)
+            mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                           w.block_m, out=out, stream=s)
+
+    def per_call_us(fn):
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                flush.fill_(1)
+                g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        barrier(world)
+        with torch.cuda.stream(s):
+            for k, (a, b) in enumerate(ev):
+                flush.fill_(k & 0xFF)
+                a.record(s)
+                g.replay()
+                b.record(s)
+        torch.cuda.synchronize()
+        ms = dist_max(sum(a.elapsed_time(b) for a, b in ev), world)
+        return ms * 1e3 / (steps * n_sets)
+
+    us = per_call_us(fused)
+    gate_bytes = 2 * E * H + 2 * T * H + 2 * T * E
+    res = {"T": T, "E": E, "H": H, "us_per_call": us, "calls_per_step": n_sets,
+           "gate_bytes_per_call": gate_bytes,
+           "gate_bytes_over_whole_call_gbs": gate_bytes / (us * 1e-6) / 1e9,
+           "gate_bytes_over_whole_call_frac": gate_bytes / (us * 1e-6) / 1e9 / peak_gbs,
+           "launches_per_call": 2}
+    if unfused:
+        with torch.cuda.stream(s):
+            split()  # cuBLAS picks its kernel outside capture
+        res["unfused_cublas_gate_us_per_call"] = per_call_us(split)
+    return res
+
+
 # ----------------------------------------------------------------- CPU oracle
 def cpu_oracle_rate(w, budget_s: float):
     """Time the oracle on a bounded sample of workload w: (seconds per token, sample text)."""
@@ -468,12 +541,20 @@ def main():
                     "deterministic": measure_sort_only(ws, n, args.warmup, world, False),
                     "atomic_order": measure_sort_only(ws, n, args.warmup, world, True)}
 
+    if not args.no_secondary:
+        # the router gate projection fused ahead of the path (batch-one decode shape)
+        n = max(3, min(args.steps, 10))
+        configs["gate_decode_T1_E896_H7168"] = measure_gate(1, 896, 7168, n, args.warmup,
+                                                            world, peak)
+
     cpu = None
     if rank == 0:
         secs, sample = cpu_oracle_rate(w, args.cpu_budget)
         cpu = {"value": secs * 1e6, "unit": "us/call", "cores": 1, "kind": "oracle",
                "sample": sample}
         for name in configs:
+            if name not in datagen.WORKLOADS:
+                continue
             ws = datagen.workload(name)
             s2, samp2 = cpu_oracle_rate(ws, 3.0)
             configs[name]["cpu_oracle_tokens_per_s"] = 1.0 / s2

@@ -145,9 +145,10 @@ int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, floa
  * hidden_bf16: [T,H] bf16, w_gate_bf16: [E,H] bf16 (one row per expert, the layout of a
  * linear layer's weight), both 16-byte aligned device memory, read only; logits_bf16: [T,E]
  * bf16 device output owned by the caller (16-byte aligned), also the path's input.  The
- * projection reads the gate matrix once (E*H*2 bytes) with CUDA-core FMAs: at T <= 8 it is a
- * matrix-vector product bound by that read.  The route kernels start while it runs and wait
- * for its results on the device, so the call is one stream-ordered sequence.
+ * projection reads the gate matrix once (E*H*2 bytes); at T <= 8 it is bound by that read, and
+ * its arithmetic runs as m16n8k16 bf16 tensor-core MMAs with fp32 accumulation (tokens on the
+ * N side).  The route kernels start while it runs and wait for its results on the device, so
+ * the call is one stream-ordered sequence.
  * Limits: those of moe_route_sort, plus 0 <= T <= 8 and H a multiple of 8 in [8, 8192].
  * Errors: those of moe_route_sort, plus MOE_RS_ERR_BAD_HIDDEN, MOE_RS_ERR_BAD_TOKENS for
  * T > 8, MOE_RS_ERR_NULL_POINTER / MOE_RS_ERR_MISALIGNED for hidden, w_gate or logits, and

@@ -1,123 +1,116 @@
 // mrs_gate.cu -- the router gate projection ahead of the path, for a few tokens (a GEMV).
 //
 // logits[t, e] = bf16(sum over h of hidden[t, h] * w_gate[e, h]) for T <= 8 tokens.  At these
-// sizes the projection is a matrix-vector product bound by one read of the E x H bf16 gate
-// matrix, so it runs on CUDA-core FMAs: a tensor-core tile would be at most 8/128 full.
-//   rows     CTA c owns gate rows [c * rpc, (c + 1) * rpc), rpc = ceil(E / SMs): one wave
-//   hidden   the T hidden rows are staged in shared memory once per CTA
-//   chunks   a row is cut into chunks of 32 lanes x kGateVec 16-byte vectors (coalesced
-//            512-byte warp loads); warps take the CTA's (row, chunk) items in a fixed order,
-//            reduce each over the lanes with a fixed butterfly and park the partial in
-//            shared memory; a row's partials are then added in chunk order
-// The fp32 result therefore does not depend on scheduling, and it is exact (so its single
-// rounding to bf16 is that of the exact dot product) whenever the products and partial sums
-// are exactly representable.  The route kernels that follow are programmatic dependents:
-// they are launched while this grid runs and wait (griddepcontrol.wait) for its completion
-// before reading the logits, which are still in L2.
-// Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary --
-// the stack specialises the Kimi-K3 batch-one gate projection that feeds the route-sort.
+// sizes the projection is bound by one read of the E x H bf16 gate matrix; the arithmetic goes
+// to the tensor cores so that it never competes with the loads for issue slots:
+//   tile     CTA c owns gate rows [c * rpc, c * rpc + nr), nr <= 16: the M side of an
+//            m16n8k16 bf16 MMA (fp32 accumulate); the tokens are its N = 8 side
+//   k split  the hidden dimension is cut into steps of 32 columns; warp w takes steps
+//            w, w + warps, ... and accumulates its two MMAs per step in order
+//   k order  the sum over k does not care how columns are assigned to the MMA's k slots, as
+//            long as A and B agree: lane (g, q) (g = lane / 4, q = lane % 4) loads the 16
+//            bytes of columns [32 s + 8 q, 32 s + 8 q + 8) of gate rows g and g + 8 and of
+//            hidden row g, and hands words 0-1 to the first MMA's k slots {2q, 2q+1, 2q+8,
+//            2q+9} and words 2-3 to the second's: every load is a contiguous 16 bytes
+//   combine  each warp parks its 16 x 8 partial tile in shared memory; the CTA adds the
+//            warps' partials in warp order and rounds once to bf16
+// The fp32 result therefore does not depend on scheduling, and it is exact (so its rounding to
+// bf16 is that of the exact dot product) whenever the partial sums are exactly representable.
+// The route kernels that follow are programmatic dependents: they are launched while this grid
+// runs and wait (griddepcontrol.wait) for its completion before reading the logits.
+// Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary -- the
+// stack specialises the Kimi-K3 batch-one gate projection that feeds the route-sort.
 #include <cuda_bf16.h>
 
 #include "mrs_internal.h"
 
 namespace mrs {
 
-constexpr int kGateThreads = 512;
+constexpr int kGateThreads = 256;
 constexpr int kGateWarps = kGateThreads / 32;
-constexpr int kGateVec = 4;  // 16-byte vectors per lane per chunk
+constexpr int kGateRows = 16;  // M of the MMA tile: gate rows per CTA, at most
+constexpr int kGateWin = 4;    // steps whose loads a warp keeps in flight
 
-__device__ __forceinline__ void bf16x8_to_float(const uint4& q, float (&f)[8]) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+// D += A * B for one m16n8k16 bf16 MMA with fp32 accumulation (A row-major, B column-major).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(kGateThreads, 1) mrs_gate_kernel(const GateArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+__global__ void __launch_bounds__(kGateThreads, 2) mrs_gate_kernel(const GateArgs a) {
+  __shared__ float part[kGateWarps][kGateRows][kGateMaxTokens];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T = a.T, H8 = a.H >> 3, nch = a.nch, rpc = a.rpc;
-  uint4* hs = reinterpret_cast<uint4*>(smem);  // [T][H8]
-  float* part = reinterpret_cast<float*>(smem + align16(sizeof(uint4) * T * H8));  // [T][rpc][nch]
-  const int r0 = blockIdx.x * rpc;
-  const int nr = min(rpc, a.E - r0);
+  const int g = lane >> 2, q = lane & 3;
+  const int T = a.T, H = a.H;
+  const int r0 = blockIdx.x * a.rpc;
+  const int nr = min(a.rpc, a.E - r0);
+  const int steps = (H + 31) >> 5;
+  const int mine = (steps - warp + kGateWarps - 1) / kGateWarps;  // steps w, w + warps, ...
   pdl_trigger();
   pdl_wait();
 
-  const uint4* h4 = reinterpret_cast<const uint4*>(a.hidden);
-  for (int i = tid; i < T * H8; i += kGateThreads) hs[i] = h4[i];
-  __syncthreads();
-
-  const uint4* w4 = reinterpret_cast<const uint4*>(a.w);
-  const int items = nr * nch;
-  for (int it = warp; it < items; it += kGateWarps) {
-    const int r = it / nch, c = it - r * nch;
-    const uint4* wrow = w4 + static_cast<size_t>(r0 + r) * H8;
-    uint4 wv[kGateVec];
+  const bool row_lo = g < nr, row_hi = g + 8 < nr, tok = g < T;
+  const uint16_t* wlo = a.w + static_cast<size_t>(r0 + (row_lo ? g : 0)) * H;
+  const uint16_t* whi = a.w + static_cast<size_t>(r0 + (row_hi ? g + 8 : 0)) * H;
+  const uint16_t* hrow = a.hidden + static_cast<size_t>(tok ? g : 0) * H;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 wl[kGateWin], wh[kGateWin], hv[kGateWin];
+  auto load = [&](int k, int slot) {
+    const int col = 32 * (warp + k * kGateWarps) + 8 * q;
+    const bool in = k < mine && col < H;  // H is a multiple of 8: 8 columns all in or all out
+    wl[slot] = (in && row_lo) ? __ldg(reinterpret_cast<const uint4*>(wlo + col)) : zero;
+    wh[slot] = (in && row_hi) ? __ldg(reinterpret_cast<const uint4*>(whi + col)) : zero;
+    hv[slot] = (in && tok) ? __ldg(reinterpret_cast<const uint4*>(hrow + col)) : zero;
+  };
 #pragma unroll
-    for (int v = 0; v < kGateVec; ++v) {  // all of the item's loads in flight at once
-      const int j = (c * kGateVec + v) * 32 + lane;
-      wv[v] = (j < H8) ? __ldg(wrow + j) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    float acc[kGateMaxTokens];
+  for (int k = 0; k < kGateWin; ++k) load(k, k);
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int k0 = 0; k0 < mine; k0 += kGateWin) {
 #pragma unroll
-    for (int t = 0; t < kGateMaxTokens; ++t) acc[t] = 0.0f;
-#pragma unroll
-    for (int v = 0; v < kGateVec; ++v) {
-      const int j = (c * kGateVec + v) * 32 + lane;
-      if (j < H8) {
-        float wf[8];
-        bf16x8_to_float(wv[v], wf);
-#pragma unroll
-        for (int t = 0; t < kGateMaxTokens; ++t) {
-          if (t < T) {
-            float hf[8];
-            bf16x8_to_float(hs[t * H8 + j], hf);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[t] = fmaf(wf[q], hf[q], acc[t]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < kGateMaxTokens; ++t) {
-      if (t < T) {  // uniform over the warp
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(kFull, acc[t], d));
-        if (lane == 0) part[(t * rpc + r) * nch + c] = acc[t];
-      }
+    for (int b = 0; b < kGateWin; ++b) {
+      if (k0 + b >= mine) break;  // uniform over the warp
+      const uint4 x = wl[b], y = wh[b], z = hv[b];
+      mma_bf16_16816(d, x.x, y.x, x.y, y.y, z.x, z.y);
+      mma_bf16_16816(d, x.z, y.z, x.w, y.w, z.z, z.w);
+      load(k0 + b + kGateWin, b);  // refill the slot (nothing past the warp's steps)
     }
   }
+  // d[0], d[1]: row g, tokens 2q, 2q + 1; d[2], d[3]: row g + 8, the same tokens
+  part[warp][g][2 * q] = d[0];
+  part[warp][g][2 * q + 1] = d[1];
+  part[warp][g + 8][2 * q] = d[2];
+  part[warp][g + 8][2 * q + 1] = d[3];
   __syncthreads();
-  for (int i = tid; i < T * nr; i += kGateThreads) {
-    const int t = i / nr, r = i - t * nr;
-    const float* p = part + (t * rpc + r) * nch;
-    float s = p[0];
-    for (int c = 1; c < nch; ++c) s = __fadd_rn(s, p[c]);
-    a.logits[static_cast<size_t>(t) * a.E + r0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  for (int i = tid; i < nr * T; i += kGateThreads) {
+    const int r = i / T, t = i - r * T;
+    float sum = part[0][r][t];
+#pragma unroll
+    for (int w = 1; w < kGateWarps; ++w) sum = __fadd_rn(sum, part[w][r][t]);
+    a.logits[static_cast<size_t>(t) * a.E + r0 + r] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(sum));
   }
 }
 
 GatePlan gate_plan(int T, int E, int H, int sms) {
   GatePlan p{};
-  const int s = sms > 0 ? sms : 1;
-  p.rpc = (E + s - 1) / s;
-  p.grid = (E + p.rpc - 1) / p.rpc;
-  const int H8 = H / 8;
-  p.nch = (H8 + 32 * kGateVec - 1) / (32 * kGateVec);
-  p.smem = align16(sizeof(uint4) * static_cast<size_t>(T) * H8) +
-           sizeof(float) * static_cast<size_t>(T) * p.rpc * p.nch;
+  const int slots = 2 * (sms > 0 ? sms : 1);  // two CTAs per SM
+  int rpc = (E + slots - 1) / slots;
+  if (rpc > kGateRows) rpc = kGateRows;
+  p.rpc = rpc;
+  p.grid = (E + rpc - 1) / rpc;
+  p.nch = (H + 31) / 32;
+  p.smem = 0;
+  (void)T;
   return p;
 }
 
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(mrs_gate_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(p.smem));
-  if (err != cudaSuccess) return err;
-  return launch_pdl(mrs_gate_kernel, dim3(p.grid), dim3(kGateThreads), p.smem, st, a);
+  return launch_pdl(mrs_gate_kernel, dim3(p.grid), dim3(kGateThreads), 0, st, a);
 }
 
 }  // namespace mrs

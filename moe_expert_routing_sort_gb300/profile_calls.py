@@ -5,6 +5,7 @@ outputs of one workload once, issues ``--calls`` back-to-back ``route_sort`` cal
 current stream and synchronizes.  Example::
 
     python -m moe_expert_routing_sort_gb300.profile_calls --workload wide_T16384_E4096 --calls 4
+    python -m moe_expert_routing_sort_gb300.profile_calls --gate-hidden 7168 --calls 4
 """
 from __future__ import annotations
 
@@ -20,6 +21,8 @@ def main(argv=None) -> int:
     p.add_argument("--workload", default="decode_T1_E896_G8", choices=list(datagen.WORKLOADS))
     p.add_argument("--calls", type=int, default=8)
     p.add_argument("--tokens", type=int, default=None, help="override the workload's T")
+    p.add_argument("--gate-hidden", type=int, default=None,
+                   help="run moe_gate_route_sort with this hidden size (gate GEMV ahead)")
     args = p.parse_args(argv)
 
     import torch
@@ -32,6 +35,18 @@ def main(argv=None) -> int:
     logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).cuda()
     bias = torch.from_numpy(inp.bias).cuda()
     out = binding.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
+    if args.gate_hidden is not None:
+        g = datagen.make_gate_inputs(w.T, w.E, args.gate_hidden, seed=w.seed)
+        hid = torch.from_numpy(g.hidden_bf16.view(np.int16)).view(torch.bfloat16).cuda()
+        wg = torch.from_numpy(g.w_gate_bf16.view(np.int16)).view(torch.bfloat16).cuda()
+        gb = torch.from_numpy(g.bias).cuda()
+        for _ in range(args.calls):
+            binding.gate_route_sort(hid, wg, gb, w.n_group, w.topk_group, w.topk,
+                                    w.routed_scale, w.block_m, out=out, logits=logits)
+        torch.cuda.synchronize()
+        print(f"{w.name} with gate H={args.gate_hidden}: {args.calls} calls, "
+              f"status={out.status_word()}")
+        return 0
     for _ in range(args.calls):
         binding.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
                            w.block_m, out=out)
