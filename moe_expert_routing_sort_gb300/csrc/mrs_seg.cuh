@@ -40,6 +40,9 @@ struct SegShape {
   int softmax;   // 1: values are the logits (LogitRow), weights the renormalised softmax
 };
 
+// Hot units listed for the compacted survivor scan (the list reuses SegScratch::cand_s).
+constexpr int kHotCap = 2 * kCandCap;
+
 // Route scratch of one token (shared memory).
 struct __align__(16) SegScratch {
   unsigned long long cand[kCandCap];
@@ -388,9 +391,11 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
   }
   const float theta = tau - 2.0f * delta;
 
-  // ---- survivors: values >= theta in units whose bound may reach theta.  The lanes walk
-  // their hot units in step (one unit per lane per round, the next one's words loaded
-  // ahead) and append records (bf16 bits << 16) | expert at a segment-wide running count.
+  // ---- survivors: values >= theta in units whose bound may reach theta.  The segment's hot
+  // units are first compacted into one list (first expert of each unit, in lane order), so a
+  // round reads LT of them whichever lanes own them; the next round's words are loaded
+  // ahead.  Hits are appended as records (bf16 bits << 16) | expert at a segment-wide
+  // running count.  (A list longer than kHotCap falls back to each lane walking its own.)
   if (ll < sh.K) {
     ws.sel_id[ll] = -1;
     ws.sel_s[ll] = 0.0f;
@@ -398,28 +403,21 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
   const bool scan_mine = kept && m1 >= theta;
   unsigned long long hot = scan_mine ? hot_units(umax, lane, sh.nu, theta) : 0ull;
   const unsigned lt = lanemask_lt(lane) & lanes;
-  int total = 0;
-  bool have = hot != 0ull;
-  int u = 0;
-  uint2 wd = make_uint2(0u, 0u);
-  if (have) {
-    u = __ffsll(static_cast<long long>(hot)) - 1;
-    hot &= hot - 1ull;
-    wd = row.late_words(seg0 + 4 * u);
+  const int nh = __popcll(static_cast<long long>(hot));
+  int incl = nh;  // inclusive prefix of the hot-unit counts over the segment
+#pragma unroll
+  for (int d = 1; d < LT; d <<= 1) {
+    const int o = __shfl_up_sync(kFull, incl, d, LT);
+    if (ll >= d) incl += o;
   }
-  while (__any_sync(kFull, have)) {
-    const bool have_n = hot != 0ull;
-    int u_n = 0;
-    uint2 wd_n = make_uint2(0u, 0u);
-    if (have_n) {
-      u_n = __ffsll(static_cast<long long>(hot)) - 1;
-      hot &= hot - 1ull;
-      wd_n = row.late_words(seg0 + 4 * u_n);
-    }
+  const int htot = __shfl_sync(kFull, incl, LT - 1, LT);
+  int total = 0;
+  // one record round: lane's unit at e0 (if have) with words wd
+  auto round = [&](bool have, int e0, uint2 wd) {
     unsigned hits = 0u;
     if (have) {
       float v[4];
-      row.values(seg0 + 4 * u, wd, v);
+      row.values(e0, wd, v);
 #pragma unroll
       for (int t = 0; t < 4; ++t) hits |= (v[t] >= theta) ? (1u << t) : 0u;
     }
@@ -433,13 +431,54 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
     for (int t = 0; t < 4; ++t) {
       if ((hits >> t) & 1u) {
         if (pos < kCandCap)
-          ws.cand[pos] = (unit_bits(wd, t) << 16) | static_cast<uint32_t>(seg0 + 4 * u + t);
+          ws.cand[pos] = (unit_bits(wd, t) << 16) | static_cast<uint32_t>(e0 + t);
         ++pos;
       }
     }
-    have = have_n;
-    u = u_n;
-    wd = wd_n;
+  };
+  if (__all_sync(kFull, htot <= kHotCap)) {
+    unsigned short* list = reinterpret_cast<unsigned short*>(ws.cand_s);  // free until the
+    for (int i = incl - nh; hot != 0ull; ++i) {                           // exact evaluation
+      list[i] = static_cast<unsigned short>(seg0 + 4 * (__ffsll(static_cast<long long>(hot)) - 1));
+      hot &= hot - 1ull;
+    }
+    __syncwarp();
+    bool have = ll < htot;
+    int e0 = have ? list[ll] : 0;
+    uint2 wd = have ? row.late_words(e0) : make_uint2(0u, 0u);
+    for (int r = 0; __any_sync(kFull, r < htot); r += LT) {
+      const bool have_n = r + LT + ll < htot;
+      const int e0_n = have_n ? list[r + LT + ll] : 0;
+      const uint2 wd_n = have_n ? row.late_words(e0_n) : make_uint2(0u, 0u);
+      round(have, e0, wd);
+      have = have_n;
+      e0 = e0_n;
+      wd = wd_n;
+    }
+    __syncwarp();  // the list is overwritten by the exact scores below
+  } else {
+    bool have = hot != 0ull;
+    int u = 0;
+    uint2 wd = make_uint2(0u, 0u);
+    if (have) {
+      u = __ffsll(static_cast<long long>(hot)) - 1;
+      hot &= hot - 1ull;
+      wd = row.late_words(seg0 + 4 * u);
+    }
+    while (__any_sync(kFull, have)) {
+      const bool have_n = hot != 0ull;
+      int u_n = 0;
+      uint2 wd_n = make_uint2(0u, 0u);
+      if (have_n) {
+        u_n = __ffsll(static_cast<long long>(hot)) - 1;
+        hot &= hot - 1ull;
+        wd_n = row.late_words(seg0 + 4 * u_n);
+      }
+      round(have, seg0 + 4 * u, wd);
+      have = have_n;
+      u = u_n;
+      wd = wd_n;
+    }
   }
   const bool fits = __all_sync(kFull, total <= kCandCap);
   if (fits) release();  // the records hold the logit bits; the row is not read again
@@ -523,22 +562,20 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
   const bool mine = ll < sh.K;
   const float s = mine ? ws.sel_s[ll] : 0.0f;
   id = mine ? ws.sel_id[ll] : -1;
+  // every lane forms the same sum from the slot scores in shared memory, slot 0 first
+  float4 q4[kMaxTopk / 4];
+  const float4* s4 = reinterpret_cast<const float4*>(ws.sel_s);
+#pragma unroll
+  for (int i = 0; i < kMaxTopk / 4; ++i)
+    q4[i] = (4 * i < sh.K) ? s4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   float sum = 0.0f;
-  if (ll == 0) {
-    float4 q4[kMaxTopk / 4];
-    const float4* s4 = reinterpret_cast<const float4*>(ws.sel_s);
 #pragma unroll
-    for (int i = 0; i < kMaxTopk / 4; ++i)
-      q4[i] = (4 * i < sh.K) ? s4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < kMaxTopk / 4; ++i) {
-      if (4 * i < sh.K) sum = __fadd_rn(sum, q4[i].x);
-      if (4 * i + 1 < sh.K) sum = __fadd_rn(sum, q4[i].y);
-      if (4 * i + 2 < sh.K) sum = __fadd_rn(sum, q4[i].z);
-      if (4 * i + 3 < sh.K) sum = __fadd_rn(sum, q4[i].w);
-    }
+  for (int i = 0; i < kMaxTopk / 4; ++i) {
+    if (4 * i < sh.K) sum = __fadd_rn(sum, q4[i].x);
+    if (4 * i + 1 < sh.K) sum = __fadd_rn(sum, q4[i].y);
+    if (4 * i + 2 < sh.K) sum = __fadd_rn(sum, q4[i].z);
+    if (4 * i + 3 < sh.K) sum = __fadd_rn(sum, q4[i].w);
   }
-  sum = __shfl_sync(kFull, sum, 0, LT);
   w = mine ? __fmul_rn(__fdiv_rn(s, sum), sh.R) : 0.0f;
   __syncwarp();
 }
