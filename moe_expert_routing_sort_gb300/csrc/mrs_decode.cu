@@ -59,6 +59,8 @@ __host__ __device__ inline int decode_tpg(int G) {
   return t;
 }
 
+// kSoftmax: softmax scoring (keys are the logits, no bias).
+template <bool kSoftmax>
 __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
   __shared__ DecodeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       const int li = i + TPG * r;
       if (in_group && li < g) {
         x[r] = a.logits[j * g + li];
-        b[r] = a.softmax ? 0.0f : a.bias[j * g + li];
+        b[r] = kSoftmax ? 0.0f : a.bias[j * g + li];
       }
     }
     for (int p = tid; p < K * B; p += kDecodeThreads) {
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       key[r] = -INFINITY;
       sv[r] = 0.0f;
       if (r < R && in_group && li < g) {
-        key[r] = score_key(bf16_bits_to_float(x[r]), b[r], a.softmax != 0, sv[r]);
+        key[r] = score_key(bf16_bits_to_float(x[r]), b[r], kSoftmax, sv[r]);
         t2 = fmaxf(t2, fminf(t1, key[r]));
         t1 = fmaxf(t1, key[r]);
       }
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   }
 
   // ---- warp 0: weights, outputs and the one-token sort
-  if (a.softmax) softmax_terms(sm.sel_s, lane, K);
+  if (kSoftmax) softmax_terms(sm.sel_s, lane, K);
   const bool mine = lane < K;
   const int id = mine ? sm.sel_id[lane] : 0x7fffffff;
   const float s = mine ? sm.sel_s[lane] : 0.0f;
@@ -290,7 +292,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  return launch_pdl(mrs_decode_kernel, dim3(1), dim3(kDecodeThreads), 0, st, a);
+  if (a.softmax) return launch_pdl(mrs_decode_kernel<true>, dim3(1), dim3(kDecodeThreads), 0, st, a);
+  return launch_pdl(mrs_decode_kernel<false>, dim3(1), dim3(kDecodeThreads), 0, st, a);
 }
 
 }  // namespace mrs
