@@ -15,17 +15,21 @@ __device__ __forceinline__ void unit_range(int u, int T, int U, int& t0, int& t1
 }
 
 // Exclusive prefix sum of v[0..n) by the whole block into out[0..n], out[n] = total.
-// scan_tmp: 33 ints.  Ends with a block barrier.
+// Warp w owns the contiguous chunk [w * per, (w + 1) * per) and reads it in rows of 32
+// consecutive elements (conflict-free): one pass for the chunk total, then, after the
+// cross-warp prefix, each row's warp scan plus the running carry.  scan_tmp: 33 ints.
+// Ends with a block barrier.
 __device__ __forceinline__ void block_exclusive_scan(const int32_t* v, int32_t* out, int n,
                                                      int32_t* scan_tmp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-  const int per = (n + nthreads - 1) / nthreads;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  const int nwarps = blockDim.x >> 5;
+  const int per = (n + nwarps - 1) / nwarps;
+  const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
   int s = 0;
-  for (int i = lo; i < hi; ++i) s += v[i];
-  const int incl = warp_inclusive_sum(s, lane);
-  if (lane == 31) scan_tmp[warp] = incl;
+  for (int i = w0 + lane; i < w1; i += 32) s += v[i];
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(kFull, s, d);
+  if (lane == 0) scan_tmp[warp] = s;
   __syncthreads();
   if (warp == 0) {
     const int x = (lane < nwarps) ? scan_tmp[lane] : 0;
@@ -35,11 +39,14 @@ __device__ __forceinline__ void block_exclusive_scan(const int32_t* v, int32_t* 
     if (lane == 31) scan_tmp[32] = xi;
   }
   __syncthreads();
-  int run = scan_tmp[warp] + incl - s;
-  for (int i = lo; i < hi; ++i) {
-    const int x = v[i];
-    out[i] = run;
-    run += x;
+  int carry = scan_tmp[warp];
+#pragma unroll 4
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const int x = (i < w1) ? v[i] : 0;
+    const int incl = warp_inclusive_sum(x, lane);
+    if (i < w1) out[i] = carry + incl - x;
+    carry += __shfl_sync(kFull, incl, 31);
   }
   if (tid == 0) out[n] = scan_tmp[32];
   __syncthreads();
@@ -59,14 +66,15 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
   const int nslices = uo.nslices;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  unsigned* masks = reinterpret_cast<unsigned*>(scratch);  // one bit per token of a 32-token tile
+  // one bit per token of a 32-token tile, two buffers (tiles alternate)
+  unsigned* masks = reinterpret_cast<unsigned*>(scratch);
   size_t o = align16(sizeof(unsigned long long) * E);
   int32_t* run = reinterpret_cast<int32_t*>(scratch + o);
   o += align16(sizeof(int32_t) * E);
   int32_t* loc = reinterpret_cast<int32_t*>(scratch + o);
   o += align16(sizeof(int32_t) * (E + 1));
   o += align16(sizeof(int32_t) * E);
-  int32_t* misc = reinterpret_cast<int32_t*>(scratch + o);  // [0..32] scan, [40] dup flag
+  int32_t* misc = reinterpret_cast<int32_t*>(scratch + o);  // [0..32] scan, [40..41] dup flags
 
   // clear the look-back words and the status word for the slice kernel
   for (int c = u + tid * U; c < nslices; c += blockDim.x * U) slice_flags[c] = 0ull;
@@ -78,30 +86,47 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
   for (int e = tid; e < E; e += blockDim.x) {
     run[e] = loc[e];
     masks[e] = 0u;
+    masks[E + e] = 0u;
   }
-  if (tid == 0) misc[40] = 0;
+  if (tid == 0) {
+    misc[40] = 0;
+    misc[41] = 0;
+  }
   __syncthreads();
 
-  // tiles of 32 tokens: warp w takes tokens w, w + nwarps, ... of the tile, lane k slot k
+  // Tiles of 32 tokens: warp w takes tokens w, w + nwarps, ... of the tile, lane k slot k.
+  // Per tile: mark (bit of the token in its experts' masks), place (rank = earlier tokens of
+  // the tile in the mask, plus the expert's running count), advance (the tile's last token of
+  // an expert adds the mask's count and clears it).  Tile j uses mask buffer j & 1, so the
+  // next tile is marked in the same phase as this one advances: two barriers per tile.
   int2* out = uo.unit_buf + static_cast<size_t>(t0) * K;
   uint16_t* out_e = uo.unit_e + static_cast<size_t>(t0) * K;
   const int nt_all = t1 - t0;
-  for (int tb = 0; tb < nt_all; tb += 32) {
+  auto mark = [&](int tb, unsigned* m, int32_t* dup) {
     const int nt = min(32, nt_all - tb);
     for (int tl = warp; tl < nt; tl += nwarps) {
       const int e = (lane < K) ? rid[(tb + tl) * K + lane] : -1;
       if (e >= 0 && e < E) {
         const unsigned bit = 1u << tl;
-        if (atomicOr(&masks[e], bit) & bit) misc[40] = 1;  // an expert twice in one token
+        if (atomicOr(&m[e], bit) & bit) *dup = 1;  // an expert twice in one token
       }
     }
-    __syncthreads();
-    if (misc[40] == 0) {
+  };
+  if (nt_all > 0) mark(0, masks, &misc[40]);
+  __syncthreads();
+  for (int tb = 0, j = 0; tb < nt_all; tb += 32, ++j) {
+    const int nt = min(32, nt_all - tb);
+    unsigned* m = masks + (j & 1) * E;
+    unsigned* m_next = masks + ((j + 1) & 1) * E;
+    int32_t* dup = &misc[40 + (j & 1)];
+    int32_t* dup_next = &misc[40 + ((j + 1) & 1)];
+    const bool more = tb + 32 < nt_all;
+    if (*dup == 0) {
       for (int tl = warp; tl < nt; tl += nwarps) {
         const int r = (tb + tl) * K + lane;
         const int e = (lane < K) ? rid[r] : -1;
         if (e >= 0 && e < E) {
-          const int pos = run[e] + __popc(masks[e] & ((1u << tl) - 1u));
+          const int pos = run[e] + __popc(m[e] & ((1u << tl) - 1u));
           out[pos] = make_int2(t0 * K + r, __float_as_int(rw[r]));
           out_e[pos] = static_cast<uint16_t>(e);
         }
@@ -110,13 +135,14 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
       for (int tl = warp; tl < nt; tl += nwarps) {
         const int e = (lane < K) ? rid[(tb + tl) * K + lane] : -1;
         if (e >= 0 && e < E) {
-          const unsigned m = masks[e];
-          if ((m >> tl) == 1u) {  // the tile's last token routed to e
-            run[e] += __popc(m);
-            masks[e] = 0u;
+          const unsigned mm = m[e];
+          if ((mm >> tl) == 1u) {  // the tile's last token routed to e
+            run[e] += __popc(mm);
+            m[e] = 0u;
           }
         }
       }
+      if (more) mark(tb + 32, m_next, dup_next);
       __syncthreads();
     } else {
       // repeated ids inside a token: place this tile's routes in flat order, 32 at a time
@@ -124,7 +150,7 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
       const int r0 = tb * K;
       for (int i = tid; i < nr; i += blockDim.x) {
         const int e = rid[r0 + i];
-        if (e >= 0 && e < E) masks[e] = 0u;
+        if (e >= 0 && e < E) m[e] = 0u;
       }
       __syncthreads();
       if (warp == 0) {
@@ -145,10 +171,10 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
           __syncwarp();
         }
       }
-      __syncthreads();
-      if (tid == 0) misc[40] = 0;
+      if (more) mark(tb + 32, m_next, dup_next);
       __syncthreads();
     }
+    if (tid == 0) *dup = 0;  // read by every thread before this tile's first barrier
   }
 }
 
