@@ -199,23 +199,6 @@ __device__ __forceinline__ unsigned seg_lanes(int lane) {
   return (LT == 32) ? kFull : (((1u << LT) - 1u) << (lane & ~(LT - 1)));
 }
 
-// Value of rank k (0-based, descending) among the values of my LT-lane segment: bitonic
-// sort inside each segment.
-template <int LT>
-__device__ __forceinline__ float seg_kth_desc(float v, int ll, int k) {
-#pragma unroll
-  for (int kk = 2; kk <= LT; kk <<= 1) {
-#pragma unroll
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(kFull, v, j);
-      const bool desc = (ll & kk) == 0;
-      const bool lower = (ll & j) == 0;
-      v = (desc == lower) ? fmaxf(v, o) : fminf(v, o);
-    }
-  }
-  return __shfl_sync(kFull, v, k, LT);
-}
-
 // Descending rank k (0-based) among two values per lane of my LT-lane segment (2 * LT
 // values; element 2 * ll + r is register r of lane ll): bitonic sort over the segment.
 template <int LT>
@@ -242,6 +225,48 @@ __device__ __forceinline__ float seg_kth_desc2(float v0, float v1, int ll, int k
   const float a0 = __shfl_sync(kFull, v0, k >> 1, LT);
   const float a1 = __shfl_sync(kFull, v1, k >> 1, LT);
   return (k & 1) ? a1 : a0;
+}
+
+// Descending rank k (0-based) among four values per lane of my LT-lane segment (4 * LT values;
+// element 4 * ll + r is register r of lane ll): bitonic sort over the segment, the two lowest
+// index bits inside the lane.
+template <int LT>
+__device__ __forceinline__ float seg_kth_desc4(float v0, float v1, float v2, float v3, int ll,
+                                               int k) {
+  float v[4] = {v0, v1, v2, v3};
+#pragma unroll
+  for (int kk = 2; kk <= 4 * LT; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      if (j < 4) {  // partners are registers r and r ^ j of the lane
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if ((r & j) == 0) {
+            const bool desc = ((4 * ll + r) & kk) == 0;
+            const float hi = fmaxf(v[r], v[r ^ j]), lo = fminf(v[r], v[r ^ j]);
+            v[r] = desc ? hi : lo;
+            v[r ^ j] = desc ? lo : hi;
+          }
+        }
+      } else {
+        const int d = j >> 2;  // lane distance
+        const bool lower = (ll & d) == 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const bool desc = ((4 * ll + r) & kk) == 0;
+          const float o = __shfl_xor_sync(kFull, v[r], d);
+          v[r] = (desc == lower) ? fmaxf(v[r], o) : fminf(v[r], o);
+        }
+      }
+    }
+  }
+  const int src = k >> 2;
+  const float a0 = __shfl_sync(kFull, v[0], src, LT);
+  const float a1 = __shfl_sync(kFull, v[1], src, LT);
+  const float a2 = __shfl_sync(kFull, v[2], src, LT);
+  const float a3 = __shfl_sync(kFull, v[3], src, LT);
+  const int r = k & 3;
+  return r == 0 ? a0 : (r == 1 ? a1 : (r == 2 ? a2 : a3));
 }
 
 // Pass-1 summary of a lane: top-2 over its segment in V interleaved parts (part = unit
@@ -374,20 +399,16 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
     }
   }
 
-  // ---- top-K threshold from the pass-1 samples of kept groups: at least ceil(K/2) parts
-  // hold two values >= t2, so at least K values are >= t2; t1 = the K-th best part maximum
-  // is also such a bound.  -inf when too few parts are kept.
+  // ---- top-K threshold from the pass-1 samples of kept groups: the top-2 values of the
+  // parts are values of distinct experts, so the K-th best of all of them has at least K
+  // values at or above it.  -inf when the kept parts hold fewer than K samples.
   float tau;
   const float ninf = -INFINITY;
   if (V == 1) {
-    tau = seg_kth_desc<LT>(kept ? m2 : ninf, ll, (sh.K - 1) >> 1);
-    if (sh.K <= LT && __any_sync(kFull, tau == -INFINITY))
-      tau = fmaxf(tau, seg_kth_desc<LT>(kept ? m1 : ninf, ll, sh.K - 1));
+    tau = seg_kth_desc2<LT>(kept ? top.a1 : ninf, kept ? top.a2 : ninf, ll, sh.K - 1);
   } else {
-    tau = seg_kth_desc2<LT>(kept ? top.a2 : ninf, kept ? top.b2 : ninf, ll, (sh.K - 1) >> 1);
-    if (sh.K <= 2 * LT && __any_sync(kFull, tau == -INFINITY))
-      tau = fmaxf(tau, seg_kth_desc2<LT>(kept ? top.a1 : ninf, kept ? top.b1 : ninf, ll,
-                                         sh.K - 1));
+    tau = seg_kth_desc4<LT>(kept ? top.a1 : ninf, kept ? top.a2 : ninf, kept ? top.b1 : ninf,
+                            kept ? top.b2 : ninf, ll, sh.K - 1);
   }
   const float theta = tau - 2.0f * delta;
 
