@@ -239,44 +239,59 @@ def time_graph_steps(rep: Replica, steps: int, warmup: int, world: int, clocks=N
 
 
 def e2e_time(w, steps: int, warmup: int, world: int):
-    """Whole calls through the public API with host buffers: pinned H2D of the logits, the
-    route-sort call, D2H of every output (full buffers, one copy of the block that holds
-    them), timed with events on the stream."""
+    """Whole calls through the public C ABI with host buffers: every step the host writes a
+    fresh batch of logits into pinned host memory, and one moe_route_sort call reads it from
+    there and writes every output into pinned host memory (both mapped into the device's
+    address space with moe_route_sort_map_host: the transfers happen inside the call, over the
+    host link, with no copies enqueued).  A ring of sets is reused only after a stream
+    synchronisation (one per ring, inside the timed region).  CUDA events on the stream."""
     import torch
 
     import moe_expert_routing_sort_gb300 as mrs
 
-    inp = datagen.make_inputs(w)
-    h_logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
-    bias = torch.from_numpy(inp.bias).cuda()  # router parameter, resident
-    d_logits = torch.empty_like(h_logits, device="cuda")
-    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
-    outs = [out.outputs]  # all six outputs, one contiguous block
-    h_outs = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    n_sets, n_batches = 32, 64
+    src = [datagen.make_inputs(datagen.workload(w.name, seed=w.seed + i) if w.name in
+                               datagen.WORKLOADS else w).logits_bf16 for i in range(n_batches)]
+    bias = torch.from_numpy(datagen.make_inputs(w).bias).cuda()  # router parameter, resident
+    h_logits = [torch.empty(w.T, w.E, dtype=torch.bfloat16, pin_memory=True)
+                for _ in range(n_sets)]
+    h_views = [t.view(torch.int16).numpy().view(np.uint16) for t in h_logits]
+    outs = [mrs.RouteSortBuffers.allocate_pinned(w.T, w.E, w.topk, w.block_m)
+            for _ in range(n_sets)]
     s = torch.cuda.Stream()
+    lib = mrs.load()
+    args = [(mrs.map_host(h_logits[i]), bias.data_ptr(), w.T, w.E, w.n_group, w.topk_group,
+             w.topk, float(w.routed_scale), w.block_m, o.addr(o.topk_ids),
+             o.addr(o.topk_weights), o.addr(o.sorted_token_ids), o.addr(o.sorted_weights),
+             o.addr(o.expert_ids), o.addr(o.num_tokens_post_pad), o.workspace.data_ptr(),
+             o.workspace.numel(), s.cuda_stream) for i, o in enumerate(outs)]
 
-    def one():
-        # one library call: H2D of the logits, the route-sort, D2H of the output block
-        mrs.route_sort_from_host(h_logits, d_logits, bias, w.n_group, w.topk_group, w.topk,
-                                 w.routed_scale, w.block_m, out, h_outs[0], stream=s)
+    def one(k):
+        i = k % n_sets
+        if i == 0 and k > 0:
+            s.synchronize()  # every set's previous call has finished: the ring may be rewritten
+        np.copyto(h_views[i], src[k % n_batches])  # this step's logits, written by the host
+        rc = lib.moe_route_sort(*args[i])
+        if rc != 0:
+            raise RuntimeError(f"moe_route_sort: {mrs.strerror(rc)}")
 
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
+    for k in range(max(warmup, n_sets)):
+        one(k)
+    s.synchronize()
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
         a.record(s)
-    for _ in range(steps):
-        one()
+    for k in range(steps):
+        one(k)
     with torch.cuda.stream(s):
         b.record(s)
     torch.cuda.synchronize()
     barrier(world)
     ms = dist_max(a.elapsed_time(b), world)
-    h2d = h_logits.numel() * 2
-    d2h = sum(t.numel() * t.element_size() for t in outs)
+    h2d = h_logits[0].numel() * 2
+    d2h = outs[0].outputs.numel()
     return ms, h2d, d2h
 
 

@@ -36,8 +36,12 @@
  * contiguous.  logits_bf16: [T, E] bf16 (16-byte aligned base); bias: [E] fp32;
  * topk_ids, topk_weights: [T, K]; sorted_token_ids, sorted_weights:
  * [moe_sort_max_padded(T,E,K,B)]; expert_ids: [moe_sort_max_blocks(T,E,K,B)];
- * num_tokens_post_pad: [1].  The library allocates nothing and keeps no device state
- * between calls; inputs are never written.  Calls only enqueue work on `stream` (no host
+ * num_tokens_post_pad: [1].  "Device memory" includes pinned host memory mapped into the
+ * device's address space (zero-copy): pass the address moe_route_sort_map_host returns for it.
+ * The kernels then read the logits from, and write the outputs to, host memory over the host
+ * link, with no copy enqueued, and the host may read the outputs once the stream has passed the
+ * call.  The workspace must be ordinary device memory.  The library allocates nothing and keeps
+ * no device state between calls; inputs are never written.  Calls only enqueue work on `stream` (no host
  * synchronisation), so they can be captured in a CUDA graph once the first call on the
  * current device has been made outside capture (that call caches device attributes).
  *
@@ -81,6 +85,7 @@ extern "C" {
 #define MOE_RS_ERR_TOO_LARGE (-13)        /* shape needs more than the static scratch of
                                              moe_route_sort_noalloc                        */
 #define MOE_RS_ERR_BAD_HIDDEN (-14)       /* H not a multiple of 8 in [8, 8192]            */
+#define MOE_RS_ERR_NOT_MAPPED (-15)       /* host memory not mapped into the device space  */
 
 /* Device-side status bits, written to the first int32 of the workspace by every call. */
 #define MOE_RS_DEVICE_BAD_EXPERT_ID 0x1   /* moe_sort saw an id >= E; those routes dropped */
@@ -100,6 +105,14 @@ size_t moe_sort_max_blocks(int T, int E, int topk, int block_m);
  * aligned, any contents; the library overwrites what it uses).  One workspace must not be
  * used by two calls that can run at the same time. */
 size_t moe_route_sort_workspace_bytes(int T, int E, int topk, int block_m);
+
+/* Device address of pinned host memory, for passing host buffers to the operations below
+ * without copies (zero-copy): `host_ptr` must lie in memory allocated with cudaHostAlloc /
+ * cudaMallocHost, or registered with cudaHostRegister and the mapped flag.  On systems with
+ * unified addressing the address is host_ptr itself.  Writes it to *device_ptr and returns
+ * MOE_RS_OK, or MOE_RS_ERR_NOT_MAPPED (host memory the device cannot address) or
+ * MOE_RS_ERR_NULL_POINTER.  A host-side query: it enqueues nothing. */
+int moe_route_sort_map_host(const void* host_ptr, void** device_ptr);
 
 /* Static text for a status code (host codes above). */
 const char* moe_route_sort_strerror(int status);

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     library_path,
     gate_route_sort,
     load,
+    map_host,
     moe_gate_route_sort,
     moe_route_sort,
     moe_route_sort_noalloc,
@@ -25,6 +26,7 @@ from .binding import (  # noqa: F401
     moe_topk,
     route_sort,
     route_sort_from_host,
+    route_sort_mapped,
     route_sort_softmax,
     strerror,
 )

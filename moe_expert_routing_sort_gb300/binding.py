@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
         lib.moe_route_sort_workspace_bytes.argtypes = [I, I, I, I]
         lib.moe_route_sort_workspace_bytes.restype = S
         lib.moe_route_sort_strerror.argtypes = [I]
+        lib.moe_route_sort_map_host.argtypes = [P, ctypes.POINTER(ctypes.c_void_p)]
+        lib.moe_route_sort_map_host.restype = I
         lib.moe_route_sort_strerror.restype = ctypes.c_char_p
         lib.moe_route_sort.argtypes = [P, P, I, I, I, I, I, F, I, P, P, P, P, P, P, P, S, P]
         lib.moe_route_sort.restype = I
@@ -304,6 +306,7 @@ class RouteSortBuffers:
     num_tokens_post_pad: torch.Tensor
     workspace: torch.Tensor
     outputs: Optional[torch.Tensor] = None
+    host_alias: Optional[int] = None  # device address of `outputs` when it is pinned host memory
 
     @classmethod
     def allocate(cls, T, E, topk, block_m, device="cuda") -> "RouteSortBuffers":
@@ -327,6 +330,28 @@ class RouteSortBuffers:
                  for (name, dt, shape), (o, n) in zip(parts, offs)}
         return cls(workspace=torch.empty(ws, dtype=torch.uint8, device=device), outputs=block,
                    **views)
+
+    @classmethod
+    def allocate_pinned(cls, T, E, topk, block_m) -> "RouteSortBuffers":
+        """Like ``allocate``, but the outputs block is pinned host memory mapped into the
+        device's address space (zero-copy): the kernels write the results straight to the host.
+        The workspace stays in device memory."""
+        dev = cls.allocate(T, E, topk, block_m, device="cuda")
+        block = torch.empty(dev.outputs.numel(), dtype=torch.uint8, pin_memory=True)
+        base = dev.outputs.data_ptr()
+        views = {}
+        for name in ("topk_ids", "topk_weights", "sorted_token_ids", "sorted_weights",
+                     "expert_ids", "num_tokens_post_pad"):
+            t = getattr(dev, name)
+            o = t.data_ptr() - base
+            views[name] = block[o:o + t.numel() * 4].view(t.dtype).view(t.shape)
+        return cls(workspace=dev.workspace, outputs=block, host_alias=map_host(block), **views)
+
+    def addr(self, t: torch.Tensor) -> int:
+        """Device address of one of the output views."""
+        if self.host_alias is None:
+            return t.data_ptr()
+        return self.host_alias + (t.data_ptr() - self.outputs.data_ptr())
 
     def status_word(self) -> int:
         """Device status bits of the last completed call (synchronises the device)."""
@@ -361,6 +386,31 @@ def route_sort_from_host(logits_host, logits_dev, bias, n_group, topk_group, top
         out.outputs.data_ptr(), result_host.data_ptr(), out.outputs.numel(),
         _stream_handle(stream))
     _check(rc, "moe_route_sort_from_host")
+    return out
+
+
+def map_host(t: torch.Tensor) -> int:
+    """Device address of a pinned CPU tensor's memory (moe_route_sort_map_host)."""
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("map_host needs a pinned CPU tensor")
+    d = ctypes.c_void_p()
+    _check(load().moe_route_sort_map_host(t.data_ptr(), ctypes.byref(d)), "moe_route_sort_map_host")
+    return int(d.value)
+
+
+def route_sort_mapped(logits_addr: int, T: int, E: int, bias, n_group, topk_group, topk,
+                      routed_scale, block_m, out: RouteSortBuffers, stream=None):
+    """moe_route_sort with the logits at device address ``logits_addr`` (for example the
+    ``map_host`` address of pinned host logits) and the outputs of ``out`` (device buffers, or
+    pinned host buffers from ``RouteSortBuffers.allocate_pinned``): zero-copy when host."""
+    _need(bias, torch.float32, "bias")
+    rc = load().moe_route_sort(
+        logits_addr, bias.data_ptr(), T, E, n_group, topk_group, topk, float(routed_scale),
+        block_m, out.addr(out.topk_ids), out.addr(out.topk_weights),
+        out.addr(out.sorted_token_ids), out.addr(out.sorted_weights), out.addr(out.expert_ids),
+        out.addr(out.num_tokens_post_pad), out.workspace.data_ptr(), out.workspace.numel(),
+        _stream_handle(stream))
+    _check(rc, "moe_route_sort")
     return out
 
 

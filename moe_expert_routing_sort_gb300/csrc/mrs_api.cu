@@ -300,6 +300,17 @@ size_t moe_route_sort_workspace_bytes(int T, int E, int topk, int block_m) {
   return ws_layout(T, E, topk).total;
 }
 
+int moe_route_sort_map_host(const void* host_ptr, void** device_ptr) {
+  if (!host_ptr || !device_ptr) return MOE_RS_ERR_NULL_POINTER;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0) != cudaSuccess || !d) {
+    cudaGetLastError();  // clear the non-sticky error
+    return MOE_RS_ERR_NOT_MAPPED;
+  }
+  *device_ptr = d;
+  return MOE_RS_OK;
+}
+
 const char* moe_route_sort_strerror(int status) {
   switch (status) {
     case MOE_RS_OK: return "success";
@@ -323,6 +334,8 @@ const char* moe_route_sort_strerror(int status) {
       return "the shape needs more scratch than moe_route_sort_noalloc's static 32 MiB";
     case MOE_RS_ERR_BAD_HIDDEN:
       return "hidden size H must be a multiple of 8 in [8, 8192]";
+    case MOE_RS_ERR_NOT_MAPPED:
+      return "host memory is not pinned and mapped into the device address space";
     default: return "unknown status";
   }
 }

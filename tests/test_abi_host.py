@@ -48,7 +48,7 @@ def test_size_queries():
 
 
 def test_strerror_covers_codes():
-    for code in range(-14, 1):
+    for code in range(-15, 1):
         assert mrs.strerror(code) != "unknown status"
     assert mrs.strerror(-99) == "unknown status"
 
@@ -185,3 +185,9 @@ def test_gate_variant_validates(lib):
     assert _gate(lib, w_gate=BASE + 0x100000) == -9  # gate rows over the workspace
     assert _gate(lib, ids=BASE + 0x300010) == -9     # topk ids over the logits
     assert _gate(lib, ws_bytes=16) == -10
+
+
+def test_map_host_rejects_null(lib):
+    d = ctypes.c_void_p()
+    assert lib.moe_route_sort_map_host(None, ctypes.byref(d)) == -1
+    assert lib.moe_route_sort_map_host(BASE, None) == -1

@@ -7,6 +7,7 @@ the oracle's selection margin is below 1e-6, so ulp-level differences between tw
 sigmoid evaluations cannot change an id.  The full-size workloads are compared on every
 token, in the launch configuration the benchmark times.
 """
+import ctypes
 import functools
 import hashlib
 
@@ -404,3 +405,28 @@ def test_metadata_drives_a_block_grouped_gemm(name):
     ids = out.topk_ids.long()
     ref = torch.einsum("th,tkhn,tk->tn", X, W[ids], out.topk_weights)
     assert torch.allclose(got, ref, rtol=1e-4, atol=1e-4), (got - ref).abs().max().item()
+
+
+@pytest.mark.parametrize("name,T", [("decode_T1_E896_G8", None), ("prefill_T512_E896", None),
+                                    ("skewed_T8192_E896", 3000)])
+def test_zero_copy_host_buffers(name, T):
+    # logits read from, and every output written to, pinned host memory mapped into the
+    # device's address space: the same results as the device buffers, with no copies
+    w, inp, ref = inputs_for(name, T=T)
+    h_logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    out = mrs.RouteSortBuffers.allocate_pinned(w.T, w.E, w.topk, w.block_m)
+    out.outputs.fill_(0xA5)
+    mrs.route_sort_mapped(mrs.map_host(h_logits), w.T, w.E, bias, w.n_group, w.topk_group,
+                          w.topk, w.routed_scale, w.block_m, out)
+    torch.cuda.synchronize()
+    assert not out.topk_ids.is_cuda
+    assert_matches(out, ref, w)
+
+
+def test_map_host_address():
+    t = torch.arange(1024, dtype=torch.int32).pin_memory()
+    addr = mrs.map_host(t)
+    assert addr != 0  # usable by the kernels: see test_zero_copy_host_buffers
+    with pytest.raises(ValueError):
+        mrs.map_host(torch.zeros(4))  # pageable: not accepted by the binding
