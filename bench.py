@@ -44,7 +44,7 @@ METRIC = "route-sort µs/call at T=1 E=896; routed tokens/s and % HBM roofline a
 # DRAM bytes (read + write) of one decode-kernel launch on the headline workload, from the
 # ncu capture summarised in profiles/decode_kernel_decode_T1_E896_G8.md (caches flushed
 # before the launch, so it includes the kernel's code and parameters).
-DECODE_TRAFFIC_BYTES = 64512
+DECODE_TRAFFIC_BYTES = 64256
 
 
 def parse_args():
