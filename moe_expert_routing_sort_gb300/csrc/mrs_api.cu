@@ -417,8 +417,7 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   if (gate) {
     DeviceInfo gd;
     if (!device_info(gd)) return MOE_RS_ERR_LAUNCH;
-    const GatePlan gp = gate_plan(T, E, gate->H, gd.sms);
-    if (gp.smem > static_cast<size_t>(gd.smem_optin)) return MOE_RS_ERR_LAUNCH;
+    const GatePlan gp = gate_plan(E, gd.sms);
     GateArgs ga{};
     ga.hidden = static_cast<const uint16_t*>(gate->hidden);
     ga.w = static_cast<const uint16_t*>(gate->w_gate);
@@ -427,7 +426,6 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     ga.E = E;
     ga.H = gate->H;
     ga.rpc = gp.rpc;
-    ga.nch = gp.nch;
     rc = launch_status(launch_gate(ga, gp, stream));
     if (rc) return rc;
   }

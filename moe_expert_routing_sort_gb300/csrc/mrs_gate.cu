@@ -96,16 +96,13 @@ __global__ void __launch_bounds__(kGateThreads, 2) mrs_gate_kernel(const GateArg
   }
 }
 
-GatePlan gate_plan(int T, int E, int H, int sms) {
+GatePlan gate_plan(int E, int sms) {
   GatePlan p{};
   const int slots = 2 * (sms > 0 ? sms : 1);  // two CTAs per SM
   int rpc = (E + slots - 1) / slots;
   if (rpc > kGateRows) rpc = kGateRows;
   p.rpc = rpc;
   p.grid = (E + rpc - 1) / rpc;
-  p.nch = (H + 31) / 32;
-  p.smem = 0;
-  (void)T;
   return p;
 }
 

@@ -222,15 +222,13 @@ struct GateArgs {
   const uint16_t* w;       // [E, H] bf16, one gate row per expert
   uint16_t* logits;        // [T, E] bf16
   int T, E, H;
-  int rpc;  // gate rows per CTA
-  int nch;  // chunks per row
+  int rpc;  // gate rows per CTA (<= 16)
 };
-// Launch plan: rows per CTA, grid, chunks per row and shared memory for `sms` SMs.
+// Launch plan for `sms` SMs: gate rows per CTA and the grid.
 struct GatePlan {
-  int rpc, grid, nch;
-  size_t smem;
+  int rpc, grid;
 };
-GatePlan gate_plan(int T, int E, int H, int sms);
+GatePlan gate_plan(int E, int sms);
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
 
 // Launchers return the cudaError_t of the launch.
