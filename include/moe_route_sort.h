@@ -40,10 +40,11 @@
  * device's address space (zero-copy): pass the address moe_route_sort_map_host returns for it.
  * The kernels then read the logits from, and write the outputs to, host memory over the host
  * link, with no copy enqueued, and the host may read the outputs once the stream has passed the
- * call.  The workspace must be ordinary device memory.  The library allocates nothing and keeps
- * no device state between calls; inputs are never written.  Calls only enqueue work on `stream` (no host
- * synchronisation), so they can be captured in a CUDA graph once the first call on the
- * current device has been made outside capture (that call caches device attributes).
+ * call.  The workspace must be ordinary device memory.  The library allocates nothing and
+ * keeps no device state between calls; inputs are never written.  Calls only enqueue work on
+ * `stream` (no host synchronisation), so they can be captured in a CUDA graph once the first
+ * call on the current device has been made outside capture (that call caches device
+ * attributes).
  *
  * Limits: 1 <= E <= 4096, 1 <= G <= 64, E % G == 0, 1 <= Kg <= G, 1 <= K <= 32,
  * K <= Kg * g, B a power of two in [1, 1024], T >= 0, N and the padded length fit in
@@ -165,7 +166,8 @@ int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, floa
  * Limits: those of moe_route_sort, plus 0 <= T <= 8 and H a multiple of 8 in [8, 8192].
  * Errors: those of moe_route_sort, plus MOE_RS_ERR_BAD_HIDDEN, MOE_RS_ERR_BAD_TOKENS for
  * T > 8, MOE_RS_ERR_NULL_POINTER / MOE_RS_ERR_MISALIGNED for hidden, w_gate or logits, and
- * MOE_RS_ERR_ALIAS if hidden or w_gate overlaps any output or the workspace. */
+ * MOE_RS_ERR_ALIAS if hidden, w_gate or bias overlaps any output (the logits included) or
+ * the workspace. */
 int moe_gate_route_sort(const void* hidden_bf16, const void* w_gate_bf16, const float* bias,
                         int T, int E, int H, int n_group, int topk_group, int topk,
                         float routed_scale, int block_m, void* logits_bf16, int32_t* topk_ids,

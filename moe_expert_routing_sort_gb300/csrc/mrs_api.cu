@@ -537,8 +537,10 @@ int moe_gate_route_sort(const void* hidden_bf16, const void* w_gate_bf16, const 
                          span(expert_ids, expert_ids ? 4 * NB : 0),
                          span(num_tokens_post_pad, num_tokens_post_pad ? 4 : 0),
                          span(workspace, workspace ? workspace_bytes : 0)};
+    // (the bias, read by the route step, must not overlap the logits the gate writes either)
     const Span ins[] = {span(hidden_bf16, 2 * static_cast<size_t>(T) * H),
-                        span(w_gate_bf16, 2 * static_cast<size_t>(E) * H)};
+                        span(w_gate_bf16, 2 * static_cast<size_t>(E) * H),
+                        span(bias, bias ? 4 * static_cast<size_t>(E) : 0)};
     for (const Span& o : outs)
       for (const Span& i : ins)
         if (overlap(o, i)) return MOE_RS_ERR_ALIAS;
@@ -556,8 +558,8 @@ int moe_route_sort_softmax(const void* logits_bf16, int T, int E, int topk, floa
                            int32_t* expert_ids, int32_t* num_tokens_post_pad,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return route_sort_impl(logits_bf16, nullptr, T, E, 1, 1, topk, routed_scale, block_m, true,
-                         nullptr, topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
-                         num_tokens_post_pad, workspace, workspace_bytes, stream);
+                         nullptr, topk_ids, topk_weights, sorted_token_ids, sorted_weights,
+                         expert_ids, num_tokens_post_pad, workspace, workspace_bytes, stream);
 }
 
 int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, int topk,

@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  if (a.softmax) return launch_pdl(mrs_decode_kernel<true>, dim3(1), dim3(kDecodeThreads), 0, st, a);
-  return launch_pdl(mrs_decode_kernel<false>, dim3(1), dim3(kDecodeThreads), 0, st, a);
+  auto* kern = a.softmax ? mrs_decode_kernel<true> : mrs_decode_kernel<false>;
+  return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
 }
 
 }  // namespace mrs

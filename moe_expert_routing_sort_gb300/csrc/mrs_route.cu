@@ -302,7 +302,8 @@ struct GenCtaLayout {
   size_t bias, counts, rid, rw, warps, per_warp, total;
 };
 
-__host__ __device__ inline GenCtaLayout gen_cta_layout(int E, int nwarps, int max_routes, bool sort) {
+__host__ __device__ inline GenCtaLayout gen_cta_layout(int E, int nwarps, int max_routes,
+                                                       bool sort) {
   GenCtaLayout l{};
   size_t o = 0;
   l.bias = o;

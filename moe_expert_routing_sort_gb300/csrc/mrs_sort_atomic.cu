@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kScanThreads) mrs_atomic_scan_kernel(const Ato
   if (tid == 0) *a.npp = wtot[32];
 }
 
-__global__ void __launch_bounds__(kAtomicThreads) mrs_atomic_scatter_kernel(const AtomicSortArgs a) {
+__global__ void __launch_bounds__(kAtomicThreads)
+    mrs_atomic_scatter_kernel(const AtomicSortArgs a) {
   extern __shared__ int32_t sm[];  // cnt_s[E], base_s[E]
   int32_t* cnt_s = sm;
   int32_t* base_s = sm + a.E;

@@ -184,6 +184,7 @@ def test_gate_variant_validates(lib):
     assert _gate(lib, hidden=BASE + 0x300000) == -9  # hidden over the logits output
     assert _gate(lib, w_gate=BASE + 0x100000) == -9  # gate rows over the workspace
     assert _gate(lib, ids=BASE + 0x300010) == -9     # topk ids over the logits
+    assert _gate(lib, logits=BASE + 0x10000) == -9   # the gate's logits over the bias
     assert _gate(lib, ws_bytes=16) == -10
 
 
