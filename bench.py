@@ -295,6 +295,43 @@ def e2e_time(w, steps: int, warmup: int, world: int):
     return ms, h2d, d2h
 
 
+def e2e_time_copies(w, steps: int, warmup: int, world: int):
+    """The same end-to-end measurement where pinned host memory cannot be mapped: per step,
+    one moe_route_sort_from_host call (copy of the host logits in, the call, one copy of the
+    output block back), CUDA events on its stream."""
+    import torch
+
+    import moe_expert_routing_sort_gb300 as mrs
+
+    inp = datagen.make_inputs(w)
+    h_logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    bias = torch.from_numpy(inp.bias).cuda()
+    d_logits = torch.empty_like(h_logits, device="cuda")
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
+    h_out = torch.empty_like(out.outputs, device="cpu").pin_memory()
+    s = torch.cuda.Stream()
+
+    def one():
+        mrs.route_sort_from_host(h_logits, d_logits, bias, w.n_group, w.topk_group, w.topk,
+                                 w.routed_scale, w.block_m, out, h_out, stream=s)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record(s)
+    for _ in range(steps):
+        one()
+    with torch.cuda.stream(s):
+        b.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    return dist_max(a.elapsed_time(b), world), h_logits.numel() * 2, out.outputs.numel()
+
+
 def n_sets_for(w) -> int:
     per = 2 * w.T * w.E
     return int(min(64, max(2, math.ceil(2 * L2_BYTES / max(per, 1)))))
@@ -539,7 +576,12 @@ def main():
     sampler.start()
     head = measure_workload(w, args.steps, args.warmup, world, peak, clocks=True)
     clocks = sampler.stop()
-    e2e_ms, h2d, d2h = e2e_time(w, args.steps * 32, args.warmup, world)
+    try:
+        e2e_ms, h2d, d2h = e2e_time(w, args.steps * 32, args.warmup, world)
+        e2e_path = "zero-copy: pinned host logits and outputs mapped into the device space"
+    except (mrs.RouteSortError, ValueError):  # host memory cannot be mapped on this system
+        e2e_ms, h2d, d2h = e2e_time_copies(w, args.steps * 32, args.warmup, world)
+        e2e_path = "copies: cudaMemcpyAsync in, the call, cudaMemcpyAsync out"
     e2e_us = e2e_ms * 1e3 / (args.steps * 32)
 
     configs = {}
@@ -604,7 +646,7 @@ def main():
                      "traffic": DECODE_TRAFFIC_BYTES if w.name == HEADLINE else None},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "path": e2e_path},
         "gpu_launches": head["launches"],
         "clocks": clocks,
         "configs": configs,
