@@ -192,3 +192,17 @@ def test_map_host_rejects_null(lib):
     d = ctypes.c_void_p()
     assert lib.moe_route_sort_map_host(None, ctypes.byref(d)) == -1
     assert lib.moe_route_sort_map_host(BASE, None) == -1
+
+
+def test_moe_sort_atomic_validates(lib):
+    # same contract as moe_sort: checked before the memset or any launch
+    P = mrs.moe_sort_max_padded(4, 64, 6, 16)
+    ws = mrs.moe_route_sort_workspace_bytes(4, 64, 6, 16)
+    args = [BASE, BASE + 0x1000, 4, 64, 6, 16, BASE + 0x2000, BASE + 0x2000 + 4 * P,
+            BASE + 0x8000, BASE + 0x9000, BASE + 0x10000, ws, None]
+    for i, v, code in [(5, 12, -5), (3, 0, -2), (4, 33, -4), (2, -1, -6),
+                       (7, BASE + 0x2000, -9), (11, 8, -10), (10, 0, -10), (0, 0, -1),
+                       (6, BASE + 0x2002, -8)]:
+        bad = list(args)
+        bad[i] = v
+        assert lib.moe_sort_atomic(*bad) == code, (i, v, code)
