@@ -321,7 +321,29 @@ def test_margins_detect_planted_ties(oracle_mod):
     assert m2[0] == 0.0
 
 
-# ------------------------------------------------------ softmax variant (reading R9)
+def test_margins_match_a_direct_computation(oracle_mod):
+    # the three gaps of the margin, recomputed here in float64 from float64 keys: they agree
+    # with the oracle's float32 values to float32 rounding
+    rng = np.random.default_rng(31)
+    T, E, G, Kg, K = 30, 48, 6, 3, 5
+    logits = datagen.float32_to_bf16_bits(rng.standard_normal((T, E)).astype(np.float32))
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    m = oracle_mod.margins(logits, bias, G, Kg, K)
+    x = (logits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    key = 1.0 / (1.0 + np.exp(-x)) + bias.astype(np.float64)
+    g = E // G
+    for t in range(T):
+        kg = key[t].reshape(G, g)
+        gs = np.sort(kg, axis=1)[:, -2:].sum(axis=1)
+        order = np.argsort(-gs, kind="stable")
+        gaps = [gs[order[Kg - 1]] - gs[order[Kg]]]
+        cand = np.sort(kg[order[:Kg]].ravel())[::-1]
+        gaps.append(cand[K - 1] - cand[K])
+        gaps += list(cand[:K - 1] - cand[1:K])
+        assert abs(m[t] - min(gaps)) < 1e-6, (t, m[t], min(gaps))
+
+
+# ----------------------------------------------------- softmax variant (reading R13)
 def test_softmax_topk_is_argsort_of_logits(oracle_mod):
     # selection is on the logits themselves: a textbook stable argsort of -x (ties -> lower
     # index), on coarse values so that exact ties are frequent
