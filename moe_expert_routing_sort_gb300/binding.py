@@ -124,6 +124,23 @@ def _check(rc: int, what: str) -> None:
         raise RouteSortError(rc, what)
 
 
+def _sort_sizes(T: int, E: int, topk: int, block_m: int):
+    """Element counts the sort outputs need (sorted rows, block owners); 0 for a shape the
+    library rejects anyway."""
+    return moe_sort_max_padded(T, E, topk, block_m), moe_sort_max_blocks(T, E, topk, block_m)
+
+
+def _need_room(T: int, topk: int, P: int, NB: int, **bufs) -> None:
+    """Raise before any launch if an output is smaller than the shape needs (the kernels
+    would write past it)."""
+    want = {"topk_ids": T * topk, "topk_weights": T * topk, "sorted_token_ids": P,
+            "sorted_weights": P, "expert_ids": NB, "num_tokens_post_pad": 1}
+    for name, t in bufs.items():
+        n = want[name] if T > 0 or name == "num_tokens_post_pad" else 0
+        if n > 0 and t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements; this shape needs {n}")
+
+
 # -------------------------------------------------------------------- operations
 def moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
                    topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
@@ -139,6 +156,10 @@ def moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_
                      (num_tokens_post_pad, torch.int32, "num_tokens_post_pad"),
                      (workspace, torch.uint8, "workspace")]:
         _need(t, dt, n)
+    _need_room(T, topk, *_sort_sizes(T, E, topk, block_m), topk_ids=topk_ids,
+               topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
+               sorted_weights=sorted_weights, expert_ids=expert_ids,
+               num_tokens_post_pad=num_tokens_post_pad)
     rc = load().moe_route_sort(
         _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
         block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
@@ -160,6 +181,10 @@ def moe_route_sort_softmax(logits, topk, routed_scale, block_m, topk_ids, topk_w
                      (num_tokens_post_pad, torch.int32, "num_tokens_post_pad"),
                      (workspace, torch.uint8, "workspace")]:
         _need(t, dt, n)
+    _need_room(T, topk, *_sort_sizes(T, E, topk, block_m), topk_ids=topk_ids,
+               topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
+               sorted_weights=sorted_weights, expert_ids=expert_ids,
+               num_tokens_post_pad=num_tokens_post_pad)
     rc = load().moe_route_sort_softmax(
         _ptr(logits), T, E, topk, float(routed_scale), block_m, _ptr(topk_ids),
         _ptr(topk_weights), _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
@@ -200,6 +225,10 @@ def moe_gate_route_sort(hidden, w_gate, bias, n_group, topk_group, topk, routed_
                      (num_tokens_post_pad, torch.int32, "num_tokens_post_pad"),
                      (workspace, torch.uint8, "workspace")]:
         _need(t, dt, n)
+    _need_room(T, topk, *_sort_sizes(T, E, topk, block_m), topk_ids=topk_ids,
+               topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
+               sorted_weights=sorted_weights, expert_ids=expert_ids,
+               num_tokens_post_pad=num_tokens_post_pad)
     rc = load().moe_gate_route_sort(
         _ptr(hidden), _ptr(w_gate), _ptr(bias), T, E, H, n_group, topk_group, topk,
         float(routed_scale), block_m, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
@@ -241,6 +270,10 @@ def moe_route_sort_noalloc(logits, bias, n_group, topk_group, topk, routed_scale
                      (expert_ids, torch.int32, "expert_ids"),
                      (num_tokens_post_pad, torch.int32, "num_tokens_post_pad")]:
         _need(t, dt, n)
+    _need_room(T, topk, *_sort_sizes(T, E, topk, block_m), topk_ids=topk_ids,
+               topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
+               sorted_weights=sorted_weights, expert_ids=expert_ids,
+               num_tokens_post_pad=num_tokens_post_pad)
     rc = load().moe_route_sort_noalloc(
         _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
         block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
@@ -256,6 +289,7 @@ def moe_topk(logits, bias, n_group, topk_group, topk, routed_scale, topk_ids, to
     _need(bias, torch.float32, "bias")
     _need(topk_ids, torch.int32, "topk_ids")
     _need(topk_weights, torch.float32, "topk_weights")
+    _need_room(T, topk, 0, 0, topk_ids=topk_ids, topk_weights=topk_weights)
     rc = load().moe_topk(_ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk,
                          float(routed_scale), _ptr(topk_ids), _ptr(topk_weights),
                          _stream_handle(stream))
@@ -274,6 +308,11 @@ def moe_sort(topk_ids, topk_weights, E, block_m, sorted_token_ids, sorted_weight
     _need(expert_ids, torch.int32, "expert_ids")
     _need(num_tokens_post_pad, torch.int32, "num_tokens_post_pad")
     _need(workspace, torch.uint8, "workspace")
+    if topk_weights.numel() < T * K:
+        raise ValueError("topk_weights must hold T * topk weights")
+    _need_room(T, K, *_sort_sizes(T, E, K, block_m), sorted_token_ids=sorted_token_ids,
+               sorted_weights=sorted_weights, expert_ids=expert_ids,
+               num_tokens_post_pad=num_tokens_post_pad)
     fn = load().moe_sort_atomic if atomic else load().moe_sort
     rc = fn(_ptr(topk_ids), _ptr(topk_weights), T, E, K, block_m, _ptr(sorted_token_ids),
             _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
@@ -307,6 +346,7 @@ class RouteSortBuffers:
     workspace: torch.Tensor
     outputs: Optional[torch.Tensor] = None
     host_alias: Optional[int] = None  # device address of `outputs` when it is pinned host memory
+    shape: Optional[tuple] = None  # (T, E, topk, block_m) the buffers were allocated for
 
     @classmethod
     def allocate(cls, T, E, topk, block_m, device="cuda") -> "RouteSortBuffers":
@@ -329,7 +369,7 @@ class RouteSortBuffers:
         views = {name: block[o:o + n].view(dt).view(shape)
                  for (name, dt, shape), (o, n) in zip(parts, offs)}
         return cls(workspace=torch.empty(ws, dtype=torch.uint8, device=device), outputs=block,
-                   **views)
+                   shape=(T, E, topk, block_m), **views)
 
     @classmethod
     def allocate_pinned(cls, T, E, topk, block_m) -> "RouteSortBuffers":
@@ -345,7 +385,8 @@ class RouteSortBuffers:
             t = getattr(dev, name)
             o = t.data_ptr() - base
             views[name] = block[o:o + t.numel() * 4].view(t.dtype).view(t.shape)
-        return cls(workspace=dev.workspace, outputs=block, host_alias=map_host(block), **views)
+        return cls(workspace=dev.workspace, outputs=block, host_alias=map_host(block),
+                   shape=dev.shape, **views)
 
     def addr(self, t: torch.Tensor) -> int:
         """Device address of one of the output views."""
@@ -404,6 +445,10 @@ def route_sort_mapped(logits_addr: int, T: int, E: int, bias, n_group, topk_grou
     ``map_host`` address of pinned host logits) and the outputs of ``out`` (device buffers, or
     pinned host buffers from ``RouteSortBuffers.allocate_pinned``): zero-copy when host."""
     _need(bias, torch.float32, "bias")
+    _need_room(T, topk, *_sort_sizes(T, E, topk, block_m), topk_ids=out.topk_ids,
+               topk_weights=out.topk_weights, sorted_token_ids=out.sorted_token_ids,
+               sorted_weights=out.sorted_weights, expert_ids=out.expert_ids,
+               num_tokens_post_pad=out.num_tokens_post_pad)
     rc = load().moe_route_sort(
         logits_addr, bias.data_ptr(), T, E, n_group, topk_group, topk, float(routed_scale),
         block_m, out.addr(out.topk_ids), out.addr(out.topk_weights),
@@ -420,7 +465,7 @@ def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
     T, E = logits.shape
     if out is None:
         out = RouteSortBuffers.allocate(T, E, topk, block_m, device=logits.device)
-    if out.outputs is None:
+    if out.outputs is None or out.shape != (T, E, topk, block_m) or out.host_alias is not None:
         moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
                        out.topk_ids, out.topk_weights, out.sorted_token_ids, out.sorted_weights,
                        out.expert_ids, out.num_tokens_post_pad, out.workspace, stream=stream)

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import moe_expert_routing_sort_gb300 as mrs
 from moe_expert_routing_sort_gb300 import _build
@@ -206,3 +207,26 @@ def test_moe_sort_atomic_validates(lib):
         bad = list(args)
         bad[i] = v
         assert lib.moe_sort_atomic(*bad) == code, (i, v, code)
+
+
+def test_binding_rejects_undersized_outputs(lib):
+    # the Python binding checks buffer sizes against the shape before calling the library
+    from moe_expert_routing_sort_gb300 import binding
+    T, E, K, B = 5, 64, 6, 16
+    P, NB = binding._sort_sizes(T, E, K, B)
+    assert (P, NB) == (mrs.moe_sort_max_padded(T, E, K, B), mrs.moe_sort_max_blocks(T, E, K, B))
+    ok = dict(topk_ids=torch.empty(T * K), topk_weights=torch.empty(T * K),
+              sorted_token_ids=torch.empty(P), sorted_weights=torch.empty(P),
+              expert_ids=torch.empty(NB), num_tokens_post_pad=torch.empty(1))
+    binding._need_room(T, K, P, NB, **ok)
+    for name in ok:
+        bad = dict(ok)
+        bad[name] = torch.empty(max(ok[name].numel() - 1, 0))
+        with pytest.raises(ValueError, match=name):
+            binding._need_room(T, K, P, NB, **bad)
+    binding._need_room(0, K, 0, 0, topk_ids=torch.empty(0), num_tokens_post_pad=torch.empty(1))
+    b = mrs.RouteSortBuffers.allocate(T, E, K, B, device="cpu")
+    assert b.shape == (T, E, K, B)
+    binding._need_room(T, K, P, NB, topk_ids=b.topk_ids, topk_weights=b.topk_weights,
+                       sorted_token_ids=b.sorted_token_ids, sorted_weights=b.sorted_weights,
+                       expert_ids=b.expert_ids, num_tokens_post_pad=b.num_tokens_post_pad)
