@@ -230,3 +230,19 @@ def test_binding_rejects_undersized_outputs(lib):
     binding._need_room(T, K, P, NB, topk_ids=b.topk_ids, topk_weights=b.topk_weights,
                        sorted_token_ids=b.sorted_token_ids, sorted_weights=b.sorted_weights,
                        expert_ids=b.expert_ids, num_tokens_post_pad=b.num_tokens_post_pad)
+
+
+def test_header_is_plain_c(tmp_path):
+    # the C ABI header compiles as C99 (no C++ or torch types leak into the signatures)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.isdir(cuda_inc):
+        pytest.skip("gcc or the CUDA headers are not available")
+    src = tmp_path / "use.c"
+    src.write_text('#include "moe_route_sort.h"\nint main(void) { return MOE_RS_OK; }\n')
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
