@@ -10,9 +10,13 @@ tokens/s and fraction of the HBM roofline.
 Timing: a step is one CUDA graph of C calls, each the whole path (route step + both sort
 phases) on its own input set and output set; the sets rotate so that their total is larger
 than twice the L2, and L2 is flushed (a 256 MiB write) before every timed step.  Each step
-is bracketed by CUDA events on the launching stream; warm-up steps are not timed.  Under
-torchrun each rank times its own replica (the path does not shard: replicas only), the step
-times are reduced with MAX over ranks and ``value`` is the per-call time of the whole job.
+is bracketed by CUDA events on the launching stream; warm-up steps are not timed; a
+workload's figure is the median over its timed steps.  Under torchrun each rank times its own
+replica (the path does not shard: replicas only), the step times are reduced with MAX over
+ranks, ``value`` is the per-call latency of the slowest rank (never divided by the rank count)
+and ``job_calls_per_s`` the whole job's call rate.  For the one-token headline,
+``single_call`` also times one call alone (a graph of one call, L2 flushed) beside the same
+measurement of a T = 0 call, the launch floor.
 
 ``--impl reference`` times the CPU oracle (single thread, the slow plain definition) on a
 bounded sample of the same workload instead.
@@ -20,9 +24,11 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -41,10 +47,8 @@ SECONDARY = ["prefill_T512_E896", "skewed_T8192_E896", "wide_T16384_E4096"]
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024
 METRIC = "route-sort µs/call at T=1 E=896; routed tokens/s and % HBM roofline at T≥512"
-# DRAM bytes (read + write) of one decode-kernel launch on the headline workload, from the
-# ncu capture summarised in profiles/decode_kernel_decode_T1_E896_G8.md (caches flushed
-# before the launch, so it includes the kernel's code and parameters).
-DECODE_TRAFFIC_BYTES = 64256
+CSRC = os.path.join(ROOT, "moe_expert_routing_sort_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
 
 def parse_args():
@@ -65,6 +69,78 @@ def parse_args():
 def algorithmic_bytes(w, npp: int) -> int:
     """Logits + bias read, top-k ids/weights, sorted ids/weights, block owners, npp written."""
     return (2 * w.T * w.E + 4 * w.E + 8 * w.T * w.topk + 8 * npp + 4 * (npp // w.block_m) + 4)
+
+
+def kernel_source_hash() -> str:
+    """sha256 (first 16 hex digits) of the CUDA sources, in name order: names the kernels a
+    DRAM-traffic capture was taken on."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the workload's dominant kernel from the ncu
+    capture recorded in profiles/dram_traffic.md, or None when no capture of the current
+    kernel sources exists (a table row: | workload | kernel | bytes | source hash | ...)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = kernel_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == workload and cells[3] == want:
+                try:
+                    return int(float(cells[2]))
+                except ValueError:
+                    return None
+    return None
+
+
+def cpu_info():
+    """Host cores and CPU model, for the CPU baseline record."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in text.splitlines():
+                if line.lower().startswith(key.lower()):
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"nproc": os.cpu_count(), "model": model or platform.machine()}
+
+
+class OneCore:
+    """Pin this process to one core while timing the single-threaded oracle."""
+
+    def __enter__(self):
+        self.saved = None
+        if hasattr(os, "sched_getaffinity"):
+            self.saved = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {min(self.saved)})
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+        return False
 
 
 def load_peaks():
@@ -238,6 +314,53 @@ def time_graph_steps(rep: Replica, steps: int, warmup: int, world: int, clocks=N
     return total_ms, step_ms
 
 
+def single_call_us(rep: Replica, samples: int, world: int, T0: bool = False):
+    """Median time of ONE call, from CUDA events around the replay of a graph that holds that
+    call alone, L2 flushed before each sample (cold caches, launch latency included).  With
+    T0, the same for a T = 0 call of the public API (one one-thread kernel that writes
+    npp = 0): the floor that events, graph launch and one kernel launch cost by themselves."""
+    import torch
+
+    s = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    logits, bias, out = rep.sets[0]
+    w = rep.w
+    if T0:
+        empty = torch.empty(0, w.E, dtype=torch.bfloat16, device="cuda")
+        out0 = rep.mrs.RouteSortBuffers.allocate(0, w.E, w.topk, w.block_m, device="cuda")
+
+    def call():
+        if T0:
+            rep.mrs.route_sort(empty, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                               w.block_m, out=out0, stream=s)
+        else:
+            rep.call(0, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(samples)]
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            flush.fill_(1)
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with torch.cuda.stream(s):
+        for k, (a, b) in enumerate(ev):
+            flush.fill_(k & 0xFF)
+            a.record(s)
+            g.replay()
+            b.record(s)
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+    return dist_max(us, world)
+
+
 def e2e_time(w, steps: int, warmup: int, world: int):
     """Whole calls through the public C ABI with host buffers: every step the host writes a
     fresh batch of logits into pinned host memory, and one moe_route_sort call reads it from
@@ -342,13 +465,16 @@ def measure_workload(w, steps, warmup, world, peak_gbs, clocks=None):
     rep = Replica(w, n_sets)
     total_ms, step_ms = time_graph_steps(rep, steps, warmup, world, clocks)
     calls = steps * n_sets
-    us_per_call = total_ms * 1e3 / calls
+    # median over the timed steps (each step one graph of n_sets calls), slowest rank
+    us_per_call = dist_max(statistics.median(step_ms), world) * 1e3 / n_sets
     npps = rep.npp()
     bytes_per_call = float(np.mean([algorithmic_bytes(w, n) for n in npps]))
     achieved = bytes_per_call / (us_per_call * 1e-6) / 1e9
     return {
         "us_per_call": us_per_call,
+        "us_per_call_mean": total_ms * 1e3 / calls,
         "ms_per_step": total_ms / steps,
+        "rep": rep,
         "calls_per_step": n_sets,
         "tokens_per_s": w.T / (us_per_call * 1e-6),
         "routes_per_s": w.T * w.topk / (us_per_call * 1e-6),
@@ -483,34 +609,44 @@ def measure_gate(T, E, H, steps, warmup, world, peak_gbs, unfused=True):
 
 
 # ----------------------------------------------------------------- CPU oracle
-def cpu_oracle_rate(w, budget_s: float):
-    """Time the oracle on a bounded sample of workload w: (seconds per token, sample text)."""
+def cpu_oracle_rate(w, budget_s: float, runs: int = 5):
+    """Time the oracle, pinned to one host core, on a bounded sample of workload w: the median
+    of `runs` runs, each about budget_s / runs seconds.  Returns (seconds per token, sample)."""
     import oracle
 
     oracle.build()
-    if w.T == 1:
-        inp = datagen.make_inputs(w)
-        n = 0
+    per_run = budget_s / runs
+    with OneCore():
+        if w.T == 1:
+            inp = datagen.make_inputs(w)
+            rates, total = [], 0
+            for _ in range(runs):
+                n = 0
+                t0 = time.perf_counter()
+                while time.perf_counter() - t0 < per_run:
+                    oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group,
+                                      w.topk, w.routed_scale, w.block_m)
+                    n += 1
+                rates.append((time.perf_counter() - t0) / n)
+                total += n
+            return statistics.median(rates), (f"median of {runs} runs, {total} whole calls on "
+                                              f"the T=1 input ({budget_s:.0f} s), one core")
+        # a token sample of the full workload: the whole path on the first n_tok tokens
+        inp = datagen.make_inputs(w, T=min(w.T, 64))
         t0 = time.perf_counter()
-        while time.perf_counter() - t0 < budget_s:
+        oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                          w.routed_scale, w.block_m)
+        per_tok = (time.perf_counter() - t0) / inp.logits_bf16.shape[0]
+        n_tok = int(max(16, min(w.T, per_run / max(per_tok, 1e-7))))
+        inp = datagen.make_inputs(w, T=n_tok)
+        rates = []
+        for _ in range(runs):
+            t0 = time.perf_counter()
             oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
                               w.routed_scale, w.block_m)
-            n += 1
-        dt = time.perf_counter() - t0
-        return dt / n, f"{n} whole calls on the T=1 input ({dt:.1f} s)"
-    # a token sample of the full workload: route step on the sample, sort step scaled
-    inp = datagen.make_inputs(w, T=min(w.T, 64))
-    t0 = time.perf_counter()
-    oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
-                      w.routed_scale, w.block_m)
-    per_tok = (time.perf_counter() - t0) / inp.logits_bf16.shape[0]
-    n_tok = int(max(16, min(w.T, budget_s / max(per_tok, 1e-7))))
-    inp = datagen.make_inputs(w, T=n_tok)
-    t0 = time.perf_counter()
-    oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
-                      w.routed_scale, w.block_m)
-    dt = time.perf_counter() - t0
-    return dt / n_tok, f"first {n_tok} of {w.T} tokens, whole path ({dt:.1f} s)"
+            rates.append((time.perf_counter() - t0) / n_tok)
+        return statistics.median(rates), (f"median of {runs} runs of the whole path on the "
+                                          f"first {n_tok} of {w.T} tokens, one core")
 
 
 def run_reference(args, w, rank, world):
@@ -528,14 +664,15 @@ def run_reference(args, w, rank, world):
         sample = f"first 64 of {w.T} tokens per step, scaled to the full call"
     scale = w.T / inp.logits_bf16.shape[0]
     t_steps = []
-    for k in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
-                          w.routed_scale, w.block_m)
-        el = (time.perf_counter() - t0) * scale
-        if k >= args.warmup:
-            t_steps.append(el)
-    us = sum(t_steps) / len(t_steps) * 1e6
+    with OneCore():
+        for k in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                              w.routed_scale, w.block_m)
+            el = (time.perf_counter() - t0) * scale
+            if k >= args.warmup:
+                t_steps.append(el)
+    us = statistics.median(t_steps) * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -545,7 +682,8 @@ def run_reference(args, w, rank, world):
                    "topk_group": w.topk_group, "topk": w.topk, "block_m": w.block_m,
                    "parallelism": "replicas" if world > 1 else "single"},
         "cpu_baseline": {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample + " (median over steps, one core)",
+                         "host": cpu_info()},
         "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -576,6 +714,15 @@ def main():
     sampler.start()
     head = measure_workload(w, args.steps, args.warmup, world, peak, clocks=True)
     clocks = sampler.stop()
+    single = None
+    if w.T <= 64:
+        # one call alone (graph of one call, L2 flushed), beside the floor of a T = 0 call
+        one = single_call_us(head["rep"], 200, world)
+        floor = single_call_us(head["rep"], 200, world, T0=True)
+        single = {"us": one, "t0_call_floor_us": floor, "us_above_floor": one - floor,
+                  "how": "median of 200 samples: CUDA events around the replay of a graph "
+                         "holding one call, L2 flushed before each; the floor is the same "
+                         "measurement of a T=0 call (one one-thread kernel)"}
     try:
         e2e_ms, h2d, d2h = e2e_time(w, args.steps * 32, args.warmup, world)
         e2e_path = "zero-copy: pinned host logits and outputs mapped into the device space"
@@ -589,7 +736,8 @@ def main():
         for name in SECONDARY:
             ws = datagen.workload(name)
             r = measure_workload(ws, max(3, min(args.steps, 10)), args.warmup, world, peak)
-            configs[name] = {k: r[k] for k in ("us_per_call", "tokens_per_s", "routes_per_s",
+            configs[name] = {k: r[k] for k in ("us_per_call", "us_per_call_mean",
+                                                 "tokens_per_s", "routes_per_s",
                                                  "achieved_gbs", "roofline_frac",
                                                  "algorithmic_bytes_per_call", "calls_per_step")}
             if ws.T > 1024:  # the sort step alone: deterministic order vs atomic slot order
@@ -608,7 +756,7 @@ def main():
     if rank == 0:
         secs, sample = cpu_oracle_rate(w, args.cpu_budget)
         cpu = {"value": secs * 1e6, "unit": "us/call", "cores": 1, "kind": "oracle",
-               "sample": sample}
+               "sample": sample, "host": cpu_info()}
         for name in configs:
             if name not in datagen.WORKLOADS:
                 continue
@@ -619,7 +767,10 @@ def main():
 
     if rank != 0:
         return 0
-    value = head["us_per_call"] / world
+    # replicas: every rank makes its own calls, so the per-call latency is the slowest rank's;
+    # the job's call rate is world times that rank's rate
+    value = head["us_per_call"]
+    traffic = captured_traffic(w.name)
     line = {
         "metric": METRIC,
         "value": value,
@@ -643,7 +794,13 @@ def main():
                                "moe_route_sort (whole call)",
                      "achieved": head["achieved_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": head["roofline_frac"], "peak_kind": peak_kind,
-                     "traffic": DECODE_TRAFFIC_BYTES if w.name == HEADLINE else None},
+                     "traffic": traffic,
+                     "traffic_source": ("profiles/dram_traffic.md, capture of the current "
+                                        "kernel sources " + kernel_source_hash())
+                                       if traffic is not None else
+                                       "no ncu capture of the current kernel sources"},
+        "single_call": single,
+        "job_calls_per_s": world * 1e6 / head["us_per_call"],
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "path": e2e_path},

@@ -40,11 +40,12 @@
  * device's address space (zero-copy): pass the address moe_route_sort_map_host returns for it.
  * The kernels then read the logits from, and write the outputs to, host memory over the host
  * link, with no copy enqueued, and the host may read the outputs once the stream has passed the
- * call.  The workspace must be ordinary device memory.  The library allocates nothing and
- * keeps no device state between calls; inputs are never written.  Calls only enqueue work on
- * `stream` (no host synchronisation), so they can be captured in a CUDA graph once the first
- * call on the current device has been made outside capture (that call caches device
- * attributes).
+ * call.  The workspace must be ordinary device memory.  The library allocates nothing, and
+ * between calls it keeps on the device only the word that records its proxy check (below)
+ * and the scratch of moe_route_sort_noalloc; inputs are never written.  The operations that
+ * take a workspace argument only enqueue work on `stream` (no host synchronisation), so they
+ * can be captured in a CUDA graph once the first call on the current device has been made
+ * outside capture (that call caches device attributes and enqueues the proxy check).
  *
  * Limits: 1 <= E <= 4096, 1 <= G <= 64, E % G == 0, 1 <= Kg <= G, 1 <= K <= 32,
  * K <= Kg * g, B a power of two in [1, 1024], T >= 0, N and the padded length fit in
@@ -55,6 +56,16 @@
  * CUDA runtime refuses a launch).  Problems only the device can see are reported in the
  * workspace's status word (the first int32 of the workspace, MOE_RS_DEVICE_* bits), valid
  * once the call has completed on the stream; read it with cudaMemcpyAsync if wanted.
+ *
+ * Devices: a call runs on the CUDA device current in the calling thread, and every pointer
+ * must be memory that device can address (its own, or mapped host memory).
+ *
+ * Exactness of the pruned selection: the multi-CTA route kernels discard experts with a cheap
+ * score whose error bound is a property of the GPU's tanh approximation.  The first such call
+ * in each device context (made outside stream capture) enqueues an exhaustive check of that
+ * bound over all bf16 inputs ahead of its own kernels (one 1024-thread block, once); the
+ * kernels prune only where the check has passed and otherwise evaluate every expert exactly
+ * (same results, slower).  moe_route_sort_proxy_state reports the outcome.
  */
 #ifndef MOE_ROUTE_SORT_H_
 #define MOE_ROUTE_SORT_H_
@@ -87,6 +98,7 @@ extern "C" {
                                              moe_route_sort_noalloc                        */
 #define MOE_RS_ERR_BAD_HIDDEN (-14)       /* H not a multiple of 8 in [8, 8192]            */
 #define MOE_RS_ERR_NOT_MAPPED (-15)       /* host memory not mapped into the device space  */
+#define MOE_RS_ERR_BAD_DEBUG_KNOB (-16)   /* moe_route_sort_debug_set: unknown knob         */
 
 /* Device-side status bits, written to the first int32 of the workspace by every call. */
 #define MOE_RS_DEVICE_BAD_EXPERT_ID 0x1   /* moe_sort saw an id >= E; those routes dropped */
@@ -240,18 +252,29 @@ int moe_route_sort_from_host(const void* logits_host, void* logits_dev, const fl
  * Arguments, outputs, results and errors are those of moe_route_sort, plus
  * MOE_RS_ERR_TOO_LARGE when moe_route_sort_workspace_bytes(T, E, topk, block_m) exceeds
  * MOE_RS_NOALLOC_SCRATCH_BYTES (for example 16384 tokens x 4096 experts x top-8 needs about
- * 9.3 MiB and is accepted).  The first call on each device looks up the array's device
- * address with that device current; make that first call before any stream capture.
+ * 9.3 MiB and is accepted); shapes are checked before that, and a rejected call touches
+ * nothing.  The first call on each device context looks up the array's device address with
+ * that device current and caches it (a context created again, for example after
+ * cudaDeviceReset, gets a fresh lookup); make that first call before any stream capture.
  * All calls on a device share the one array and it keeps whatever the previous call left in
  * it (the path needs no zeroed scratch); two calls that can run on the GPU at the same time
  * (different streams, or graphs replayed concurrently) race on it and give wrong results.
- * The status word of moe_route_sort is written into that shared array and is not exposed. */
+ * The status word of moe_route_sort lands in that shared array: read it with
+ * moe_route_sort_noalloc_status. */
 int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, int E,
                            int n_group, int topk_group, int topk, float routed_scale,
                            int block_m, int32_t* topk_ids, float* topk_weights,
                            int32_t* sorted_token_ids, float* sorted_weights,
                            int32_t* expert_ids, int32_t* num_tokens_post_pad,
                            cudaStream_t stream);
+
+/* Copies the device status word (MOE_RS_DEVICE_* bits) of the last moe_route_sort_noalloc
+ * call on the current device into dst[0] (device memory or mapped pinned host memory, one
+ * int32, caller-owned), as a copy enqueued on `stream`: the value is that of the last such
+ * call ordered before the copy, valid once the stream reaches it.  It has no counterpart in
+ * the source pages.  Returns MOE_RS_OK, MOE_RS_ERR_NULL_POINTER, MOE_RS_ERR_MISALIGNED or
+ * MOE_RS_ERR_LAUNCH; it allocates nothing. */
+int moe_route_sort_noalloc_status(int32_t* dst, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ diagnostics */
 
@@ -261,8 +284,34 @@ int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, in
  * selected; that proof assumes |cheap - exact sigmoid| <= bound for every bf16 x.  Writes
  * out2[0] = the largest difference over all finite bf16 inputs on this device and
  * out2[1] = the bound assumed (device memory, 2 floats, caller-owned; valid after the
- * stream reaches this call).  Selection stays exact only if out2[0] <= out2[1]. */
+ * stream reaches this call).  Selection stays exact only if out2[0] <= out2[1]; the library
+ * runs the same check itself (see "Exactness of the pruned selection" above). */
 int moe_route_sort_proxy_selftest(float* out2, cudaStream_t stream);
+
+/* The library's own record of that check on the current device: copies into dst[0] (device
+ * memory or mapped pinned host memory, one int32) 0 if no check has run in this context yet,
+ * 1 if the bound held (the route kernels prune), 2 if it failed (they evaluate every expert
+ * exactly).  Enqueued on `stream`; valid once the stream reaches it. */
+int moe_route_sort_proxy_state(int32_t* dst, cudaStream_t stream);
+
+/* Test hooks (process-wide settings read when later calls launch; no counterpart in the source
+ * pages).  They exist so that the failure paths can be exercised on a healthy GPU:
+ *   MOE_RS_DEBUG_WAIT_LIMIT_NS     every bounded device wait of the multi-CTA path (row copies,
+ *                                  the sort step's look-back) gives up after `value` ns;
+ *                                  0 gives up at once without waiting, which makes those calls
+ *                                  report MOE_RS_DEVICE_WAIT_TIMEOUT (outputs invalid, every
+ *                                  write still inside the caller's buffers); a negative value
+ *                                  restores the default of 200 ms.  Copies already in flight
+ *                                  are still waited for (with the default bound) before a CTA
+ *                                  exits.
+ *   MOE_RS_DEBUG_FORCE_PROXY_FAIL  `value` != 0: the in-library proxy check reports a failure
+ *                                  (it runs again in each context on the next call that would
+ *                                  prune), so the route kernels evaluate every expert exactly;
+ *                                  0 restores the real check.
+ * Returns MOE_RS_OK or MOE_RS_ERR_BAD_DEBUG_KNOB. */
+#define MOE_RS_DEBUG_WAIT_LIMIT_NS 1
+#define MOE_RS_DEBUG_FORCE_PROXY_FAIL 2
+int moe_route_sort_debug_set(int knob, long long value);
 
 #ifdef __cplusplus
 }

@@ -7,6 +7,8 @@ and the seeded input generator used by the tests and the benchmark.
 from . import datagen  # noqa: F401
 from ._build import build  # noqa: F401
 from .binding import (  # noqa: F401
+    DEBUG_FORCE_PROXY_FAIL,
+    DEBUG_WAIT_LIMIT_NS,
     DEVICE_BAD_EXPERT_ID,
     RouteSortBuffers,
     RouteSortError,
@@ -16,8 +18,11 @@ from .binding import (  # noqa: F401
     map_host,
     moe_gate_route_sort,
     moe_route_sort,
+    moe_route_sort_debug_set,
     moe_route_sort_noalloc,
+    moe_route_sort_noalloc_status,
     moe_route_sort_proxy_selftest,
+    moe_route_sort_proxy_state,
     moe_route_sort_softmax,
     moe_route_sort_workspace_bytes,
     moe_sort,

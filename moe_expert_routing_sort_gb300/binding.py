@@ -78,6 +78,12 @@ def load() -> ctypes.CDLL:
         lib.moe_route_sort_from_host.restype = I
         lib.moe_route_sort_proxy_selftest.argtypes = [P, P]
         lib.moe_route_sort_proxy_selftest.restype = I
+        lib.moe_route_sort_proxy_state.argtypes = [P, P]
+        lib.moe_route_sort_proxy_state.restype = I
+        lib.moe_route_sort_noalloc_status.argtypes = [P, P]
+        lib.moe_route_sort_noalloc_status.restype = I
+        lib.moe_route_sort_debug_set.argtypes = [I, ctypes.c_longlong]
+        lib.moe_route_sort_debug_set.restype = I
         _lib = lib
         return lib
 
@@ -117,6 +123,20 @@ def _need(t: torch.Tensor, dtype, name: str):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _one_device(*tensors) -> torch.device:
+    """The one CUDA device that every given tensor (None skipped) lives on.
+
+    The library runs on the current device and reads every pointer from there, so a call whose
+    buffers sit on different devices (or on the host) is refused here, before any launch."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all buffers must be on one device, got {sorted(map(str, devs))}")
+    dev = devs.pop()
+    if dev.type != "cuda":
+        raise ValueError(f"buffers must be CUDA tensors, got {dev}")
+    return dev
 
 
 def _check(rc: int, what: str) -> None:
@@ -160,11 +180,14 @@ def moe_route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_
                topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
                sorted_weights=sorted_weights, expert_ids=expert_ids,
                num_tokens_post_pad=num_tokens_post_pad)
-    rc = load().moe_route_sort(
-        _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
-        block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
-        _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
-        workspace.numel(), _stream_handle(stream))
+    dev = _one_device(logits, bias, topk_ids, topk_weights, sorted_token_ids, sorted_weights,
+                      expert_ids, num_tokens_post_pad, workspace)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort(
+            _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
+            block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
+            _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad),
+            _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(rc, "moe_route_sort")
 
 
@@ -185,10 +208,14 @@ def moe_route_sort_softmax(logits, topk, routed_scale, block_m, topk_ids, topk_w
                topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
                sorted_weights=sorted_weights, expert_ids=expert_ids,
                num_tokens_post_pad=num_tokens_post_pad)
-    rc = load().moe_route_sort_softmax(
-        _ptr(logits), T, E, topk, float(routed_scale), block_m, _ptr(topk_ids),
-        _ptr(topk_weights), _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
-        _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    dev = _one_device(logits, topk_ids, topk_weights, sorted_token_ids, sorted_weights,
+                      expert_ids, num_tokens_post_pad, workspace)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort_softmax(
+            _ptr(logits), T, E, topk, float(routed_scale), block_m, _ptr(topk_ids),
+            _ptr(topk_weights), _ptr(sorted_token_ids), _ptr(sorted_weights),
+            _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream))
     _check(rc, "moe_route_sort_softmax")
 
 
@@ -229,11 +256,15 @@ def moe_gate_route_sort(hidden, w_gate, bias, n_group, topk_group, topk, routed_
                topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
                sorted_weights=sorted_weights, expert_ids=expert_ids,
                num_tokens_post_pad=num_tokens_post_pad)
-    rc = load().moe_gate_route_sort(
-        _ptr(hidden), _ptr(w_gate), _ptr(bias), T, E, H, n_group, topk_group, topk,
-        float(routed_scale), block_m, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
-        _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
-        _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    dev = _one_device(hidden, w_gate, bias, logits, topk_ids, topk_weights, sorted_token_ids,
+                      sorted_weights, expert_ids, num_tokens_post_pad, workspace)
+    with torch.cuda.device(dev):
+        rc = load().moe_gate_route_sort(
+            _ptr(hidden), _ptr(w_gate), _ptr(bias), T, E, H, n_group, topk_group, topk,
+            float(routed_scale), block_m, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
+            _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(expert_ids),
+            _ptr(num_tokens_post_pad), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream))
     _check(rc, "moe_gate_route_sort")
 
 
@@ -274,12 +305,25 @@ def moe_route_sort_noalloc(logits, bias, n_group, topk_group, topk, routed_scale
                topk_weights=topk_weights, sorted_token_ids=sorted_token_ids,
                sorted_weights=sorted_weights, expert_ids=expert_ids,
                num_tokens_post_pad=num_tokens_post_pad)
-    rc = load().moe_route_sort_noalloc(
-        _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
-        block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
-        _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad),
-        _stream_handle(stream))
+    dev = _one_device(logits, bias, topk_ids, topk_weights, sorted_token_ids, sorted_weights,
+                      expert_ids, num_tokens_post_pad)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort_noalloc(
+            _ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk, float(routed_scale),
+            block_m, _ptr(topk_ids), _ptr(topk_weights), _ptr(sorted_token_ids),
+            _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad),
+            _stream_handle(stream))
     _check(rc, "moe_route_sort_noalloc")
+
+
+def moe_route_sort_noalloc_status(dst, stream=None) -> None:
+    """Copy the device status word of the last moe_route_sort_noalloc call on dst's device
+    into dst[0] (an int32 CUDA tensor), enqueued on the stream."""
+    _need(dst, torch.int32, "dst")
+    dev = _one_device(dst)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort_noalloc_status(_ptr(dst), _stream_handle(stream))
+    _check(rc, "moe_route_sort_noalloc_status")
 
 
 def moe_topk(logits, bias, n_group, topk_group, topk, routed_scale, topk_ids, topk_weights,
@@ -290,9 +334,11 @@ def moe_topk(logits, bias, n_group, topk_group, topk, routed_scale, topk_ids, to
     _need(topk_ids, torch.int32, "topk_ids")
     _need(topk_weights, torch.float32, "topk_weights")
     _need_room(T, topk, 0, 0, topk_ids=topk_ids, topk_weights=topk_weights)
-    rc = load().moe_topk(_ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk,
-                         float(routed_scale), _ptr(topk_ids), _ptr(topk_weights),
-                         _stream_handle(stream))
+    dev = _one_device(logits, bias, topk_ids, topk_weights)
+    with torch.cuda.device(dev):
+        rc = load().moe_topk(_ptr(logits), _ptr(bias), T, E, n_group, topk_group, topk,
+                             float(routed_scale), _ptr(topk_ids), _ptr(topk_weights),
+                             _stream_handle(stream))
     _check(rc, "moe_topk")
 
 
@@ -314,9 +360,12 @@ def moe_sort(topk_ids, topk_weights, E, block_m, sorted_token_ids, sorted_weight
                sorted_weights=sorted_weights, expert_ids=expert_ids,
                num_tokens_post_pad=num_tokens_post_pad)
     fn = load().moe_sort_atomic if atomic else load().moe_sort
-    rc = fn(_ptr(topk_ids), _ptr(topk_weights), T, E, K, block_m, _ptr(sorted_token_ids),
-            _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad), _ptr(workspace),
-            workspace.numel(), _stream_handle(stream))
+    dev = _one_device(topk_ids, topk_weights, sorted_token_ids, sorted_weights, expert_ids,
+                      num_tokens_post_pad, workspace)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(topk_ids), _ptr(topk_weights), T, E, K, block_m, _ptr(sorted_token_ids),
+                _ptr(sorted_weights), _ptr(expert_ids), _ptr(num_tokens_post_pad),
+                _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(rc, "moe_sort_atomic" if atomic else "moe_sort")
 
 
@@ -325,8 +374,27 @@ def moe_route_sort_proxy_selftest(out2, stream=None) -> None:
     _need(out2, torch.float32, "out2")
     if out2.numel() < 2:
         raise ValueError("out2 needs 2 floats")
-    _check(load().moe_route_sort_proxy_selftest(_ptr(out2), _stream_handle(stream)),
-           "moe_route_sort_proxy_selftest")
+    with torch.cuda.device(_one_device(out2)):
+        rc = load().moe_route_sort_proxy_selftest(_ptr(out2), _stream_handle(stream))
+    _check(rc, "moe_route_sort_proxy_selftest")
+
+
+def moe_route_sort_proxy_state(dst, stream=None) -> None:
+    """The library's record of its proxy-bound check on dst's device into dst[0] (int32):
+    0 not checked yet, 1 bound holds (pruning), 2 bound failed (exact keys everywhere)."""
+    _need(dst, torch.int32, "dst")
+    with torch.cuda.device(_one_device(dst)):
+        rc = load().moe_route_sort_proxy_state(_ptr(dst), _stream_handle(stream))
+    _check(rc, "moe_route_sort_proxy_state")
+
+
+DEBUG_WAIT_LIMIT_NS = 1
+DEBUG_FORCE_PROXY_FAIL = 2
+
+
+def moe_route_sort_debug_set(knob: int, value: int) -> None:
+    """Test hook of the library (see include/moe_route_sort.h): process-wide."""
+    _check(load().moe_route_sort_debug_set(int(knob), int(value)), "moe_route_sort_debug_set")
 
 
 # ---------------------------------------------------------- convenience buffers
@@ -418,14 +486,16 @@ def route_sort_from_host(logits_host, logits_dev, bias, n_group, topk_group, top
     if out.outputs is None or result_host.is_cuda or result_host.numel() != out.outputs.numel():
         raise ValueError("out must come from RouteSortBuffers.allocate; result_host must be a "
                          "CPU tensor of out.outputs' size")
-    rc = load().moe_route_sort_from_host(
-        logits_host.data_ptr(), logits_dev.data_ptr(), bias.data_ptr(), T, E, n_group,
-        topk_group, topk, float(routed_scale), block_m, out.topk_ids.data_ptr(),
-        out.topk_weights.data_ptr(), out.sorted_token_ids.data_ptr(),
-        out.sorted_weights.data_ptr(), out.expert_ids.data_ptr(),
-        out.num_tokens_post_pad.data_ptr(), out.workspace.data_ptr(), out.workspace.numel(),
-        out.outputs.data_ptr(), result_host.data_ptr(), out.outputs.numel(),
-        _stream_handle(stream))
+    dev = _one_device(logits_dev, bias, out.outputs, out.workspace)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort_from_host(
+            logits_host.data_ptr(), logits_dev.data_ptr(), bias.data_ptr(), T, E, n_group,
+            topk_group, topk, float(routed_scale), block_m, out.topk_ids.data_ptr(),
+            out.topk_weights.data_ptr(), out.sorted_token_ids.data_ptr(),
+            out.sorted_weights.data_ptr(), out.expert_ids.data_ptr(),
+            out.num_tokens_post_pad.data_ptr(), out.workspace.data_ptr(),
+            out.workspace.numel(), out.outputs.data_ptr(), result_host.data_ptr(),
+            out.outputs.numel(), _stream_handle(stream))
     _check(rc, "moe_route_sort_from_host")
     return out
 
@@ -449,12 +519,14 @@ def route_sort_mapped(logits_addr: int, T: int, E: int, bias, n_group, topk_grou
                topk_weights=out.topk_weights, sorted_token_ids=out.sorted_token_ids,
                sorted_weights=out.sorted_weights, expert_ids=out.expert_ids,
                num_tokens_post_pad=out.num_tokens_post_pad)
-    rc = load().moe_route_sort(
-        logits_addr, bias.data_ptr(), T, E, n_group, topk_group, topk, float(routed_scale),
-        block_m, out.addr(out.topk_ids), out.addr(out.topk_weights),
-        out.addr(out.sorted_token_ids), out.addr(out.sorted_weights), out.addr(out.expert_ids),
-        out.addr(out.num_tokens_post_pad), out.workspace.data_ptr(), out.workspace.numel(),
-        _stream_handle(stream))
+    dev = _one_device(bias, out.workspace)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort(
+            logits_addr, bias.data_ptr(), T, E, n_group, topk_group, topk,
+            float(routed_scale), block_m, out.addr(out.topk_ids), out.addr(out.topk_weights),
+            out.addr(out.sorted_token_ids), out.addr(out.sorted_weights),
+            out.addr(out.expert_ids), out.addr(out.num_tokens_post_pad),
+            out.workspace.data_ptr(), out.workspace.numel(), _stream_handle(stream))
     _check(rc, "moe_route_sort")
     return out
 
@@ -473,11 +545,13 @@ def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m,
     # buffers from allocate() have the right types and layout: check the inputs only
     _need(logits, torch.bfloat16, "logits")
     _need(bias, torch.float32, "bias")
-    rc = load().moe_route_sort(
-        logits.data_ptr(), bias.data_ptr(), T, E, n_group, topk_group, topk,
-        float(routed_scale), block_m, out.topk_ids.data_ptr(), out.topk_weights.data_ptr(),
-        out.sorted_token_ids.data_ptr(), out.sorted_weights.data_ptr(),
-        out.expert_ids.data_ptr(), out.num_tokens_post_pad.data_ptr(), out.workspace.data_ptr(),
-        out.workspace.numel(), _stream_handle(stream))
+    dev = _one_device(logits, bias, out.outputs, out.workspace)
+    with torch.cuda.device(dev):
+        rc = load().moe_route_sort(
+            logits.data_ptr(), bias.data_ptr(), T, E, n_group, topk_group, topk,
+            float(routed_scale), block_m, out.topk_ids.data_ptr(), out.topk_weights.data_ptr(),
+            out.sorted_token_ids.data_ptr(), out.sorted_weights.data_ptr(),
+            out.expert_ids.data_ptr(), out.num_tokens_post_pad.data_ptr(),
+            out.workspace.data_ptr(), out.workspace.numel(), _stream_handle(stream))
     _check(rc, "moe_route_sort")
     return out

@@ -222,6 +222,9 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   }
   if (smem > static_cast<size_t>(d.smem_optin)) return MOE_RS_ERR_LAUNCH;
   a.sh = sh;
+  a.wait_limit_ns = debug_wait_limit_ns();
+  // the segment kernel prunes with proxy scores once their bound is verified on the device
+  a.proxy_state = (a.use_seg && !sh.softmax) ? proxy_state_for_launch(st) : nullptr;
   a.topk_ids = topk_ids;
   a.topk_w = topk_w;
   if (sort) {
@@ -248,6 +251,7 @@ int run_slices(int T, int E, int K, int B, int U, int nslices, int32_t* sorted_i
   c.B = B;
   c.N = T * K;
   c.nslices = nslices;
+  c.wait_limit_ns = debug_wait_limit_ns();
   c.loc_off = reinterpret_cast<const int32_t*>(ws + l.loc_off);
   c.unit_buf = reinterpret_cast<const int2*>(ws + l.unit_buf);
   c.unit_e = reinterpret_cast<const uint16_t*>(ws + l.unit_e);
@@ -336,6 +340,7 @@ const char* moe_route_sort_strerror(int status) {
       return "hidden size H must be a multiple of 8 in [8, 8192]";
     case MOE_RS_ERR_NOT_MAPPED:
       return "host memory is not pinned and mapped into the device address space";
+    case MOE_RS_ERR_BAD_DEBUG_KNOB: return "unknown moe_route_sort_debug_set knob";
     default: return "unknown status";
   }
 }
@@ -378,12 +383,14 @@ struct GatePre {
 // softmax over the logits with plain top-k (softmax == true: n_group = topk_group = 1 and
 // bias unused, may be NULL).  With `gate`, the gate projection producing logits_bf16 is
 // launched first, once every argument has been accepted.
-int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, int n_group,
-                    int topk_group, int topk, float routed_scale, int block_m, bool softmax,
-                    const GatePre* gate, int32_t* topk_ids, float* topk_weights,
-                    int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
-                    int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
-                    cudaStream_t stream) {
+// Every host-side check of the whole path (shapes, pointers, workspace, alignment, aliasing),
+// in the order the status codes are documented; MOE_RS_OK if the call may launch.
+int validate_route_sort(const void* logits_bf16, const float* bias, int T, int E, int n_group,
+                        int topk_group, int topk, float routed_scale, int block_m, bool softmax,
+                        int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
+                        float* sorted_weights, int32_t* expert_ids,
+                        int32_t* num_tokens_post_pad, void* workspace,
+                        size_t workspace_bytes) {
   int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
   if (rc) return rc;
   rc = check_sort_shape(T, E, topk, block_m);
@@ -411,6 +418,22 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   const Span ins[] = {span(logits_bf16, 2 * static_cast<size_t>(T) * E),
                       span(bias, (T > 0 && bias) ? 4 * static_cast<size_t>(E) : 0)};
   if (any_alias(outs, 7, ins, 2)) return MOE_RS_ERR_ALIAS;
+  return MOE_RS_OK;
+}
+
+int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, int n_group,
+                    int topk_group, int topk, float routed_scale, int block_m, bool softmax,
+                    const GatePre* gate, int32_t* topk_ids, float* topk_weights,
+                    int32_t* sorted_token_ids, float* sorted_weights, int32_t* expert_ids,
+                    int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
+  int rc = validate_route_sort(logits_bf16, bias, T, E, n_group, topk_group, topk,
+                               routed_scale, block_m, softmax, topk_ids, topk_weights,
+                               sorted_token_ids, sorted_weights, expert_ids,
+                               num_tokens_post_pad, workspace, workspace_bytes);
+  if (rc) return rc;
+  if (softmax) bias = nullptr;
+  const WsLayout l = ws_layout(T, E, topk);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
   if (T == 0) return launch_status(launch_empty(num_tokens_post_pad, status, stream));
@@ -647,7 +670,12 @@ int moe_route_sort_from_host(const void* logits_host, void* logits_dev, const fl
                              size_t result_bytes, cudaStream_t stream) {
   if (T > 0 && (!logits_host || !logits_dev)) return MOE_RS_ERR_NULL_POINTER;
   if (result_bytes > 0 && (!result_dev || !result_host)) return MOE_RS_ERR_NULL_POINTER;
-  int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
+  // every check of moe_route_sort, on the device copy of the logits (which must not overlap an
+  // output or the workspace), before anything is enqueued
+  int rc = validate_route_sort(logits_dev, bias, T, E, n_group, topk_group, topk, routed_scale,
+                               block_m, false, topk_ids, topk_weights, sorted_token_ids,
+                               sorted_weights, expert_ids, num_tokens_post_pad, workspace,
+                               workspace_bytes);
   if (rc) return rc;
   const size_t in_bytes = 2 * static_cast<size_t>(T) * static_cast<size_t>(E);
   if (in_bytes > 0 &&
@@ -726,23 +754,33 @@ int moe_sort_atomic(const int32_t* topk_ids, const float* topk_weights, int T, i
 // the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_RS_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the array on the current device, looked up once per device (with that
-// device current) and cached; nullptr if the lookup fails.
+// Device address of the array in the current device's context, looked up once per context
+// (with that device current) and cached: a context created again (after cudaDeviceReset, for
+// example) gets a new id and a new lookup.  nullptr if the lookup fails.
 static void* noalloc_scratch_ptr() {
   static std::mutex mu;
-  static void* ptrs[64] = {};
+  struct Entry {
+    int dev = -1;
+    unsigned long long ctx = 0;
+    void* ptr = nullptr;
+  };
+  static Entry cache[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  unsigned long long ctx = 0;
+  if (!current_context(dev, ctx) || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (ptrs[dev] == nullptr) {
+  Entry& en = cache[dev];
+  if (en.ptr == nullptr || en.dev != dev || en.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
       cudaGetLastError();
       return nullptr;
     }
-    ptrs[dev] = p;
+    en.dev = dev;
+    en.ctx = ctx;
+    en.ptr = p;
   }
-  return ptrs[dev];
+  return en.ptr;
 }
 
 int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, int E,
@@ -751,6 +789,11 @@ int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, in
                            int32_t* sorted_token_ids, float* sorted_weights,
                            int32_t* expert_ids, int32_t* num_tokens_post_pad,
                            cudaStream_t stream) {
+  // shapes first, so a rejected shape gets its own status and nothing is looked up
+  int rc = check_route_shape(T, E, n_group, topk_group, topk, routed_scale);
+  if (rc) return rc;
+  rc = check_sort_shape(T, E, topk, block_m);
+  if (rc) return rc;
   const size_t need = moe_route_sort_workspace_bytes(T, E, topk, block_m);
   if (need > MOE_RS_NOALLOC_SCRATCH_BYTES) return MOE_RS_ERR_TOO_LARGE;
   void* scratch = noalloc_scratch_ptr();
@@ -759,6 +802,20 @@ int moe_route_sort_noalloc(const void* logits_bf16, const float* bias, int T, in
                         block_m, topk_ids, topk_weights, sorted_token_ids, sorted_weights,
                         expert_ids, num_tokens_post_pad, scratch, MOE_RS_NOALLOC_SCRATCH_BYTES,
                         stream);
+}
+
+int moe_route_sort_noalloc_status(int32_t* dst, cudaStream_t stream) {
+  if (!dst) return MOE_RS_ERR_NULL_POINTER;
+  if (!aligned(dst, 4)) return MOE_RS_ERR_MISALIGNED;
+  void* scratch = noalloc_scratch_ptr();
+  if (scratch == nullptr) return MOE_RS_ERR_LAUNCH;
+  // the status word is the first int32 of the workspace (offset 0 of the layout)
+  if (cudaMemcpyAsync(dst, scratch, sizeof(int32_t), cudaMemcpyDefault, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MOE_RS_ERR_LAUNCH;
+  }
+  return MOE_RS_OK;
 }
 
 }  // extern "C"

@@ -440,7 +440,9 @@ struct SmemExactSrc {
 };
 
 // ------------------------------------------------------- TMA bulk copies, mbarriers
-// A device wait gives up after this long (an error bit is raised instead of hanging).
+// A device wait gives up after this long (an error bit is raised instead of hanging).  The
+// launch argument `wait_limit_ns` carries it (a test hook can lower it to 0); waits for copies
+// still in flight before a CTA exits always use this value.
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -498,14 +500,17 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* mbar, uint32_t
   return done != 0u;
 }
 
-// Wait for phase `phase` of `mbar` to complete, at most kWaitLimitNs.  Every lane waits
-// (each gets the acquire); the result is made warp-uniform.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* mbar, uint32_t phase) {
+// Wait for phase `phase` of `mbar` to complete, at most `limit_ns` (0: report a timeout at
+// once without looking, a test hook).  Every lane waits (each gets the acquire); the result
+// is made warp-uniform.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* mbar, uint32_t phase,
+                                                  unsigned long long limit_ns) {
+  if (limit_ns == 0ull) return __all_sync(kFull, false);
   bool ok = mbar_try_wait(mbar, phase);
   if (!ok) {
     const unsigned long long t0 = globaltimer_ns();
     while (!(ok = mbar_try_wait(mbar, phase))) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      if (globaltimer_ns() - t0 > limit_ns) break;
     }
   }
   return __all_sync(kFull, ok);

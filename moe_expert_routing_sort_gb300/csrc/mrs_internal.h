@@ -151,6 +151,8 @@ struct RouteArgs {
   int nbuf;      // segment kernel: row buffers per warp (1 or 2)
   RouteShape sh;
   SegShape seg;
+  unsigned long long wait_limit_ns;  // bound of the row-copy waits (0: give up at once)
+  const int32_t* proxy_state;        // 1 once the proxy bound has been verified on the device
   int32_t* topk_ids;
   float* topk_w;
   UnitOut uo;
@@ -165,6 +167,7 @@ struct UnitArgs {
 
 struct SliceArgs {
   int T, K, E, U, B, N, nslices;
+  unsigned long long wait_limit_ns;  // bound of the look-back wait (0: give up at once)
   const int32_t* loc_off;
   const int2* unit_buf;
   const uint16_t* unit_e;
@@ -230,6 +233,17 @@ struct GatePlan {
 };
 GatePlan gate_plan(int E, int sms);
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
+
+// ------------------------------------------------------------ per-context host state
+// Test hooks set through moe_route_sort_debug_set (process-wide).
+unsigned long long debug_wait_limit_ns();  // kWaitLimitNs unless lowered
+// Identity of the current device and context (the context's unique id, 0 if the driver cannot
+// tell): host caches of device addresses are keyed on it.
+bool current_context(int& dev, unsigned long long& ctx_id);
+// Device address of the proxy-bound state word on the current device (1: the bound has been
+// verified there; see mrs_selftest.cu).  The first call on a context, outside stream capture,
+// enqueues the exhaustive check on `st` ahead of the caller's kernels.  nullptr on failure.
+const int32_t* proxy_state_for_launch(cudaStream_t st);
 
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st);

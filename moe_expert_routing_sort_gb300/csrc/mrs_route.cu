@@ -519,9 +519,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   }
   if (lane == 0) atomicMax(&cta_bmax_bits, (bmax != bmax) ? 0x7fffffffu : __float_as_uint(bmax));
   __syncthreads();
-  // the proxy bound holds for |bias| <= kProxyBiasLimit; beyond that every step is exact
+  // the proxy bound holds for |bias| <= kProxyBiasLimit once it has been verified on this
+  // device; otherwise every step is exact
   const float bm = __uint_as_float(cta_bmax_bits);
-  const float delta = kSoftmax ? 0.0f : (bm <= kProxyBiasLimit) ? proxy_delta(bm) : INFINITY;
+  const bool proxy_ok = a.proxy_state != nullptr && *a.proxy_state == 1;
+  const float delta = kSoftmax ? 0.0f
+                      : (bm <= kProxyBiasLimit && proxy_ok) ? proxy_delta(bm) : INFINITY;
 
   uint32_t phase = 0u;  // bit b = parity to wait for on buffer b
   int issued = n_mine < nbuf ? n_mine : nbuf;
@@ -529,7 +532,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   bool ok = true;
   for (int k = 0; k < n_mine; ++k) {
     const int b = (nbuf == 2) ? (k & 1) : 0;
-    if (!mbar_wait_bounded(&mbar[b], (phase >> b) & 1u)) {
+    if (!mbar_wait_bounded(&mbar[b], (phase >> b) & 1u, a.wait_limit_ns)) {
       ok = false;
       break;
     }
@@ -573,7 +576,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
     if (lane == 0) atomicOr(&cta_flags, MOE_RS_DEVICE_WAIT_TIMEOUT);
     for (int k = consumed; k < issued; ++k) {
       const int b = (nbuf == 2) ? (k & 1) : 0;
-      drained &= mbar_wait_bounded(&mbar[b], (phase >> b) & 1u);
+      drained &= mbar_wait_bounded(&mbar[b], (phase >> b) & 1u, kWaitLimitNs);
       phase ^= 1u << b;
     }
   }

@@ -186,28 +186,37 @@ __global__ void __launch_bounds__(kSliceThreads) mrs_slices_kernel(const SliceAr
   }
   // this slice's first row = sum of the padded sizes of all earlier slices: warp 0 polls
   // all their words at once (lane l holds slices l, l + 32, ...; bounded wait)
+  // (a wait limit of 0, a test hook, gives up at once: every slice but the first reports a
+  // timeout and sums nothing, so its rows start too low but stay inside the buffers)
   if (warp == 0) {
     const unsigned long long t_start = globaltimer_ns();
     unsigned long long f[kMaxSlices / 32];
     bool ok = true;
-    for (;;) {
-      bool missing = false;
+    if (a.wait_limit_ns == 0ull) {
 #pragma unroll
-      for (int k = 0; k < kMaxSlices / 32; ++k) {
-        const int p = lane + 32 * k;
-        f[k] = (p < c) ? ld_relaxed_u64(&a.slice_flags[p]) : kFlagReady;
-        missing |= (f[k] & kFlagReady) == 0ull;
-      }
-      if (!__any_sync(kFull, missing)) break;
-      if (globaltimer_ns() - t_start > kWaitLimitNs) {
-        ok = false;
-        break;
+      for (int k = 0; k < kMaxSlices / 32; ++k) f[k] = 0ull;
+      ok = (c == 0);
+    } else {
+      for (;;) {
+        bool missing = false;
+#pragma unroll
+        for (int k = 0; k < kMaxSlices / 32; ++k) {
+          const int p = lane + 32 * k;
+          f[k] = (p < c) ? ld_relaxed_u64(&a.slice_flags[p]) : kFlagReady;
+          missing |= (f[k] & kFlagReady) == 0ull;
+        }
+        if (!__any_sync(kFull, missing)) break;
+        if (globaltimer_ns() - t_start > a.wait_limit_ns) {
+          ok = false;
+          break;
+        }
       }
     }
     int v = 0;
 #pragma unroll
     for (int k = 0; k < kMaxSlices / 32; ++k)
-      v += (lane + 32 * k < c) ? static_cast<int>(f[k] & 0xffffffffull) : 0;
+      v += (lane + 32 * k < c && (f[k] & kFlagReady)) ? static_cast<int>(f[k] & 0xffffffffull)
+                                                       : 0;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
     if (lane == 0) {

@@ -24,7 +24,10 @@ logits), numpy ``default_rng(seed)``, in draw order:
   4. redraws of hidden rows as in step 4 above.
 Both grids are exact in bf16, and every partial sum of a dot product is a multiple of 2^-10
 below 2^9 (H <= 8192), so a float32 accumulation of it is exact in any order.  With H = 7168
-the logits have a standard deviation of about 1.6.
+the logits have a standard deviation of about 1.6.  ``grid="general"`` draws instead, in the
+same order, gate rows ``rng.standard_normal((E, H)) / sqrt(H)`` and hidden rows
+``rng.standard_normal((T, H))``, both rounded to bf16 (logits of standard deviation about 1,
+whose float32 sums are rounded).
 """
 from __future__ import annotations
 
@@ -161,13 +164,22 @@ def make_gate_inputs(
     seed: int = 0,
     needs_redraw: Optional[Callable[[np.ndarray, np.ndarray, np.ndarray], Iterable[int]]] = None,
     max_rounds: int = 64,
+    grid: str = "coarse",
 ) -> GateInputs:
-    """Draw hidden states and gate rows on the coarse grids of the recipe above."""
+    """Draw hidden states and gate rows on the coarse grids of the recipe above (or, with
+    ``grid="general"``, general normal values rounded to bf16)."""
+    if grid not in ("coarse", "general"):
+        raise ValueError(f"unknown grid {grid!r}")
     rng = np.random.default_rng(seed)
     bias = rng.uniform(-bias_half_range, bias_half_range, E).astype(np.float32)
-    w = float32_to_bf16_bits((rng.integers(-3, 4, (E, H)) / 64.0).astype(np.float32))
+    if grid == "coarse":
+        w = float32_to_bf16_bits((rng.integers(-3, 4, (E, H)) / 64.0).astype(np.float32))
+    else:
+        w = float32_to_bf16_bits((rng.standard_normal((E, H)) / np.sqrt(H)).astype(np.float32))
 
     def rows(n):
+        if grid == "general":
+            return float32_to_bf16_bits(rng.standard_normal((n, H)).astype(np.float32))
         return float32_to_bf16_bits((rng.integers(-16, 17, (n, H)) / 16.0).astype(np.float32))
 
     hidden = rows(T)

@@ -78,8 +78,6 @@ def _load():
         lib.oracle_route.argtypes = [P, P, i32, i32, i32, i32, i32, f32, P, P]
         lib.oracle_route.restype = i32
         lib.oracle_route_softmax.argtypes = [P, i32, i32, i32, f32, P, P]
-        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
-        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_gate_logits.argtypes = [P, P, i32, i32, i32, P]
         lib.oracle_route_softmax.restype = i32
         lib.oracle_max_padded.argtypes = [i32, i32, i32, i32]
@@ -271,13 +269,9 @@ def route_sort(logits, bias, n_group, topk_group, topk, routed_scale, block_m):
     return res
 
 
-def double_to_bf16(v: float) -> int:
-    """R14: the bf16 bit pattern nearest to v (ties to even), one rounding."""
-    return int(_load().oracle_double_to_bf16(float(v)))
-
-
 def gate_logits(hidden, w_gate) -> np.ndarray:
-    """R14: bf16 logits [T,E] of bf16 hidden [T,H] and bf16 gate rows [E,H]."""
+    """R14: bf16 logits [T,E] of bf16 hidden [T,H] and bf16 gate rows [E,H]: each the exact
+    dot product rounded once to bf16 (nearest, ties to even)."""
     hs = _u16(hidden)
     ws = _u16(w_gate)
     T, H = hs.shape

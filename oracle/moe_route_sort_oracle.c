@@ -38,8 +38,8 @@
  *                 over all E cancels), so selection and weights need no full-row sum
  *   R14 gate      the router gate projection ahead of the path: logits[t,e] = the bf16
  *                 nearest (ties to even) to the dot product of hidden row t and gate row e,
- *                 both bf16; one rounding of the exact sum (formed here in double, whose
- *                 products of two bf16 values are exact)
+ *                 both bf16; one rounding of the exact sum (formed here as an exact
+ *                 fixed-point integer, so no intermediate rounding happens at all)
  *
  * Parity pins: every function here is pinned by the tests in tests/test_oracle_pins.py
  * (bf16 decoding against a library conversion over all 65536 patterns, sigmoid against a
@@ -333,39 +333,106 @@ int oracle_route_sort_softmax(const uint16_t* logits, int T, int E, int K, float
 
 /* ------------------------------------------------------------ gate projection */
 
-/* R14: the bf16 nearest to v, ties to even, in one rounding.  The bf16 spacing at v is
- * 2^(e-8) for |v| in [2^(e-1), 2^e) and 2^-133 below the normal range; scaling by it turns the
- * rounding into rint (round-half-even in the default rounding mode) on an exact double. */
-uint16_t oracle_double_to_bf16(double v) {
-  if (v != v) return 0x7fc0;
-  if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
-  int e = 0;
-  (void)frexp(fabs(v), &e);
-  int q = e - 8;
-  if (q < -133) q = -133;
-  double r = ldexp(rint(ldexp(fabs(v), -q)), q);
-  float f = (r >= 0x1p128) ? INFINITY : (float)r; /* r has at most 8 significant bits */
+/* R14, exactly: the dot product of a bf16 row pair as an exact integer.  A finite bf16 value is
+ * m * 2^q with an integer |m| < 2^8 and q >= -133, so a product of two is m * 2^q with
+ * |m| < 2^16 and q >= -266; scaled by 2^266 every product, and so the exact sum, is an
+ * integer.  The sum is held in 32-bit limbs (kept in int64, carries settled at the end): bit
+ * positions up to 266 + 240 + 16 plus 13 bits of headroom for H <= 8192 need 17 limbs. */
+#define ORACLE_ACC_LIMBS 18
+#define ORACLE_ACC_SHIFT 266
+
+typedef struct {
+  int64_t limb[ORACLE_ACC_LIMBS];
+} oracle_acc;
+
+/* Integer significand and exponent of a finite bf16 value: v = m * 2^q. */
+static void oracle_bf16_split(uint16_t bits, int32_t* m, int* q) {
+  int32_t mag = (int32_t)(bits & 0x7fu);
+  int ex = (int)((bits >> 7) & 0xffu);
+  if (ex == 0) {
+    *q = -133; /* subnormal: 0.mag * 2^-126 = mag * 2^-133 */
+  } else {
+    mag |= 0x80; /* hidden bit: 1.mag * 2^(ex-127) = (128 + mag) * 2^(ex-134) */
+    *q = ex - 134;
+  }
+  *m = (bits & 0x8000u) ? -mag : mag;
+}
+
+static void oracle_acc_add_product(oracle_acc* acc, uint16_t a, uint16_t b) {
+  int32_t ma, mb;
+  int qa, qb;
+  oracle_bf16_split(a, &ma, &qa);
+  oracle_bf16_split(b, &mb, &qb);
+  int64_t m = (int64_t)ma * (int64_t)mb; /* |m| < 2^16 */
+  if (m == 0) return;
+  int pos = qa + qb + ORACLE_ACC_SHIFT; /* >= 0 */
+  acc->limb[pos / 32] += m * ((int64_t)1 << (pos % 32)); /* |term| < 2^47 */
+}
+
+/* The bf16 nearest (ties to even) to the accumulated exact value; +0 for an exact zero. */
+static uint16_t oracle_acc_to_bf16(const oracle_acc* acc) {
+  /* settle the carries: limbs 0..n-2 in [0, 2^32), the top limb signed */
+  int64_t l[ORACLE_ACC_LIMBS];
+  memcpy(l, acc->limb, sizeof l);
+  for (int i = 0; i + 1 < ORACLE_ACC_LIMBS; ++i) {
+    int64_t carry = l[i] >> 32; /* floor division by 2^32 (arithmetic shift) */
+    l[i] -= carry * ((int64_t)1 << 32);
+    l[i + 1] += carry;
+  }
+  uint16_t sign = 0;
+  if (l[ORACLE_ACC_LIMBS - 1] < 0) { /* negate: two's complement over the limbs */
+    sign = 0x8000u;
+    int64_t borrow = 0;
+    for (int i = 0; i < ORACLE_ACC_LIMBS; ++i) {
+      int64_t v = -l[i] - borrow;
+      borrow = 0;
+      if (i + 1 < ORACLE_ACC_LIMBS && v < 0) {
+        v += (int64_t)1 << 32;
+        borrow = 1;
+      }
+      l[i] = v;
+    }
+  }
+  int top = -1; /* highest set bit of the magnitude N */
+  for (int i = ORACLE_ACC_LIMBS - 1; i >= 0 && top < 0; --i)
+    if (l[i] != 0)
+      for (int b = 31; b >= 0; --b)
+        if ((l[i] >> b) & 1) {
+          top = 32 * i + b;
+          break;
+        }
+  if (top < 0) return 0x0000; /* exact zero */
+  /* keep 8 significant bits, but never below bf16's last subnormal bit (2^-133) */
+  int lsb = top - 7;
+  if (lsb < ORACLE_ACC_SHIFT - 133) lsb = ORACLE_ACC_SHIFT - 133;
+  int64_t mant = 0;
+  for (int p = top; p >= lsb; --p) mant = 2 * mant + ((l[p / 32] >> (p % 32)) & 1);
+  /* remainder below lsb against half of the lsb weight */
+  int half = (lsb >= 1) ? ((l[(lsb - 1) / 32] >> ((lsb - 1) % 32)) & 1) : 0;
+  int rest = 0; /* any set bit below lsb - 1 */
+  for (int p = lsb - 2; p >= 0 && !rest; --p) rest = (l[p / 32] >> (p % 32)) & 1;
+  if (half && (rest || (mant & 1))) mant += 1;
+  /* value = mant * 2^(lsb - 266), at most 9 significant bits (a carry into a power of two) */
+  double v = ldexp((double)mant, lsb - ORACLE_ACC_SHIFT);
+  float f = (v >= 0x1p128) ? INFINITY : (float)v; /* exact: few significant bits */
   uint32_t bits;
   memcpy(&bits, &f, sizeof bits);
-  bits >>= 16;
-  if (v < 0) bits |= 0x8000u;
-  return (uint16_t)bits;
+  return (uint16_t)((bits >> 16) | sign);
 }
 
 /* R14: logits [T,E] (bf16) of hidden [T,H] (bf16) times gate weights [E,H] (bf16, one row per
- * expert): each entry one dot product in h order, in double, rounded once to bf16. */
+ * expert): each entry the exact dot product (as an integer above), rounded once to bf16.
+ * Inputs must be finite. */
 int oracle_gate_logits(const uint16_t* hidden, const uint16_t* w, int T, int E, int H,
                        uint16_t* logits) {
-  if (T < 0 || E < 1 || H < 1) return ORACLE_ERR_ARGS;
+  if (T < 0 || E < 1 || H < 1 || H > 8192) return ORACLE_ERR_ARGS;
   for (int t = 0; t < T; ++t) {
     for (int e = 0; e < E; ++e) {
-      double sum = 0.0;
-      for (int h = 0; h < H; ++h) {
-        double a = (double)oracle_bf16_to_float(hidden[(size_t)t * H + h]);
-        double b = (double)oracle_bf16_to_float(w[(size_t)e * H + h]);
-        sum = sum + a * b;
-      }
-      logits[(size_t)t * E + e] = oracle_double_to_bf16(sum);
+      oracle_acc acc;
+      memset(&acc, 0, sizeof acc);
+      for (int h = 0; h < H; ++h)
+        oracle_acc_add_product(&acc, hidden[(size_t)t * H + h], w[(size_t)e * H + h]);
+      logits[(size_t)t * E + e] = oracle_acc_to_bf16(&acc);
     }
   }
   return ORACLE_OK;

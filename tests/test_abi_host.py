@@ -49,7 +49,7 @@ def test_size_queries():
 
 
 def test_strerror_covers_codes():
-    for code in range(-15, 1):
+    for code in range(-16, 1):
         assert mrs.strerror(code) != "unknown status"
     assert mrs.strerror(-99) == "unknown status"
 
@@ -137,6 +137,68 @@ def test_from_host_rejects_missing_copy_pointers(lib):
     assert _from_host(lib, logits_dev=None) == -1
     assert _from_host(lib, result_dev=None) == -1
     assert _from_host(lib, result_host=None) == -1
+
+
+def _from_host_full(lib, B=16, ws=BASE + 0x100000, ws_bytes=None, logits_dev=BASE,
+                    ids=BASE + 0x20000):
+    if ws_bytes is None:
+        ws_bytes = mrs.moe_route_sort_workspace_bytes(4, 64, 6, 16)
+    return lib.moe_route_sort_from_host(
+        BASE + 0x200000, logits_dev, BASE + 0x10000, 4, 64, 8, 4, 6, 2.5, B, ids,
+        BASE + 0x30000, BASE + 0x40000, BASE + 0x80000, BASE + 0xC0000, BASE + 0xD0000, ws,
+        ws_bytes, BASE + 0x300000, BASE + 0x400000, 64, None)
+
+
+def test_from_host_checks_everything_before_the_copy(lib):
+    # Every check of moe_route_sort runs before the host-to-device copy is enqueued.  With fake
+    # addresses (and no GPU here) an enqueued copy would fail with the launch status -12, so
+    # each specific status below also shows that nothing was enqueued first.
+    assert _from_host_full(lib, B=12) == -5                       # bad block_m
+    assert _from_host_full(lib, ws_bytes=16) == -10               # short workspace
+    assert _from_host_full(lib, ws=0) == -10                      # no workspace
+    assert _from_host_full(lib, logits_dev=BASE + 8) == -8        # misaligned device logits
+    assert _from_host_full(lib, logits_dev=BASE + 0x100000) == -9  # device logits over workspace
+    assert _from_host_full(lib, logits_dev=BASE + 0x40000) == -9   # over sorted_token_ids
+    assert _from_host_full(lib, ids=BASE + 0x10) == -9             # topk ids over device logits
+
+
+def test_noalloc_checks_shapes_first(lib):
+    # a shape the library rejects gets its own status, before the scratch size check and the
+    # device address lookup (which would give -12 here, with no GPU)
+    args = [BASE, BASE + 0x100000, 300000, 4096, 16, 4, 8, 1.0, 128, BASE + 0x200000,
+            BASE + 0x300000, BASE + 0x400000, BASE + 0x500000, BASE + 0x600000,
+            BASE + 0x700000, None]
+    for i, v, code in [(8, 3, -5), (3, 0, -2), (3, 4097, -2), (4, 7, -3), (6, 0, -4),
+                       (2, -1, -6), (7, float("nan"), -11)]:
+        bad = list(args)
+        bad[i] = v
+        assert lib.moe_route_sort_noalloc(*bad) == code, (i, v, code)
+    assert lib.moe_route_sort_noalloc(*args) == -13  # valid shape, too large for the scratch
+
+
+def test_state_accessors_validate(lib):
+    assert lib.moe_route_sort_noalloc_status(None, None) == -1
+    assert lib.moe_route_sort_noalloc_status(BASE + 2, None) == -8
+    assert lib.moe_route_sort_proxy_state(None, None) == -1
+    assert lib.moe_route_sort_proxy_state(BASE + 1, None) == -8
+
+
+def test_debug_knobs(lib):
+    assert lib.moe_route_sort_debug_set(99, 0) == -16
+    assert lib.moe_route_sort_debug_set(0, 0) == -16
+    assert lib.moe_route_sort_debug_set(1, 0) == 0   # wait limit 0 ...
+    assert lib.moe_route_sort_debug_set(1, -1) == 0  # ... and back to the default
+    assert lib.moe_route_sort_debug_set(2, 1) == 0   # forced proxy failure ...
+    assert lib.moe_route_sort_debug_set(2, 0) == 0   # ... and back to the real check
+
+
+def test_binding_refuses_buffers_on_different_devices():
+    # the library runs on one device and reads every pointer there: the binding refuses a mix
+    from moe_expert_routing_sort_gb300 import binding
+    with pytest.raises(ValueError, match="one device"):
+        binding._one_device(torch.empty(1), torch.empty(1, device="meta"))
+    with pytest.raises(ValueError, match="CUDA"):
+        binding._one_device(torch.empty(1), None, torch.empty(2))
 
 
 def _softmax(lib, T=4, E=64, K=6, R=1.0, B=16, logits=BASE, ids=BASE + 0x20000,

@@ -387,22 +387,33 @@ def test_softmax_two_experts_closed_form(oracle_mod):
 
 
 # -------------------------------------------- gate projection (reading R14)
-def _bf16_neighbours_rne(v: float) -> int:
-    # independent rounding: exact rational comparison against the two bracketing finite
-    # bf16 values from the full table, ties to the even pattern
+def _bf16_rne_exact(v) -> int:
+    # independent rounding of an exact rational v (a Fraction): comparison against the two
+    # bracketing finite bf16 values from the full table, ties to the even pattern, +0 for 0
     # (on |v| over the non-negative patterns 0x0000..0x7f80; the sign is put back after)
     from fractions import Fraction
-    sign = 0x8000 if math.copysign(1.0, v) < 0 else 0
+    v = Fraction(v)
+    if v == 0:
+        return 0x0000
+    sign = 0x8000 if v < 0 else 0
     a = abs(v)
     bits = np.arange(0x7F81, dtype=np.uint32)
     vals = (bits << 16).view(np.float32).astype(np.float64)  # ascending, ends at +inf
-    i = int(np.searchsorted(vals, a, side="left"))
-    if vals[i] == a:
+    i = int(np.searchsorted(vals, float(a), side="left"))
+    # float(a) may round: step to the exact bracket
+    while i > 0 and Fraction(float(vals[i - 1])) >= a:
+        i -= 1
+    while np.isfinite(vals[i]) and Fraction(float(vals[i])) < a:
+        i += 1
+    if np.isfinite(vals[i]) and Fraction(float(vals[i])) == a:
         return int(bits[i]) | sign
     lo, hi = i - 1, i
-    dl = Fraction(a) - Fraction(float(vals[lo]))
-    dh = (Fraction(float(vals[hi])) - Fraction(a)) if np.isfinite(vals[hi]) else None
-    if dh is None or dl < dh:
+    dl = a - Fraction(float(vals[lo]))
+    dh = (Fraction(float(vals[hi])) - a) if np.isfinite(vals[hi]) else None
+    if dh is None:
+        # past the largest finite bf16: round to nearest with the infinity step 2^120
+        pick = hi if dl >= Fraction(2) ** 119 else lo
+    elif dl < dh:
         pick = lo
     elif dh < dl:
         pick = hi
@@ -411,22 +422,57 @@ def _bf16_neighbours_rne(v: float) -> int:
     return int(bits[pick]) | sign
 
 
-def test_double_to_bf16_rounds_once_to_nearest_even(oracle_mod):
+def _bf16_value(b):
+    from fractions import Fraction
+    return Fraction(float((np.uint32(b) << np.uint32(16)).view(np.float32)))
+
+
+def _bf16_of(x: float) -> int:
+    b = int(datagen.float32_to_bf16_bits(np.float32([x]))[0])
+    assert float(_bf16_value(b)) == x, x  # only exact bf16 values here
+    return b
+
+
+def _gate_one(oracle_mod, pairs):
+    """The oracle's logit for one hidden row and one gate row given as (h, w) float pairs."""
+    hb = np.array([[_bf16_of(h) for h, _ in pairs]], np.uint16)
+    wb = np.array([[_bf16_of(w) for _, w in pairs]], np.uint16)
+    return int(oracle_mod.gate_logits(hb, wb)[0, 0])
+
+
+def test_gate_logits_round_the_exact_sum_once(oracle_mod):
     # ties: 1 + 2^-8 lies halfway between 1 (0x3f80) and 1 + 2^-7 (0x3f81): even is 0x3f80;
     # 1 + 3 * 2^-8 lies halfway between 0x3f81 and 0x3f82: even is 0x3f82
-    assert oracle_mod.double_to_bf16(1 + 2 ** -8) == 0x3F80
-    assert oracle_mod.double_to_bf16(1 + 3 * 2 ** -8) == 0x3F82
-    assert oracle_mod.double_to_bf16(-(1 + 3 * 2 ** -8)) == 0xBF82
-    # just above a tie rounds up (a double rounding through float32 would lose this)
-    assert oracle_mod.double_to_bf16(1 + 2 ** -8 + 2 ** -40) == 0x3F81
-    assert oracle_mod.double_to_bf16(0.0) == 0x0000
-    assert oracle_mod.double_to_bf16(-0.0) == 0x8000
-    assert oracle_mod.double_to_bf16(1e39) == 0x7F80
-    rng = np.random.default_rng(21)
-    vals = np.concatenate([rng.standard_normal(300) * 10.0 ** rng.integers(-30, 30, 300),
-                           rng.standard_normal(100) * 1e-39])  # subnormal range too
-    for v in vals:
-        assert oracle_mod.double_to_bf16(float(v)) == _bf16_neighbours_rne(float(v)), v
+    assert _gate_one(oracle_mod, [(1.0, 1.0), (2 ** -4, 2 ** -4)]) == 0x3F80
+    assert _gate_one(oracle_mod, [(1.0, 1.0), (2 ** -4, 2 ** -4), (2 ** -7, 1.0)]) == 0x3F82
+    assert _gate_one(oracle_mod, [(-1.0, 1.0), (2 ** -4, -2 ** -4), (-(2 ** -7), 1.0)]) == 0xBF82
+    # just above a tie rounds up, even when the excess is far below a double's precision
+    assert _gate_one(oracle_mod, [(1.0, 1.0), (2 ** -4, 2 ** -4), (2 ** -60, 2 ** -60)]) == 0x3F81
+    # cancellation: 2^60 + 2^-30 - 2^60 = 2^-30 exactly (a sum in double gives 0)
+    assert _gate_one(oracle_mod, [(2 ** 30, 2 ** 30), (2 ** -15, 2 ** -15),
+                                  (2 ** 30, -2 ** 30)]) == _bf16_of(2 ** -30)
+    # exact zero is +0; the smallest subnormal survives; overflow gives infinity
+    assert _gate_one(oracle_mod, [(1.0, 1.0), (1.0, -1.0)]) == 0x0000
+    assert _gate_one(oracle_mod, [(2 ** -70, 2 ** -63)]) == 0x0001
+    assert _gate_one(oracle_mod, [(2 ** -70, 2 ** -64)]) == 0x0000  # half the smallest: even
+    assert _gate_one(oracle_mod, [(2 ** 100, 2 ** 100)]) == 0x7F80
+    assert _gate_one(oracle_mod, [(-(2 ** 100), 2 ** 100)]) == 0xFF80
+
+
+def test_gate_logits_equal_exact_rational_rounding(oracle_mod):
+    # random rows with widely spread exponents (so sums in double would lose bits), checked
+    # entry by entry against the exact rational dot product rounded once
+    rng = np.random.default_rng(24)
+    T, E, H = 3, 6, 64
+    hx = rng.standard_normal((T, H)) * 2.0 ** rng.integers(-40, 40, (T, H))
+    wx = rng.standard_normal((E, H)) * 2.0 ** rng.integers(-40, 40, (E, H))
+    hb = datagen.float32_to_bf16_bits(hx.astype(np.float32))
+    wb = datagen.float32_to_bf16_bits(wx.astype(np.float32))
+    got = oracle_mod.gate_logits(hb, wb)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(_bf16_value(hb[t, h]) * _bf16_value(wb[e, h]) for h in range(H))
+            assert got[t, e] == _bf16_rne_exact(exact), (t, e)
 
 
 def test_gate_logits_exact_on_a_coarse_grid(oracle_mod):
@@ -461,4 +507,5 @@ def test_gate_logits_within_half_ulp_of_float64(oracle_mod):
     assert np.all(np.abs(g - ref) <= 0.5 * spacing * (1 + 1e-12))
     for t in range(T):  # and the row/column roles are not swapped
         for e in (0, 17, 39):
-            assert got[t, e] == _bf16_neighbours_rne(float(np.dot(hx[t], wx[e])))
+            exact = sum(_bf16_value(hb[t, h]) * _bf16_value(wb[e, h]) for h in range(H))
+            assert got[t, e] == _bf16_rne_exact(exact)
