@@ -5,8 +5,11 @@ Inputs are on the coarse grids of datagen.make_gate_inputs, where every fp32 par
 dot product is exact: the GPU's logits must then equal the oracle's (one nearest-even
 rounding of the exact dot product) bit for bit, and everything downstream is compared as in
 the route-sort parity tests (hidden rows whose oracle selection margin is below 1e-6 are
-redrawn).  On general bf16 inputs the fp32 sum is rounded, so there the logits are checked to
-lie within one bf16 step of the oracle's and to be identical from call to call; every token
+redrawn).  On general bf16 inputs the fp32 sum is rounded, so there each logit is checked
+against the oracle's within one bf16 step plus the worst-case error of an fp32 sum of H terms
+(H * 2^-24 * the sum of the terms' magnitudes: cancellation makes a small logit's bf16 step
+smaller than that), nearly all of them must be equal, and they are identical from call to
+call; every token
 whose logits row equals the oracle's routes bit for bit like the oracle's (the oracle only
 ever routes its own logits: no expected value comes from the GPU), and the sort metadata is
 compared exactly when every row matches, else through the sort invariants.
@@ -36,6 +39,20 @@ def _built():
 
 def _bf16_dev(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+def _logit_bound(hb, wb):
+    """Per logit: one bf16 step at the oracle's value plus the worst-case rounding error of an
+    fp32 sum of the H products (H * 2^-24 * sum |h * w|)."""
+    hx = (hb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wx = (wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    H = hx.shape[1]
+    return H * 2.0 ** -24 * (np.abs(hx) @ np.abs(wx).T)
+
+
+def _bf16_step(bits):
+    v = np.abs((bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    return 2.0 ** (np.floor(np.log2(np.maximum(v, 2.0 ** -126))) - 7)
 
 
 def _run(inp, G, Kg, K, R, B, poison=False):
@@ -108,9 +125,8 @@ def test_general_inputs_within_one_bf16_step(T, E, H):
     ref = oracle.gate_logits(hb, wb)
     ga = (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     gr = (ref.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(gr), 1e-30))) - 7)
-    assert np.all(np.abs(ga - gr) <= step)
-    assert np.mean(a == ref) > 0.95  # fp32 accumulation rarely moves the rounding
+    assert np.all(np.abs(ga - gr) <= _bf16_step(ref) + _logit_bound(hb, wb))
+    assert np.mean(a == ref) > 0.99  # fp32 accumulation rarely moves the rounding
 
 
 @pytest.mark.parametrize("T,E,G,Kg,K,B,H", [(1, 896, 8, 4, 16, 32, 7168),
@@ -124,11 +140,12 @@ def test_general_inputs_route_like_the_oracle(T, E, G, Kg, K, B, H):
                                    needs_redraw=gate_redraw_callback(oracle, G, Kg, K))
     logits, out = _run(inp, G, Kg, K, R, B)
     ref = oracle.gate_route_sort(inp.hidden_bf16, inp.w_gate_bf16, inp.bias, G, Kg, K, R, B)
-    # logits: one bf16 step at most; the fraction that differs at all is reported
+    # logits: one bf16 step plus the fp32 accumulation bound; the fraction that differs at
+    # all is reported
     ga = (logits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     gr = (ref["logits"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(gr), 1e-30))) - 7)
-    assert np.all(np.abs(ga - gr) <= step)
+    bound = _bf16_step(ref["logits"]) + _logit_bound(inp.hidden_bf16, inp.w_gate_bf16)
+    assert np.all(np.abs(ga - gr) <= bound)
     diff = logits != ref["logits"]
     print(f"general gate inputs T={T} E={E} H={H}: {int(diff.sum())} of {diff.size} logits "
           f"({100.0 * diff.mean():.3f}%) one bf16 step from the oracle's")
