@@ -48,7 +48,7 @@ L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024
 METRIC = "route-sort µs/call at T=1 E=896; routed tokens/s and % HBM roofline at T≥512"
 CSRC = os.path.join(ROOT, "moe_expert_routing_sort_gb300", "csrc")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 def parse_args():
@@ -85,7 +85,7 @@ def kernel_source_hash() -> str:
 
 def captured_traffic(workload: str):
     """DRAM bytes (read + write) per launch of the workload's dominant kernel from the ncu
-    capture recorded in profiles/dram_traffic.md, or None when no capture of the current
+    capture recorded in profiles/dram_traffic.txt, or None when no capture of the current
     kernel sources exists (a table row: | workload | kernel | bytes | source hash | ...)."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
@@ -795,7 +795,7 @@ def main():
                      "achieved": head["achieved_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": head["roofline_frac"], "peak_kind": peak_kind,
                      "traffic": traffic,
-                     "traffic_source": ("profiles/dram_traffic.md, capture of the current "
+                     "traffic_source": ("profiles/dram_traffic.txt, capture of the current "
                                         "kernel sources " + kernel_source_hash())
                                        if traffic is not None else
                                        "no ncu capture of the current kernel sources"},

@@ -1,6 +1,8 @@
 // mrs_decode.cu -- the whole route-sort path for one token (decode), one CTA, one launch.
 //
-// Latency-oriented: three block barriers from the logits to the outputs.
+// Latency-oriented: four block barriers from the logits to the outputs; the serial steps run
+// in one warp while the others wait, so they do not share the schedulers with copies of
+// themselves.
 //   rows      group j is held by TPG consecutive threads (TPG = the largest power of two
 //             with TPG * G <= 512): thread i of the group owns experts j*g + i + TPG*r;
 //             one DRAM round trip brings logits and bias, exact scores stay in registers
@@ -8,12 +10,18 @@
 //             top-2 of every 8-thread segment (threshold samples) and, at the top, the
 //             group's top-2 (one partial per warp when a group spans several warps)
 //   ---- barrier
-//   kept      every warp merges the partials and ranks the G group scores itself
-//   threshold at least ceil(K/2) kept segments hold two keys >= t2, so at least K kept keys
-//             are >= t2 (and the K-th best segment maximum is also such a bound)
-//   survivors kept keys at or above it are compacted (warp-aggregated slots)
+//   kept      warp 0 alone merges the partials and ranks the G group scores (the other warps
+//             wait at the next barrier, so the serial steps run at one warp's full issue rate)
+//   threshold warp 0: at least ceil(K/2) kept segments hold two keys >= t2, so at least K
+//             kept keys are >= t2 (and the K-th best segment maximum is also such a bound);
+//             the kept-group masks and the threshold go to shared memory
 //   ---- barrier
-//   rank      warp 0 ranks the survivors by counting and writes the K slots
+//   survivors every thread compacts its kept keys at or above the threshold (warp-aggregated
+//             slots)
+//   ---- barrier
+//   rank      four threads per survivor count the better survivors (rank by counting)
+//   ---- barrier
+//   finish    warp 0 forms the weights and writes the K slots
 //   sort      one token: each selected expert gets one route, so expert id_k owns block
 //             (number of selected ids below id_k), its row 0 is route k and rows 1..B-1 are
 //             padding (written at the start, as they depend on nothing); npp = K * B
@@ -43,6 +51,8 @@ struct DecodeSmem {
   alignas(16) int sel_id[kMaxTopk];
   alignas(16) float sel_s[kMaxTopk];
   int count;
+  float tau;            // selection threshold (warp 0)
+  unsigned kept[2];     // kept-group masks, groups 0-31 and 32-63 (warp 0)
 };
 
 __device__ __forceinline__ void top2_merge_xor(float& m1, float& m2, int d) {
@@ -96,8 +106,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
     }
     if (tid == 0) {
       *a.npp = K * B;
-      *a.status = 0;
       sm.count = 0;
+    }
+    if (warp == kDecodeWarps - 1) {
+      // the call's status: what the work ahead of this kernel (the gate projection) reported
+      int f = 0;
+      for (int v = lane; v < a.n_pre_flags; v += 32) f |= a.pre_flags[v];
+      f = __reduce_or_sync(kFull, f);
+      if (lane == 0) *a.status = f;
     }
     float t1 = -INFINITY, t2 = -INFINITY;
 #pragma unroll
@@ -128,50 +144,57 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   }
   __syncthreads();
 
-  // ---- group scores and kept groups, by every warp (lane l holds groups l and l + 32)
-  unsigned km0 = 0xffffffffu, km1 = 0xffffffffu;
-  if (Kg < G) {
-    float gs[2];
+  if (warp == 0) {
+    // ---- group scores and kept groups (lane l holds groups l and l + 32)
+    unsigned km0 = 0xffffffffu, km1 = 0xffffffffu;
+    if (Kg < G) {
+      float gs[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int l = lane + 32 * h;
-      gs[h] = -INFINITY;
-      if (l < G) {
-        float m1 = -INFINITY, m2 = -INFINITY;
-        for (int p = 0; p < P; ++p) {
-          const float o1 = sm.part1[l * P + p], o2 = sm.part2[l * P + p];
-          m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
-          m1 = fmaxf(m1, o1);
+      for (int h = 0; h < 2; ++h) {
+        const int l = lane + 32 * h;
+        gs[h] = -INFINITY;
+        if (l < G) {
+          float m1 = -INFINITY, m2 = -INFINITY;
+          for (int p = 0; p < P; ++p) {
+            const float o1 = sm.part1[l * P + p], o2 = sm.part2[l * P + p];
+            m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+            m1 = fmaxf(m1, o1);
+          }
+          gs[h] = (g >= 2) ? __fadd_rn(m1, m2) : m1;
         }
-        gs[h] = (g >= 2) ? __fadd_rn(m1, m2) : m1;
       }
+      int rk0 = 0, rk1 = 0;
+      for (int m = 0; m < G; ++m) {
+        const float o = __shfl_sync(kFull, (m < 32) ? gs[0] : gs[1], m & 31);
+        rk0 += (o > gs[0] || (o == gs[0] && m < lane)) ? 1 : 0;
+        rk1 += (o > gs[1] || (o == gs[1] && m < lane + 32)) ? 1 : 0;
+      }
+      km0 = __ballot_sync(kFull, lane < G && rk0 < Kg);
+      km1 = __ballot_sync(kFull, lane + 32 < G && rk1 < Kg);
     }
-    int rk0 = 0, rk1 = 0;
-    for (int m = 0; m < G; ++m) {
-      const float o = __shfl_sync(kFull, (m < 32) ? gs[0] : gs[1], m & 31);
-      rk0 += (o > gs[0] || (o == gs[0] && m < lane)) ? 1 : 0;
-      rk1 += (o > gs[1] || (o == gs[1] && m < lane + 32)) ? 1 : 0;
-    }
-    km0 = __ballot_sync(kFull, lane < G && rk0 < Kg);
-    km1 = __ballot_sync(kFull, lane + 32 < G && rk1 < Kg);
-  }
-  auto kept_group = [&](int grp) {
-    return ((grp < 32 ? (km0 >> grp) : (km1 >> (grp - 32))) & 1u) != 0u;
-  };
-
-  // ---- threshold from the kept segments' samples (segment q covers threads 8q .. 8q+7)
-  float tau;
-  {
+    // ---- threshold from the kept segments' samples (segment q covers threads 8q .. 8q+7)
     const int q0 = lane, q1 = lane + 32;
     const int g0 = (8 * q0) / TPG, g1 = (8 * q1) / TPG;
-    const bool k0 = g0 < G && kept_group(g0), k1 = g1 < G && kept_group(g1);
+    const bool k0 = g0 < G && (((g0 < 32 ? (km0 >> g0) : (km1 >> (g0 - 32))) & 1u) != 0u);
+    const bool k1 = g1 < G && (((g1 < 32 ? (km0 >> g1) : (km1 >> (g1 - 32))) & 1u) != 0u);
     const float ninf = -INFINITY;
-    tau = seg_kth_desc2<32>(k0 ? sm.samp2[q0] : ninf, k1 ? sm.samp2[q1] : ninf, lane,
-                            (K - 1) >> 1);
+    float tau = seg_kth_desc2<32>(k0 ? sm.samp2[q0] : ninf, k1 ? sm.samp2[q1] : ninf, lane,
+                                  (K - 1) >> 1);
     if (__any_sync(kFull, tau == -INFINITY))
       tau = fmaxf(tau, seg_kth_desc2<32>(k0 ? sm.samp1[q0] : ninf, k1 ? sm.samp1[q1] : ninf,
                                          lane, K - 1));
+    if (lane == 0) {
+      sm.tau = tau;
+      sm.kept[0] = km0;
+      sm.kept[1] = km1;
+    }
   }
+  __syncthreads();
+  const float tau = sm.tau;
+  const unsigned km0 = sm.kept[0], km1 = sm.kept[1];
+  auto kept_group = [&](int grp) {
+    return ((grp < 32 ? (km0 >> grp) : (km1 >> (grp - 32))) & 1u) != 0u;
+  };
 
   // ---- survivors: kept keys >= tau, compacted (warp-aggregated slots)
   const bool mine_kept = in_group && kept_group(j);
@@ -197,19 +220,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   const int total = sm.count;
 
   if (total <= kDecodeCap) {
-    if (warp != 0) return;
-    // ---- warp 0: rank by counting (composites are distinct)
-    for (int c0 = lane; c0 < total; c0 += 32) {
-      const unsigned long long me = sm.cand[c0];
-      int rk = 0;
-#pragma unroll 8
-      for (int p = 0; p < total; ++p) rk += (sm.cand[p] > me) ? 1 : 0;
-      if (rk < K) {
-        sm.sel_id[rk] = composite_expert(me);
-        sm.sel_s[rk] = sm.cand_s[c0];
-      }
+    // ---- rank by counting (composites are distinct): four threads per survivor, each
+    // counting the better composites in a quarter of the list
+    static_assert(4 * kDecodeCap <= kDecodeThreads, "four threads per survivor");
+    const int c = tid >> 2, q = tid & 3;
+    int rk = 0;
+    unsigned long long me = 0ull;
+    if (c < total) {
+      me = sm.cand[c];
+      for (int p = q; p < total; p += 4) rk += (sm.cand[p] > me) ? 1 : 0;
     }
-    __syncwarp();
+    rk += __shfl_xor_sync(kFull, rk, 1);
+    rk += __shfl_xor_sync(kFull, rk, 2);
+    if (c < total && q == 0 && rk < K) {
+      sm.sel_id[rk] = composite_expert(me);
+      sm.sel_s[rk] = sm.cand_s[c];
+    }
+    __syncthreads();
+    if (warp != 0) return;
   } else {
     // very many survivors (wide exact ties): K rounds of a block-wide maximum
     unsigned long long prev = ~0ull;

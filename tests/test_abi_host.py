@@ -165,7 +165,7 @@ def test_from_host_checks_everything_before_the_copy(lib):
 def test_noalloc_checks_shapes_first(lib):
     # a shape the library rejects gets its own status, before the scratch size check and the
     # device address lookup (which would give -12 here, with no GPU)
-    args = [BASE, BASE + 0x100000, 300000, 4096, 16, 4, 8, 1.0, 128, BASE + 0x200000,
+    args = [BASE, BASE + 0x100000, 600000, 4096, 16, 4, 8, 1.0, 128, BASE + 0x200000,
             BASE + 0x300000, BASE + 0x400000, BASE + 0x500000, BASE + 0x600000,
             BASE + 0x700000, None]
     for i, v, code in [(8, 3, -5), (3, 0, -2), (3, 4097, -2), (4, 7, -3), (6, 0, -4),
@@ -174,6 +174,13 @@ def test_noalloc_checks_shapes_first(lib):
         bad[i] = v
         assert lib.moe_route_sort_noalloc(*bad) == code, (i, v, code)
     assert lib.moe_route_sort_noalloc(*args) == -13  # valid shape, too large for the scratch
+
+
+def test_filter_selftest_validates(lib):
+    assert lib.moe_route_sort_filter_selftest(BASE, BASE + 0x100, -1, BASE + 0x200, None) == -6
+    assert lib.moe_route_sort_filter_selftest(None, BASE + 0x100, 3, BASE + 0x200, None) == -1
+    assert lib.moe_route_sort_filter_selftest(BASE, BASE + 0x100, 3, None, None) == -1
+    assert lib.moe_route_sort_filter_selftest(BASE, BASE + 0x100, 3, BASE + 0x202, None) == -8
 
 
 def test_state_accessors_validate(lib):

@@ -83,7 +83,7 @@ def test_no_alloc_rejects_shapes_beyond_its_scratch():
     # the size check runs before anything touches the (fake) pointers
     lib = mrs.load()
     base = 0x7F0000000000
-    T, E, K, B = 300000, 4096, 8, 128
+    T, E, K, B = 600000, 4096, 8, 128
     assert mrs.moe_route_sort_workspace_bytes(T, E, K, B) > 32 * 1024 * 1024
     rc = lib.moe_route_sort_noalloc(base, base + 0x100000, T, E, 16, 4, K, 1.0, B,
                                     base + 0x200000, base + 0x300000, base + 0x400000,
