@@ -288,17 +288,6 @@ int moe_route_sort_noalloc_status(int32_t* dst, cudaStream_t stream);
  * runs the same check itself (see "Exactness of the pruned selection" above). */
 int moe_route_sort_proxy_selftest(float* out2, cudaStream_t stream);
 
-/* Exhaustive check of the bound behind the threshold table of the large-T route kernel (not
- * an operation of the path; no counterpart in the source pages).  That kernel compares each
- * logit with a per-expert bf16 threshold X(theta, b) and proves its selection on the experts at
- * or above it, which is exact only if every bf16 x < X(theta, b) has key
- * 1 / (1 + expf(-x)) + b < theta (as the path computes keys).  For each of the n pairs
- * (thetas[i], biases[i]) (device memory, fp32, |bias| <= 1 and |theta| <= 2 being the range the
- * kernel uses), checks all finite bf16 x and writes the number of violations to *bad (device
- * memory, one int32; 0 means the bound held everywhere), enqueued on `stream`. */
-int moe_route_sort_filter_selftest(const float* thetas, const float* biases, int n,
-                                   int32_t* bad, cudaStream_t stream);
-
 /* The library's own record of that check on the current device: copies into dst[0] (device
  * memory or mapped pinned host memory, one int32) 0 if no check has run in this context yet,
  * 1 if the bound held (the route kernels prune), 2 if it failed (they evaluate every expert

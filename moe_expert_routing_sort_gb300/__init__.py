@@ -19,7 +19,6 @@ from .binding import (  # noqa: F401
     moe_gate_route_sort,
     moe_route_sort,
     moe_route_sort_debug_set,
-    moe_route_sort_filter_selftest,
     moe_route_sort_noalloc,
     moe_route_sort_noalloc_status,
     moe_route_sort_proxy_selftest,

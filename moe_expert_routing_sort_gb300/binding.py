@@ -78,8 +78,6 @@ def load() -> ctypes.CDLL:
         lib.moe_route_sort_from_host.restype = I
         lib.moe_route_sort_proxy_selftest.argtypes = [P, P]
         lib.moe_route_sort_proxy_selftest.restype = I
-        lib.moe_route_sort_filter_selftest.argtypes = [P, P, I, P, P]
-        lib.moe_route_sort_filter_selftest.restype = I
         lib.moe_route_sort_proxy_state.argtypes = [P, P]
         lib.moe_route_sort_proxy_state.restype = I
         lib.moe_route_sort_noalloc_status.argtypes = [P, P]
@@ -379,20 +377,6 @@ def moe_route_sort_proxy_selftest(out2, stream=None) -> None:
     with torch.cuda.device(_one_device(out2)):
         rc = load().moe_route_sort_proxy_selftest(_ptr(out2), _stream_handle(stream))
     _check(rc, "moe_route_sort_proxy_selftest")
-
-
-def moe_route_sort_filter_selftest(thetas, biases, bad, stream=None) -> None:
-    """Violations of the threshold table's bound over all bf16 logits, for each (theta, bias)
-    pair (float32 CUDA tensors of one length), into bad[0] (int32 CUDA tensor)."""
-    _need(thetas, torch.float32, "thetas")
-    _need(biases, torch.float32, "biases")
-    _need(bad, torch.int32, "bad")
-    if thetas.numel() != biases.numel():
-        raise ValueError("thetas and biases differ in length")
-    with torch.cuda.device(_one_device(thetas, biases, bad)):
-        rc = load().moe_route_sort_filter_selftest(_ptr(thetas), _ptr(biases), thetas.numel(),
-                                                   _ptr(bad), _stream_handle(stream))
-    _check(rc, "moe_route_sort_filter_selftest")
 
 
 def moe_route_sort_proxy_state(dst, stream=None) -> None:

@@ -200,39 +200,6 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   // Two tokens per warp (16 lanes each) share the per-token shuffle and scan work of the
   // route step: taken when K <= 16, the unit has tokens for every warp and all warps fit
   // with two row buffers each.  Otherwise one token per warp.
-  // The threshold-table kernel for sigmoid scoring whenever the 32-lane segment layout (its
-  // fallback route) applies and all 16 warps fit.
-  if (!sh.softmax && a.vec16) {
-    SegShape fsh{};
-    if (make_seg_shape(sh.E, sh.G, sh.Kg, sh.K, sh.R, 32, fsh)) {
-      const int nw = kSegThreads / 32;
-      const size_t fsm = filter_smem_bytes(sh.E, fsh.nu, nw, a.max_routes, sort);
-      if (fsm <= static_cast<size_t>(d.smem_optin)) {
-        a.use_filter = true;
-        a.use_seg = false;
-        a.seg = fsh;
-        a.seg.softmax = 0;
-        a.lanes = 32;
-        a.nbuf = 0;
-        a.nwarps = nw;
-        a.sh = sh;
-        a.wait_limit_ns = debug_wait_limit_ns();
-        a.proxy_state = proxy_state_for_launch(st);
-        a.topk_ids = topk_ids;
-        a.topk_w = topk_w;
-        if (sort) {
-          a.uo.loc_off = reinterpret_cast<int32_t*>(ws + l.loc_off);
-          a.uo.unit_buf = reinterpret_cast<int2*>(ws + l.unit_buf);
-          a.uo.unit_e = reinterpret_cast<uint16_t*>(ws + l.unit_e);
-          a.uo.slice_flags = reinterpret_cast<unsigned long long*>(ws + l.slice_flags);
-          a.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
-          a.uo.status = reinterpret_cast<int32_t*>(ws + l.status);
-          a.uo.nslices = nslices;
-        }
-        return launch_status(launch_route(a, fsm, st));
-      }
-    }
-  }
   Plan p{};
   if (sh.K <= 16 && tpu >= 2 * (kSegThreads / 32)) p = plan_for(16);
   if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32);
@@ -470,22 +437,10 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
   if (T == 0) return launch_status(launch_empty(num_tokens_post_pad, status, stream));
-  const int32_t* pre_flags = nullptr;  // status bits the gate projection leaves per CTA
-  int n_pre_flags = 0;
   if (gate) {
     DeviceInfo gd;
     if (!device_info(gd)) return MOE_RS_ERR_LAUNCH;
-    const GatePlan gp =
-        gate_plan(T, E, gate->H, gd.sms < kMaxUnitSms ? gd.sms : kMaxUnitSms, gd.smem_optin);
-    if (gp.smem > static_cast<size_t>(gd.smem_optin)) return MOE_RS_ERR_LAUNCH;
-    if (T > 1) {  // the route step that follows must be the single-CTA kernel (checked first)
-      SmallLayout lay0;
-      int wave0 = 0, nb0 = 0;
-      SegShape seg0{};
-      const bool s0 = make_seg_shape(E, n_group, topk_group, topk, routed_scale, 32, seg0);
-      if (!small_plan(T, E, topk, block_m, false, s0 ? seg0.nu : 0, gd, lay0, wave0, nb0))
-        return MOE_RS_ERR_LAUNCH;
-    }
+    const GatePlan gp = gate_plan(E, gd.sms);
     GateArgs ga{};
     ga.hidden = static_cast<const uint16_t*>(gate->hidden);
     ga.w = static_cast<const uint16_t*>(gate->w_gate);
@@ -494,13 +449,8 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     ga.E = E;
     ga.H = gate->H;
     ga.rpc = gp.rpc;
-    ga.stages = gp.stages;
-    ga.wait_limit_ns = debug_wait_limit_ns();
-    ga.flags = reinterpret_cast<int32_t*>(ws + l.gate_flags);
     rc = launch_status(launch_gate(ga, gp, stream));
     if (rc) return rc;
-    pre_flags = ga.flags;
-    n_pre_flags = gp.grid;
   }
 
   if (T == 1) {
@@ -522,8 +472,6 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     a.expert_ids = expert_ids;
     a.npp = num_tokens_post_pad;
     a.status = status;
-    a.pre_flags = pre_flags;
-    a.n_pre_flags = n_pre_flags;
     return launch_status(launch_decode(a, stream));
   }
   DeviceInfo d;
@@ -557,11 +505,8 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     a.expert_ids = expert_ids;
     a.npp = num_tokens_post_pad;
     a.status = status;
-    a.pre_flags = pre_flags;
-    a.n_pre_flags = n_pre_flags;
     return launch_status(launch_small(a, false, stream));
   }
-  if (gate) return MOE_RS_ERR_LAUNCH;  // not reached: the plan was checked before the gate
 
   const int U = units_for_shape(T, topk, d.sms);
   const int nslices = slices_for(U, E);

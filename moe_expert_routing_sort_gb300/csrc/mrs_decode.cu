@@ -106,14 +106,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
     }
     if (tid == 0) {
       *a.npp = K * B;
+      *a.status = 0;
       sm.count = 0;
-    }
-    if (warp == kDecodeWarps - 1) {
-      // the call's status: what the work ahead of this kernel (the gate projection) reported
-      int f = 0;
-      for (int v = lane; v < a.n_pre_flags; v += 32) f |= a.pre_flags[v];
-      f = __reduce_or_sync(kFull, f);
-      if (lane == 0) *a.status = f;
     }
     float t1 = -INFINITY, t2 = -INFINITY;
 #pragma unroll

@@ -53,7 +53,6 @@ struct WsLayout {
   size_t status;       // int32
   size_t unit_flags;   // int32[U]
   size_t slice_flags;  // uint64[slices]  look-back words of the slice kernel
-  size_t gate_flags;   // int32[kMaxUnitSms] per-CTA status bits of the gate projection
   size_t loc_off;      // int32[U][E + 1] per-unit exclusive offsets of each expert
   size_t unit_buf;     // int2[T * K]     per-unit routes sorted by expert: (flat index, weight)
   size_t unit_e;       // uint16[T * K]   the expert of each unit_buf entry
@@ -74,8 +73,6 @@ inline WsLayout ws_layout(int T, int E, int K) {
   o = align16(o + sizeof(int32_t) * U);
   l.slice_flags = o;
   o = align16(o + sizeof(unsigned long long) * slices_for(U, E));
-  l.gate_flags = o;
-  o = align16(o + sizeof(int32_t) * kMaxUnitSms);
   l.loc_off = o;
   o = align16(o + sizeof(int32_t) * static_cast<size_t>(U) * (E + 1));
   l.unit_buf = o;
@@ -113,8 +110,6 @@ struct SmallArgs {
   int32_t* expert_ids;
   int32_t* npp;
   int32_t* status;
-  const int32_t* pre_flags;  // [n_pre_flags] status bits of the gate projection, or none
-  int n_pre_flags;
 };
 
 // ------------------------------------------------------------- one token (decode)
@@ -131,8 +126,6 @@ struct DecodeArgs {
   int32_t* expert_ids;
   int32_t* npp;
   int32_t* status;
-  const int32_t* pre_flags;  // [n_pre_flags] status bits of the gate projection, or none
-  int n_pre_flags;
 };
 
 // ------------------------------------------------------------- multi-CTA path
@@ -153,7 +146,6 @@ struct RouteArgs {
   int T, U, nwarps, max_routes;
   bool vec16;    // rows are 16-byte aligned (E % 8 == 0)
   bool use_seg;  // segment shape valid and rows 16-byte aligned: TMA-staged segment kernel
-  bool use_filter;  // logit threshold table kernel (sigmoid scoring, 32-lane segment shape)
   bool sort;     // run phase 1 of the sort step after routing (else route only)
   int lanes;     // segment kernel: lanes per token (32, or 16 for two tokens per warp)
   int nbuf;      // segment kernel: row buffers per warp (1 or 2)
@@ -233,17 +225,13 @@ struct GateArgs {
   const uint16_t* w;       // [E, H] bf16, one gate row per expert
   uint16_t* logits;        // [T, E] bf16
   int T, E, H;
-  int rpc;                           // gate rows per CTA
-  int stages;                        // chunks of the copy ring
-  unsigned long long wait_limit_ns;  // bound of the copy waits (0: give up at once)
-  int32_t* flags;                    // [grid] per-CTA status bits (MOE_RS_DEVICE_*)
+  int rpc;  // gate rows per CTA (<= 16)
 };
-// Launch plan for `sms` SMs: gate rows per CTA, the grid and its dynamic shared memory.
+// Launch plan for `sms` SMs: gate rows per CTA and the grid.
 struct GatePlan {
-  int rpc, grid, stages;
-  size_t smem;
+  int rpc, grid;
 };
-GatePlan gate_plan(int T, int E, int H, int sms, int smem_optin);
+GatePlan gate_plan(int E, int sms);
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
 
 // ------------------------------------------------------------ per-context host state
@@ -269,7 +257,6 @@ cudaError_t launch_empty(int32_t* npp, int32_t* status, cudaStream_t st);
 // Shared memory of the multi-CTA route kernels for a given warp count.
 size_t route_smem_bytes(int E, int nwarps, int max_routes, bool sort);
 size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw, int nbuf);
-size_t filter_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort);
 SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only);
 
 // Shared memory used by phase 1 of the sort step (mrs_unit.cuh) besides the routes.

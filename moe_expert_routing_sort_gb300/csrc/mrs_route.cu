@@ -15,7 +15,6 @@
 //
 // Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary
 // (FP32 logit conversion + correction bias, grouped top-k, both sort phases in one kernel).
-#include "mrs_filter.cuh"
 #include "mrs_internal.h"
 #include "mrs_seg.cuh"
 #include "mrs_unit.cuh"
@@ -246,15 +245,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
     }
     for (int b = o / B; b < (o + p) / B; ++b) a.expert_ids[b] = e;
   }
-  if (warp == 0) {
-    // the call's status: this kernel's flags and what the gate projection ahead reported
-    int f = 0;
-    for (int v = lane; v < a.n_pre_flags; v += 32) f |= a.pre_flags[v];
-    f = __reduce_or_sync(kFull, f);
-    if (lane == 0) {
-      *a.npp = total;
-      *a.status = misc[0] | f;
-    }
+  if (tid == 0) {
+    *a.npp = total;
+    *a.status = misc[0];
   }
 }
 
@@ -599,166 +592,6 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   }
 }
 
-// ------------------------------------------- multi-CTA route, logit threshold table
-// Shared memory: bias[E], counts[E], the unit's routes (ids, weights), then a region holding
-// the threshold table (bf16 [E]) and, per warp, the unit bounds and segment scratch of the
-// fallback route and the filter scratch; after routing, the region is reused by phase 1 of the
-// sort step.
-struct FilterCtaLayout {
-  size_t bias, counts, rid, rw, region, table, warps, per_warp, umax, seg, fsc, total;
-};
-
-__host__ __device__ inline FilterCtaLayout filter_cta_layout(int E, int nu, int nwarps,
-                                                             int max_routes, bool sort) {
-  FilterCtaLayout l{};
-  size_t o = 0;
-  l.bias = o;
-  o = align16(o + sizeof(float) * E);
-  l.counts = o;
-  o = align16(o + sizeof(int32_t) * E);
-  l.rid = o;
-  o = align16(o + (sort ? sizeof(int32_t) * max_routes : 0));
-  l.rw = o;
-  o = align16(o + (sort ? sizeof(float) * max_routes : 0));
-  l.region = o;
-  size_t r = 0;
-  l.table = r;
-  r = align16(r + sizeof(uint16_t) * E);
-  l.warps = r;
-  size_t w = 0;
-  l.umax = w;
-  w = align16(w + ub_bytes(nu));
-  l.seg = w;
-  w = align16(w + sizeof(SegScratch));
-  l.fsc = w;
-  w = align16(w + sizeof(FilterScratch));
-  l.per_warp = w;
-  r += w * nwarps;
-  if (sort && r < unit_scratch_bytes(E)) r = unit_scratch_bytes(E);
-  l.total = o + r;
-  return l;
-}
-
-size_t filter_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort) {
-  return filter_cta_layout(E, nu, nwarps, max_routes, sort).total;
-}
-
-// theta is lowered by this much below the calibration estimate: a little more room for the
-// tokens that were not sampled (fewer fallbacks) at the price of a few more candidates.
-constexpr float kFilterMargin = 0.003f;
-
-// Warp w of unit u routes tokens t0 + w, t0 + w + nwarps, ... one at a time, reading each row
-// straight from global memory (brought into L2 one step ahead by a bulk prefetch).  First every
-// warp estimates a bound from its first token's pass-1 summary; the CTA takes the smallest
-// estimate (minus kFilterMargin) as theta and builds the threshold table.  A token whose
-// selection filter_route() cannot prove takes the segment route (pass 1 + selection over the
-// row in global memory).  With |bias| above kFilterBiasLimit every token takes that route.
-template <bool kSort>
-__global__ void __launch_bounds__(kSegThreads, 1) mrs_route_filter_kernel(const RouteArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const SegShape sh = a.seg;
-  const int E = sh.E, K = sh.K;
-  const FilterCtaLayout lay = filter_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort);
-  float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
-  int32_t* counts = reinterpret_cast<int32_t*>(smem + lay.counts);
-  int32_t* rid = reinterpret_cast<int32_t*>(smem + lay.rid);
-  float* rw = reinterpret_cast<float*>(smem + lay.rw);
-  unsigned char* region = smem + lay.region;
-  uint16_t* table = reinterpret_cast<uint16_t*>(region + lay.table);
-  unsigned char* mine = region + lay.warps + lay.per_warp * warp;
-  unsigned short* umax = reinterpret_cast<unsigned short*>(mine + lay.umax);
-  SegScratch& scr = *reinterpret_cast<SegScratch*>(mine + lay.seg);
-  FilterScratch& fs = *reinterpret_cast<FilterScratch*>(mine + lay.fsc);
-  __shared__ unsigned int cta_bmax_bits;
-  __shared__ unsigned int cta_theta_bits;  // ordered bits of the smallest estimate
-
-  const int u = blockIdx.x;
-  const int t0 = static_cast<int>(static_cast<long long>(u) * a.T / a.U);
-  const int t1 = static_cast<int>(static_cast<long long>(u + 1) * a.T / a.U);
-  const uint32_t row_bytes = static_cast<uint32_t>(E) * 2u;
-  auto row_of = [&](int t) { return a.logits + static_cast<size_t>(t) * E; };
-
-  pdl_trigger();
-  pdl_wait();
-  if (lane == 0) {  // this warp's first two rows
-    if (t0 + warp < t1) prefetch_l2(row_of(t0 + warp), row_bytes);
-    if (t0 + warp + a.nwarps < t1) prefetch_l2(row_of(t0 + warp + a.nwarps), row_bytes);
-  }
-  if (tid == 0) {
-    cta_bmax_bits = 0u;
-    cta_theta_bits = 0xffffffffu;
-  }
-  ub_init_pads(umax, lane, sh.nu);
-  if (kSort)
-    for (int i = tid; i < (t1 - t0) * K; i += blockDim.x) rid[i] = -1;
-  __syncthreads();
-  float bmax = 0.0f;
-  for (int e = tid; e < E; e += blockDim.x) {
-    const float b = a.bias[e];
-    bias_s[e] = b;
-    const float ab = fabsf(b);
-    bmax = (ab > bmax || ab != ab) ? ab : bmax;
-    counts[e] = 0;
-  }
-  for (int d = 16; d > 0; d >>= 1) {
-    const float o = __shfl_xor_sync(kFull, bmax, d);
-    bmax = (o > bmax || o != o) ? o : bmax;
-  }
-  if (lane == 0) atomicMax(&cta_bmax_bits, (bmax != bmax) ? 0x7fffffffu : __float_as_uint(bmax));
-  __syncthreads();
-  const float bm = __uint_as_float(cta_bmax_bits);
-  const bool proxy_ok = a.proxy_state != nullptr && *a.proxy_state == 1;
-  const float delta = (bm <= kProxyBiasLimit && proxy_ok) ? proxy_delta(bm) : INFINITY;
-
-  // ---- theta: the smallest estimate over the warps' first tokens, then the table
-  bool use_filter = bm <= kFilterBiasLimit;
-  if (use_filter && t0 + warp < t1) {
-    const ProxyRow row{row_of(t0 + warp), bias_s};
-    const LaneTop top = seg_pass1<32, 1>(row, sh, umax, lane, true);
-    const float c = filter_calibrate(sh, top, lane);
-    if (lane == 0 && c == c) atomicMin(&cta_theta_bits, ordered_bits(c));
-  }
-  __syncthreads();
-  float theta = -INFINITY;
-  if (use_filter && cta_theta_bits != 0xffffffffu) {
-    const uint32_t ob = cta_theta_bits;
-    theta = __uint_as_float((ob & 0x80000000u) ? (ob & 0x7fffffffu) : ~ob) - kFilterMargin;
-  }
-  use_filter = use_filter && fabsf(theta) <= 2.0f;  // the table's bound needs |theta| <= 2
-  if (use_filter)
-    for (int e = tid; e < E; e += blockDim.x) table[e] = filter_threshold(theta, bias_s[e]);
-  __syncthreads();
-
-  // ---- route every token of the unit
-  for (int t = t0 + warp; t < t1; t += a.nwarps) {
-    if (lane == 0 && t + 2 * a.nwarps < t1) prefetch_l2(row_of(t + 2 * a.nwarps), row_bytes);
-    const uint16_t* row_g = row_of(t);
-    int id = -1;
-    float w = 0.0f;
-    const bool done = use_filter && filter_route(row_g, table, bias_s, theta, sh, fs, lane, id, w);
-    if (!done) {
-      const ProxyRow row{row_g, bias_s};
-      const LaneTop top = seg_pass1<32, 1>(row, sh, umax, lane, true);
-      seg_select<32, 1>(row, sh, scr, umax, lane, delta, true, top, [] {}, id, w);
-    }
-    if (lane < K) {
-      a.topk_ids[static_cast<size_t>(t) * K + lane] = id;
-      a.topk_w[static_cast<size_t>(t) * K + lane] = w;
-      if (kSort) {
-        rid[(t - t0) * K + lane] = id;
-        rw[(t - t0) * K + lane] = w;
-        if (id >= 0 && id < E) atomicAdd(&counts[id], 1);
-      }
-    }
-  }
-  if (kSort) {
-    __syncthreads();
-    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, region, a.uo, a.U);
-    if (tid == 0) a.uo.unit_flags[u] = 0;
-  }
-}
-
 template <bool kSort, int LT, bool kSoftmax>
 static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st) {
   auto* kern = mrs_route_seg_kernel<kSort, LT, kSoftmax>;
@@ -775,13 +608,6 @@ static cudaError_t launch_seg(const RouteArgs& a, size_t smem, cudaStream_t st) 
 }
 
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  if (a.use_filter) {
-    auto* kern = a.sort ? mrs_route_filter_kernel<true> : mrs_route_filter_kernel<false>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(a.U), dim3(a.nwarps * 32), smem, st, a);
-  }
   if (a.use_seg) {
     // softmax scoring only comes with the sort step (moe_route_sort_softmax)
     if (a.seg.softmax) return a.sort ? launch_seg<true, true>(a, smem, st) : cudaErrorInvalidValue;

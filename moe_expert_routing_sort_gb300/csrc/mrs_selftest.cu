@@ -12,7 +12,6 @@
 #include <atomic>
 #include <mutex>
 
-#include "mrs_filter.cuh"
 #include "mrs_internal.h"
 #include "moe_route_sort.h"
 
@@ -56,28 +55,6 @@ __global__ void __launch_bounds__(kCheckThreads) mrs_proxy_check_kernel(float bo
     for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
     if (tid == 0) g_proxy_state = (m <= bound) ? 1 : 2;
   }
-}
-
-// Exhaustive check of the threshold table's bound (mrs_filter.cuh): for pair i, every finite
-// bf16 x below filter_threshold(theta_i, b_i) must have exact_key(x, b_i) < theta_i.  Block
-// (i, part) checks 4096 patterns of pair i; violations are counted in *bad.
-__global__ void __launch_bounds__(256) mrs_filter_selftest_kernel(const float* thetas,
-                                                                   const float* biases, int n,
-                                                                   unsigned int* bad) {
-  const int i = blockIdx.x;
-  if (i >= n) return;
-  const float theta = thetas[i], b = biases[i];
-  const uint16_t xe = filter_threshold(theta, b);
-  const float X = bf16_bits_to_float(xe);
-  unsigned int local = 0;
-  for (uint32_t h = blockIdx.y * 4096u + threadIdx.x; h < (blockIdx.y + 1) * 4096u; h += 256u) {
-    const float x = bf16_bits_to_float(h);
-    if (!isfinite(x) || !(x < X)) continue;
-    float sc;
-    if (exact_key(x, b, sc) >= theta) ++local;
-  }
-  for (int d = 16; d > 0; d >>= 1) local += __shfl_xor_sync(kFull, local, d);
-  if ((threadIdx.x & 31) == 0 && local) atomicAdd(bad, local);
 }
 
 // ------------------------------------------------------------------- host state
@@ -222,19 +199,4 @@ extern "C" int moe_route_sort_debug_set(int knob, long long value) {
     default:
       return MOE_RS_ERR_BAD_DEBUG_KNOB;
   }
-}
-
-extern "C" int moe_route_sort_filter_selftest(const float* thetas, const float* biases, int n,
-                                              int32_t* bad, cudaStream_t stream) {
-  if (n < 0) return MOE_RS_ERR_BAD_TOKENS;
-  if (!bad || (n > 0 && (!thetas || !biases))) return MOE_RS_ERR_NULL_POINTER;
-  if (reinterpret_cast<uintptr_t>(bad) % 4 || reinterpret_cast<uintptr_t>(thetas) % 4 ||
-      reinterpret_cast<uintptr_t>(biases) % 4)
-    return MOE_RS_ERR_MISALIGNED;
-  if (cudaMemsetAsync(bad, 0, sizeof(int32_t), stream) != cudaSuccess) return MOE_RS_ERR_LAUNCH;
-  if (n == 0) return MOE_RS_OK;
-  mrs::mrs_filter_selftest_kernel<<<dim3(n, 16), 256, 0, stream>>>(
-      thetas, biases, n, reinterpret_cast<unsigned int*>(bad));
-  if (cudaGetLastError() != cudaSuccess) return MOE_RS_ERR_LAUNCH;
-  return MOE_RS_OK;
 }

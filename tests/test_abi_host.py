@@ -176,13 +176,6 @@ def test_noalloc_checks_shapes_first(lib):
     assert lib.moe_route_sort_noalloc(*args) == -13  # valid shape, too large for the scratch
 
 
-def test_filter_selftest_validates(lib):
-    assert lib.moe_route_sort_filter_selftest(BASE, BASE + 0x100, -1, BASE + 0x200, None) == -6
-    assert lib.moe_route_sort_filter_selftest(None, BASE + 0x100, 3, BASE + 0x200, None) == -1
-    assert lib.moe_route_sort_filter_selftest(BASE, BASE + 0x100, 3, None, None) == -1
-    assert lib.moe_route_sort_filter_selftest(BASE, BASE + 0x100, 3, BASE + 0x202, None) == -8
-
-
 def test_state_accessors_validate(lib):
     assert lib.moe_route_sort_noalloc_status(None, None) == -1
     assert lib.moe_route_sort_noalloc_status(BASE + 2, None) == -8

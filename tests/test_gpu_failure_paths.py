@@ -137,33 +137,6 @@ def test_wait_timeout_in_the_sort_step_alone():
     _assert_intact(bufs, "timed-out moe_sort")
 
 
-def test_wait_timeout_in_the_gate_projection():
-    # the gate kernel's copy waits give up at once; every CTA records it and the route step's
-    # status word carries it
-    T, E, H = 3, 896, 2048
-    g = datagen.make_gate_inputs(T, E, H, seed=5)
-    hid = torch.from_numpy(g.hidden_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
-    wg = torch.from_numpy(g.w_gate_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
-    gb = torch.from_numpy(g.bias).to(DEV)
-    lg = Guarded(T * E, torch.bfloat16)
-    bufs = _guarded_outputs(T, E, 16, 32)
-    v = {k: b.t for k, b in bufs.items()}
-    mrs.moe_route_sort_debug_set(mrs.DEBUG_WAIT_LIMIT_NS, 0)
-    try:
-        mrs.moe_gate_route_sort(hid, wg, gb, 8, 4, 16, 2.5, 32, lg.t.view(T, E), **v)
-        torch.cuda.synchronize()
-    finally:
-        mrs.moe_route_sort_debug_set(mrs.DEBUG_WAIT_LIMIT_NS, -1)
-    assert _status(v["workspace"]) & 0x2
-    assert lg.intact()
-    _assert_intact(bufs, "timed-out gate call")
-    mrs.moe_gate_route_sort(hid, wg, gb, 8, 4, 16, 2.5, 32, lg.t.view(T, E), **v)
-    torch.cuda.synchronize()
-    assert _status(v["workspace"]) == 0
-    ref = oracle.gate_logits(g.hidden_bf16, g.w_gate_bf16)
-    assert np.array_equal(lg.t.view(torch.int16).cpu().numpy().view(np.uint16).reshape(T, E), ref)
-
-
 # ------------------------------------------------------------------ guard regions
 @pytest.mark.parametrize("name,T", [(n, None) for n in datagen.WORKLOADS] +
                          [("prefill_T512_E896", 1), ("prefill_T512_E896", 65),
