@@ -7,6 +7,7 @@ and the seeded input generator used by the tests and the benchmark.
 from . import datagen  # noqa: F401
 from ._build import build  # noqa: F401
 from .binding import (  # noqa: F401
+    DEBUG_CLUSTER_TOKENS,
     DEBUG_FORCE_PROXY_FAIL,
     DEBUG_WAIT_LIMIT_NS,
     DEVICE_BAD_EXPERT_ID,

@@ -20,6 +20,7 @@ constexpr int kMaxBlockM = 1024;
 struct DeviceInfo {
   int sms = 0;
   int smem_optin = 0;
+  int clusters = 0;  // kClusterCtas-CTA clusters of the segment kernel the device can hold
 };
 
 // Device attributes, cached per device on first use (host-only queries, no sync).
@@ -37,6 +38,11 @@ bool device_info(DeviceInfo& out) {
   if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
       cudaSuccess)
     return false;
+  // the limit covers static and dynamic shared memory together: keep room for the kernels'
+  // own static variables, so that a planned dynamic size can always be granted
+  d.smem_optin -= 1024;
+  // at the largest shared-memory size: a launch that needs less fits wherever this one does
+  d.clusters = seg_cluster_capacity(static_cast<size_t>(d.smem_optin));
   if (dev < 64) cache[dev] = d;
   out = d;
   return true;
@@ -153,10 +159,14 @@ int launch_status(cudaError_t e) {
 
 // Multi-CTA route step.  Units are contiguous token ranges, one CTA each; with `sort`,
 // each CTA also runs phase 1 of the sort step into the workspace.
+// With `co`, the grid is one cluster of U CTAs that also runs both sort phases into co
+// (the segment kernel only; the caller checks that the shape has a segment layout).
 int run_route(const void* logits, const float* bias, int T, const RouteShape& sh, bool sort,
               int32_t* topk_ids, float* topk_w, unsigned char* ws, const WsLayout& l, int U,
-              int nslices, const DeviceInfo& d, cudaStream_t st) {
+              int nslices, const DeviceInfo& d, cudaStream_t st,
+              const ClusterOut* co = nullptr) {
   RouteArgs a{};
+  const bool cluster = co != nullptr;
   a.logits = static_cast<const uint16_t*>(logits);
   a.bias = bias;
   a.T = T;
@@ -182,11 +192,13 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
     const int tpw = 32 / lanes;
     const int steps = (tpu + tpw - 1) / tpw;
     const int cap = kSegThreads / 32;
-    p.want = steps < cap ? steps : cap;
+    // (the cluster path keeps every warp for its sort step, whose exchange and scan are
+    // spread over the CTA's threads)
+    p.want = (steps < cap && !cluster) ? steps : cap;
     for (int nbuf = 2; nbuf >= 1; --nbuf) {
       int w = p.want;
       auto bytes = [&](int ww) {
-        return seg_smem_bytes(sh.E, p.shape.nu, ww, a.max_routes, sort, tpw, nbuf);
+        return seg_smem_bytes(sh.E, p.shape.nu, ww, a.max_routes, sort, tpw, nbuf, cluster);
       };
       while (w > 1 && bytes(w) > static_cast<size_t>(d.smem_optin)) --w;
       if (w > p.nwarps) {
@@ -204,6 +216,7 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
   if (sh.K <= 16 && tpu >= 2 * (kSegThreads / 32)) p = plan_for(16);
   if (!(p.seg && p.nwarps == p.want && p.nbuf == 2)) p = plan_for(32);
   a.use_seg = p.seg;
+  if (cluster && !p.seg) return MOE_RS_ERR_LAUNCH;
   size_t smem;
   if (p.seg) {
     a.seg = p.shape;
@@ -235,6 +248,10 @@ int run_route(const void* logits, const float* bias, int T, const RouteShape& sh
     a.uo.unit_flags = reinterpret_cast<int32_t*>(ws + l.unit_flags);
     a.uo.status = reinterpret_cast<int32_t*>(ws + l.status);
     a.uo.nslices = nslices;
+  }
+  if (cluster) {
+    a.cluster = true;
+    a.co = *co;
   }
   return launch_status(launch_route(a, smem, st));
 }
@@ -506,6 +523,23 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     a.npp = num_tokens_post_pad;
     a.status = status;
     return launch_status(launch_small(a, false, stream));
+  }
+
+  // mid-sized calls: one cluster routes and sorts in a single launch
+  if (use_seg && d.clusters > 0 && cluster_reach(T, E) &&
+      static_cast<int64_t>(T) * topk <= static_cast<int64_t>(kClusterCtas) * kUnitRouteCap) {
+    ClusterOut co{};
+    co.sorted_ids = sorted_token_ids;
+    co.sorted_w = sorted_weights;
+    co.expert_ids = expert_ids;
+    co.npp = num_tokens_post_pad;
+    co.status = status;
+    co.B = block_m;
+    co.N = T * topk;
+    rc = run_route(logits_bf16, bias, T, sh, true, topk_ids, topk_weights, ws, l, kClusterCtas,
+                   0, d, stream, &co);
+    // a rejected cluster launch enqueued nothing: the three-kernel path below takes the call
+    if (rc != MOE_RS_ERR_LAUNCH) return rc;
   }
 
   const int U = units_for_shape(T, topk, d.sms);

@@ -82,6 +82,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   // experts per thread: 2 * 256 / G < TPG, so g = E / G <= 4096 / G < 16 * TPG
   const int R = (g + TPG - 1) / TPG;
   pdl_trigger();
+  // the inputs start towards L2 while the kernel ahead in the stream finishes
+  if (tid < 64)
+    prefetch_l2_range(a.logits, 2 * static_cast<size_t>(a.E), tid, 64);
+  else if (!kSoftmax && tid < 192)
+    prefetch_l2_range(a.bias, 4 * static_cast<size_t>(a.E), tid - 64, 128);
   pdl_wait();
 
   // ---- loads (one DRAM round trip); rows that depend on nothing meanwhile

@@ -83,6 +83,22 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Ask L2 for the line that holds byte p of global memory.  A prefetch is only a hint: it
+// changes no value that any load observes (L2 is where the device's writes become
+// coherent), so it may be issued before pdl_wait, while the kernel ahead in the stream is
+// still running, for inputs that kernel does not produce.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Prefetch bytes [0, n) of the buffer at p into L2, one line per thread and step; threads
+// [t0, t0 + nt) of the block take part.
+__device__ __forceinline__ void prefetch_l2_range(const void* p, size_t n, int t, int nt) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t o = static_cast<size_t>(t) * 128u; o < n; o += static_cast<size_t>(nt) * 128u)
+    prefetch_l2(c + o);
+}
+
 // ------------------------------------------------------------------ proxy score
 // Cheap stand-in for the selection key, shifted by the constant -0.5 that every expert
 // shares: p = 0.5 * tanh.approx(0.5 x) + bias.  0.5 + 0.5 tanh(x / 2) is the logistic

@@ -1,8 +1,9 @@
 // mrs_gate.cu -- the router gate projection ahead of the path, for a few tokens (a GEMV).
 //
 // logits[t, e] = bf16(sum over h of hidden[t, h] * w_gate[e, h]) for T <= 8 tokens.  At these
-// sizes the projection is bound by one read of the E x H bf16 gate matrix; the arithmetic goes
-// to the tensor cores so that it never competes with the loads for issue slots:
+// sizes the projection is bound by one read of the E x H bf16 gate matrix.  One token takes
+// mrs_gate1_kernel (below).  For 2..8 tokens the arithmetic goes to the tensor cores so that
+// it never competes with the loads for issue slots:
 //   tile     CTA c owns gate rows [c * rpc, c * rpc + nr), nr <= 16: the M side of an
 //            m16n8k16 bf16 MMA (fp32 accumulate); the tokens are its N = 8 side
 //   k split  the hidden dimension is cut into steps of 32 columns; warp w takes steps
@@ -52,6 +53,10 @@ __global__ void __launch_bounds__(kGateThreads, 2) mrs_gate_kernel(const GateArg
   const int steps = (H + 31) >> 5;
   const int mine = (steps - warp + kGateWarps - 1) / kGateWarps;  // steps w, w + warps, ...
   pdl_trigger();
+  // the CTA's gate rows (contiguous; weights, which the kernel ahead in the stream does not
+  // normally write) start towards L2 while that kernel finishes
+  prefetch_l2_range(a.w + static_cast<size_t>(r0) * H, 2 * static_cast<size_t>(nr) * H, tid,
+                    kGateThreads);
   pdl_wait();
 
   const bool row_lo = g < nr, row_hi = g + 8 < nr, tok = g < T;
@@ -96,6 +101,77 @@ __global__ void __launch_bounds__(kGateThreads, 2) mrs_gate_kernel(const GateArg
   }
 }
 
+// One token (T = 1): the same sum with every load of a row group in flight at once, and the
+// arithmetic on the FMA pipes (an MMA would leave 7 of its 8 token columns empty).  Thread t
+// of the CTA takes the 16-byte column chunks t, t + 256, ... (at most four: H <= 8192) of
+// each gate row and of the hidden row; it accumulates a row's products in fp32 in chunk
+// order, the warp adds its 32 partial sums in a fixed shuffle tree, and the CTA adds the
+// warps' sums in warp order and rounds once to bf16.  The rows of a group of kGate1Rows are
+// requested together (up to 4 x 4 loads of 16 bytes per thread).
+constexpr int kGate1Chunks = 4;  // chunks of a row per thread: 4 * 256 * 8 >= 8192 columns
+constexpr int kGate1Rows = 4;
+
+__global__ void __launch_bounds__(kGateThreads, 2) mrs_gate1_kernel(const GateArgs a) {
+  __shared__ float part[kGateWarps][kGateRows];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = a.H, nch = H >> 3;  // 16-byte chunks of a row
+  const int r0 = blockIdx.x * a.rpc;
+  const int nr = min(a.rpc, a.E - r0);
+  pdl_trigger();
+  // the CTA's gate rows (contiguous; weights, which the kernel ahead in the stream does not
+  // normally write) start towards L2 while that kernel finishes
+  prefetch_l2_range(a.w + static_cast<size_t>(r0) * H, 2 * static_cast<size_t>(nr) * H, tid,
+                    kGateThreads);
+  pdl_wait();
+
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 hv[kGate1Chunks];
+#pragma unroll
+  for (int i = 0; i < kGate1Chunks; ++i) {
+    const int c = tid + kGateThreads * i;
+    hv[i] = (c < nch) ? __ldg(reinterpret_cast<const uint4*>(a.hidden) + c) : zero;
+  }
+  const uint4* wrow = reinterpret_cast<const uint4*>(a.w + static_cast<size_t>(r0) * H);
+  for (int j0 = 0; j0 < nr; j0 += kGate1Rows) {
+    uint4 wv[kGate1Rows][kGate1Chunks];
+#pragma unroll
+    for (int jj = 0; jj < kGate1Rows; ++jj) {
+#pragma unroll
+      for (int i = 0; i < kGate1Chunks; ++i) {
+        const int c = tid + kGateThreads * i;
+        wv[jj][i] = (j0 + jj < nr && c < nch)
+                        ? __ldg(wrow + static_cast<size_t>(j0 + jj) * nch + c)
+                        : zero;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < kGate1Rows; ++jj) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kGate1Chunks; ++i) {
+        const uint32_t wq[4] = {wv[jj][i].x, wv[jj][i].y, wv[jj][i].z, wv[jj][i].w};
+        const uint32_t hq[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc = fmaf(__uint_as_float(wq[q] << 16), __uint_as_float(hq[q] << 16), acc);
+          acc = fmaf(__uint_as_float(wq[q] & 0xffff0000u), __uint_as_float(hq[q] & 0xffff0000u),
+                     acc);
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, d));
+      if (lane == 0 && j0 + jj < nr) part[warp][j0 + jj] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < nr) {
+    float sum = part[0][tid];
+#pragma unroll
+    for (int w = 1; w < kGateWarps; ++w) sum = __fadd_rn(sum, part[w][tid]);
+    a.logits[r0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+  }
+}
+
 GatePlan gate_plan(int E, int sms) {
   GatePlan p{};
   const int slots = 2 * (sms > 0 ? sms : 1);  // two CTAs per SM
@@ -107,6 +183,7 @@ GatePlan gate_plan(int E, int sms) {
 }
 
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st) {
+  if (a.T == 1) return launch_pdl(mrs_gate1_kernel, dim3(p.grid), dim3(kGateThreads), 0, st, a);
   return launch_pdl(mrs_gate_kernel, dim3(p.grid), dim3(kGateThreads), 0, st, a);
 }
 

@@ -140,6 +140,26 @@ struct UnitOut {
   int nslices;
 };
 
+// Outputs of the sort step when the route step runs as one thread-block cluster.
+struct ClusterOut {
+  int32_t* sorted_ids;
+  float* sorted_w;
+  int32_t* expert_ids;
+  int32_t* npp;
+  int32_t* status;
+  int B, N;
+};
+
+// CTAs of the cluster that runs a mid-sized route-sort call (a non-portable cluster size,
+// used only where the device can place such a cluster).
+constexpr int kClusterCtas = 16;
+// Default reach of the cluster path: at most this many tokens and this many bytes of logits.
+// The cluster sits on one GPC, so it reads its inputs through that GPC's share of the memory
+// system and routes on 16 SMs; past these sizes the three-kernel path, spread over the whole
+// GPU, is faster on a GB300.
+constexpr int kClusterMaxTokens = 256;
+constexpr long long kClusterMaxLogitBytes = 512 << 10;
+
 struct RouteArgs {
   const uint16_t* logits;
   const float* bias;
@@ -156,6 +176,8 @@ struct RouteArgs {
   int32_t* topk_ids;
   float* topk_w;
   UnitOut uo;
+  bool cluster;   // the grid is one cluster that runs both sort phases itself (co)
+  ClusterOut co;
 };
 
 struct UnitArgs {
@@ -183,7 +205,9 @@ struct SliceArgs {
 
 // Launch with programmatic dependent launch allowed: the kernel may be scheduled while the
 // previous kernel of the stream is finishing; every kernel launched this way executes
-// griddepcontrol.wait (pdl_wait) before it touches global memory, so stream order holds.
+// griddepcontrol.wait (pdl_wait) before it reads or writes global memory, so stream order
+// holds (an L2 prefetch of its own inputs, which changes no value a load observes, may come
+// earlier).
 template <class... Params, class... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args&&... args) {
@@ -237,6 +261,9 @@ cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
 // ------------------------------------------------------------ per-context host state
 // Test hooks set through moe_route_sort_debug_set (process-wide).
 unsigned long long debug_wait_limit_ns();  // kWaitLimitNs unless lowered
+// Whether a call of T tokens over E experts takes the cluster path: the defaults above, or,
+// once a test hook has set a token limit, T <= that limit (0: never).
+bool cluster_reach(int T, int E);
 // Identity of the current device and context (the context's unique id, 0 if the driver cannot
 // tell): host caches of device addresses are keyed on it.
 bool current_context(int& dev, unsigned long long& ctx_id);
@@ -256,13 +283,23 @@ cudaError_t launch_empty(int32_t* npp, int32_t* status, cudaStream_t st);
 
 // Shared memory of the multi-CTA route kernels for a given warp count.
 size_t route_smem_bytes(int E, int nwarps, int max_routes, bool sort);
-size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw, int nbuf);
+size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw, int nbuf,
+                      bool cluster);
+int seg_cluster_capacity(size_t smem);
 SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only);
 
 // Shared memory used by phase 1 of the sort step (mrs_unit.cuh) besides the routes.
 __host__ __device__ inline size_t unit_scratch_bytes(int E) {
   return align16(sizeof(unsigned long long) * E) + align16(sizeof(int32_t) * E) +
          align16(sizeof(int32_t) * (E + 1)) + align16(sizeof(int32_t) * E) + 256;
+}
+
+// Shared memory the cluster sort step needs besides the routes and counts.
+__host__ __device__ inline size_t cluster_scratch_bytes(int E) {
+  return align16(sizeof(unsigned) * 2 * static_cast<size_t>(E)) +   // masks
+         3 * align16(sizeof(int32_t) * static_cast<size_t>(E)) +    // run, pad, tot
+         align16(sizeof(int32_t) * (static_cast<size_t>(E) + 1)) +  // base
+         256;                                                       // scan, dup flags
 }
 
 }  // namespace mrs

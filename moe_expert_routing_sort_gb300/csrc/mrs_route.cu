@@ -17,6 +17,7 @@
 // (FP32 logit conversion + correction bias, grouped top-k, both sort phases in one kernel).
 #include "mrs_internal.h"
 #include "mrs_seg.cuh"
+#include "mrs_cluster.cuh"
 #include "mrs_unit.cuh"
 #include "moe_route_sort.h"
 
@@ -141,6 +142,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
   int32_t* misc = reinterpret_cast<int32_t*>(smem + a.lay.misc);  // [0] flags, [4..37] scan
   unsigned* masks = reinterpret_cast<unsigned*>(smem + a.lay.masks);  // [2][E]: tokens 0-31, 32-63
   pdl_trigger();
+  // the inputs start towards L2 while the kernel ahead in the stream finishes
+  if (!kSortOnly) {
+    if (tid < 384)
+      prefetch_l2_range(a.logits, 2 * static_cast<size_t>(a.T) * E, tid, 384);
+    else if (a.bias)
+      prefetch_l2_range(a.bias, 4 * static_cast<size_t>(E), tid - 384, 128);
+  }
   pdl_wait();
 
   if (!kSortOnly) {
@@ -408,7 +416,7 @@ struct SegCtaLayout {
 
 __host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps,
                                                        int max_routes, bool sort, int tpw,
-                                                       int nbuf) {
+                                                       int nbuf, bool cluster) {
   SegCtaLayout l{};
   size_t o = 0;
   l.bias = o;
@@ -431,14 +439,15 @@ __host__ __device__ inline SegCtaLayout seg_cta_layout(int E, int nu, int nwarps
   w = align16(w + ub_bytes(nu));
   l.per_warp = w;
   size_t region = w * nwarps;
-  if (sort && region < unit_scratch_bytes(E)) region = unit_scratch_bytes(E);
+  const size_t tail = cluster ? cluster_scratch_bytes(E) : unit_scratch_bytes(E);
+  if (sort && region < tail) region = tail;
   l.total = o + region;
   return l;
 }
 
 size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw,
-                      int nbuf) {
-  return seg_cta_layout(E, nu, nwarps, max_routes, sort, tpw, nbuf).total;
+                      int nbuf, bool cluster) {
+  return seg_cta_layout(E, nu, nwarps, max_routes, sort, tpw, nbuf, cluster).total;
 }
 
 // Warp w of unit u takes steps w, w + nwarps, ...; step i covers the 32 / LT consecutive
@@ -446,7 +455,9 @@ size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int 
 // of a step are contiguous, so one bulk copy brings them in.  A buffer goes back to the copy
 // engine (for the warp's step nbuf further on) as soon as the selection stops reading it.
 // kSoftmax: softmax scoring, selection on the logits themselves (LogitRow, no bias, exact).
-template <bool kSort, int LT, bool kSoftmax>
+// kCluster: the grid is one thread-block cluster and runs both sort phases itself
+// (cluster_sort_tail) instead of phase 1 into the workspace.
+template <bool kSort, int LT, bool kSoftmax, bool kCluster>
 __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const RouteArgs a) {
   constexpr int kTpw = 32 / LT;
   constexpr int kParts = (LT == 16) ? 2 : 1;
@@ -455,7 +466,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   const int h = lane / LT, ll = lane & (LT - 1);
   const SegShape sh = a.seg;
   const int E = sh.E, K = sh.K, nbuf = a.nbuf;
-  const SegCtaLayout lay = seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort, kTpw, nbuf);
+  const SegCtaLayout lay =
+      seg_cta_layout(E, sh.nu, a.nwarps, a.max_routes, kSort, kTpw, nbuf, kCluster);
   float* bias_s = reinterpret_cast<float*>(smem + lay.bias);
   int32_t* counts = reinterpret_cast<int32_t*>(smem + lay.counts);
   int32_t* rid = reinterpret_cast<int32_t*>(smem + lay.rid);
@@ -587,31 +599,93 @@ __global__ void __launch_bounds__(kSegThreads, 1) mrs_route_seg_kernel(const Rou
   }
   if (kSort) {
     __syncthreads();
-    unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo, a.U);
-    if (tid == 0) a.uo.unit_flags[u] = cta_flags & MOE_RS_DEVICE_WAIT_TIMEOUT;
+    if (kCluster) {
+      if (tid == 0) cta_flags &= MOE_RS_DEVICE_WAIT_TIMEOUT;
+      __syncthreads();
+      cluster_sort_tail(rid, rw, counts, &cta_flags, E, K, t0, t1, static_cast<uint32_t>(u),
+                        static_cast<uint32_t>(a.U), smem + lay.warps, a.co);
+    } else {
+      unit_sort_tail(rid, rw, counts, E, K, u, t0, t1, smem + lay.warps, a.uo, a.U);
+      if (tid == 0) a.uo.unit_flags[u] = cta_flags & MOE_RS_DEVICE_WAIT_TIMEOUT;
+    }
   }
 }
 
-template <bool kSort, int LT, bool kSoftmax>
+template <bool kSort, int LT, bool kSoftmax, bool kCluster>
 static cudaError_t launch_seg_h(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  auto* kern = mrs_route_seg_kernel<kSort, LT, kSoftmax>;
+  auto* kern = mrs_route_seg_kernel<kSort, LT, kSoftmax, kCluster>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(a.U), dim3(a.nwarps * 32), smem, st, a);
+  if (!kCluster) return launch_pdl(kern, dim3(a.U), dim3(a.nwarps * 32), smem, st, a);
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.U);
+  cfg.blockDim = dim3(a.nwarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.U;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <bool kSort, bool kSoftmax>
+template <bool kSort, bool kSoftmax, bool kCluster>
 static cudaError_t launch_seg(const RouteArgs& a, size_t smem, cudaStream_t st) {
-  return a.lanes == 16 ? launch_seg_h<kSort, 16, kSoftmax>(a, smem, st)
-                       : launch_seg_h<kSort, 32, kSoftmax>(a, smem, st);
+  return a.lanes == 16 ? launch_seg_h<kSort, 16, kSoftmax, kCluster>(a, smem, st)
+                       : launch_seg_h<kSort, 32, kSoftmax, kCluster>(a, smem, st);
+}
+
+// Clusters of kClusterCtas CTAs of the segment kernel (one per SM: 512 threads of up to 128
+// registers) that the device can hold at once; 0 when it cannot place one (the cluster path
+// is then not taken).
+int seg_cluster_capacity(size_t smem) {
+  auto* kern = mrs_route_seg_kernel<true, 16, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kClusterCtas);
+  cfg.blockDim = dim3(kSegThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_route(const RouteArgs& a, size_t smem, cudaStream_t st) {
   if (a.use_seg) {
     // softmax scoring only comes with the sort step (moe_route_sort_softmax)
-    if (a.seg.softmax) return a.sort ? launch_seg<true, true>(a, smem, st) : cudaErrorInvalidValue;
-    return a.sort ? launch_seg<true, false>(a, smem, st) : launch_seg<false, false>(a, smem, st);
+    if (a.cluster) {
+      if (!a.sort) return cudaErrorInvalidValue;
+      return a.seg.softmax ? launch_seg<true, true, true>(a, smem, st)
+                           : launch_seg<true, false, true>(a, smem, st);
+    }
+    if (a.seg.softmax)
+      return a.sort ? launch_seg<true, true, false>(a, smem, st) : cudaErrorInvalidValue;
+    return a.sort ? launch_seg<true, false, false>(a, smem, st)
+                  : launch_seg<false, false, false>(a, smem, st);
   }
   cudaError_t err;
   const int threads = a.nwarps * 32;

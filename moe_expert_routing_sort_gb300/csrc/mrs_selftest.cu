@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kCheckThreads) mrs_proxy_check_kernel(float bo
 namespace {
 
 std::atomic<long long> g_wait_limit{-1};   // < 0: kWaitLimitNs
+std::atomic<int> g_cluster_tokens{-1};     // < 0: the default reach
 std::atomic<int> g_force_proxy_fail{0};
 std::atomic<int> g_proxy_generation{1};    // bumped when the forced failure changes
 
@@ -107,6 +108,13 @@ ProxyEntry g_proxy_entries[64];
 unsigned long long debug_wait_limit_ns() {
   const long long v = g_wait_limit.load(std::memory_order_relaxed);
   return v < 0 ? kWaitLimitNs : static_cast<unsigned long long>(v);
+}
+
+bool cluster_reach(int T, int E) {
+  const int v = g_cluster_tokens.load(std::memory_order_relaxed);
+  if (v >= 0) return T <= v;
+  return T <= kClusterMaxTokens &&
+         2ll * static_cast<long long>(T) * E <= kClusterMaxLogitBytes;
 }
 
 bool current_context(int& dev, unsigned long long& ctx_id) {
@@ -194,6 +202,11 @@ extern "C" int moe_route_sort_debug_set(int knob, long long value) {
     case MOE_RS_DEBUG_FORCE_PROXY_FAIL: {
       const int v = value != 0 ? 1 : 0;
       if (mrs::g_force_proxy_fail.exchange(v) != v) mrs::g_proxy_generation.fetch_add(1);
+      return MOE_RS_OK;
+    }
+    case MOE_RS_DEBUG_CLUSTER_TOKENS: {
+      const long long v = value < 0 ? -1 : (value > (1ll << 30) ? (1ll << 30) : value);
+      mrs::g_cluster_tokens.store(static_cast<int>(v));
       return MOE_RS_OK;
     }
     default:

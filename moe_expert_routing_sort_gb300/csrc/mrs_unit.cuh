@@ -53,54 +53,24 @@ __device__ __forceinline__ void block_exclusive_scan(const int32_t* v, int32_t* 
 }
 
 
-// Phase 1 for unit u (see the file comment).  rid/rw: the unit's routes in shared memory,
-// index (t - t0) * K + k; an id outside [0, E) is not placed.  cnt: the unit's per-expert
-// counts of placed routes (shared memory, may be overwritten).  scratch: shared memory of
-// unit_scratch_bytes(E), free for use.  Writes the unit's offsets, its sorted routes and
-// their experts to uo.  All threads of the CTA call this.
-__device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* rw, int32_t* cnt,
-                                               int E, int K, int u, int t0, int t1,
-                                               unsigned char* scratch, const UnitOut& uo,
-                                               int U) {
-  unsigned long long* slice_flags = uo.slice_flags;
-  const int nslices = uo.nslices;
+// Places the routes of tokens [t0, t1) (rid/rw: shared memory, index (t - t0) * K + k; an id
+// outside [0, E) is not placed) in expert order, stable by token then slot: route r of
+// expert e goes to position run[e] + (number of earlier routes of e), and place(pos, r, e)
+// stores it.  run[e] must hold each expert's first position; masks (2 * E words, zero on
+// entry) and dup (two ints, zero on entry) are scratch.  All threads of the CTA call this;
+// it ends with a block barrier.
+//
+// Tiles of 32 tokens: warp w takes tokens w, w + nwarps, ... of the tile, lane k slot k.
+// Per tile: mark (bit of the token in its experts' masks), place (rank = earlier tokens of
+// the tile in the mask, plus the expert's running count), advance (the tile's last token of
+// an expert adds the mask's count and clears it).  Tile j uses mask buffer j & 1, so the
+// next tile is marked in the same phase as this one advances: two barriers per tile.
+template <class Place>
+__device__ __forceinline__ void place_unit_routes(const int32_t* rid, int E, int K, int t0,
+                                                  int t1, unsigned* masks, int32_t* run,
+                                                  int32_t* dup2, const Place& place) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  // one bit per token of a 32-token tile, two buffers (tiles alternate)
-  unsigned* masks = reinterpret_cast<unsigned*>(scratch);
-  size_t o = align16(sizeof(unsigned long long) * E);
-  int32_t* run = reinterpret_cast<int32_t*>(scratch + o);
-  o += align16(sizeof(int32_t) * E);
-  int32_t* loc = reinterpret_cast<int32_t*>(scratch + o);
-  o += align16(sizeof(int32_t) * (E + 1));
-  o += align16(sizeof(int32_t) * E);
-  int32_t* misc = reinterpret_cast<int32_t*>(scratch + o);  // [0..32] scan, [40..41] dup flags
-
-  // clear the look-back words and the status word for the slice kernel
-  for (int c = u + tid * U; c < nslices; c += blockDim.x * U) slice_flags[c] = 0ull;
-  if (u == 0 && tid == 0) *uo.status = 0;
-
-  block_exclusive_scan(cnt, loc, E, misc);
-  int32_t* loc_g = uo.loc_off + static_cast<size_t>(u) * (E + 1);
-  for (int e = tid; e <= E; e += blockDim.x) loc_g[e] = loc[e];
-  for (int e = tid; e < E; e += blockDim.x) {
-    run[e] = loc[e];
-    masks[e] = 0u;
-    masks[E + e] = 0u;
-  }
-  if (tid == 0) {
-    misc[40] = 0;
-    misc[41] = 0;
-  }
-  __syncthreads();
-
-  // Tiles of 32 tokens: warp w takes tokens w, w + nwarps, ... of the tile, lane k slot k.
-  // Per tile: mark (bit of the token in its experts' masks), place (rank = earlier tokens of
-  // the tile in the mask, plus the expert's running count), advance (the tile's last token of
-  // an expert adds the mask's count and clears it).  Tile j uses mask buffer j & 1, so the
-  // next tile is marked in the same phase as this one advances: two barriers per tile.
-  int2* out = uo.unit_buf + static_cast<size_t>(t0) * K;
-  uint16_t* out_e = uo.unit_e + static_cast<size_t>(t0) * K;
   const int nt_all = t1 - t0;
   auto mark = [&](int tb, unsigned* m, int32_t* dup) {
     const int nt = min(32, nt_all - tb);
@@ -112,24 +82,20 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
       }
     }
   };
-  if (nt_all > 0) mark(0, masks, &misc[40]);
+  if (nt_all > 0) mark(0, masks, &dup2[0]);
   __syncthreads();
   for (int tb = 0, j = 0; tb < nt_all; tb += 32, ++j) {
     const int nt = min(32, nt_all - tb);
     unsigned* m = masks + (j & 1) * E;
     unsigned* m_next = masks + ((j + 1) & 1) * E;
-    int32_t* dup = &misc[40 + (j & 1)];
-    int32_t* dup_next = &misc[40 + ((j + 1) & 1)];
+    int32_t* dup = &dup2[j & 1];
+    int32_t* dup_next = &dup2[(j + 1) & 1];
     const bool more = tb + 32 < nt_all;
     if (*dup == 0) {
       for (int tl = warp; tl < nt; tl += nwarps) {
         const int r = (tb + tl) * K + lane;
         const int e = (lane < K) ? rid[r] : -1;
-        if (e >= 0 && e < E) {
-          const int pos = run[e] + __popc(m[e] & ((1u << tl) - 1u));
-          out[pos] = make_int2(t0 * K + r, __float_as_int(rw[r]));
-          out_e[pos] = static_cast<uint16_t>(e);
-        }
+        if (e >= 0 && e < E) place(run[e] + __popc(m[e] & ((1u << tl) - 1u)), r, e);
       }
       __syncthreads();
       for (int tl = warp; tl < nt; tl += nwarps) {
@@ -162,9 +128,7 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
           int p0 = 0;
           if (valid) {
             p0 = run[e];
-            const int pos = p0 + __popc(peers & lanemask_lt(lane));
-            out[pos] = make_int2(t0 * K + r0 + i, __float_as_int(rw[r0 + i]));
-            out_e[pos] = static_cast<uint16_t>(e);
+            place(p0 + __popc(peers & lanemask_lt(lane)), r0 + i, e);
           }
           __syncwarp();
           if (valid && (peers >> lane) == 1u) run[e] = p0 + __popc(peers);
@@ -176,6 +140,53 @@ __device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* 
     }
     if (tid == 0) *dup = 0;  // read by every thread before this tile's first barrier
   }
+}
+
+// Phase 1 for unit u (see the file comment).  rid/rw: the unit's routes in shared memory,
+// index (t - t0) * K + k; an id outside [0, E) is not placed.  cnt: the unit's per-expert
+// counts of placed routes (shared memory, may be overwritten).  scratch: shared memory of
+// unit_scratch_bytes(E), free for use.  Writes the unit's offsets, its sorted routes and
+// their experts to uo.  All threads of the CTA call this.
+__device__ __forceinline__ void unit_sort_tail(const int32_t* rid, const float* rw, int32_t* cnt,
+                                               int E, int K, int u, int t0, int t1,
+                                               unsigned char* scratch, const UnitOut& uo,
+                                               int U) {
+  unsigned long long* slice_flags = uo.slice_flags;
+  const int nslices = uo.nslices;
+  const int tid = threadIdx.x;
+  // one bit per token of a 32-token tile, two buffers (tiles alternate)
+  unsigned* masks = reinterpret_cast<unsigned*>(scratch);
+  size_t o = align16(sizeof(unsigned long long) * E);
+  int32_t* run = reinterpret_cast<int32_t*>(scratch + o);
+  o += align16(sizeof(int32_t) * E);
+  int32_t* loc = reinterpret_cast<int32_t*>(scratch + o);
+  o += align16(sizeof(int32_t) * (E + 1));
+  o += align16(sizeof(int32_t) * E);
+  int32_t* misc = reinterpret_cast<int32_t*>(scratch + o);  // [0..32] scan, [40..41] dup flags
+
+  // clear the look-back words and the status word for the slice kernel
+  for (int c = u + tid * U; c < nslices; c += blockDim.x * U) slice_flags[c] = 0ull;
+  if (u == 0 && tid == 0) *uo.status = 0;
+
+  block_exclusive_scan(cnt, loc, E, misc);
+  int32_t* loc_g = uo.loc_off + static_cast<size_t>(u) * (E + 1);
+  for (int e = tid; e <= E; e += blockDim.x) loc_g[e] = loc[e];
+  for (int e = tid; e < E; e += blockDim.x) {
+    run[e] = loc[e];
+    masks[e] = 0u;
+    masks[E + e] = 0u;
+  }
+  if (tid == 0) {
+    misc[40] = 0;
+    misc[41] = 0;
+  }
+  __syncthreads();
+  int2* out = uo.unit_buf + static_cast<size_t>(t0) * K;
+  uint16_t* out_e = uo.unit_e + static_cast<size_t>(t0) * K;
+  place_unit_routes(rid, E, K, t0, t1, masks, run, &misc[40], [&](int pos, int r, int e) {
+    out[pos] = make_int2(t0 * K + r, __float_as_int(rw[r]));
+    out_e[pos] = static_cast<uint16_t>(e);
+  });
 }
 
 }  // namespace mrs

@@ -190,6 +190,8 @@ def test_debug_knobs(lib):
     assert lib.moe_route_sort_debug_set(1, -1) == 0  # ... and back to the default
     assert lib.moe_route_sort_debug_set(2, 1) == 0   # forced proxy failure ...
     assert lib.moe_route_sort_debug_set(2, 0) == 0   # ... and back to the real check
+    assert lib.moe_route_sort_debug_set(3, 0) == 0   # cluster path off ...
+    assert lib.moe_route_sort_debug_set(3, -1) == 0  # ... and back to the default
 
 
 def test_binding_refuses_buffers_on_different_devices():

@@ -1,0 +1,184 @@
+"""The cluster path of moe_route_sort: for mid-sized calls (by default 64 < T <= 256 and at
+most 512 KiB of logits, segment-shaped groups) one cluster of 16 CTAs runs the route step and
+both sort phases in a single launch, exchanging per-expert counts through distributed shared
+memory.  Every case is compared with the CPU oracle bit for bit (weights within 1e-6) and with
+the three-kernel multi-CTA path on the same inputs; the library's test hook forces the cluster
+path on (any size) or off.  The cluster path touches no workspace byte beyond the status word;
+the tests use that to check which path ran.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_expert_routing_sort_gb300 as mrs
+from _support import WEIGHT_ATOL, check_sort_invariants, redraw_callback
+from moe_expert_routing_sort_gb300 import datagen
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+POISON = 0xA5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mrs.build()
+    oracle.build()
+    mrs.load()
+    yield
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+
+
+def _case(name, T, seed=0, **over):
+    w = datagen.workload(name, T=T, seed=seed, **over)
+    inp = datagen.make_inputs(w, needs_redraw=redraw_callback(oracle, w))
+    ref = oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,
+                            w.routed_scale, w.block_m)
+    return w, inp, ref
+
+
+def _run(w, inp, cluster_tokens):
+    """One call with the cluster path limited to T <= cluster_tokens; returns the buffers and
+    whether any workspace byte past the status word changed."""
+    logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
+    bias = torch.from_numpy(inp.bias).to(DEV)
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    out.workspace.fill_(POISON)
+    out.sorted_token_ids.fill_(-7)
+    out.expert_ids.fill_(-7)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, cluster_tokens)
+    try:
+        mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                       w.block_m, out=out)
+        torch.cuda.synchronize()
+    finally:
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+    touched = bool(torch.any(out.workspace[16:] != POISON).item())
+    return out, touched
+
+
+def _assert_matches(out, ref, w):
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref.num_tokens_post_pad
+    ids = out.topk_ids.cpu().numpy()
+    wt = out.topk_weights.cpu().numpy()
+    assert np.array_equal(ids, ref.topk_ids)
+    assert np.max(np.abs(wt - ref.topk_weights), initial=0.0) <= WEIGHT_ATOL
+    sid = out.sorted_token_ids[:npp].cpu().numpy()
+    sw = out.sorted_weights[:npp].cpu().numpy()
+    assert np.array_equal(sid, ref.sorted_token_ids)
+    assert np.array_equal(out.expert_ids[: npp // w.block_m].cpu().numpy(), ref.expert_ids)
+    real = sid != w.T * w.topk
+    assert np.all(sw[~real] == 0.0)
+    assert np.array_equal(sw[real], wt.reshape(-1)[sid[real]])
+    assert out.status_word() == 0
+    check_sort_invariants(ref.topk_ids, w.E, w.block_m, out.sorted_token_ids.cpu().numpy(),
+                          out.expert_ids.cpu().numpy(), ref.num_tokens_post_pad)
+
+
+FORCE = 1 << 20  # the hook's token limit that puts every call of these tests on the cluster
+
+
+def _both_paths(w, inp, ref, cluster=True):
+    a, touched_a = _run(w, inp, FORCE)
+    if cluster:
+        assert not touched_a, "the cluster path wrote into the workspace (did it run?)"
+    else:
+        assert touched_a, "a shape without a segment layout took the cluster path"
+    _assert_matches(a, ref, w)
+    b, touched_b = _run(w, inp, 0)
+    assert touched_b, "the three-kernel path left the workspace alone (did it run?)"
+    _assert_matches(b, ref, w)
+    npp = int(a.num_tokens_post_pad.item())
+    assert torch.equal(a.sorted_token_ids[:npp], b.sorted_token_ids[:npp])
+    assert torch.equal(a.sorted_weights[:npp], b.sorted_weights[:npp])
+    assert torch.equal(a.topk_weights, b.topk_weights)
+
+
+# T spans one token per CTA-warp, ragged CTA ranges (T not a multiple of 16) and sizes past
+# the default reach.
+@pytest.mark.parametrize("T", [65, 100, 256, 257, 511, 512, 777, 1024])
+def test_prefill_shape(T):
+    w, inp, ref = _case("prefill_T512_E896", T)
+    _both_paths(w, inp, ref)
+
+
+@pytest.mark.parametrize("T", [65, 300, 1000])
+def test_skewed_distribution(T):
+    # a few hot experts: most CTAs hold routes of the same experts, so `before` sums matter
+    w, inp, ref = _case("skewed_T8192_E896", T)
+    _both_paths(w, inp, ref)
+
+
+@pytest.mark.parametrize("T", [70, 600])
+def test_wide_experts(T):
+    w, inp, ref = _case("wide_T16384_E4096", T)
+    _both_paths(w, inp, ref)
+
+
+# cluster: whether the shape has a segment layout (a group splits into equal lane segments
+# of a multiple of 4 experts), which the cluster path needs; the other shapes keep the
+# three-kernel path whatever the limit.
+@pytest.mark.parametrize("E,G,Kg,K,B,T,cluster", [(256, 8, 4, 8, 16, 130, True),
+                                                   (64, 8, 4, 6, 16, 200, False),
+                                                   (128, 4, 2, 4, 64, 99, True),
+                                                   (512, 16, 16, 10, 8, 515, True),
+                                                   (120, 8, 4, 8, 16, 333, False),
+                                                   (96, 3, 2, 8, 16, 333, True)])
+def test_other_shapes(E, G, Kg, K, B, T, cluster):
+    w, inp, ref = _case("prefill_T512_E896", T, E=E, n_group=G, topk_group=Kg, topk=K,
+                        block_m=B)
+    _both_paths(w, inp, ref, cluster)
+
+
+def test_widened_limit_runs_larger_calls_in_one_cluster():
+    w, inp, ref = _case("prefill_T512_E896", 2048)
+    out, touched = _run(w, inp, 4096)
+    assert not touched
+    _assert_matches(out, ref, w)
+
+
+@pytest.mark.parametrize("name,T,cluster", [("prefill_T512_E896", 65, True),
+                                             ("prefill_T512_E896", 256, True),
+                                             ("prefill_T512_E896", 257, False),
+                                             ("prefill_T512_E896", 512, False),
+                                             ("skewed_T8192_E896", 200, True),
+                                             ("wide_T16384_E4096", 65, False)])
+def test_default_reach(name, T, cluster):
+    # by default: T <= 256 and at most 512 KiB of logits
+    w, inp, ref = _case(name, T)
+    out, touched = _run(w, inp, -1)
+    assert touched != cluster
+    _assert_matches(out, ref, w)
+
+
+def test_softmax_scoring_on_the_cluster_path():
+    w = datagen.workload("prefill_T512_E896", T=300, n_group=1, topk_group=1, topk=8)
+    inp = datagen.make_inputs(w)
+    ref = oracle.route_sort_softmax(inp.logits_bf16, w.topk, w.routed_scale, w.block_m)
+    logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
+    outs = []
+    for limit in (FORCE, 0):
+        out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+        out.workspace.fill_(POISON)
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, limit)
+        try:
+            mrs.route_sort_softmax(logits, w.topk, w.routed_scale, w.block_m, out=out)
+            torch.cuda.synchronize()
+        finally:
+            mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+        assert bool(torch.any(out.workspace[16:] != POISON).item()) == (limit == 0)
+        npp = int(out.num_tokens_post_pad.item())
+        assert npp == ref["num_tokens_post_pad"]
+        assert np.array_equal(out.topk_ids.cpu().numpy(), ref["topk_ids"])
+        assert np.max(np.abs(out.topk_weights.cpu().numpy() - ref["topk_weights"]),
+                      initial=0.0) <= WEIGHT_ATOL
+        assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref["sorted_token_ids"])
+        assert np.array_equal(out.expert_ids[: npp // w.block_m].cpu().numpy(),
+                              ref["expert_ids"])
+        assert out.status_word() == 0
+        outs.append(out)
+    assert torch.equal(outs[0].topk_weights, outs[1].topk_weights)
