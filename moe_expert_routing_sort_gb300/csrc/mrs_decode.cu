@@ -70,7 +70,10 @@ __host__ __device__ inline int decode_tpg(int G) {
 }
 
 // kSoftmax: softmax scoring (keys are the logits, no bias).
-template <bool kSoftmax>
+// kEpt: experts per thread the code is unrolled for (>= ceil(g / TPG)); the smallest fitting
+// instance is launched, so that a launch fetches only the instructions it runs (the kernel
+// usually lands on an SM whose instruction cache has never held it).
+template <bool kSoftmax, int kEpt>
 __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
   __shared__ DecodeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -90,12 +93,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   pdl_wait();
 
   // ---- loads (one DRAM round trip); rows that depend on nothing meanwhile
-  float key[kDecodeEpt], sv[kDecodeEpt];
+  float key[kEpt], sv[kEpt];
   {
-    uint16_t x[kDecodeEpt];
-    float b[kDecodeEpt];
+    uint16_t x[kEpt];
+    float b[kEpt];
 #pragma unroll
-    for (int r = 0; r < kDecodeEpt; ++r) {
+    for (int r = 0; r < kEpt; ++r) {
       if (r >= R) break;
       const int li = i + TPG * r;
       if (in_group && li < g) {
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
     }
     float t1 = -INFINITY, t2 = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < kDecodeEpt; ++r) {
+    for (int r = 0; r < kEpt; ++r) {
       const int li = i + TPG * r;
       key[r] = -INFINITY;
       sv[r] = 0.0f;
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   // ---- survivors: kept keys >= tau, compacted (warp-aggregated slots)
   const bool mine_kept = in_group && kept_group(j);
 #pragma unroll
-  for (int r = 0; r < kDecodeEpt; ++r) {
+  for (int r = 0; r < kEpt; ++r) {
     if (r >= R) break;
     const bool s_ok = mine_kept && key[r] >= tau;
     const unsigned bl = __ballot_sync(kFull, s_ok);
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       unsigned long long best = 0ull;
       float best_s = 0.0f;
 #pragma unroll
-      for (int r = 0; r < kDecodeEpt; ++r) {
+      for (int r = 0; r < kEpt; ++r) {
         if (mine_kept && key[r] >= tau) {
           const unsigned long long c = composite(key[r], j * g + i + TPG * r);
           if (c < prev && c > best) {
@@ -318,9 +321,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   }
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  auto* kern = a.softmax ? mrs_decode_kernel<true> : mrs_decode_kernel<false>;
+template <int kEpt>
+static cudaError_t launch_decode_ept(const DecodeArgs& a, cudaStream_t st) {
+  auto* kern = a.softmax ? mrs_decode_kernel<true, kEpt> : mrs_decode_kernel<false, kEpt>;
   return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  const int tpg = decode_tpg(a.G);
+  const int r = (a.g + tpg - 1) / tpg;  // <= kDecodeEpt (g <= 4096 / G < 16 * TPG)
+  if (r <= 2) return launch_decode_ept<2>(a, st);
+  if (r <= 4) return launch_decode_ept<4>(a, st);
+  if (r <= 8) return launch_decode_ept<8>(a, st);
+  return launch_decode_ept<kDecodeEpt>(a, st);
 }
 
 }  // namespace mrs

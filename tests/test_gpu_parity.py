@@ -129,6 +129,7 @@ SHAPES = [
     (1, 1, 1, 1, 8, 1.0),         # one expert
     (96, 6, 6, 1, 2, 2.0),
     (2048, 32, 5, 12, 32, 1.0),
+    (4000, 5, 2, 8, 32, 1.0),     # 800 experts per group: the one-token kernel's widest rows
 ]
 
 
