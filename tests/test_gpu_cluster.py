@@ -127,7 +127,8 @@ def test_wide_experts(T):
                                                    (128, 4, 2, 4, 64, 99, True),
                                                    (512, 16, 16, 10, 8, 515, True),
                                                    (120, 8, 4, 8, 16, 333, False),
-                                                   (96, 3, 2, 8, 16, 333, True)])
+                                                   (96, 3, 2, 8, 16, 333, True),
+                                                   (4096, 16, 16, 32, 1024, 150, True)])
 def test_other_shapes(E, G, Kg, K, B, T, cluster):
     w, inp, ref = _case("prefill_T512_E896", T, E=E, n_group=G, topk_group=Kg, topk=K,
                         block_m=B)
