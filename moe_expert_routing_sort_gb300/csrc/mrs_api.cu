@@ -526,7 +526,7 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   }
 
   // mid-sized calls: one cluster routes and sorts in a single launch
-  if (use_seg && d.clusters > 0 && cluster_reach(T, E) &&
+  if (use_seg && d.clusters > 0 && cluster_reach(T, E, topk, block_m) &&
       static_cast<int64_t>(T) * topk <= static_cast<int64_t>(kClusterCtas) * kUnitRouteCap) {
     ClusterOut co{};
     co.sorted_ids = sorted_token_ids;
@@ -670,6 +670,29 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
     a.npp = num_tokens_post_pad;
     a.status = status;
     return launch_status(launch_small(a, true, stream));
+  }
+  // mid-sized calls: one cluster counts and places every route in a single launch
+  if (d.clusters > 0 && cluster_reach_sort(T, E, topk, block_m) &&
+      static_cast<int64_t>(T) * topk <= static_cast<int64_t>(kClusterCtas) * kUnitRouteCap) {
+    UnitArgs c{};
+    c.ids = topk_ids;
+    c.w = topk_weights;
+    c.T = T;
+    c.K = topk;
+    c.E = E;
+    c.U = kClusterCtas;
+    c.max_routes = ((T + kClusterCtas - 1) / kClusterCtas) * topk;
+    c.cluster = true;
+    c.co.sorted_ids = sorted_token_ids;
+    c.co.sorted_w = sorted_weights;
+    c.co.expert_ids = expert_ids;
+    c.co.npp = num_tokens_post_pad;
+    c.co.status = status;
+    c.co.B = block_m;
+    c.co.N = T * topk;
+    rc = launch_status(launch_unit(c, stream));
+    // a rejected cluster launch enqueued nothing: the three-kernel path below takes the call
+    if (rc != MOE_RS_ERR_LAUNCH) return rc;
   }
   const int U = units_for_shape(T, topk, d.sms);
   const int nslices = slices_for(U, E);

@@ -153,12 +153,16 @@ struct ClusterOut {
 // CTAs of the cluster that runs a mid-sized route-sort call (a non-portable cluster size,
 // used only where the device can place such a cluster).
 constexpr int kClusterCtas = 16;
-// Default reach of the cluster path: at most this many tokens and this many bytes of logits.
-// The cluster sits on one GPC, so it reads its inputs through that GPC's share of the memory
-// system and routes on 16 SMs; past these sizes the three-kernel path, spread over the whole
-// GPU, is faster on a GB300.
+// Default reach of the cluster paths.  The cluster sits on one GPC, so it reads its inputs
+// through that GPC's share of the memory system, routes on 16 SMs and writes every padding row
+// from those 16 SMs; past these sizes the three-kernel path, spread over the whole GPU, is
+// faster on a GB300.  moe_route_sort: at most kClusterMaxTokens tokens and
+// kClusterMaxLogitBytes of logits; moe_sort: at most kClusterMaxSortRoutes routes; both: at
+// most kClusterMaxPadded rows of the worst-case padded length.
 constexpr int kClusterMaxTokens = 256;
 constexpr long long kClusterMaxLogitBytes = 512 << 10;
+constexpr long long kClusterMaxSortRoutes = 8192;
+constexpr long long kClusterMaxPadded = 65536;
 
 struct RouteArgs {
   const uint16_t* logits;
@@ -185,6 +189,8 @@ struct UnitArgs {
   const float* w;
   int T, K, E, U, max_routes;
   UnitOut uo;
+  bool cluster;   // the grid is one cluster that runs both sort phases itself (co)
+  ClusterOut co;
 };
 
 struct SliceArgs {
@@ -261,9 +267,12 @@ cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
 // ------------------------------------------------------------ per-context host state
 // Test hooks set through moe_route_sort_debug_set (process-wide).
 unsigned long long debug_wait_limit_ns();  // kWaitLimitNs unless lowered
-// Whether a call of T tokens over E experts takes the cluster path: the defaults above, or,
-// once a test hook has set a token limit, T <= that limit (0: never).
-bool cluster_reach(int T, int E);
+// Whether a call of T tokens over E experts (K routes per token, blocks of B rows) takes the
+// cluster path: the defaults above, or, once a test hook has set a token limit, T <= that
+// limit (0: never).
+bool cluster_reach(int T, int E, int K, int B);
+// The same for moe_sort.
+bool cluster_reach_sort(int T, int E, int K, int B);
 // Identity of the current device and context (the context's unique id, 0 if the driver cannot
 // tell): host caches of device addresses are keyed on it.
 bool current_context(int& dev, unsigned long long& ctx_id);

@@ -110,11 +110,25 @@ unsigned long long debug_wait_limit_ns() {
   return v < 0 ? kWaitLimitNs : static_cast<unsigned long long>(v);
 }
 
-bool cluster_reach(int T, int E) {
+namespace {
+long long padded_rows(int T, int E, int K, int B) {
+  const long long N = static_cast<long long>(T) * K;
+  return N + (N < E ? N : E) * static_cast<long long>(B - 1);
+}
+}  // namespace
+
+bool cluster_reach(int T, int E, int K, int B) {
   const int v = g_cluster_tokens.load(std::memory_order_relaxed);
   if (v >= 0) return T <= v;
-  return T <= kClusterMaxTokens &&
-         2ll * static_cast<long long>(T) * E <= kClusterMaxLogitBytes;
+  return T <= kClusterMaxTokens && 2ll * static_cast<long long>(T) * E <= kClusterMaxLogitBytes &&
+         padded_rows(T, E, K, B) <= kClusterMaxPadded;
+}
+
+bool cluster_reach_sort(int T, int E, int K, int B) {
+  const int v = g_cluster_tokens.load(std::memory_order_relaxed);
+  if (v >= 0) return T <= v;
+  return static_cast<long long>(T) * K <= kClusterMaxSortRoutes &&
+         padded_rows(T, E, K, B) <= kClusterMaxPadded;
 }
 
 bool current_context(int& dev, unsigned long long& ctx_id) {

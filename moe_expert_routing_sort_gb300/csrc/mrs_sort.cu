@@ -22,12 +22,16 @@
 // Entries of one expert stay in token-then-slot order by construction; no global atomics
 // are used, and every wait is bounded.
 #include "mrs_internal.h"
+#include "mrs_cluster.cuh"
 #include "mrs_unit.cuh"
 #include "moe_route_sort.h"
 
 namespace mrs {
 
 // ------------------------------------------------- phase 1 for moe_sort (given routes)
+// kCluster: the grid is one thread-block cluster that runs both sort phases itself
+// (cluster_sort_tail) instead of phase 1 into the workspace.
+template <bool kCluster>
 __global__ void __launch_bounds__(kUnitThreads) mrs_unit_kernel(const UnitArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -54,21 +58,44 @@ __global__ void __launch_bounds__(kUnitThreads) mrs_unit_kernel(const UnitArgs a
     else if (e >= 0) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
-  unit_sort_tail(rid, rw, cnt, a.E, a.K, blockIdx.x, t0, t1, scratch, a.uo, a.U);
-  if (tid == 0) a.uo.unit_flags[blockIdx.x] = bad;
+  if (kCluster) {
+    cluster_sort_tail(rid, rw, cnt, &bad, a.E, a.K, t0, t1, blockIdx.x,
+                      static_cast<uint32_t>(a.U), scratch, a.co);
+  } else {
+    unit_sort_tail(rid, rw, cnt, a.E, a.K, blockIdx.x, t0, t1, scratch, a.uo, a.U);
+    if (tid == 0) a.uo.unit_flags[blockIdx.x] = bad;
+  }
 }
 
-size_t unit_kernel_smem(int E, int max_routes) {
-  return 2 * align16(sizeof(int32_t) * max_routes) + align16(sizeof(int32_t) * (E + 1)) +
-         unit_scratch_bytes(E);
+size_t unit_kernel_smem(int E, int max_routes, bool cluster) {
+  const size_t tail = cluster ? cluster_scratch_bytes(E) : unit_scratch_bytes(E);
+  return 2 * align16(sizeof(int32_t) * max_routes) + align16(sizeof(int32_t) * (E + 1)) + tail;
 }
 
 cudaError_t launch_unit(const UnitArgs& a, cudaStream_t st) {
-  const size_t smem = unit_kernel_smem(a.E, a.max_routes);
-  cudaError_t err = cudaFuncSetAttribute(mrs_unit_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = unit_kernel_smem(a.E, a.max_routes, a.cluster);
+  auto* kern = a.cluster ? mrs_unit_kernel<true> : mrs_unit_kernel<false>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(mrs_unit_kernel, dim3(a.U), dim3(kUnitThreads), smem, st, a);
+  if (!a.cluster) return launch_pdl(kern, dim3(a.U), dim3(kUnitThreads), smem, st, a);
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.U);
+  cfg.blockDim = dim3(kUnitThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.U;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // ------------------------------------------------------------------ phase 2: slices

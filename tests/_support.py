@@ -109,3 +109,26 @@ def check_sort_invariants(topk_ids, E, block_m, sorted_token_ids, expert_ids, np
         tw = np.asarray(topk_weights).reshape(-1)
         assert np.array_equal(sw[real], tw[sid[real]])
         assert np.all(sw[~real] == 0.0)
+
+
+def ids_for(dist, T, K, E, rng):
+    """Route ids [T, K] int32 for moe_sort tests: distinct uniform experts per token, one
+    expert shared by every token, all routes to one expert, every third route dropped (-1),
+    all dropped, or repeated ids inside a token."""
+    if dist == "uniform":
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+    elif dist == "shared":
+        ids = np.stack([np.concatenate([[0], 1 + rng.permutation(E - 1)[:K - 1]])
+                        for _ in range(T)])
+    elif dist == "one_expert":
+        ids = np.full((T, K), E // 2)
+    elif dist == "every_third_dropped":
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+        ids.reshape(-1)[::3] = -1
+    elif dist == "all_dropped":
+        ids = np.full((T, K), -1)
+    elif dist == "dup_in_token":
+        ids = rng.integers(0, E, (T, K))
+    else:
+        raise ValueError(dist)
+    return ids.astype(np.int32)

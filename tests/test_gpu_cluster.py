@@ -1,10 +1,11 @@
-"""The cluster path of moe_route_sort: for mid-sized calls (by default 64 < T <= 256 and at
+"""The cluster paths of moe_route_sort and moe_sort: for mid-sized calls (by default 64 < T <= 256 and at
 most 512 KiB of logits, segment-shaped groups) one cluster of 16 CTAs runs the route step and
 both sort phases in a single launch, exchanging per-expert counts through distributed shared
 memory.  Every case is compared with the CPU oracle bit for bit (weights within 1e-6) and with
 the three-kernel multi-CTA path on the same inputs; the library's test hook forces the cluster
-path on (any size) or off.  The cluster path touches no workspace byte beyond the status word;
-the tests use that to check which path ran.
+path on (any size) or off.  moe_sort does the same from given routes (by default up to 8192
+routes).  The cluster paths touch no workspace byte beyond the status word; the tests use that to
+check which path ran.
 """
 import numpy as np
 import pytest
@@ -12,7 +13,7 @@ import torch
 
 import oracle
 import moe_expert_routing_sort_gb300 as mrs
-from _support import WEIGHT_ATOL, check_sort_invariants, redraw_callback
+from _support import WEIGHT_ATOL, check_sort_invariants, ids_for, redraw_callback
 from moe_expert_routing_sort_gb300 import datagen
 
 pytestmark = pytest.mark.gpu
@@ -183,3 +184,77 @@ def test_softmax_scoring_on_the_cluster_path():
         assert out.status_word() == 0
         outs.append(out)
     assert torch.equal(outs[0].topk_weights, outs[1].topk_weights)
+
+
+# ------------------------------------------------------------------ moe_sort
+def _sort(ids, wts, E, B, limit):
+    T, K = ids.shape
+    out = mrs.RouteSortBuffers.allocate(T, E, K, B, device=DEV)
+    out.workspace.fill_(POISON)
+    out.sorted_token_ids.fill_(-7)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, limit)
+    try:
+        mrs.moe_sort(torch.from_numpy(ids).to(DEV), torch.from_numpy(wts).to(DEV), E, B,
+                     out.sorted_token_ids, out.sorted_weights, out.expert_ids,
+                     out.num_tokens_post_pad, out.workspace)
+        torch.cuda.synchronize()
+    finally:
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+    touched = bool(torch.any(out.workspace[16:] != POISON).item())
+    return out, touched
+
+
+@pytest.mark.parametrize("dist", ["uniform", "shared", "one_expert", "every_third_dropped",
+                                  "all_dropped", "dup_in_token"])
+@pytest.mark.parametrize("T,K,E,B", [(129, 16, 896, 32), (500, 16, 896, 64), (1000, 8, 4096, 128),
+                                     (3001, 8, 256, 64)])
+def test_moe_sort_on_one_cluster(dist, T, K, E, B):
+    rng = np.random.default_rng(T + K + E + B)
+    ids = ids_for(dist, T, K, E, rng)
+    wts = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
+    ref = oracle.sort(ids, wts, E, B)
+    outs = []
+    for limit, cluster in ((FORCE, True), (0, False)):
+        out, touched = _sort(ids, wts, E, B, limit)
+        assert touched != cluster
+        npp = int(out.num_tokens_post_pad.item())
+        assert npp == ref.num_tokens_post_pad
+        assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)
+        assert np.array_equal(out.sorted_weights[:npp].cpu().numpy(), ref.sorted_weights)
+        assert np.array_equal(out.expert_ids[: npp // B].cpu().numpy(), ref.expert_ids)
+        assert out.status_word() == ref.flags == 0
+        outs.append(out)
+    npp = ref.num_tokens_post_pad
+    assert torch.equal(outs[0].sorted_token_ids[:npp], outs[1].sorted_token_ids[:npp])
+
+
+def test_moe_sort_cluster_flags_out_of_range_ids():
+    rng = np.random.default_rng(5)
+    T, E, K, B = 700, 64, 4, 16
+    ids = rng.integers(0, E, (T, K)).astype(np.int32)
+    ids[T // 3, 2] = E
+    ids[T - 1, 0] = E + 100
+    wts = np.ones((T, K), np.float32)
+    ref = oracle.sort(ids, wts, E, B)
+    out, touched = _sort(ids, wts, E, B, FORCE)
+    assert not touched
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref.num_tokens_post_pad
+    assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)
+    assert out.status_word() == mrs.DEVICE_BAD_EXPERT_ID
+
+
+@pytest.mark.parametrize("T,K,cluster", [(129, 16, True), (512, 16, True), (513, 16, False),
+                                         (2000, 4, True), (1025, 8, False)])
+def test_moe_sort_default_reach(T, K, cluster):
+    # by default up to 8192 routes (T * K); smaller calls (up to 2048 routes) take the
+    # single-CTA kernel, which leaves the workspace alone too
+    E, B = 896, 32
+    rng = np.random.default_rng(T)
+    ids = ids_for("uniform", T, K, E, rng)
+    wts = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
+    ref = oracle.sort(ids, wts, E, B)
+    out, touched = _sort(ids, wts, E, B, -1)
+    assert touched != cluster
+    npp = int(out.num_tokens_post_pad.item())
+    assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)

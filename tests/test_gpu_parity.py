@@ -17,7 +17,7 @@ import torch
 
 import oracle
 import moe_expert_routing_sort_gb300 as mrs
-from _support import WEIGHT_ATOL, check_sort_invariants, redraw_callback
+from _support import WEIGHT_ATOL, check_sort_invariants, ids_for, redraw_callback
 from moe_expert_routing_sort_gb300 import datagen
 
 pytestmark = pytest.mark.gpu
@@ -225,33 +225,13 @@ def test_moe_topk(name):
     assert np.max(np.abs(wt.cpu().numpy() - ref.topk_weights)) <= WEIGHT_ATOL
 
 
-def _ids_for(dist, T, K, E, rng):
-    if dist == "uniform":
-        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
-    elif dist == "shared":
-        ids = np.stack([np.concatenate([[0], 1 + rng.permutation(E - 1)[:K - 1]])
-                        for _ in range(T)])
-    elif dist == "one_expert":
-        ids = np.full((T, K), E // 2)
-    elif dist == "every_third_dropped":
-        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
-        ids.reshape(-1)[::3] = -1
-    elif dist == "all_dropped":
-        ids = np.full((T, K), -1)
-    elif dist == "dup_in_token":
-        ids = rng.integers(0, E, (T, K))
-    else:
-        raise ValueError(dist)
-    return ids.astype(np.int32)
-
-
 @pytest.mark.parametrize("dist", ["uniform", "shared", "one_expert", "every_third_dropped",
                                   "all_dropped", "dup_in_token"])
 @pytest.mark.parametrize("T,K,E,B", [(5, 4, 33, 8), (64, 16, 896, 32), (3001, 8, 256, 64),
                                      (16384, 8, 4096, 128)])
 def test_moe_sort_distributions(dist, T, K, E, B):
     rng = np.random.default_rng(T + K + E + B)
-    ids = _ids_for(dist, T, K, E, rng)
+    ids = ids_for(dist, T, K, E, rng)
     wts = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
     ref = oracle.sort(ids, wts, E, B)
     out = mrs.RouteSortBuffers.allocate(T, E, K, B, device=DEV)
@@ -277,7 +257,7 @@ def test_moe_sort_atomic_places_the_same_routes(dist, T, K, E, B):
     # order inside an expert's segment is unspecified: compare each segment as a set, and
     # everything else exactly
     rng = np.random.default_rng(T + K + E + B)
-    ids = _ids_for(dist, T, K, E, rng)
+    ids = ids_for(dist, T, K, E, rng)
     wts = rng.uniform(0.01, 1.0, (T, K)).astype(np.float32)
     ref = oracle.sort(ids, wts, E, B)
     out = mrs.RouteSortBuffers.allocate(T, E, K, B, device=DEV)
