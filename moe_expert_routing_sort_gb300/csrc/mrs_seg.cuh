@@ -183,6 +183,7 @@ __device__ __forceinline__ unsigned long long hot_units(const unsigned short* um
   const uint2* q = reinterpret_cast<const uint2*>(umax) + lane;
   unsigned long long hot = 0ull;
   const int nq = (nu + 3) >> 2;
+#pragma unroll 4
   for (int i = 0; i < nq; ++i) {
     const uint2 x = q[i * 32];
     const unsigned ma = __hge2_mask(*reinterpret_cast<const __half2*>(&x.x), th2);
@@ -342,6 +343,7 @@ __device__ __forceinline__ void seg_select(const Row& row, const SegShape& sh, S
   if (sh.Kg < sh.G) {
     const float gs = active ? __fadd_rn(g1, g2) : -INFINITY;
     int rank = 0;  // groups that beat mine (group i's first lane is lane i * L)
+#pragma unroll 4
     for (int i = 0; i < sh.G; ++i) {
       const float o = __shfl_sync(kFull, gs, i << sh.log2L, LT);
       rank += (o > gs || (o == gs && i < j)) ? 1 : 0;
