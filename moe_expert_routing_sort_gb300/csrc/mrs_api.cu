@@ -501,7 +501,7 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   SegShape seg{};
   const bool use_seg = make_seg_shape(E, n_group, topk_group, topk, routed_scale, 32, seg);
   seg.softmax = sh.softmax;
-  if (T <= kSmallMaxTokens &&
+  if (T <= kSmallRouteTokens &&
       small_plan(T, E, topk, block_m, false, use_seg ? seg.nu : 0, d, lay, wave, nb_max)) {
     SmallArgs a{};
     a.use_seg = use_seg;
@@ -653,7 +653,8 @@ int moe_sort(const int32_t* topk_ids, const float* topk_weights, int T, int E, i
   if (!device_info(d)) return MOE_RS_ERR_LAUNCH;
   SmallLayout lay;
   int wave = 0, nb_max = 0;
-  if (T * topk <= 2048 && small_plan(T, E, topk, block_m, true, 0, d, lay, wave, nb_max)) {
+  if (T * topk <= kSmallSortRoutes &&
+      small_plan(T, E, topk, block_m, true, 0, d, lay, wave, nb_max)) {
     SmallArgs a{};
     a.in_ids = topk_ids;
     a.in_w = topk_weights;

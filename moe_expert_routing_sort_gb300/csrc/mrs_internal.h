@@ -11,8 +11,15 @@
 
 namespace mrs {
 
-// Largest T that takes the single-CTA path (its ranks use one 64-bit token mask).
+// Largest T the single-CTA kernel can take (its ranks use one 64-bit token mask).
 constexpr int kSmallMaxTokens = 64;
+// Largest T (moe_route_sort) and T * K (moe_sort) that the dispatch gives the single-CTA
+// kernel: it routes a wave of up to 16 tokens at a time, one per warp, and ranks given routes
+// with one warp, so past these sizes the one-cluster or three-kernel paths are faster on a
+// GB300 (measured: T = 8 12.1 against 12.6 µs on the cluster, T = 64 53.7 against 13.6;
+// moe_sort, 64 routes 5.3 against 7.9, 256 routes 12.0 against 8.5).
+constexpr int kSmallRouteTokens = 8;
+constexpr int kSmallSortRoutes = 128;
 constexpr int kSmallThreads = 512;
 constexpr int kSegThreads = 512;
 constexpr int kUnitThreads = 512;

@@ -129,7 +129,9 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
 
 static_assert(sizeof(SegScratch) <= sizeof(WarpScratch), "segment scratch reuses WarpScratch");
 
-template <bool kSortOnly>
+// kSeg (route step only): route with the segment routine (a.use_seg), else the generic one;
+// one instance per routine, so that a launch fetches and holds only the code it runs.
+template <bool kSortOnly, bool kSeg>
 __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const SmallArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
     float* svals = reinterpret_cast<float*>(smem + a.lay.svals);
     WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem + a.lay.scratch);
     for (int e = tid; e < 2 * E; e += kSmallThreads) masks[e] = 0u;
-    if (a.use_seg && warp < a.wave)
+    if (kSeg && warp < a.wave)
       ub_init_pads(reinterpret_cast<unsigned short*>(smem + a.lay.umax + ub_bytes(a.seg.nu) * warp),
                    lane, a.seg.nu);
     for (int t0 = 0; t0 < a.T; t0 += a.wave) {
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
       for (int tl = warp; tl < nt; tl += kSmallThreads / 32) {
         int id;
         float w;
-        if (a.use_seg) {
+        if (kSeg) {
           unsigned short* umax = reinterpret_cast<unsigned short*>(
               smem + a.lay.umax + ub_bytes(a.seg.nu) * warp);
           const ExactKeyRow row{keys + tl * E, svals + tl * E};
@@ -287,19 +289,13 @@ SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only) {
 
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(a.lay.total);
-  cudaError_t err;
-  if (sort_only) {
-    err = cudaFuncSetAttribute(mrs_small_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(mrs_small_kernel<true>, dim3(1), dim3(kSmallThreads), smem, st, a);
-  } else {
-    err = cudaFuncSetAttribute(mrs_small_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(mrs_small_kernel<false>, dim3(1), dim3(kSmallThreads), smem, st, a);
-  }
-  return err;
+  auto* kern = sort_only ? mrs_small_kernel<true, false>
+                         : (a.use_seg ? mrs_small_kernel<false, true>
+                                      : mrs_small_kernel<false, false>);
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(kern, dim3(1), dim3(kSmallThreads), smem, st, a);
 }
 
 // --------------------------------------------------------- multi-CTA route, any shape

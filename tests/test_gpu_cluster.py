@@ -1,11 +1,11 @@
-"""The cluster paths of moe_route_sort and moe_sort: for mid-sized calls (by default 64 < T <= 256 and at
-most 512 KiB of logits, segment-shaped groups) one cluster of 16 CTAs runs the route step and
-both sort phases in a single launch, exchanging per-expert counts through distributed shared
-memory.  Every case is compared with the CPU oracle bit for bit (weights within 1e-6) and with
-the three-kernel multi-CTA path on the same inputs; the library's test hook forces the cluster
-path on (any size) or off.  moe_sort does the same from given routes (by default up to 8192
-routes).  The cluster paths touch no workspace byte beyond the status word; the tests use that to
-check which path ran.
+"""The cluster paths of moe_route_sort and moe_sort: for mid-sized calls (by default
+8 < T <= 256 and at most 512 KiB of logits, segment-shaped groups) one cluster of 16 CTAs runs
+the route step and both sort phases in a single launch, exchanging per-expert counts through
+distributed shared memory.  Every case is compared with the CPU oracle bit for bit (weights
+within 1e-6) and with the three-kernel multi-CTA path on the same inputs; the library's test
+hook forces the cluster path on (any size) or off.  moe_sort does the same from given routes
+(by default 128 to 8192 routes).  The cluster paths touch no workspace byte beyond the status
+word; the tests use that to check which path ran.
 """
 import numpy as np
 import pytest
@@ -247,7 +247,7 @@ def test_moe_sort_cluster_flags_out_of_range_ids():
 @pytest.mark.parametrize("T,K,cluster", [(129, 16, True), (512, 16, True), (513, 16, False),
                                          (2000, 4, True), (1025, 8, False)])
 def test_moe_sort_default_reach(T, K, cluster):
-    # by default up to 8192 routes (T * K); smaller calls (up to 2048 routes) take the
+    # by default up to 8192 routes (T * K); the smallest calls (up to 128 routes) take the
     # single-CTA kernel, which leaves the workspace alone too
     E, B = 896, 32
     rng = np.random.default_rng(T)

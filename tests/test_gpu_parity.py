@@ -112,7 +112,7 @@ def test_other_seeds(seed):
 
 
 # ------------------------------------------------------ ragged sizes, both paths
-@pytest.mark.parametrize("T", [1, 2, 3, 31, 32, 33, 63, 64, 65, 100, 151, 152, 153, 997])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 8, 9, 31, 32, 33, 63, 64, 65, 100, 151, 152, 153, 997])
 def test_ragged_token_counts(T):
     w, inp, ref = inputs_for("prefill_T512_E896", T=T)
     assert_matches(run_gpu(w, inp), ref, w)
@@ -133,7 +133,7 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("T", [1, 17, 64, 65, 700])
+@pytest.mark.parametrize("T", [1, 8, 17, 64, 65, 700])
 @pytest.mark.parametrize("E,G,Kg,K,B,std", SHAPES)
 def test_shapes(E, G, Kg, K, B, std, T):
     w = datagen.Workload("shape", T=T, E=E, n_group=G, topk_group=Kg, topk=K,

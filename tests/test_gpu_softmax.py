@@ -94,7 +94,7 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("T", [1, 17, 64, 65, 700, 5000])
+@pytest.mark.parametrize("T", [1, 8, 17, 64, 65, 700, 5000])
 @pytest.mark.parametrize("E,K,B", SHAPES)
 def test_shapes(E, K, B, T):
     _check(_logits(T, E, 2.0, seed=E + T), K, 1.0, B)
