@@ -470,6 +470,31 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     if (rc) return rc;
   }
 
+  if (decode_cluster_reach(T)) {
+    // a few tokens: one CTA per token on one cluster, both sort phases across the cluster
+    DecodeArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.bias = bias;
+    a.E = E;
+    a.G = n_group;
+    a.g = E / n_group;
+    a.Kg = topk_group;
+    a.K = topk;
+    a.B = block_m;
+    a.R = routed_scale;
+    a.softmax = softmax ? 1 : 0;
+    a.topk_ids = topk_ids;
+    a.topk_w = topk_weights;
+    a.sorted_ids = sorted_token_ids;
+    a.sorted_w = sorted_weights;
+    a.expert_ids = expert_ids;
+    a.npp = num_tokens_post_pad;
+    a.status = status;
+    rc = launch_status(launch_decode_cluster(a, T, stream));
+    // a rejected cluster launch enqueued nothing: the paths below take the call
+    if (rc != MOE_RS_ERR_LAUNCH) return rc;
+  }
+
   if (T == 1) {
     DecodeArgs a{};
     a.logits = static_cast<const uint16_t*>(logits_bf16);

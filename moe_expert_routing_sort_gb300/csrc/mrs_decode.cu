@@ -30,6 +30,7 @@
 // Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary --
 // the B1 (batch-one) route-sort: FP32 logits, correction bias, grouped top-k, both sort
 // phases, in one kernel.
+#include "mrs_cluster.cuh"
 #include "mrs_internal.h"
 #include "moe_route_sort.h"
 
@@ -50,6 +51,7 @@ struct DecodeSmem {
   float wbest_s[kDecodeWarps];
   alignas(16) int sel_id[kMaxTopk];
   alignas(16) float sel_s[kMaxTopk];
+  alignas(16) float sel_w[kMaxTopk];  // the token's weights (several tokens on one cluster)
   int count;
   float tau;            // selection threshold (warp 0)
   unsigned kept[2];     // kept-group masks, groups 0-31 and 32-63 (warp 0)
@@ -69,14 +71,21 @@ __host__ __device__ inline int decode_tpg(int G) {
   return t;
 }
 
+__device__ void decode_cluster_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T);
+
 // kSoftmax: softmax scoring (keys are the logits, no bias).
 // kEpt: experts per thread the code is unrolled for (>= ceil(g / TPG)); the smallest fitting
 // instance is launched, so that a launch fetches only the instructions it runs (the kernel
 // usually lands on an SM whose instruction cache has never held it).
-template <bool kSoftmax, int kEpt>
+// kMulti: T tokens (2 <= T <= 16) on one cluster of T CTAs, CTA t routing token t; the CTAs
+// then sort all T * K routes together (decode_cluster_sort).
+template <bool kSoftmax, int kEpt, bool kMulti>
 __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
   __shared__ DecodeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = kMulti ? static_cast<int>(blockIdx.x) : 0;
+  const int T = kMulti ? static_cast<int>(gridDim.x) : 1;
+  const uint16_t* logits = a.logits + static_cast<size_t>(t) * a.E;
   const int G = a.G, g = a.g, Kg = a.Kg, K = a.K, B = a.B;
   const int TPG = decode_tpg(G);
   const int P = TPG > 32 ? TPG / 32 : 1;  // partials per group
@@ -87,7 +96,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   pdl_trigger();
   // the inputs start towards L2 while the kernel ahead in the stream finishes
   if (tid < 64)
-    prefetch_l2_range(a.logits, 2 * static_cast<size_t>(a.E), tid, 64);
+    prefetch_l2_range(logits, 2 * static_cast<size_t>(a.E), tid, 64);
   else if (!kSoftmax && tid < 192)
     prefetch_l2_range(a.bias, 4 * static_cast<size_t>(a.E), tid - 64, 128);
   pdl_wait();
@@ -102,19 +111,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       if (r >= R) break;
       const int li = i + TPG * r;
       if (in_group && li < g) {
-        x[r] = a.logits[j * g + li];
+        x[r] = logits[j * g + li];
         b[r] = kSoftmax ? 0.0f : a.bias[j * g + li];
       }
     }
-    for (int p = tid; p < K * B; p += kDecodeThreads) {
-      if ((p & (B - 1)) != 0) {
-        a.sorted_ids[p] = K;  // sentinel T * K with T = 1
-        a.sorted_w[p] = 0.0f;
+    if (!kMulti) {
+      for (int p = tid; p < K * B; p += kDecodeThreads) {
+        if ((p & (B - 1)) != 0) {
+          a.sorted_ids[p] = K;  // sentinel T * K with T = 1
+          a.sorted_w[p] = 0.0f;
+        }
       }
     }
     if (tid == 0) {
-      *a.npp = K * B;
-      *a.status = 0;
+      if (!kMulti) {
+        *a.npp = K * B;
+        *a.status = 0;
+      }
       sm.count = 0;
     }
     float t1 = -INFINITY, t2 = -INFINITY;
@@ -239,7 +252,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       sm.sel_s[rk] = sm.cand_s[c];
     }
     __syncthreads();
-    if (warp != 0) return;
+    if (!kMulti && warp != 0) return;
   } else {
     // very many survivors (wide exact ties): K rounds of a block-wide maximum
     unsigned long long prev = ~0ull;
@@ -284,56 +297,165 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       prev = all;
       __syncthreads();
     }
-    if (warp != 0) return;
+    if (!kMulti && warp != 0) return;
   }
 
   // ---- warp 0: weights, outputs and the one-token sort
-  if (kSoftmax) softmax_terms(sm.sel_s, lane, K);
-  const bool mine = lane < K;
-  const int id = mine ? sm.sel_id[lane] : 0x7fffffff;
-  const float s = mine ? sm.sel_s[lane] : 0.0f;
-  float sum = 0.0f;
-  if (lane == 0) {  // slot order
-    float4 q4[kMaxTopk / 4];
-    const float4* s4 = reinterpret_cast<const float4*>(sm.sel_s);
+  if (!kMulti || warp == 0) {
+    if (kSoftmax) softmax_terms(sm.sel_s, lane, K);
+    const bool mine = lane < K;
+    const int id = mine ? sm.sel_id[lane] : 0x7fffffff;
+    const float s = mine ? sm.sel_s[lane] : 0.0f;
+    float sum = 0.0f;
+    if (lane == 0) {  // slot order
+      float4 q4[kMaxTopk / 4];
+      const float4* s4 = reinterpret_cast<const float4*>(sm.sel_s);
 #pragma unroll
-    for (int h = 0; h < kMaxTopk / 4; ++h)
-      q4[h] = (4 * h < K) ? s4[h] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int h = 0; h < kMaxTopk / 4; ++h)
+        q4[h] = (4 * h < K) ? s4[h] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-    for (int h = 0; h < kMaxTopk / 4; ++h) {
-      if (4 * h < K) sum = __fadd_rn(sum, q4[h].x);
-      if (4 * h + 1 < K) sum = __fadd_rn(sum, q4[h].y);
-      if (4 * h + 2 < K) sum = __fadd_rn(sum, q4[h].z);
-      if (4 * h + 3 < K) sum = __fadd_rn(sum, q4[h].w);
+      for (int h = 0; h < kMaxTopk / 4; ++h) {
+        if (4 * h < K) sum = __fadd_rn(sum, q4[h].x);
+        if (4 * h + 1 < K) sum = __fadd_rn(sum, q4[h].y);
+        if (4 * h + 2 < K) sum = __fadd_rn(sum, q4[h].z);
+        if (4 * h + 3 < K) sum = __fadd_rn(sum, q4[h].w);
+      }
+    }
+    sum = __shfl_sync(kFull, sum, 0);
+    const float w = __fmul_rn(__fdiv_rn(s, sum), a.R);
+    if (kMulti) {
+      if (mine) {
+        a.topk_ids[t * K + lane] = id;
+        a.topk_w[t * K + lane] = w;
+        sm.sel_w[lane] = w;
+      }
+    } else {
+      int blk = 0;  // number of selected ids below mine
+#pragma unroll
+      for (int m = 0; m < 32; ++m) blk += (__shfl_sync(kFull, id, m) < id) ? 1 : 0;
+      if (mine) {
+        a.topk_ids[lane] = id;
+        a.topk_w[lane] = w;
+        a.sorted_ids[blk * B] = lane;
+        a.sorted_w[blk * B] = w;
+        a.expert_ids[blk] = id;
+      }
     }
   }
-  sum = __shfl_sync(kFull, sum, 0);
-  const float w = __fmul_rn(__fdiv_rn(s, sum), a.R);
-  int blk = 0;  // number of selected ids below mine
-#pragma unroll
-  for (int m = 0; m < 32; ++m) blk += (__shfl_sync(kFull, id, m) < id) ? 1 : 0;
-  if (mine) {
-    a.topk_ids[lane] = id;
-    a.topk_w[lane] = w;
-    a.sorted_ids[blk * B] = lane;
-    a.sorted_w[blk * B] = w;
-    a.expert_ids[blk] = id;
-  }
+  if (kMulti) decode_cluster_sort(a, sm, t, T);
 }
 
-template <int kEpt>
-static cudaError_t launch_decode_ept(const DecodeArgs& a, cudaStream_t st) {
-  auto* kern = a.softmax ? mrs_decode_kernel<true, kEpt> : mrs_decode_kernel<false, kEpt>;
-  return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
+// Both sort phases for T tokens on one cluster (kMulti), every thread of every CTA: after a
+// cluster barrier each CTA copies all T * K selected ids from the CTAs' shared memory, counts
+// them per expert and forms the same block_m-padded prefix; its own K routes go to row
+// base(e) + (tokens before t routed to e), which is the token-then-slot order because a token
+// holds each expert at most once; CTA t writes the padding rows and block owners of experts
+// [t E / T, (t + 1) E / T), CTA 0 npp and the status word.  Dynamic shared memory:
+// decode_cluster_smem(E, T * K).
+__device__ void decode_cluster_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T) {
+  extern __shared__ __align__(16) int32_t dsm[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, K = a.K, B = a.B, N = T * K;
+  int32_t* cnt = dsm;                                  // [E]
+  int32_t* padv = cnt + E;                             // [E]
+  int32_t* base = padv + E;                            // [E + 1]
+  int32_t* all_id = base + E + 1;                      // [N]
+  int32_t* misc = all_id + ((N + 3) & ~3);             // [64]: scan
+  __syncthreads();  // warp 0's weights are in shared memory
+  cluster_arrive();
+  cluster_wait();
+  for (int e = tid; e < E; e += kDecodeThreads) cnt[e] = 0;
+  for (int i = tid; i < N; i += kDecodeThreads)
+    all_id[i] = ld_cluster_s32(&sm.sel_id[i % K], static_cast<uint32_t>(i / K));
+  // no other CTA's shared memory is read after this; the matching wait at the end keeps this
+  // CTA's alive until every CTA has read it
+  cluster_arrive();
+  __syncthreads();
+  for (int i = tid; i < N; i += kDecodeThreads) {
+    const int e = all_id[i];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kDecodeThreads) padv[e] = (cnt[e] + B - 1) & ~(B - 1);
+  __syncthreads();
+  block_exclusive_scan(padv, base, E, misc);  // base[E] = the padded total
+  if (warp == 0 && lane < K) {
+    const int e = sm.sel_id[lane];
+    int rank = 0;
+    for (int i = 0; i < t * K; ++i) rank += (all_id[i] == e) ? 1 : 0;
+    const int dst = base[e] + rank;
+    a.sorted_ids[dst] = t * K + lane;
+    a.sorted_w[dst] = sm.sel_w[lane];
+  }
+  const int e0 = static_cast<int>(static_cast<long long>(t) * E / T);
+  const int e1 = static_cast<int>(static_cast<long long>(t + 1) * E / T);
+  for (int e = e0 + warp; e < e1; e += kDecodeWarps) {
+    const int c = cnt[e];
+    if (c == 0) continue;
+    const int off = base[e];
+    const int end = off + padv[e];
+    for (int p = off + c + lane; p < end; p += 32) {
+      a.sorted_ids[p] = N;
+      a.sorted_w[p] = 0.0f;
+    }
+    for (int b = off / B + lane; b < end / B; b += 32) a.expert_ids[b] = e;
+  }
+  if (t == 0 && tid == 0) {
+    *a.npp = base[E];
+    *a.status = 0;
+  }
+  cluster_wait();
+}
+
+size_t decode_cluster_smem(int E, int N) {
+  return sizeof(int32_t) * (3 * static_cast<size_t>(E) + 1 + ((N + 3) & ~3) + 64);
+}
+
+template <int kEpt, bool kMulti>
+static cudaError_t launch_decode_ept(const DecodeArgs& a, int T, cudaStream_t st) {
+  auto* kern = a.softmax ? mrs_decode_kernel<true, kEpt, kMulti>
+                         : mrs_decode_kernel<false, kEpt, kMulti>;
+  if (!kMulti) return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
+  const size_t smem = decode_cluster_smem(a.E, T * a.K);
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = T;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <bool kMulti>
+static cudaError_t launch_decode_any(const DecodeArgs& a, int T, cudaStream_t st) {
+  const int tpg = decode_tpg(a.G);
+  const int r = (a.g + tpg - 1) / tpg;  // <= kDecodeEpt (g <= 4096 / G < 16 * TPG)
+  if (r <= 2) return launch_decode_ept<2, kMulti>(a, T, st);
+  if (r <= 4) return launch_decode_ept<4, kMulti>(a, T, st);
+  if (r <= 8) return launch_decode_ept<8, kMulti>(a, T, st);
+  return launch_decode_ept<kDecodeEpt, kMulti>(a, T, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  const int tpg = decode_tpg(a.G);
-  const int r = (a.g + tpg - 1) / tpg;  // <= kDecodeEpt (g <= 4096 / G < 16 * TPG)
-  if (r <= 2) return launch_decode_ept<2>(a, st);
-  if (r <= 4) return launch_decode_ept<4>(a, st);
-  if (r <= 8) return launch_decode_ept<8>(a, st);
-  return launch_decode_ept<kDecodeEpt>(a, st);
+  return launch_decode_any<false>(a, 1, st);
+}
+
+cudaError_t launch_decode_cluster(const DecodeArgs& a, int T, cudaStream_t st) {
+  if (T < 2 || T > kDecodeClusterTokens) return cudaErrorInvalidValue;
+  return launch_decode_any<true>(a, T, st);
 }
 
 }  // namespace mrs

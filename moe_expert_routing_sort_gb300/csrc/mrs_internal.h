@@ -270,6 +270,13 @@ struct GatePlan {
 };
 GatePlan gate_plan(int E, int sms);
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
+// One cluster of T CTAs (2 <= T <= kDecodeClusterTokens), one token each, then both sort phases
+// across the cluster.  Taken by default from kDecodeClusterMinTokens on: a cluster launch costs
+// several microseconds more than a plain one on a GB300, which the single-CTA kernel does not
+// pay for two or three tokens.
+constexpr int kDecodeClusterTokens = 16;
+constexpr int kDecodeClusterMinTokens = 4;
+cudaError_t launch_decode_cluster(const DecodeArgs& a, int T, cudaStream_t st);
 
 // ------------------------------------------------------------ per-context host state
 // Test hooks set through moe_route_sort_debug_set (process-wide).
@@ -280,6 +287,10 @@ unsigned long long debug_wait_limit_ns();  // kWaitLimitNs unless lowered
 bool cluster_reach(int T, int E, int K, int B);
 // The same for moe_sort.
 bool cluster_reach_sort(int T, int E, int K, int B);
+// Whether the few-token cluster path takes T tokens: kDecodeClusterMinTokens <= T <=
+// kDecodeClusterTokens by default, 2 <= T <= min(kDecodeClusterTokens, limit) once a test hook
+// has set a token limit.
+bool decode_cluster_reach(int T);
 // Identity of the current device and context (the context's unique id, 0 if the driver cannot
 // tell): host caches of device addresses are keyed on it.
 bool current_context(int& dev, unsigned long long& ctx_id);

@@ -124,6 +124,12 @@ bool cluster_reach(int T, int E, int K, int B) {
          padded_rows(T, E, K, B) <= kClusterMaxPadded;
 }
 
+bool decode_cluster_reach(int T) {
+  const int v = g_cluster_tokens.load(std::memory_order_relaxed);
+  if (T < 2 || T > kDecodeClusterTokens) return false;
+  return v < 0 ? T >= kDecodeClusterMinTokens : T <= v;
+}
+
 bool cluster_reach_sort(int T, int E, int K, int B) {
   const int v = g_cluster_tokens.load(std::memory_order_relaxed);
   if (v >= 0) return T <= v;

@@ -258,3 +258,52 @@ def test_moe_sort_default_reach(T, K, cluster):
     assert touched != cluster
     npp = int(out.num_tokens_post_pad.item())
     assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)
+
+
+# ------------------------------------------------- a few tokens: one CTA each, one cluster
+@pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 15, 16])
+@pytest.mark.parametrize("E,G,Kg,K,B", [(896, 8, 4, 16, 32), (896, 1, 1, 16, 32),
+                                         (4096, 16, 4, 8, 128), (64, 8, 4, 6, 16),
+                                         (129, 3, 2, 5, 16), (4000, 5, 2, 8, 32)])
+def test_few_tokens_on_one_cluster(T, E, G, Kg, K, B):
+    w, inp, ref = _case("decode_T1_E896_G8", T, E=E, n_group=G, topk_group=Kg, topk=K,
+                        block_m=B, seed=E + T)
+    a, _ = _run(w, inp, FORCE)  # one CTA per token on a cluster (2 <= T <= 16)
+    _assert_matches(a, ref, w)
+    b, _ = _run(w, inp, 0)    # single-CTA kernel (T <= 8) or the three-kernel path
+    _assert_matches(b, ref, w)
+    npp = int(a.num_tokens_post_pad.item())
+    assert torch.equal(a.sorted_token_ids[:npp], b.sorted_token_ids[:npp])
+
+
+@pytest.mark.parametrize("T", [2, 7, 16])
+def test_few_tokens_exact_ties(T):
+    # every logit equal: many survivors per token (the kernel's fallback ranking)
+    w = datagen.workload("decode_T1_E896_G8", T=T)
+    logits = np.full((T, 896), datagen.float32_to_bf16_bits(np.float32([0.75]))[0], np.uint16)
+    bias = np.zeros(896, np.float32)
+    bias[::7] = 0.03125
+    inp = datagen.RouterInputs(w, logits, bias)
+    ref = oracle.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                            w.block_m)
+    out, _ = _run(w, inp, FORCE)
+    _assert_matches(out, ref, w)
+
+
+@pytest.mark.parametrize("T", [4, 9, 16])
+def test_few_tokens_softmax(T):
+    w = datagen.workload("prefill_T512_E896", T=T, n_group=1, topk_group=1, topk=8)
+    inp = datagen.make_inputs(w)
+    ref = oracle.route_sort_softmax(inp.logits_bf16, w.topk, w.routed_scale, w.block_m)
+    logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    mrs.route_sort_softmax(logits, w.topk, w.routed_scale, w.block_m, out=out)
+    torch.cuda.synchronize()
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref["num_tokens_post_pad"]
+    assert np.array_equal(out.topk_ids.cpu().numpy(), ref["topk_ids"])
+    assert np.max(np.abs(out.topk_weights.cpu().numpy() - ref["topk_weights"]),
+                  initial=0.0) <= WEIGHT_ATOL
+    assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref["sorted_token_ids"])
+    assert np.array_equal(out.expert_ids[: npp // w.block_m].cpu().numpy(), ref["expert_ids"])
+    assert out.status_word() == 0
