@@ -311,19 +311,24 @@ int moe_route_sort_proxy_state(int32_t* dst, cudaStream_t stream);
  *   MOE_RS_DEBUG_CLUSTER_TOKENS    largest T that moe_route_sort and moe_route_sort_softmax run
  *                                  as one thread-block cluster (route step and both sort
  *                                  phases in one launch) instead of the three-kernel multi-CTA
- *                                  path, and moe_sort likewise, whatever the sizes (calls of 2
- *                                  to 16 tokens: one CTA per token on one cluster); 0 turns the
- *                                  cluster paths off, a negative value restores the default
- *                                  reach (moe_route_sort: 4 <= T <= 16 on the per-token
- *                                  cluster, else T <= 256 and at most 512 KiB of logits for
- *                                  shapes the segment route kernel takes; moe_sort: at most
- *                                  8192 routes; both: a worst-case padded length of at most
- *                                  65536 rows).  Both paths give the same outputs; the hook
- *                                  lets tests compare them on one shape.
+ *                                  path, and moe_sort likewise, whatever the sizes; 0 turns
+ *                                  the cluster paths off, a negative value restores the
+ *                                  default reach (moe_route_sort: T <= 256 and at most 512 KiB
+ *                                  of logits, for shapes the segment route kernel takes;
+ *                                  moe_sort: at most 8192 routes; both: a worst-case padded
+ *                                  length of at most 65536 rows).
+ *   MOE_RS_DEBUG_GRID_TOKENS       largest T that moe_route_sort and moe_route_sort_softmax run
+ *                                  on a cooperative grid with one CTA per token (taken before
+ *                                  every other multi-token path; 2 <= T <= min(128, value));
+ *                                  0 turns it off, a negative value restores the default
+ *                                  (4 <= T <= 128).
+ *                                  The paths give the same outputs; these hooks let tests
+ *                                  compare them on one shape.
  * Returns MOE_RS_OK or MOE_RS_ERR_BAD_DEBUG_KNOB. */
 #define MOE_RS_DEBUG_WAIT_LIMIT_NS 1
 #define MOE_RS_DEBUG_FORCE_PROXY_FAIL 2
 #define MOE_RS_DEBUG_CLUSTER_TOKENS 3
+#define MOE_RS_DEBUG_GRID_TOKENS 4
 int moe_route_sort_debug_set(int knob, long long value);
 
 #ifdef __cplusplus

@@ -9,6 +9,7 @@ from ._build import build  # noqa: F401
 from .binding import (  # noqa: F401
     DEBUG_CLUSTER_TOKENS,
     DEBUG_FORCE_PROXY_FAIL,
+    DEBUG_GRID_TOKENS,
     DEBUG_WAIT_LIMIT_NS,
     DEVICE_BAD_EXPERT_ID,
     RouteSortBuffers,

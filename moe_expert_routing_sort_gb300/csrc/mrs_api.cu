@@ -470,9 +470,13 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     if (rc) return rc;
   }
 
-  if (decode_cluster_reach(T)) {
-    // a few tokens: one CTA per token on one cluster, both sort phases across the cluster
+  DeviceInfo dg;
+  if (decode_grid_reach(T) && device_info(dg) && T <= dg.sms) {
+    // a few tokens: one CTA per token on a cooperative grid, both sort phases across the grid
     DecodeArgs a{};
+    a.xchg = reinterpret_cast<int32_t*>(ws + l.unit_buf);  // T * K int32 fit in [T * K] int2
+    a.bar = reinterpret_cast<unsigned*>(ws + l.status + 8);
+    a.wait_limit_ns = debug_wait_limit_ns();
     a.logits = static_cast<const uint16_t*>(logits_bf16);
     a.bias = bias;
     a.E = E;
@@ -490,8 +494,9 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     a.expert_ids = expert_ids;
     a.npp = num_tokens_post_pad;
     a.status = status;
-    rc = launch_status(launch_decode_cluster(a, T, stream));
-    // a rejected cluster launch enqueued nothing: the paths below take the call
+    rc = launch_status(launch_decode_grid(a, T, stream));
+    // a rejected launch (more CTAs than the device holds at once) enqueued nothing: the paths
+    // below take the call
     if (rc != MOE_RS_ERR_LAUNCH) return rc;
   }
 

@@ -30,8 +30,8 @@
 // Source: "perf(flydsl): Kimi-K3 B1 route-sort + prepared-MoE handoff (stack)", Summary --
 // the B1 (batch-one) route-sort: FP32 logits, correction bias, grouped top-k, both sort
 // phases, in one kernel.
-#include "mrs_cluster.cuh"
 #include "mrs_internal.h"
+#include "mrs_unit.cuh"
 #include "moe_route_sort.h"
 
 namespace mrs {
@@ -71,14 +71,46 @@ __host__ __device__ inline int decode_tpg(int G) {
   return t;
 }
 
-__device__ void decode_cluster_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T);
+__device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T);
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a cooperative launch over the word at bar (zeroed by
+// mrs_grid_prep_kernel ahead of this call): thread 0 of each CTA publishes the CTA's earlier
+// writes and arrives, then waits, at most limit_ns (0: not at all, a test hook), until all n
+// CTAs have arrived.  Every thread of the CTA calls this; returns false on a timeout.
+__device__ bool grid_barrier_bounded(unsigned* bar, unsigned n, unsigned long long limit_ns) {
+  __shared__ int ok_s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    bool ok = limit_ns != 0ull;
+    if (ok) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (ld_acquire_u32(bar) < n) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    ok_s = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
 
 // kSoftmax: softmax scoring (keys are the logits, no bias).
 // kEpt: experts per thread the code is unrolled for (>= ceil(g / TPG)); the smallest fitting
 // instance is launched, so that a launch fetches only the instructions it runs (the kernel
 // usually lands on an SM whose instruction cache has never held it).
-// kMulti: T tokens (2 <= T <= 16) on one cluster of T CTAs, CTA t routing token t; the CTAs
-// then sort all T * K routes together (decode_cluster_sort).
+// kMulti: T tokens (2 <= T <= kDecodeGridTokens) on a cooperative grid of T CTAs, CTA t routing
+// token t; the CTAs then sort all T * K routes together (decode_grid_sort).
 template <bool kSoftmax, int kEpt, bool kMulti>
 __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
   __shared__ DecodeSmem sm;
@@ -327,6 +359,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       if (mine) {
         a.topk_ids[t * K + lane] = id;
         a.topk_w[t * K + lane] = w;
+        a.xchg[t * K + lane] = id;
         sm.sel_w[lane] = w;
       }
     } else {
@@ -342,38 +375,43 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       }
     }
   }
-  if (kMulti) decode_cluster_sort(a, sm, t, T);
+  if (kMulti) decode_grid_sort(a, sm, t, T);
 }
 
-// Both sort phases for T tokens on one cluster (kMulti), every thread of every CTA: after a
-// cluster barrier each CTA copies all T * K selected ids from the CTAs' shared memory, counts
-// them per expert and forms the same block_m-padded prefix; its own K routes go to row
-// base(e) + (tokens before t routed to e), which is the token-then-slot order because a token
-// holds each expert at most once; CTA t writes the padding rows and block owners of experts
-// [t E / T, (t + 1) E / T), CTA 0 npp and the status word.  Dynamic shared memory:
-// decode_cluster_smem(E, T * K).
-__device__ void decode_cluster_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T) {
+// Both sort phases for T tokens on a cooperative grid (kMulti), every thread of every CTA:
+// after a grid-wide barrier (bounded; on a timeout the CTA reports MOE_RS_DEVICE_WAIT_TIMEOUT
+// and writes nothing more) each CTA reads all T * K selected ids from the exchange buffer,
+// counts them per expert (with a token bit mask per expert) and forms the same block_m-padded
+// prefix; its own K routes go to row base(e) + (tokens before t routed to e), which is the
+// token-then-slot order because a token holds each expert at most once; CTA t writes the padding
+// rows and block owners of experts [t E / T, (t + 1) E / T), CTA 0 npp (the status word is
+// zeroed by mrs_grid_prep_kernel and only ever ORed here).  Dynamic shared memory:
+// decode_grid_smem(E, T).
+__device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T) {
   extern __shared__ __align__(16) int32_t dsm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, K = a.K, B = a.B, N = T * K;
+  const int W = (T + 31) >> 5;                         // token mask words per expert
   int32_t* cnt = dsm;                                  // [E]
   int32_t* padv = cnt + E;                             // [E]
   int32_t* base = padv + E;                            // [E + 1]
-  int32_t* all_id = base + E + 1;                      // [N]
-  int32_t* misc = all_id + ((N + 3) & ~3);             // [64]: scan
-  __syncthreads();  // warp 0's weights are in shared memory
-  cluster_arrive();
-  cluster_wait();
+  unsigned* tmask = reinterpret_cast<unsigned*>(base + E + 1);  // [E][W]
+  int32_t* misc = reinterpret_cast<int32_t*>(tmask + static_cast<size_t>(E) * W);  // [64]
   for (int e = tid; e < E; e += kDecodeThreads) cnt[e] = 0;
-  for (int i = tid; i < N; i += kDecodeThreads)
-    all_id[i] = ld_cluster_s32(&sm.sel_id[i % K], static_cast<uint32_t>(i / K));
-  // no other CTA's shared memory is read after this; the matching wait at the end keeps this
-  // CTA's alive until every CTA has read it
-  cluster_arrive();
-  __syncthreads();
+  for (int i = tid; i < E * W; i += kDecodeThreads) tmask[i] = 0u;
+  // every CTA's ids are in the exchange buffer once the whole grid has arrived (the barrier
+  // orders the writes before it with the reads after it)
+  if (!grid_barrier_bounded(a.bar, static_cast<unsigned>(T), a.wait_limit_ns)) {
+    if (tid == 0) atomicOr(a.status, MOE_RS_DEVICE_WAIT_TIMEOUT);
+    return;
+  }
   for (int i = tid; i < N; i += kDecodeThreads) {
-    const int e = all_id[i];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    const int e = __ldcg(a.xchg + i);
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[e], 1);
+      const int tt = i / K;
+      atomicOr(&tmask[e * W + (tt >> 5)], 1u << (tt & 31));
+    }
   }
   __syncthreads();
   for (int e = tid; e < E; e += kDecodeThreads) padv[e] = (cnt[e] + B - 1) & ~(B - 1);
@@ -381,8 +419,9 @@ __device__ void decode_cluster_sort(const DecodeArgs& a, const DecodeSmem& sm, i
   block_exclusive_scan(padv, base, E, misc);  // base[E] = the padded total
   if (warp == 0 && lane < K) {
     const int e = sm.sel_id[lane];
-    int rank = 0;
-    for (int i = 0; i < t * K; ++i) rank += (all_id[i] == e) ? 1 : 0;
+    const unsigned* m = tmask + e * W;
+    int rank = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int w = 0; w < (t >> 5); ++w) rank += __popc(m[w]);
     const int dst = base[e] + rank;
     a.sorted_ids[dst] = t * K + lane;
     a.sorted_w[dst] = sm.sel_w[lane];
@@ -400,15 +439,21 @@ __device__ void decode_cluster_sort(const DecodeArgs& a, const DecodeSmem& sm, i
     }
     for (int b = off / B + lane; b < end / B; b += 32) a.expert_ids[b] = e;
   }
-  if (t == 0 && tid == 0) {
-    *a.npp = base[E];
-    *a.status = 0;
-  }
-  cluster_wait();
+  if (t == 0 && tid == 0) *a.npp = base[E];
 }
 
-size_t decode_cluster_smem(int E, int N) {
-  return sizeof(int32_t) * (3 * static_cast<size_t>(E) + 1 + ((N + 3) & ~3) + 64);
+// Ahead of a grid-path call: zero its barrier word and status word, once the kernel ahead in the
+// stream (possibly the previous grid-path call on the same workspace) has completed.
+__global__ void mrs_grid_prep_kernel(unsigned* bar, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
+  *bar = 0u;
+  *status = 0;
+}
+
+size_t decode_grid_smem(int E, int T) {
+  const size_t W = static_cast<size_t>(T + 31) / 32;
+  return sizeof(int32_t) * (3 * static_cast<size_t>(E) + 1 + W * E + 64);
 }
 
 template <int kEpt, bool kMulti>
@@ -416,12 +461,12 @@ static cudaError_t launch_decode_ept(const DecodeArgs& a, int T, cudaStream_t st
   auto* kern = a.softmax ? mrs_decode_kernel<true, kEpt, kMulti>
                          : mrs_decode_kernel<false, kEpt, kMulti>;
   if (!kMulti) return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
-  const size_t smem = decode_cluster_smem(a.E, T * a.K);
+  const size_t smem = decode_grid_smem(a.E, T);
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (err != cudaSuccess) return err;
+  // a cooperative launch: all T CTAs are resident together (the launch fails otherwise), which
+  // the grid-wide barrier needs
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(T);
   cfg.blockDim = dim3(kDecodeThreads);
@@ -430,10 +475,8 @@ static cudaError_t launch_decode_ept(const DecodeArgs& a, int T, cudaStream_t st
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = T;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a);
@@ -453,8 +496,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   return launch_decode_any<false>(a, 1, st);
 }
 
-cudaError_t launch_decode_cluster(const DecodeArgs& a, int T, cudaStream_t st) {
-  if (T < 2 || T > kDecodeClusterTokens) return cudaErrorInvalidValue;
+cudaError_t launch_decode_grid(const DecodeArgs& a, int T, cudaStream_t st) {
+  if (T < 2 || T > kDecodeGridTokens || a.xchg == nullptr || a.bar == nullptr)
+    return cudaErrorInvalidValue;
+  cudaError_t err = launch_pdl(mrs_grid_prep_kernel, dim3(1), dim3(1), 0, st, a.bar, a.status);
+  if (err != cudaSuccess) return err;
   return launch_decode_any<true>(a, T, st);
 }
 

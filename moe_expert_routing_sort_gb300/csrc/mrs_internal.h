@@ -57,7 +57,7 @@ inline int slices_for(int U, int E) {
 
 // Workspace layout (byte offsets), identical for every call with the same (T, E, K).
 struct WsLayout {
-  size_t status;       // int32
+  size_t status;       // int32 (bytes 8..11: the grid barrier word of the few-token path)
   size_t unit_flags;   // int32[U]
   size_t slice_flags;  // uint64[slices]  look-back words of the slice kernel
   size_t loc_off;      // int32[U][E + 1] per-unit exclusive offsets of each expert
@@ -121,6 +121,9 @@ struct SmallArgs {
 
 // ------------------------------------------------------------- one token (decode)
 struct DecodeArgs {
+  int32_t* xchg;  // several tokens on a grid: T * K selected ids exchanged through global memory
+  unsigned* bar;  // several tokens on a grid: the grid barrier's word (zeroed ahead of the call)
+  unsigned long long wait_limit_ns;  // several tokens: bound of the grid barrier's wait
   const uint16_t* logits;
   const float* bias;
   int E, G, g, Kg, K, B;
@@ -270,13 +273,15 @@ struct GatePlan {
 };
 GatePlan gate_plan(int E, int sms);
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
-// One cluster of T CTAs (2 <= T <= kDecodeClusterTokens), one token each, then both sort phases
-// across the cluster.  Taken by default from kDecodeClusterMinTokens on: a cluster launch costs
-// several microseconds more than a plain one on a GB300, which the single-CTA kernel does not
-// pay for two or three tokens.
-constexpr int kDecodeClusterTokens = 16;
-constexpr int kDecodeClusterMinTokens = 4;
-cudaError_t launch_decode_cluster(const DecodeArgs& a, int T, cudaStream_t st);
+// A cooperative grid of T CTAs (2 <= T <= kDecodeGridTokens and no more than the device can
+// hold at once, one CTA per SM), one token each, then both sort phases across the grid through
+// a.xchg (T * K int32 of the workspace) and one bounded grid-wide barrier on a.bar; a one-thread
+// kernel ahead of it zeroes a.bar and the status word.
+constexpr int kDecodeGridTokens = 128;
+// Default lower end of that path: for two or three tokens the single-CTA kernel is faster
+// (measured: T = 2 7.7 against 9.8 us per call).
+constexpr int kDecodeGridMinTokens = 4;
+cudaError_t launch_decode_grid(const DecodeArgs& a, int T, cudaStream_t st);
 
 // ------------------------------------------------------------ per-context host state
 // Test hooks set through moe_route_sort_debug_set (process-wide).
@@ -287,10 +292,10 @@ unsigned long long debug_wait_limit_ns();  // kWaitLimitNs unless lowered
 bool cluster_reach(int T, int E, int K, int B);
 // The same for moe_sort.
 bool cluster_reach_sort(int T, int E, int K, int B);
-// Whether the few-token cluster path takes T tokens: kDecodeClusterMinTokens <= T <=
-// kDecodeClusterTokens by default, 2 <= T <= min(kDecodeClusterTokens, limit) once a test hook
+// Whether the few-token grid path takes T tokens: kDecodeGridMinTokens <= T <=
+// kDecodeGridTokens by default, 2 <= T <= min(kDecodeGridTokens, limit) once the grid test hook
 // has set a token limit.
-bool decode_cluster_reach(int T);
+bool decode_grid_reach(int T);
 // Identity of the current device and context (the context's unique id, 0 if the driver cannot
 // tell): host caches of device addresses are keyed on it.
 bool current_context(int& dev, unsigned long long& ctx_id);

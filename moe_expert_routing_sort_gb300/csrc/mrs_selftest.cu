@@ -62,6 +62,7 @@ namespace {
 
 std::atomic<long long> g_wait_limit{-1};   // < 0: kWaitLimitNs
 std::atomic<int> g_cluster_tokens{-1};     // < 0: the default reach
+std::atomic<int> g_grid_tokens{-1};        // < 0: kDecodeGridTokens
 std::atomic<int> g_force_proxy_fail{0};
 std::atomic<int> g_proxy_generation{1};    // bumped when the forced failure changes
 
@@ -124,10 +125,10 @@ bool cluster_reach(int T, int E, int K, int B) {
          padded_rows(T, E, K, B) <= kClusterMaxPadded;
 }
 
-bool decode_cluster_reach(int T) {
-  const int v = g_cluster_tokens.load(std::memory_order_relaxed);
-  if (T < 2 || T > kDecodeClusterTokens) return false;
-  return v < 0 ? T >= kDecodeClusterMinTokens : T <= v;
+bool decode_grid_reach(int T) {
+  const int v = g_grid_tokens.load(std::memory_order_relaxed);
+  if (T < 2 || T > kDecodeGridTokens) return false;
+  return v < 0 ? T >= kDecodeGridMinTokens : T <= v;
 }
 
 bool cluster_reach_sort(int T, int E, int K, int B) {
@@ -224,9 +225,11 @@ extern "C" int moe_route_sort_debug_set(int knob, long long value) {
       if (mrs::g_force_proxy_fail.exchange(v) != v) mrs::g_proxy_generation.fetch_add(1);
       return MOE_RS_OK;
     }
-    case MOE_RS_DEBUG_CLUSTER_TOKENS: {
+    case MOE_RS_DEBUG_CLUSTER_TOKENS:
+    case MOE_RS_DEBUG_GRID_TOKENS: {
       const long long v = value < 0 ? -1 : (value > (1ll << 30) ? (1ll << 30) : value);
-      mrs::g_cluster_tokens.store(static_cast<int>(v));
+      (knob == MOE_RS_DEBUG_GRID_TOKENS ? mrs::g_grid_tokens : mrs::g_cluster_tokens)
+          .store(static_cast<int>(v));
       return MOE_RS_OK;
     }
     default:

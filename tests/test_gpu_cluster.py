@@ -1,11 +1,13 @@
-"""The cluster paths of moe_route_sort and moe_sort: for mid-sized calls (by default
-8 < T <= 256 and at most 512 KiB of logits, segment-shaped groups) one cluster of 16 CTAs runs
-the route step and both sort phases in a single launch, exchanging per-expert counts through
-distributed shared memory.  Every case is compared with the CPU oracle bit for bit (weights
-within 1e-6) and with the three-kernel multi-CTA path on the same inputs; the library's test
-hook forces the cluster path on (any size) or off.  moe_sort does the same from given routes
-(by default 128 to 8192 routes).  The cluster paths touch no workspace byte beyond the status
-word; the tests use that to check which path ran.
+"""The one-launch paths of moe_route_sort and moe_sort.  Calls of 4 to 128 tokens (2 to 128
+with the test hook) run on a cooperative grid, one CTA per token, with a grid-wide exchange of
+the selected ids.  For mid-sized calls (by default up to 256 tokens and at most 512 KiB of
+logits, segment-shaped groups; the per-token grid is switched off in those tests) one cluster of
+16 CTAs runs the route step and both sort phases in a single launch, exchanging per-expert
+counts through distributed shared memory.  Every case is compared with the CPU oracle bit for
+bit (weights within 1e-6) and with the three-kernel multi-CTA path on the same inputs; the
+library's test hooks force the paths on (any size) or off.  moe_sort does the same from given
+routes on one cluster (by default 128 to 8192 routes).  The cluster paths touch no workspace
+byte beyond the status word; the tests use that to check which path ran.
 """
 import numpy as np
 import pytest
@@ -31,6 +33,7 @@ def _built():
     mrs.load()
     yield
     mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, -1)
 
 
 def _case(name, T, seed=0, **over):
@@ -41,9 +44,10 @@ def _case(name, T, seed=0, **over):
     return w, inp, ref
 
 
-def _run(w, inp, cluster_tokens):
-    """One call with the cluster path limited to T <= cluster_tokens; returns the buffers and
-    whether any workspace byte past the status word changed."""
+def _run(w, inp, cluster_tokens, grid=0):
+    """One call with the cluster paths limited to T <= cluster_tokens and the per-token grid path
+    to T <= grid (off unless given); returns the buffers and whether any workspace byte past the
+    status word changed."""
     logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
     bias = torch.from_numpy(inp.bias).to(DEV)
     out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
@@ -51,12 +55,14 @@ def _run(w, inp, cluster_tokens):
     out.sorted_token_ids.fill_(-7)
     out.expert_ids.fill_(-7)
     mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, cluster_tokens)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, grid)
     try:
         mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
                        w.block_m, out=out)
         torch.cuda.synchronize()
     finally:
         mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, -1)
     touched = bool(torch.any(out.workspace[16:] != POISON).item())
     return out, touched
 
@@ -167,11 +173,13 @@ def test_softmax_scoring_on_the_cluster_path():
         out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
         out.workspace.fill_(POISON)
         mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, limit)
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, 0)
         try:
             mrs.route_sort_softmax(logits, w.topk, w.routed_scale, w.block_m, out=out)
             torch.cuda.synchronize()
         finally:
             mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
+            mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, -1)
         assert bool(torch.any(out.workspace[16:] != POISON).item()) == (limit == 0)
         npp = int(out.num_tokens_post_pad.item())
         assert npp == ref["num_tokens_post_pad"]
@@ -260,17 +268,17 @@ def test_moe_sort_default_reach(T, K, cluster):
     assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref.sorted_token_ids)
 
 
-# ------------------------------------------------- a few tokens: one CTA each, one cluster
-@pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 15, 16])
+# ----------------------------------------- a few tokens: one CTA each, a cooperative grid
+@pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 15, 16, 33, 64, 127, 128])
 @pytest.mark.parametrize("E,G,Kg,K,B", [(896, 8, 4, 16, 32), (896, 1, 1, 16, 32),
                                          (4096, 16, 4, 8, 128), (64, 8, 4, 6, 16),
                                          (129, 3, 2, 5, 16), (4000, 5, 2, 8, 32)])
 def test_few_tokens_on_one_cluster(T, E, G, Kg, K, B):
     w, inp, ref = _case("decode_T1_E896_G8", T, E=E, n_group=G, topk_group=Kg, topk=K,
                         block_m=B, seed=E + T)
-    a, _ = _run(w, inp, FORCE)  # one CTA per token on a cluster (2 <= T <= 16)
+    a, _ = _run(w, inp, -1, grid=FORCE)  # one CTA per token on a cooperative grid
     _assert_matches(a, ref, w)
-    b, _ = _run(w, inp, 0)    # single-CTA kernel (T <= 8) or the three-kernel path
+    b, _ = _run(w, inp, 0)            # single-CTA kernel (T <= 8) or the three-kernel path
     _assert_matches(b, ref, w)
     npp = int(a.num_tokens_post_pad.item())
     assert torch.equal(a.sorted_token_ids[:npp], b.sorted_token_ids[:npp])
@@ -286,11 +294,11 @@ def test_few_tokens_exact_ties(T):
     inp = datagen.RouterInputs(w, logits, bias)
     ref = oracle.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
                             w.block_m)
-    out, _ = _run(w, inp, FORCE)
+    out, _ = _run(w, inp, -1, grid=FORCE)
     _assert_matches(out, ref, w)
 
 
-@pytest.mark.parametrize("T", [4, 9, 16])
+@pytest.mark.parametrize("T", [2, 9, 100])
 def test_few_tokens_softmax(T):
     w = datagen.workload("prefill_T512_E896", T=T, n_group=1, topk_group=1, topk=8)
     inp = datagen.make_inputs(w)
