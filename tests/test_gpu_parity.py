@@ -308,8 +308,11 @@ def test_moe_sort_flags_out_of_range_ids(T):
 
 
 # ------------------------------------------------------------------ CUDA graphs
-@pytest.mark.parametrize("name,T", [("decode_T1_E896_G8", None), ("prefill_T512_E896", None),
-                                    ("skewed_T8192_E896", 2048)])
+# every dispatch: one token, the single-CTA kernel, the per-token grid, the 16-CTA cluster and
+# the three-kernel path
+@pytest.mark.parametrize("name,T", [("decode_T1_E896_G8", None), ("prefill_T512_E896", 3),
+                                    ("prefill_T512_E896", 40), ("prefill_T512_E896", 200),
+                                    ("prefill_T512_E896", None), ("skewed_T8192_E896", 2048)])
 def test_graph_replay_with_changed_inputs(name, T):
     w, inp, _ = inputs_for(name, T=T)
     logits = to_dev_bf16(inp.logits_bf16)
