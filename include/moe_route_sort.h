@@ -319,9 +319,9 @@ int moe_route_sort_proxy_state(int32_t* dst, cudaStream_t stream);
  *                                  length of at most 65536 rows).
  *   MOE_RS_DEBUG_GRID_TOKENS       largest T that moe_route_sort and moe_route_sort_softmax run
  *                                  on a cooperative grid with one CTA per token (taken before
- *                                  every other multi-token path; 2 <= T <= min(128, value));
+ *                                  every other multi-token path; 2 <= T <= min(320, value));
  *                                  0 turns it off, a negative value restores the default
- *                                  (4 <= T <= 128).
+ *                                  (4 <= T <= 320, when the grid's shared memory fits).
  *                                  The paths give the same outputs; these hooks let tests
  *                                  compare them on one shape.
  * Returns MOE_RS_OK or MOE_RS_ERR_BAD_DEBUG_KNOB. */

@@ -471,7 +471,8 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
   }
 
   DeviceInfo dg;
-  if (decode_grid_reach(T) && device_info(dg) && T <= dg.sms) {
+  if (decode_grid_reach(T) && device_info(dg) &&
+      decode_grid_smem(E, T, topk) <= static_cast<size_t>(dg.smem_optin)) {
     // a few tokens: one CTA per token on a cooperative grid, both sort phases across the grid
     DecodeArgs a{};
     a.xchg = reinterpret_cast<int32_t*>(ws + l.unit_buf);  // T * K int32 fit in [T * K] int2
@@ -494,7 +495,8 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     a.expert_ids = expert_ids;
     a.npp = num_tokens_post_pad;
     a.status = status;
-    rc = launch_status(launch_decode_grid(a, T, stream));
+    a.T = T;
+    rc = launch_status(launch_decode_grid(a, T < dg.sms ? T : dg.sms, stream));
     // a rejected launch (more CTAs than the device holds at once) enqueued nothing: the paths
     // below take the call
     if (rc != MOE_RS_ERR_LAUNCH) return rc;

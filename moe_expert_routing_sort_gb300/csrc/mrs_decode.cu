@@ -41,6 +41,8 @@ constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kDecodeEpt = 16;   // experts per thread, at most (g <= TPG * kDecodeEpt)
 constexpr int kDecodeCap = 128;  // survivors kept for ranking
 constexpr int kDecodeSamples = kDecodeThreads / 8;
+// Tokens one CTA of the grid path routes at most: ceil(kDecodeGridTokens / 152 SMs) with room.
+constexpr int kDecodeGridOwn = 4;
 
 struct DecodeSmem {
   float samp1[kDecodeSamples], samp2[kDecodeSamples];  // 8-thread segments' top-2
@@ -51,7 +53,7 @@ struct DecodeSmem {
   float wbest_s[kDecodeWarps];
   alignas(16) int sel_id[kMaxTopk];
   alignas(16) float sel_s[kMaxTopk];
-  alignas(16) float sel_w[kMaxTopk];  // the token's weights (several tokens on one cluster)
+  alignas(16) float own_w[kDecodeGridOwn][kMaxTopk];  // several tokens: this CTA's weights
   int count;
   float tau;            // selection threshold (warp 0)
   unsigned kept[2];     // kept-group masks, groups 0-31 and 32-63 (warp 0)
@@ -71,7 +73,7 @@ __host__ __device__ inline int decode_tpg(int G) {
   return t;
 }
 
-__device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T);
+__device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int T);
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
@@ -109,14 +111,11 @@ __device__ bool grid_barrier_bounded(unsigned* bar, unsigned n, unsigned long lo
 // kEpt: experts per thread the code is unrolled for (>= ceil(g / TPG)); the smallest fitting
 // instance is launched, so that a launch fetches only the instructions it runs (the kernel
 // usually lands on an SM whose instruction cache has never held it).
-// kMulti: T tokens (2 <= T <= kDecodeGridTokens) on a cooperative grid of T CTAs, CTA t routing
-// token t; the CTAs then sort all T * K routes together (decode_grid_sort).
+// The route step of token t by the whole CTA (and, with one token, both sort phases).
+// kMulti: one of several tokens of a cooperative grid: no sort here (decode_grid_sort).
 template <bool kSoftmax, int kEpt, bool kMulti>
-__global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
-  __shared__ DecodeSmem sm;
+__device__ __forceinline__ void decode_token(const DecodeArgs& a, DecodeSmem& sm, int t) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = kMulti ? static_cast<int>(blockIdx.x) : 0;
-  const int T = kMulti ? static_cast<int>(gridDim.x) : 1;
   const uint16_t* logits = a.logits + static_cast<size_t>(t) * a.E;
   const int G = a.G, g = a.g, Kg = a.Kg, K = a.K, B = a.B;
   const int TPG = decode_tpg(G);
@@ -125,13 +124,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   const bool in_group = j < G;
   // experts per thread: 2 * 256 / G < TPG, so g = E / G <= 4096 / G < 16 * TPG
   const int R = (g + TPG - 1) / TPG;
-  pdl_trigger();
-  // the inputs start towards L2 while the kernel ahead in the stream finishes
-  if (tid < 64)
-    prefetch_l2_range(logits, 2 * static_cast<size_t>(a.E), tid, 64);
-  else if (!kSoftmax && tid < 192)
-    prefetch_l2_range(a.bias, 4 * static_cast<size_t>(a.E), tid - 64, 128);
-  pdl_wait();
 
   // ---- loads (one DRAM round trip); rows that depend on nothing meanwhile
   float key[kEpt], sv[kEpt];
@@ -360,7 +352,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
         a.topk_ids[t * K + lane] = id;
         a.topk_w[t * K + lane] = w;
         a.xchg[t * K + lane] = id;
-        sm.sel_w[lane] = w;
+        sm.own_w[(t - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x)][lane] = w;
       }
     } else {
       int blk = 0;  // number of selected ids below mine
@@ -375,41 +367,85 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
       }
     }
   }
-  if (kMulti) decode_grid_sort(a, sm, t, T);
+}
+
+// kSoftmax: softmax scoring (keys are the logits, no bias).
+// kEpt: experts per thread the code is unrolled for (>= ceil(g / TPG)); the smallest fitting
+// instance is launched, so that a launch fetches only the instructions it runs (the kernel
+// usually lands on an SM whose instruction cache has never held it).
+// kGrid: 0 for one token; otherwise a.T tokens (2 <= a.T <= kDecodeGridTokens) on a cooperative
+// grid, CTA b routing tokens b, b + gridDim.x, ... (1: exactly one token per CTA, 2: several),
+// after which the CTAs sort all T * K routes together (decode_grid_sort).
+template <bool kSoftmax, int kEpt, int kGrid>
+__global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const DecodeArgs a) {
+  constexpr bool kMulti = kGrid != 0;
+  __shared__ DecodeSmem sm;
+  const int tid = threadIdx.x;
+  const int t0 = kMulti ? static_cast<int>(blockIdx.x) : 0;
+  const int T = kMulti ? a.T : 1;
+  const int step = kMulti ? static_cast<int>(gridDim.x) : 1;
+  pdl_trigger();
+  // the inputs start towards L2 while the kernel ahead in the stream finishes
+  if (tid < 64)
+    prefetch_l2_range(a.logits + static_cast<size_t>(t0) * a.E, 2 * static_cast<size_t>(a.E),
+                      tid, 64);
+  else if (!kSoftmax && tid < 192)
+    prefetch_l2_range(a.bias, 4 * static_cast<size_t>(a.E), tid - 64, 128);
+  pdl_wait();
+  if (!kMulti) {
+    decode_token<kSoftmax, kEpt, false>(a, sm, 0);
+    return;
+  }
+  if (kGrid == 1) {
+    decode_token<kSoftmax, kEpt, true>(a, sm, t0);
+    decode_grid_sort(a, sm, T);
+    return;
+  }
+  for (int t = t0; t < T; t += step) {
+    if (t + step < T && tid < 64)  // the CTA's next row starts towards L2
+      prefetch_l2_range(a.logits + static_cast<size_t>(t + step) * a.E,
+                        2 * static_cast<size_t>(a.E), tid, 64);
+    decode_token<kSoftmax, kEpt, true>(a, sm, t);
+    __syncthreads();  // the token's scratch is reused by the next one
+  }
+  decode_grid_sort(a, sm, T);
 }
 
 // Both sort phases for T tokens on a cooperative grid (kMulti), every thread of every CTA:
 // after a grid-wide barrier (bounded; on a timeout the CTA reports MOE_RS_DEVICE_WAIT_TIMEOUT
 // and writes nothing more) each CTA reads all T * K selected ids from the exchange buffer,
 // counts them per expert (with a token bit mask per expert) and forms the same block_m-padded
-// prefix; its own K routes go to row base(e) + (tokens before t routed to e), which is the
-// token-then-slot order because a token holds each expert at most once; CTA t writes the padding
-// rows and block owners of experts [t E / T, (t + 1) E / T), CTA 0 npp (the status word is
-// zeroed by mrs_grid_prep_kernel and only ever ORed here).  Dynamic shared memory:
-// decode_grid_smem(E, T).
-__device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int t, int T) {
+// prefix; the routes of its own tokens go to row base(e) + (tokens before t routed to e), which
+// is the token-then-slot order because a token holds each expert at most once; CTA b of n
+// writes the padding rows and block owners of experts [b E / n, (b + 1) E / n), CTA 0 npp (the
+// status word is zeroed by mrs_grid_prep_kernel and only ever ORed here).  Dynamic shared
+// memory: decode_grid_smem(E, T).
+__device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int T) {
   extern __shared__ __align__(16) int32_t dsm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = static_cast<int>(blockIdx.x), n = static_cast<int>(gridDim.x);
   const int E = a.E, K = a.K, B = a.B, N = T * K;
   const int W = (T + 31) >> 5;                         // token mask words per expert
   int32_t* cnt = dsm;                                  // [E]
   int32_t* padv = cnt + E;                             // [E]
   int32_t* base = padv + E;                            // [E + 1]
   unsigned* tmask = reinterpret_cast<unsigned*>(base + E + 1);  // [E][W]
-  int32_t* misc = reinterpret_cast<int32_t*>(tmask + static_cast<size_t>(E) * W);  // [64]
+  int32_t* all_id = reinterpret_cast<int32_t*>(tmask + static_cast<size_t>(E) * W);  // [N]
+  int32_t* misc = all_id + N;                                                          // [64]
   for (int e = tid; e < E; e += kDecodeThreads) cnt[e] = 0;
-  for (int i = tid; i < E * W; i += kDecodeThreads) tmask[i] = 0u;
+  for (int x = tid; x < E * W; x += kDecodeThreads) tmask[x] = 0u;
   // every CTA's ids are in the exchange buffer once the whole grid has arrived (the barrier
   // orders the writes before it with the reads after it)
-  if (!grid_barrier_bounded(a.bar, static_cast<unsigned>(T), a.wait_limit_ns)) {
+  if (!grid_barrier_bounded(a.bar, static_cast<unsigned>(n), a.wait_limit_ns)) {
     if (tid == 0) atomicOr(a.status, MOE_RS_DEVICE_WAIT_TIMEOUT);
     return;
   }
-  for (int i = tid; i < N; i += kDecodeThreads) {
-    const int e = __ldcg(a.xchg + i);
+  for (int x = tid; x < N; x += kDecodeThreads) {
+    const int e = __ldcg(a.xchg + x);
+    all_id[x] = e;
     if (e >= 0 && e < E) {
       atomicAdd(&cnt[e], 1);
-      const int tt = i / K;
+      const int tt = x / K;
       atomicOr(&tmask[e * W + (tt >> 5)], 1u << (tt & 31));
     }
   }
@@ -417,17 +453,22 @@ __device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int 
   for (int e = tid; e < E; e += kDecodeThreads) padv[e] = (cnt[e] + B - 1) & ~(B - 1);
   __syncthreads();
   block_exclusive_scan(padv, base, E, misc);  // base[E] = the padded total
-  if (warp == 0 && lane < K) {
-    const int e = sm.sel_id[lane];
+  // the routes of this CTA's tokens b, b + n, ...: thread x takes own token x / K, slot x % K
+  const int own = (T - b + n - 1) / n;
+  for (int x = tid; x < own * K; x += kDecodeThreads) {
+    const int jj = x / K, k = x - jj * K;
+    const int t = b + jj * n;
+    const int r = t * K + k;
+    const int e = all_id[r];
     const unsigned* m = tmask + e * W;
     int rank = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
     for (int w = 0; w < (t >> 5); ++w) rank += __popc(m[w]);
     const int dst = base[e] + rank;
-    a.sorted_ids[dst] = t * K + lane;
-    a.sorted_w[dst] = sm.sel_w[lane];
+    a.sorted_ids[dst] = r;
+    a.sorted_w[dst] = sm.own_w[jj][k];
   }
-  const int e0 = static_cast<int>(static_cast<long long>(t) * E / T);
-  const int e1 = static_cast<int>(static_cast<long long>(t + 1) * E / T);
+  const int e0 = static_cast<int>(static_cast<long long>(b) * E / n);
+  const int e1 = static_cast<int>(static_cast<long long>(b + 1) * E / n);
   for (int e = e0 + warp; e < e1; e += kDecodeWarps) {
     const int c = cnt[e];
     if (c == 0) continue;
@@ -437,9 +478,9 @@ __device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int 
       a.sorted_ids[p] = N;
       a.sorted_w[p] = 0.0f;
     }
-    for (int b = off / B + lane; b < end / B; b += 32) a.expert_ids[b] = e;
+    for (int q = off / B + lane; q < end / B; q += 32) a.expert_ids[q] = e;
   }
-  if (t == 0 && tid == 0) *a.npp = base[E];
+  if (b == 0 && tid == 0) *a.npp = base[E];
 }
 
 // Ahead of a grid-path call: zero its barrier word and status word, once the kernel ahead in the
@@ -451,24 +492,25 @@ __global__ void mrs_grid_prep_kernel(unsigned* bar, int32_t* status) {
   *status = 0;
 }
 
-size_t decode_grid_smem(int E, int T) {
+size_t decode_grid_smem(int E, int T, int K) {
   const size_t W = static_cast<size_t>(T + 31) / 32;
-  return sizeof(int32_t) * (3 * static_cast<size_t>(E) + 1 + W * E + 64);
+  return sizeof(int32_t) *
+         (3 * static_cast<size_t>(E) + 1 + W * E + static_cast<size_t>(T) * K + 64);
 }
 
-template <int kEpt, bool kMulti>
+template <int kEpt, int kGrid>
 static cudaError_t launch_decode_ept(const DecodeArgs& a, int T, cudaStream_t st) {
-  auto* kern = a.softmax ? mrs_decode_kernel<true, kEpt, kMulti>
-                         : mrs_decode_kernel<false, kEpt, kMulti>;
-  if (!kMulti) return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
-  const size_t smem = decode_grid_smem(a.E, T);
+  auto* kern = a.softmax ? mrs_decode_kernel<true, kEpt, kGrid>
+                         : mrs_decode_kernel<false, kEpt, kGrid>;
+  if (kGrid == 0) return launch_pdl(kern, dim3(1), dim3(kDecodeThreads), 0, st, a);
+  const size_t smem = decode_grid_smem(a.E, a.T, a.K);
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   // a cooperative launch: all T CTAs are resident together (the launch fails otherwise), which
   // the grid-wide barrier needs
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(T);
+  cfg.gridDim = dim3(T);  // CTAs of the grid (<= a.T tokens)
   cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -482,26 +524,27 @@ static cudaError_t launch_decode_ept(const DecodeArgs& a, int T, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <bool kMulti>
+template <int kGrid>
 static cudaError_t launch_decode_any(const DecodeArgs& a, int T, cudaStream_t st) {
   const int tpg = decode_tpg(a.G);
   const int r = (a.g + tpg - 1) / tpg;  // <= kDecodeEpt (g <= 4096 / G < 16 * TPG)
-  if (r <= 2) return launch_decode_ept<2, kMulti>(a, T, st);
-  if (r <= 4) return launch_decode_ept<4, kMulti>(a, T, st);
-  if (r <= 8) return launch_decode_ept<8, kMulti>(a, T, st);
-  return launch_decode_ept<kDecodeEpt, kMulti>(a, T, st);
+  if (r <= 2) return launch_decode_ept<2, kGrid>(a, T, st);
+  if (r <= 4) return launch_decode_ept<4, kGrid>(a, T, st);
+  if (r <= 8) return launch_decode_ept<8, kGrid>(a, T, st);
+  return launch_decode_ept<kDecodeEpt, kGrid>(a, T, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  return launch_decode_any<false>(a, 1, st);
+  return launch_decode_any<0>(a, 1, st);
 }
 
-cudaError_t launch_decode_grid(const DecodeArgs& a, int T, cudaStream_t st) {
-  if (T < 2 || T > kDecodeGridTokens || a.xchg == nullptr || a.bar == nullptr)
+cudaError_t launch_decode_grid(const DecodeArgs& a, int ctas, cudaStream_t st) {
+  if (a.T < 2 || a.T > kDecodeGridTokens || ctas < 1 || ctas > a.T ||
+      (a.T + ctas - 1) / ctas > kDecodeGridOwn || a.xchg == nullptr || a.bar == nullptr)
     return cudaErrorInvalidValue;
   cudaError_t err = launch_pdl(mrs_grid_prep_kernel, dim3(1), dim3(1), 0, st, a.bar, a.status);
   if (err != cudaSuccess) return err;
-  return launch_decode_any<true>(a, T, st);
+  return ctas == a.T ? launch_decode_any<1>(a, ctas, st) : launch_decode_any<2>(a, ctas, st);
 }
 
 }  // namespace mrs

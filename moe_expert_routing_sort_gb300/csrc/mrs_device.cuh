@@ -509,7 +509,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* mbar, uint32_t phase) {
   uint32_t done;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
       : "=r"(done)
       : "r"(smem_u32(mbar)), "r"(phase)
       : "memory");

@@ -121,6 +121,7 @@ struct SmallArgs {
 
 // ------------------------------------------------------------- one token (decode)
 struct DecodeArgs {
+  int T;          // tokens (several tokens on a grid; 1 otherwise)
   int32_t* xchg;  // several tokens on a grid: T * K selected ids exchanged through global memory
   unsigned* bar;  // several tokens on a grid: the grid barrier's word (zeroed ahead of the call)
   unsigned long long wait_limit_ns;  // several tokens: bound of the grid barrier's wait
@@ -273,15 +274,17 @@ struct GatePlan {
 };
 GatePlan gate_plan(int E, int sms);
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
-// A cooperative grid of T CTAs (2 <= T <= kDecodeGridTokens and no more than the device can
-// hold at once, one CTA per SM), one token each, then both sort phases across the grid through
-// a.xchg (T * K int32 of the workspace) and one bounded grid-wide barrier on a.bar; a one-thread
-// kernel ahead of it zeroes a.bar and the status word.
-constexpr int kDecodeGridTokens = 128;
+// A cooperative grid of `ctas` CTAs (no more than the device can hold at once: one CTA per SM)
+// over a.T tokens (2 <= a.T <= kDecodeGridTokens), CTA b routing tokens b, b + ctas, ..., then
+// both sort phases across the grid through a.xchg (T * K int32 of the workspace) and one
+// bounded grid-wide barrier on a.bar; a one-thread kernel ahead of it zeroes a.bar and the
+// status word.  decode_grid_smem: the grid kernel's dynamic shared memory.
+constexpr int kDecodeGridTokens = 320;
 // Default lower end of that path: for two or three tokens the single-CTA kernel is faster
 // (measured: T = 2 7.7 against 9.8 us per call).
 constexpr int kDecodeGridMinTokens = 4;
-cudaError_t launch_decode_grid(const DecodeArgs& a, int T, cudaStream_t st);
+cudaError_t launch_decode_grid(const DecodeArgs& a, int ctas, cudaStream_t st);
+size_t decode_grid_smem(int E, int T, int K);
 
 // ------------------------------------------------------------ per-context host state
 // Test hooks set through moe_route_sort_debug_set (process-wide).

@@ -1,9 +1,9 @@
-"""The one-launch paths of moe_route_sort and moe_sort.  Calls of 4 to 128 tokens (2 to 128
-with the test hook) run on a cooperative grid, one CTA per token, with a grid-wide exchange of
-the selected ids.  For mid-sized calls (by default up to 256 tokens and at most 512 KiB of
-logits, segment-shaped groups; the per-token grid is switched off in those tests) one cluster of
-16 CTAs runs the route step and both sort phases in a single launch, exchanging per-expert
-counts through distributed shared memory.  Every case is compared with the CPU oracle bit for
+"""The one-launch paths of moe_route_sort and moe_sort.  Calls of 4 to 320 tokens (2 to 320
+with the test hook) run on a cooperative grid, one CTA per token (up to four per CTA past the
+SM count), with a grid-wide exchange of the selected ids.  For mid-sized calls (by default up
+to 256 tokens and at most 512 KiB of logits, segment-shaped groups; the per-token grid is
+switched off in those tests) one cluster of 16 CTAs runs the route step and both sort phases
+in a single launch, exchanging per-expert counts through distributed shared memory.  Every case is compared with the CPU oracle bit for
 bit (weights within 1e-6) and with the three-kernel multi-CTA path on the same inputs; the
 library's test hooks force the paths on (any size) or off.  moe_sort does the same from given
 routes on one cluster (by default 128 to 8192 routes).  The cluster paths touch no workspace
@@ -269,7 +269,7 @@ def test_moe_sort_default_reach(T, K, cluster):
 
 
 # ----------------------------------------- a few tokens: one CTA each, a cooperative grid
-@pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 15, 16, 33, 64, 127, 128])
+@pytest.mark.parametrize("T", [2, 3, 5, 8, 9, 15, 16, 33, 64, 127, 128, 153, 304, 320])
 @pytest.mark.parametrize("E,G,Kg,K,B", [(896, 8, 4, 16, 32), (896, 1, 1, 16, 32),
                                          (4096, 16, 4, 8, 128), (64, 8, 4, 6, 16),
                                          (129, 3, 2, 5, 16), (4000, 5, 2, 8, 32)])
