@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     DEBUG_CLUSTER_TOKENS,
     DEBUG_FORCE_PROXY_FAIL,
     DEBUG_GRID_TOKENS,
+    DEBUG_WARP_GRID_TOKENS,
     DEBUG_WAIT_LIMIT_NS,
     DEVICE_BAD_EXPERT_ID,
     RouteSortBuffers,

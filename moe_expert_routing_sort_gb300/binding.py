@@ -392,6 +392,7 @@ DEBUG_WAIT_LIMIT_NS = 1
 DEBUG_FORCE_PROXY_FAIL = 2
 DEBUG_CLUSTER_TOKENS = 3
 DEBUG_GRID_TOKENS = 4
+DEBUG_WARP_GRID_TOKENS = 5
 
 
 def moe_route_sort_debug_set(knob: int, value: int) -> None:

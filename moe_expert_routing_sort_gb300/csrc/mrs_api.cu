@@ -293,7 +293,7 @@ bool small_plan(int T, int E, int K, int B, bool sort_only, int nu, const Device
   nb_max = static_cast<int>(max_padded64(T, E, K, B) / B);
   wave = sort_only ? 0 : (T < 16 ? T : 16);
   for (;;) {
-    lay = small_layout(E, N, wave, nu, sort_only);
+    lay = small_layout(E, N, wave, nu, sort_only, false);
     if (lay.total <= d.smem_optin) return true;
     if (sort_only || wave <= 1) return false;
     --wave;
@@ -468,6 +468,48 @@ int route_sort_impl(const void* logits_bf16, const float* bias, int T, int E, in
     ga.rpc = gp.rpc;
     rc = launch_status(launch_gate(ga, gp, stream));
     if (rc) return rc;
+  }
+
+  // a few hundred tokens: the single-CTA kernel on a cooperative grid, one warp per token and
+  // a contiguous range of at most 16 tokens per CTA
+  DeviceInfo dw;
+  int per = 0;
+  if (device_info(dw) && warp_grid_reach(T, dw.sms, per)) {
+    RouteShape wsh = make_shape(E, n_group, topk_group, topk, routed_scale);
+    wsh.softmax = softmax ? 1 : 0;
+    SegShape wseg{};
+    const bool wuse_seg = make_seg_shape(E, n_group, topk_group, topk, routed_scale, 32, wseg);
+    wseg.softmax = wsh.softmax;
+    const SmallLayout wlay =
+        small_layout(E, per * topk, per, wuse_seg ? wseg.nu : 0, false, true);
+    if (wlay.total <= dw.smem_optin) {
+      SmallArgs a{};
+      a.use_seg = wuse_seg;
+      a.seg = wseg;
+      a.logits = static_cast<const uint16_t*>(logits_bf16);
+      a.bias = bias;
+      a.T = T;
+      a.N = per * topk;
+      a.B = block_m;
+      a.wave = per;
+      a.per = per;
+      a.xchg = reinterpret_cast<int32_t*>(ws + l.unit_buf);  // T * K int32 fit in [T * K] int2
+      a.bar = reinterpret_cast<unsigned*>(ws + l.status + 8);
+      a.wait_limit_ns = debug_wait_limit_ns();
+      a.sh = wsh;
+      a.lay = wlay;
+      a.topk_ids = topk_ids;
+      a.topk_w = topk_weights;
+      a.sorted_ids = sorted_token_ids;
+      a.sorted_w = sorted_weights;
+      a.expert_ids = expert_ids;
+      a.npp = num_tokens_post_pad;
+      a.status = status;
+      rc = launch_status(launch_small_grid(a, stream));
+      // a rejected launch (more CTAs than the device holds at once) enqueued at most the
+      // zeroing kernel: the paths below take the call
+      if (rc != MOE_RS_ERR_LAUNCH) return rc;
+    }
   }
 
   DeviceInfo dg;

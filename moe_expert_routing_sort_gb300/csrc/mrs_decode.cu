@@ -75,38 +75,6 @@ __host__ __device__ inline int decode_tpg(int G) {
 
 __device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int T);
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Grid-wide barrier of a cooperative launch over the word at bar (zeroed by
-// mrs_grid_prep_kernel ahead of this call): thread 0 of each CTA publishes the CTA's earlier
-// writes and arrives, then waits, at most limit_ns (0: not at all, a test hook), until all n
-// CTAs have arrived.  Every thread of the CTA calls this; returns false on a timeout.
-__device__ bool grid_barrier_bounded(unsigned* bar, unsigned n, unsigned long long limit_ns) {
-  __shared__ int ok_s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(bar, 1u);
-    bool ok = limit_ns != 0ull;
-    if (ok) {
-      const unsigned long long t0 = globaltimer_ns();
-      while (ld_acquire_u32(bar) < n) {
-        if (globaltimer_ns() - t0 > limit_ns) {
-          ok = false;
-          break;
-        }
-      }
-    }
-    ok_s = ok ? 1 : 0;
-  }
-  __syncthreads();
-  return ok_s != 0;
-}
-
 // kSoftmax: softmax scoring (keys are the logits, no bias).
 // kEpt: experts per thread the code is unrolled for (>= ceil(g / TPG)); the smallest fitting
 // instance is launched, so that a launch fetches only the instructions it runs (the kernel
@@ -436,7 +404,7 @@ __device__ void decode_grid_sort(const DecodeArgs& a, const DecodeSmem& sm, int 
   for (int x = tid; x < E * W; x += kDecodeThreads) tmask[x] = 0u;
   // every CTA's ids are in the exchange buffer once the whole grid has arrived (the barrier
   // orders the writes before it with the reads after it)
-  if (!grid_barrier_bounded(a.bar, static_cast<unsigned>(n), a.wait_limit_ns)) {
+  if (!grid_barrier_bounded(a.bar, static_cast<unsigned>(n), a.wait_limit_ns, misc + 48)) {
     if (tid == 0) atomicOr(a.status, MOE_RS_DEVICE_WAIT_TIMEOUT);
     return;
   }
@@ -492,6 +460,10 @@ __global__ void mrs_grid_prep_kernel(unsigned* bar, int32_t* status) {
   *status = 0;
 }
 
+cudaError_t launch_grid_prep(unsigned* bar, int32_t* status, cudaStream_t st) {
+  return launch_pdl(mrs_grid_prep_kernel, dim3(1), dim3(1), 0, st, bar, status);
+}
+
 size_t decode_grid_smem(int E, int T, int K) {
   const size_t W = static_cast<size_t>(T + 31) / 32;
   return sizeof(int32_t) *
@@ -542,7 +514,7 @@ cudaError_t launch_decode_grid(const DecodeArgs& a, int ctas, cudaStream_t st) {
   if (a.T < 2 || a.T > kDecodeGridTokens || ctas < 1 || ctas > a.T ||
       (a.T + ctas - 1) / ctas > kDecodeGridOwn || a.xchg == nullptr || a.bar == nullptr)
     return cudaErrorInvalidValue;
-  cudaError_t err = launch_pdl(mrs_grid_prep_kernel, dim3(1), dim3(1), 0, st, a.bar, a.status);
+  cudaError_t err = launch_grid_prep(a.bar, a.status, st);
   if (err != cudaSuccess) return err;
   return ctas == a.T ? launch_decode_any<1>(a, ctas, st) : launch_decode_any<2>(a, ctas, st);
 }

@@ -467,6 +467,39 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a cooperative launch over the word at bar (zeroed ahead of the launch
+// by mrs_grid_prep_kernel): thread 0 of each CTA publishes the CTA's earlier writes and
+// arrives, then waits, at most limit_ns (0: not at all, a test hook), until all n CTAs have
+// arrived.  ok_s: one int of the CTA's shared memory.  Every thread of the CTA calls this;
+// returns false on a timeout.
+__device__ __forceinline__ bool grid_barrier_bounded(unsigned* bar, unsigned n,
+                                                     unsigned long long limit_ns, int* ok_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    bool ok = limit_ns != 0ull;
+    if (ok) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (ld_acquire_u32(bar) < n) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    *ok_s = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -106,6 +106,10 @@ struct SmallArgs {
   const int32_t* in_ids;  // sort-only mode
   const float* in_w;
   int T, N, B, wave, nb_max;
+  int per;                          // grid: tokens per CTA (<= wave)
+  int32_t* xchg;                    // grid: T * K selected ids exchanged through global memory
+  unsigned* bar;                    // grid: barrier word, zeroed by mrs_grid_prep_kernel
+  unsigned long long wait_limit_ns; // grid: limit of the barrier wait (0: give up at once)
   RouteShape sh;
   bool use_seg;  // route with the segment routine (SegShape valid)
   SegShape seg;
@@ -283,7 +287,19 @@ constexpr int kDecodeGridTokens = 320;
 // Default lower end of that path: for two or three tokens the single-CTA kernel is faster
 // (measured: T = 2 7.7 against 9.8 us per call).
 constexpr int kDecodeGridMinTokens = 4;
+// Largest T of the warp-per-token grid path by default (launch_small_grid).  Measured per call
+// (E = 896, K = 16, graph of calls, L2 flushed), against the next path down: T = 512 10.3 against
+// 16.9 us, T = 1536 15.8 against 19.0, T = 2048 18.9 against 19.1.
+constexpr int kWarpGridTokens = 2048;
 cudaError_t launch_decode_grid(const DecodeArgs& a, int ctas, cudaStream_t st);
+// One-thread kernel that zeroes a grid path's barrier and status words once the kernel ahead
+// in the stream has completed.
+cudaError_t launch_grid_prep(unsigned* bar, int32_t* status, cudaStream_t st);
+// The single-CTA kernel as a cooperative grid of ceil(a.T / a.per) CTAs (a.per <= a.wave tokens
+// each, one warp per token), both sort phases across the grid through a.xchg and one bounded
+// grid-wide barrier on a.bar (zeroed, with the status word, by a one-thread kernel ahead of it).
+// The layout is small_layout(E, a.per * K, a.wave, nu, false, true).
+cudaError_t launch_small_grid(const SmallArgs& a, cudaStream_t st);
 size_t decode_grid_smem(int E, int T, int K);
 
 // ------------------------------------------------------------ per-context host state
@@ -299,6 +315,10 @@ bool cluster_reach_sort(int T, int E, int K, int B);
 // kDecodeGridTokens by default, 2 <= T <= min(kDecodeGridTokens, limit) once the grid test hook
 // has set a token limit.
 bool decode_grid_reach(int T);
+// Whether a call of T tokens takes the warp-per-token grid path on a device of `sms` SMs, and
+// with how many tokens per CTA (`per`, at most 16, so that ceil(T / per) <= sms): by default
+// sms < T <= kWarpGridTokens; T > limit (and T >= 2) once the test hook has set a limit.
+bool warp_grid_reach(int T, int sms, int& per);
 // Identity of the current device and context (the context's unique id, 0 if the driver cannot
 // tell): host caches of device addresses are keyed on it.
 bool current_context(int& dev, unsigned long long& ctx_id);
@@ -321,7 +341,7 @@ size_t route_smem_bytes(int E, int nwarps, int max_routes, bool sort);
 size_t seg_smem_bytes(int E, int nu, int nwarps, int max_routes, bool sort, int tpw, int nbuf,
                       bool cluster);
 int seg_cluster_capacity(size_t smem);
-SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only);
+SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only, bool grid);
 
 // Shared memory used by phase 1 of the sort step (mrs_unit.cuh) besides the routes.
 __host__ __device__ inline size_t unit_scratch_bytes(int E) {

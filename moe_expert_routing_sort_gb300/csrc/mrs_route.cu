@@ -129,14 +129,101 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
 
 static_assert(sizeof(SegScratch) <= sizeof(WarpScratch), "segment scratch reuses WarpScratch");
 
+// The sort step of a grid-wide call (kGrid below), after this CTA has routed its tokens
+// [g0, g0 + gn): rid/rw hold their routes (index (t - g0) * K + k), masks[e] bit t - g0 is set
+// for each of them routed to e, and every CTA has written its ids to a.xchg.  After the
+// grid-wide barrier (bounded; on a timeout the CTA reports MOE_RS_DEVICE_WAIT_TIMEOUT and
+// writes nothing more) each CTA reads all T * K ids, counts them per expert (cnt) and those of
+// tokens before g0 (bef), forms the block_m-padded prefix over experts (off), and writes its own
+// routes to row off[e] + bef[e] + (its earlier tokens routed to e): token-then-slot order, as a
+// token holds each expert at most once.  CTA b of n writes the padding rows and block owners
+// of experts [b E / n, (b + 1) E / n), CTA 0 npp; the status word is zeroed by
+// mrs_grid_prep_kernel and only ever ORed here.
+__device__ __forceinline__ void small_grid_sort(const SmallArgs& a, int g0, int gn,
+                                                const int32_t* rid, const float* rw,
+                                                const unsigned* masks, int32_t* cnt,
+                                                int32_t* bef, int32_t* off, int32_t* misc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.sh.E, K = a.sh.K, B = a.B;
+  const int b = static_cast<int>(blockIdx.x), n = static_cast<int>(gridDim.x);
+  const int N = a.T * K, nb = g0 * K;
+  for (int e = tid; e < E; e += kSmallThreads) {
+    cnt[e] = 0;
+    bef[e] = 0;
+  }
+  if (!grid_barrier_bounded(a.bar, static_cast<unsigned>(n), a.wait_limit_ns, misc + 2)) {
+    if (tid == 0) atomicOr(a.status, MOE_RS_DEVICE_WAIT_TIMEOUT);
+    return;
+  }
+  // four 16-byte loads per thread in flight (the exchange buffer is 16-byte aligned)
+  for (int x0 = 4 * tid; x0 < N; x0 += 16 * kSmallThreads) {
+    int v[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + 4 * kSmallThreads * u;
+      if (x + 3 < N) {
+        const int4 q = __ldcg(reinterpret_cast<const int4*>(a.xchg + x));
+        v[u][0] = q.x;
+        v[u][1] = q.y;
+        v[u][2] = q.z;
+        v[u][3] = q.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[u][j] = (x + j < N) ? __ldcg(a.xchg + x + j) : -1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + 4 * kSmallThreads * u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = v[u][j];
+        if (e >= 0 && e < E) {
+          atomicAdd(&cnt[e], 1);
+          if (x + j < nb) atomicAdd(&bef[e], 1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int total = block_scan_padded<kSmallThreads>(cnt, off, E, B, misc + 4);
+  for (int r = tid; r < gn * K; r += kSmallThreads) {
+    const int e = rid[r];
+    if (e < 0 || e >= E) continue;
+    const int tl = r / K;
+    const int pos = off[e] + bef[e] + __popc(masks[e] & ((1u << tl) - 1u));
+    a.sorted_ids[pos] = nb + r;
+    a.sorted_w[pos] = rw[r];
+  }
+  const int e0 = static_cast<int>(static_cast<long long>(b) * E / n);
+  const int e1 = static_cast<int>(static_cast<long long>(b + 1) * E / n);
+  for (int e = e0 + warp; e < e1; e += kSmallThreads / 32) {
+    const int c = cnt[e];
+    if (c == 0) continue;
+    const int o = off[e];
+    const int end = o + ((c + B - 1) & ~(B - 1));
+    for (int p = o + c + lane; p < end; p += 32) {
+      a.sorted_ids[p] = N;
+      a.sorted_w[p] = 0.0f;
+    }
+    for (int q = o / B + lane; q < end / B; q += 32) a.expert_ids[q] = e;
+  }
+  if (b == 0 && tid == 0) *a.npp = total;
+}
+
 // kSeg (route step only): route with the segment routine (a.use_seg), else the generic one;
 // one instance per routine, so that a launch fetches and holds only the code it runs.
-template <bool kSortOnly, bool kSeg>
+// kGrid: one CTA of a cooperative grid over a.T tokens; CTA b routes tokens [b * a.per,
+// (b + 1) * a.per) (at most one wave), then the grid sorts all routes (small_grid_sort).
+template <bool kSortOnly, bool kSeg, bool kGrid>
 __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const SmallArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RouteShape sh = a.sh;
   const int E = sh.E, K = sh.K, N = a.N, B = a.B;
+  // the tokens this CTA routes: [g0, g0 + gT)
+  const int g0 = kGrid ? static_cast<int>(blockIdx.x) * a.per : 0;
+  const int gT = kGrid ? min(a.per, a.T - g0) : a.T;
   int32_t* rid = reinterpret_cast<int32_t*>(smem + a.lay.rid);
   float* rw = reinterpret_cast<float*>(smem + a.lay.rw);
   int32_t* cnt = reinterpret_cast<int32_t*>(smem + a.lay.cnt);
@@ -147,7 +234,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
   // the inputs start towards L2 while the kernel ahead in the stream finishes
   if (!kSortOnly) {
     if (tid < 384)
-      prefetch_l2_range(a.logits, 2 * static_cast<size_t>(a.T) * E, tid, 384);
+      prefetch_l2_range(a.logits + static_cast<size_t>(g0) * E, 2 * static_cast<size_t>(gT) * E,
+                        tid, 384);
     else if (a.bias)
       prefetch_l2_range(a.bias, 4 * static_cast<size_t>(E), tid - 384, 128);
   }
@@ -158,13 +246,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
     float* keys = reinterpret_cast<float*>(smem + a.lay.keys);
     float* svals = reinterpret_cast<float*>(smem + a.lay.svals);
     WarpScratch* scr = reinterpret_cast<WarpScratch*>(smem + a.lay.scratch);
-    for (int e = tid; e < 2 * E; e += kSmallThreads) masks[e] = 0u;
+    for (int e = tid; e < (kGrid ? E : 2 * E); e += kSmallThreads) masks[e] = 0u;
     if (kSeg && warp < a.wave)
       ub_init_pads(reinterpret_cast<unsigned short*>(smem + a.lay.umax + ub_bytes(a.seg.nu) * warp),
                    lane, a.seg.nu);
-    for (int t0 = 0; t0 < a.T; t0 += a.wave) {
-      const int nt = min(a.wave, a.T - t0);
-      small_scores(a, t0, nt, keys, svals);
+    for (int t0 = 0; t0 < gT; t0 += a.wave) {
+      const int nt = min(a.wave, gT - t0);
+      small_scores(a, g0 + t0, nt, keys, svals);
       __syncthreads();
       for (int tl = warp; tl < nt; tl += kSmallThreads / 32) {
         int id;
@@ -180,17 +268,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
           route_token(SmemExactSrc{keys + tl * E, svals + tl * E}, sh, scr[warp], lane, id, w);
         }
         if (lane < K) {
-          const int t = t0 + tl;
+          const int t = t0 + tl;  // of this CTA's tokens
           const int r = t * K + lane;
-          a.topk_ids[r] = id;
-          a.topk_w[r] = w;
+          const int rg = (g0 + t) * K + lane;
+          a.topk_ids[rg] = id;
+          a.topk_w[rg] = w;
           rid[r] = id;
           rw[r] = w;
+          if (kGrid) a.xchg[rg] = id;
           // experts are distinct within a token: one bit per token gives count and rank
           if (id >= 0 && id < E) atomicOr(&masks[(t >> 5) * E + id], 1u << (t & 31));
         }
       }
       __syncthreads();
+    }
+    if (kGrid) {
+      small_grid_sort(a, g0, gT, rid, rw, masks, cnt,
+                      reinterpret_cast<int32_t*>(smem + a.lay.owner), off, misc);
+      return;
     }
     for (int e = tid; e < E; e += kSmallThreads) cnt[e] = __popc(masks[e]) + __popc(masks[E + e]);
     if (tid == 0) misc[0] = 0;
@@ -261,7 +356,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
   }
 }
 
-SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only) {
+SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only, bool grid) {
   SmallLayout l{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -280,8 +375,8 @@ SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only) {
   l.rrank = sort_only ? take(sizeof(int32_t) * N) : 0;
   l.cnt = take(sizeof(int32_t) * E);
   l.off = take(sizeof(int32_t) * E);
-  l.masks = sort_only ? 0 : take(sizeof(unsigned) * 2 * E);
-  l.owner = 0;
+  l.masks = sort_only ? 0 : take(sizeof(unsigned) * (grid ? 1 : 2) * E);
+  l.owner = grid ? take(sizeof(int32_t) * E) : 0;  // grid: routes of earlier CTAs per expert
   l.misc = take(sizeof(int32_t) * 40);
   l.total = static_cast<int>(o);
   return l;
@@ -289,13 +384,42 @@ SmallLayout small_layout(int E, int N, int wave, int nu, bool sort_only) {
 
 cudaError_t launch_small(const SmallArgs& a, bool sort_only, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(a.lay.total);
-  auto* kern = sort_only ? mrs_small_kernel<true, false>
-                         : (a.use_seg ? mrs_small_kernel<false, true>
-                                      : mrs_small_kernel<false, false>);
+  auto* kern = sort_only ? mrs_small_kernel<true, false, false>
+                         : (a.use_seg ? mrs_small_kernel<false, true, false>
+                                      : mrs_small_kernel<false, false, false>);
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(kern, dim3(1), dim3(kSmallThreads), smem, st, a);
+}
+
+cudaError_t launch_small_grid(const SmallArgs& a, cudaStream_t st) {
+  const int ctas = (a.T + a.per - 1) / a.per;
+  if (a.T < 2 || a.per < 1 || a.per > a.wave || a.wave > kSmallThreads / 32 ||
+      a.xchg == nullptr || a.bar == nullptr)
+    return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(a.lay.total);
+  auto* kern = a.use_seg ? mrs_small_kernel<false, true, true> : mrs_small_kernel<false, false, true>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  err = launch_grid_prep(a.bar, a.status, st);
+  if (err != cudaSuccess) return err;
+  // a cooperative launch: all CTAs are resident together (the launch fails otherwise), which
+  // the grid-wide barrier needs
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kSmallThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // --------------------------------------------------------- multi-CTA route, any shape

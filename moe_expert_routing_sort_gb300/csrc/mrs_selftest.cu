@@ -63,6 +63,7 @@ namespace {
 std::atomic<long long> g_wait_limit{-1};   // < 0: kWaitLimitNs
 std::atomic<int> g_cluster_tokens{-1};     // < 0: the default reach
 std::atomic<int> g_grid_tokens{-1};        // < 0: kDecodeGridTokens
+std::atomic<int> g_warp_grid_tokens{-1};   // < 0: the default reach
 std::atomic<int> g_force_proxy_fail{0};
 std::atomic<int> g_proxy_generation{1};    // bumped when the forced failure changes
 
@@ -129,6 +130,14 @@ bool decode_grid_reach(int T) {
   const int v = g_grid_tokens.load(std::memory_order_relaxed);
   if (T < 2 || T > kDecodeGridTokens) return false;
   return v < 0 ? T >= kDecodeGridMinTokens : T <= v;
+}
+
+bool warp_grid_reach(int T, int sms, int& per) {
+  if (T < 2 || sms < 1) return false;
+  const int v = g_warp_grid_tokens.load(std::memory_order_relaxed);
+  if (v < 0 ? (T <= sms || T > kWarpGridTokens) : T <= v) return false;
+  per = (T + sms - 1) / sms;
+  return per <= 16;
 }
 
 bool cluster_reach_sort(int T, int E, int K, int B) {
@@ -226,9 +235,13 @@ extern "C" int moe_route_sort_debug_set(int knob, long long value) {
       return MOE_RS_OK;
     }
     case MOE_RS_DEBUG_CLUSTER_TOKENS:
-    case MOE_RS_DEBUG_GRID_TOKENS: {
+    case MOE_RS_DEBUG_GRID_TOKENS:
+    case MOE_RS_DEBUG_WARP_GRID_TOKENS: {
       const long long v = value < 0 ? -1 : (value > (1ll << 30) ? (1ll << 30) : value);
-      (knob == MOE_RS_DEBUG_GRID_TOKENS ? mrs::g_grid_tokens : mrs::g_cluster_tokens)
+      (knob == MOE_RS_DEBUG_GRID_TOKENS
+           ? mrs::g_grid_tokens
+           : (knob == MOE_RS_DEBUG_CLUSTER_TOKENS ? mrs::g_cluster_tokens
+                                                  : mrs::g_warp_grid_tokens))
           .store(static_cast<int>(v));
       return MOE_RS_OK;
     }

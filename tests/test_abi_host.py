@@ -194,6 +194,8 @@ def test_debug_knobs(lib):
     assert lib.moe_route_sort_debug_set(3, -1) == 0  # ... and back to the default
     assert lib.moe_route_sort_debug_set(4, 0) == 0   # per-token grid path off ...
     assert lib.moe_route_sort_debug_set(4, -1) == 0  # ... and back to the default
+    assert lib.moe_route_sort_debug_set(5, 1 << 30) == 0  # warp-per-token grid path off ...
+    assert lib.moe_route_sort_debug_set(5, -1) == 0       # ... and back to the default
 
 
 def test_binding_refuses_buffers_on_different_devices():

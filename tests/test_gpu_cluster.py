@@ -1,9 +1,11 @@
-"""The one-launch paths of moe_route_sort and moe_sort.  Calls of 4 to 320 tokens (2 to 320
-with the test hook) run on a cooperative grid, one CTA per token (up to four per CTA past the
-SM count), with a grid-wide exchange of the selected ids.  For mid-sized calls (by default up
-to 256 tokens and at most 512 KiB of logits, segment-shaped groups; the per-token grid is
-switched off in those tests) one cluster of 16 CTAs runs the route step and both sort phases
-in a single launch, exchanging per-expert counts through distributed shared memory.  Every case is compared with the CPU oracle bit for
+"""The one-launch paths of moe_route_sort and moe_sort.  Calls of more than one token per SM
+up to 2048 tokens run on a cooperative grid with one warp per token (up to 16 tokens per CTA);
+calls of 4 tokens up to the SM count (2 to 320 with the test hook) on a cooperative grid with one
+CTA per token (up to four per CTA past the SM count); both exchange the selected ids through
+the workspace around one grid-wide barrier.  For mid-sized calls (by default up to 256 tokens
+and at most 512 KiB of logits, segment-shaped groups; the grid paths are switched off in those
+tests) one cluster of 16 CTAs runs the route step and both sort phases in a single launch,
+exchanging per-expert counts through distributed shared memory.  Every case is compared with the CPU oracle bit for
 bit (weights within 1e-6) and with the three-kernel multi-CTA path on the same inputs; the
 library's test hooks force the paths on (any size) or off.  moe_sort does the same from given
 routes on one cluster (by default 128 to 8192 routes).  The cluster paths touch no workspace
@@ -34,6 +36,7 @@ def _built():
     yield
     mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
     mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, -1)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1)
 
 
 def _case(name, T, seed=0, **over):
@@ -44,10 +47,13 @@ def _case(name, T, seed=0, **over):
     return w, inp, ref
 
 
-def _run(w, inp, cluster_tokens, grid=0):
-    """One call with the cluster paths limited to T <= cluster_tokens and the per-token grid path
-    to T <= grid (off unless given); returns the buffers and whether any workspace byte past the
-    status word changed."""
+NEVER = 1 << 30  # the warp-grid hook's limit that keeps it off (it takes T > limit)
+
+
+def _run(w, inp, cluster_tokens, grid=0, warp=NEVER):
+    """One call with the cluster paths limited to T <= cluster_tokens, the per-token grid path
+    to T <= grid and the warp-per-token grid path to T > warp (both off unless given); returns
+    the buffers and whether any workspace byte past the status word changed."""
     logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
     bias = torch.from_numpy(inp.bias).to(DEV)
     out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
@@ -56,6 +62,7 @@ def _run(w, inp, cluster_tokens, grid=0):
     out.expert_ids.fill_(-7)
     mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, cluster_tokens)
     mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, grid)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, warp)
     try:
         mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
                        w.block_m, out=out)
@@ -63,8 +70,20 @@ def _run(w, inp, cluster_tokens, grid=0):
     finally:
         mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
         mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, -1)
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1)
     touched = bool(torch.any(out.workspace[16:] != POISON).item())
     return out, touched
+
+
+def _path(out):
+    """Which kind of path the last call on `out` took, from its workspace (poisoned before the
+    call): the three-kernel path's route kernel writes every unit's flag word (bytes 16..),
+    the grid paths only the exchanged ids further on, the cluster and single-CTA paths
+    nothing past the status word."""
+    ws = out.workspace
+    if bool(torch.any(ws[16:20] != POISON).item()):
+        return "three"
+    return "grid" if bool(torch.any(ws[16:] != POISON).item()) else "one-launch"
 
 
 def _assert_matches(out, ref, w):
@@ -174,12 +193,14 @@ def test_softmax_scoring_on_the_cluster_path():
         out.workspace.fill_(POISON)
         mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, limit)
         mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, 0)
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, NEVER)
         try:
             mrs.route_sort_softmax(logits, w.topk, w.routed_scale, w.block_m, out=out)
             torch.cuda.synchronize()
         finally:
             mrs.moe_route_sort_debug_set(mrs.DEBUG_CLUSTER_TOKENS, -1)
             mrs.moe_route_sort_debug_set(mrs.DEBUG_GRID_TOKENS, -1)
+            mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1)
         assert bool(torch.any(out.workspace[16:] != POISON).item()) == (limit == 0)
         npp = int(out.num_tokens_post_pad.item())
         assert npp == ref["num_tokens_post_pad"]
@@ -315,3 +336,89 @@ def test_few_tokens_softmax(T):
     assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref["sorted_token_ids"])
     assert np.array_equal(out.expert_ids[: npp // w.block_m].cpu().numpy(), ref["expert_ids"])
     assert out.status_word() == 0
+
+
+# ------------------------------- a few hundred tokens: one warp per token, a cooperative grid
+# T spans one token per CTA (the hook forces the path below the SM count), ragged CTA ranges
+# and the default reach's ends; shapes include ones without a segment layout (the generic warp
+# routine) and a single group.
+@pytest.mark.parametrize("T", [2, 3, 17, 152, 153, 200, 305, 512, 777, 1024, 2048])
+@pytest.mark.parametrize("E,G,Kg,K,B", [(896, 8, 4, 16, 32), (896, 1, 1, 16, 32),
+                                         (4096, 16, 4, 8, 128), (64, 8, 4, 6, 16),
+                                         (129, 3, 2, 5, 16), (4000, 5, 2, 8, 32)])
+def test_warp_grid(T, E, G, Kg, K, B):
+    if E >= 4000 and T > 600:
+        pytest.skip("the keys of ceil(T / #SMs) tokens of 4096 experts exceed shared memory")
+    w, inp, ref = _case("prefill_T512_E896", T, E=E, n_group=G, topk_group=Kg, topk=K,
+                        block_m=B, seed=7 * E + T)
+    a, _ = _run(w, inp, -1, warp=1)
+    assert _path(a) == "grid"
+    _assert_matches(a, ref, w)
+    b, _ = _run(w, inp, 0)  # single-CTA kernel (T <= 8) or the three-kernel path
+    _assert_matches(b, ref, w)
+    npp = int(a.num_tokens_post_pad.item())
+    assert torch.equal(a.sorted_token_ids[:npp], b.sorted_token_ids[:npp])
+    assert torch.equal(a.sorted_weights[:npp], b.sorted_weights[:npp])
+    assert torch.equal(a.topk_weights, b.topk_weights)
+
+
+@pytest.mark.parametrize("T", [300, 1000])
+def test_warp_grid_skewed(T):
+    # a few hot experts: most CTAs hold routes of the same experts (earlier-CTA counts matter)
+    w, inp, ref = _case("skewed_T8192_E896", T)
+    a, _ = _run(w, inp, -1, warp=1)
+    assert _path(a) == "grid"
+    _assert_matches(a, ref, w)
+
+
+@pytest.mark.parametrize("T", [200, 600])
+def test_warp_grid_exact_ties(T):
+    # every logit equal: many survivors per token, every CTA routes to the same experts
+    w = datagen.workload("prefill_T512_E896", T=T)
+    logits = np.full((T, 896), datagen.float32_to_bf16_bits(np.float32([0.75]))[0], np.uint16)
+    bias = np.zeros(896, np.float32)
+    bias[::7] = 0.03125
+    inp = datagen.RouterInputs(w, logits, bias)
+    ref = oracle.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                            w.block_m)
+    out, _ = _run(w, inp, -1, warp=1)
+    assert _path(out) == "grid"
+    _assert_matches(out, ref, w)
+
+
+@pytest.mark.parametrize("T", [5, 300, 1000])
+def test_warp_grid_softmax(T):
+    w = datagen.workload("prefill_T512_E896", T=T, n_group=1, topk_group=1, topk=8)
+    inp = datagen.make_inputs(w)
+    ref = oracle.route_sort_softmax(inp.logits_bf16, w.topk, w.routed_scale, w.block_m)
+    logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    out.workspace.fill_(POISON)
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, 1)
+    try:
+        mrs.route_sort_softmax(logits, w.topk, w.routed_scale, w.block_m, out=out)
+        torch.cuda.synchronize()
+    finally:
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1)
+    assert _path(out) == "grid"
+    npp = int(out.num_tokens_post_pad.item())
+    assert npp == ref["num_tokens_post_pad"]
+    assert np.array_equal(out.topk_ids.cpu().numpy(), ref["topk_ids"])
+    assert np.max(np.abs(out.topk_weights.cpu().numpy() - ref["topk_weights"]),
+                  initial=0.0) <= WEIGHT_ATOL
+    assert np.array_equal(out.sorted_token_ids[:npp].cpu().numpy(), ref["sorted_token_ids"])
+    assert np.array_equal(out.expert_ids[: npp // w.block_m].cpu().numpy(), ref["expert_ids"])
+    assert out.status_word() == 0
+
+
+@pytest.mark.parametrize("name,T,path", [("prefill_T512_E896", 64, "grid"),
+                                          ("prefill_T512_E896", 512, "grid"),
+                                          ("prefill_T512_E896", 2048, "grid"),
+                                          ("prefill_T512_E896", 2049, "three"),
+                                          ("wide_T16384_E4096", 600, "grid"),
+                                          ("skewed_T8192_E896", 8192, "three")])
+def test_default_dispatch(name, T, path):
+    w, inp, ref = _case(name, T)
+    out, _ = _run(w, inp, -1, grid=-1, warp=-1)
+    assert _path(out) == path
+    _assert_matches(out, ref, w)

@@ -89,22 +89,28 @@ def _status(ws):
 
 
 # ------------------------------------------------------------------ bounded waits
-# T = 40 runs on the per-token grid (its grid barrier gives up), T = 200 as one cluster (route
-# step and both sort phases in one launch); the others take the three-kernel path
-@pytest.mark.parametrize("name,T", [("prefill_T512_E896", None), ("prefill_T512_E896", 40),
-                                    ("prefill_T512_E896", 200), ("skewed_T8192_E896", 3000),
-                                    ("wide_T16384_E4096", 2000)])
-def test_wait_timeout_is_reported_and_the_context_survives(name, T):
+# T = 512 runs on the warp-per-token grid and T = 40 on the per-token grid (their grid barriers
+# give up), T = 200 with the warp grid off as one cluster (route step and both sort phases in
+# one launch; its row copies give up); the others take the three-kernel path
+@pytest.mark.parametrize("name,T,warp_grid", [("prefill_T512_E896", None, True),
+                                              ("prefill_T512_E896", 40, True),
+                                              ("prefill_T512_E896", 200, False),
+                                              ("skewed_T8192_E896", 3000, True),
+                                              ("wide_T16384_E4096", 2000, True)])
+def test_wait_timeout_is_reported_and_the_context_survives(name, T, warp_grid):
     w, inp, logits, bias = _inputs(name, T=T)
     bufs = _guarded_outputs(w.T, w.E, w.topk, w.block_m)
     v = {k: g.t for k, g in bufs.items()}
     mrs.moe_route_sort_debug_set(mrs.DEBUG_WAIT_LIMIT_NS, 0)
+    if not warp_grid:
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, 1 << 30)
     try:
         mrs.moe_route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
                            w.block_m, **v)
         torch.cuda.synchronize()
     finally:
         mrs.moe_route_sort_debug_set(mrs.DEBUG_WAIT_LIMIT_NS, -1)
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1)
     assert _status(v["workspace"]) & 0x2, "the timed-out waits were not reported"
     _assert_intact(bufs, "timed-out call")
     # the next call on the same stream, with the default limit, is correct
@@ -225,7 +231,8 @@ def test_moe_topk_and_gate_write_inside():
 
 
 # ------------------------------------------------------------------ proxy check
-@pytest.mark.parametrize("name,T", [("skewed_T8192_E896", 1500), ("wide_T16384_E4096", 600)])
+# sizes that take the pruning three-kernel path (the grid paths below them use exact keys)
+@pytest.mark.parametrize("name,T", [("skewed_T8192_E896", 1500), ("wide_T16384_E4096", 1100)])
 def test_failed_proxy_check_takes_exact_keys(name, T):
     w, inp, logits, bias = _inputs(name, T=T)
     ref = oracle.route_sort(inp.logits_bf16, inp.bias, w.n_group, w.topk_group, w.topk,

@@ -308,25 +308,34 @@ def test_moe_sort_flags_out_of_range_ids(T):
 
 
 # ------------------------------------------------------------------ CUDA graphs
-# every dispatch: one token, the single-CTA kernel, the per-token grid, the 16-CTA cluster and
-# the three-kernel path
-@pytest.mark.parametrize("name,T", [("decode_T1_E896_G8", None), ("prefill_T512_E896", 3),
-                                    ("prefill_T512_E896", 40), ("prefill_T512_E896", 200),
-                                    ("prefill_T512_E896", None), ("skewed_T8192_E896", 2048)])
-def test_graph_replay_with_changed_inputs(name, T):
+# every dispatch: one token, the single-CTA kernel, the per-token grid, the warp-per-token grid,
+# the 16-CTA cluster (with the warp grid switched off, as it would take T = 200) and the
+# three-kernel path
+@pytest.mark.parametrize("name,T,warp_grid", [("decode_T1_E896_G8", None, True),
+                                              ("prefill_T512_E896", 3, True),
+                                              ("prefill_T512_E896", 40, True),
+                                              ("prefill_T512_E896", None, True),
+                                              ("prefill_T512_E896", 200, False),
+                                              ("skewed_T8192_E896", 3000, True)])
+def test_graph_replay_with_changed_inputs(name, T, warp_grid):
     w, inp, _ = inputs_for(name, T=T)
     logits = to_dev_bf16(inp.logits_bf16)
     bias = torch.from_numpy(inp.bias).to(DEV)
     out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
     s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
-                       w.block_m, out=out)  # first call outside capture
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
-                       w.block_m, out=out)
+    # the hook is read when a call is enqueued: captured calls keep the path they took
+    mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1 if warp_grid else 1 << 30)
+    try:
+        with torch.cuda.stream(s):
+            mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                           w.block_m, out=out)  # first call outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale,
+                           w.block_m, out=out)
+    finally:
+        mrs.moe_route_sort_debug_set(mrs.DEBUG_WARP_GRID_TOKENS, -1)
     for seed in range(1, 9):
         ws = datagen.workload(name, T=w.T, seed=seed)
         new = datagen.make_inputs(ws, needs_redraw=redraw_callback(oracle, ws))
