@@ -360,23 +360,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) mrs_decode_kernel(const Dec
   else if (!kSoftmax && tid < 192)
     prefetch_l2_range(a.bias, 4 * static_cast<size_t>(a.E), tid - 64, 128);
   pdl_wait();
-  if (!kMulti) {
+  if constexpr (kGrid == 0) {
     decode_token<kSoftmax, kEpt, false>(a, sm, 0);
-    return;
-  }
-  if (kGrid == 1) {
+  } else if constexpr (kGrid == 1) {
     decode_token<kSoftmax, kEpt, true>(a, sm, t0);
     decode_grid_sort(a, sm, T);
-    return;
+  } else {
+    for (int t = t0; t < T; t += step) {
+      if (t + step < T && tid < 64)  // the CTA's next row starts towards L2
+        prefetch_l2_range(a.logits + static_cast<size_t>(t + step) * a.E,
+                          2 * static_cast<size_t>(a.E), tid, 64);
+      decode_token<kSoftmax, kEpt, true>(a, sm, t);
+      __syncthreads();  // the token's scratch is reused by the next one
+    }
+    decode_grid_sort(a, sm, T);
   }
-  for (int t = t0; t < T; t += step) {
-    if (t + step < T && tid < 64)  // the CTA's next row starts towards L2
-      prefetch_l2_range(a.logits + static_cast<size_t>(t + step) * a.E,
-                        2 * static_cast<size_t>(a.E), tid, 64);
-    decode_token<kSoftmax, kEpt, true>(a, sm, t);
-    __syncthreads();  // the token's scratch is reused by the next one
-  }
-  decode_grid_sort(a, sm, T);
 }
 
 // Both sort phases for T tokens on a cooperative grid (kMulti), every thread of every CTA:

@@ -282,14 +282,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
       }
       __syncthreads();
     }
-    if (kGrid) {
+    if constexpr (kGrid) {
       small_grid_sort(a, g0, gT, rid, rw, masks, cnt,
                       reinterpret_cast<int32_t*>(smem + a.lay.owner), off, misc);
-      return;
+    } else {
+      for (int e = tid; e < E; e += kSmallThreads)
+        cnt[e] = __popc(masks[e]) + __popc(masks[E + e]);
+      if (tid == 0) misc[0] = 0;
+      __syncthreads();
     }
-    for (int e = tid; e < E; e += kSmallThreads) cnt[e] = __popc(masks[e]) + __popc(masks[E + e]);
-    if (tid == 0) misc[0] = 0;
-    __syncthreads();
   } else {
     // ---------------------------------------- sort step only: ranks in flat route order
     for (int r = tid; r < N; r += kSmallThreads) {
@@ -322,37 +323,39 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mrs_small_kernel(const Small
     __syncthreads();
   }
 
-  // ------------------------------------------------ padded scan, scatter, padding
-  const int total = block_scan_padded<kSmallThreads>(cnt, off, E, B, misc + 4);
-  for (int r = tid; r < N; r += kSmallThreads) {
-    const int e = rid[r];
-    if (e < 0 || e >= E) continue;
-    int rank;
-    if (!kSortOnly) {
-      const int t = r / K;
-      rank = (t < 32) ? __popc(masks[e] & ((1u << t) - 1u))
-                      : __popc(masks[e]) + __popc(masks[E + e] & ((1u << (t - 32)) - 1u));
-    } else {
-      rank = reinterpret_cast<const int32_t*>(smem + a.lay.rrank)[r];
+  if constexpr (!kGrid) {
+    // ------------------------------------------------ padded scan, scatter, padding
+    const int total = block_scan_padded<kSmallThreads>(cnt, off, E, B, misc + 4);
+    for (int r = tid; r < N; r += kSmallThreads) {
+      const int e = rid[r];
+      if (e < 0 || e >= E) continue;
+      int rank;
+      if (!kSortOnly) {
+        const int t = r / K;
+        rank = (t < 32) ? __popc(masks[e] & ((1u << t) - 1u))
+                        : __popc(masks[e]) + __popc(masks[E + e] & ((1u << (t - 32)) - 1u));
+      } else {
+        rank = reinterpret_cast<const int32_t*>(smem + a.lay.rrank)[r];
+      }
+      const int pos = off[e] + rank;
+      a.sorted_ids[pos] = r;
+      a.sorted_w[pos] = rw[r];
     }
-    const int pos = off[e] + rank;
-    a.sorted_ids[pos] = r;
-    a.sorted_w[pos] = rw[r];
-  }
-  for (int e = tid; e < E; e += kSmallThreads) {
-    const int c = cnt[e];
-    if (c == 0) continue;
-    const int o = off[e];
-    const int p = (c + B - 1) & ~(B - 1);
-    for (int q = o + c; q < o + p; ++q) {
-      a.sorted_ids[q] = N;
-      a.sorted_w[q] = 0.0f;
+    for (int e = tid; e < E; e += kSmallThreads) {
+      const int c = cnt[e];
+      if (c == 0) continue;
+      const int o = off[e];
+      const int p = (c + B - 1) & ~(B - 1);
+      for (int q = o + c; q < o + p; ++q) {
+        a.sorted_ids[q] = N;
+        a.sorted_w[q] = 0.0f;
+      }
+      for (int b = o / B; b < (o + p) / B; ++b) a.expert_ids[b] = e;
     }
-    for (int b = o / B; b < (o + p) / B; ++b) a.expert_ids[b] = e;
-  }
-  if (tid == 0) {
-    *a.npp = total;
-    *a.status = misc[0];
+    if (tid == 0) {
+      *a.npp = total;
+      *a.status = misc[0];
+    }
   }
 }
 
