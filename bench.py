@@ -44,6 +44,7 @@ from moe_expert_routing_sort_gb300 import datagen  # noqa: E402
 
 HEADLINE = "decode_T1_E896_G8"
 SECONDARY = ["prefill_T512_E896", "skewed_T8192_E896", "wide_T16384_E4096"]
+SWEEP_TOKENS = [2, 8, 64, 152, 192, 384, 768, 1024, 1536, 2048, 3072, 4096]
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024
 METRIC = "route-sort µs/call at T=1 E=896; routed tokens/s and % HBM roofline at T≥512"
@@ -745,6 +746,17 @@ def main():
                 configs[name]["sort_only_us"] = {
                     "deterministic": measure_sort_only(ws, n, args.warmup, world, False),
                     "atomic_order": measure_sort_only(ws, n, args.warmup, world, True)}
+
+    if not args.no_secondary:
+        # per-call latency across token counts at the prefill shape (E = 896, G = 8, K = 16),
+        # over the dispatch: one token, the single-CTA kernel, the per-token cooperative grid,
+        # the warp-per-token cooperative grid and the three-kernel path
+        sweep = {}
+        for T in SWEEP_TOKENS:
+            ws = datagen.workload("prefill_T512_E896", T=T)
+            r = measure_workload(ws, max(3, min(args.steps, 10)), args.warmup, world, peak)
+            sweep[str(T)] = r["us_per_call"]
+        configs["prefill_E896_token_sweep"] = {"unit": "us/call", "us_per_call": sweep}
 
     if not args.no_secondary:
         # the router gate projection fused ahead of the path (batch-one decode shape)

@@ -128,8 +128,15 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ float proxy_key(float x, float bias) {
-  return fmaf(0.5f, tanh_approx(0.5f * x), bias);
+// Half of each bf16 of the pair w (low half -> lo), as fp32: one bf16-operand FMA each,
+// x * 0.5 + (-0), whose product is exact and unrounded, so the result equals 0.5f * x bit for
+// bit (the argument of tanh.approx in the proxy score 0.5 * tanh.approx(0.5 x) + bias, the form
+// the in-library check verifies) without a separate unpack.
+__device__ __forceinline__ void half_bf16x2(uint32_t w, float& lo, float& hi) {
+  asm("{ .reg .b16 l, u, c; mov.b16 c, 0x3F00; mov.b32 {l, u}, %2;\n"
+      " fma.rn.f32.bf16 %0, l, c, 0f80000000; fma.rn.f32.bf16 %1, u, c, 0f80000000; }"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
 }
 
 // Exact key and score of one logit: key = s + bias with s the exact score.

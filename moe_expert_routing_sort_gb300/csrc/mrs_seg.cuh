@@ -108,10 +108,13 @@ struct ProxyRow {
   const float* bias;    // [E] shared memory
   __device__ __forceinline__ void values(int e0, uint2 w, float (&v)[4]) const {
     const float4 bb = *reinterpret_cast<const float4*>(bias + e0);
-    v[0] = proxy_key(__uint_as_float(w.x << 16), bb.x);
-    v[1] = proxy_key(__uint_as_float(w.x & 0xffff0000u), bb.y);
-    v[2] = proxy_key(__uint_as_float(w.y << 16), bb.z);
-    v[3] = proxy_key(__uint_as_float(w.y & 0xffff0000u), bb.w);
+    float h[4];
+    half_bf16x2(w.x, h[0], h[1]);
+    half_bf16x2(w.y, h[2], h[3]);
+    v[0] = fmaf(0.5f, tanh_approx(h[0]), bb.x);
+    v[1] = fmaf(0.5f, tanh_approx(h[1]), bb.y);
+    v[2] = fmaf(0.5f, tanh_approx(h[2]), bb.z);
+    v[3] = fmaf(0.5f, tanh_approx(h[3]), bb.w);
   }
   __device__ __forceinline__ uint2 late_words(int e0) const {
     return *reinterpret_cast<const uint2*>(row + e0);
