@@ -255,7 +255,7 @@ int moe_route_sort_from_host(const void* logits_host, void* logits_dev, const fl
  * 9.3 MiB and is accepted); shapes are checked before that, and a rejected call touches
  * nothing.  The first call on each device context looks up the array's device address with
  * that device current and caches it (a context created again, for example after
- * cudaDeviceReset, gets a fresh lookup); make that first call before any stream capture.
+ * cudaDeviceReset, gets a fresh lookup).
  * All calls on a device share the one array and it keeps whatever the previous call left in
  * it (the path needs no zeroed scratch); two calls that can run on the GPU at the same time
  * (different streams, or graphs replayed concurrently) race on it and give wrong results.

@@ -273,15 +273,33 @@ __device__ __forceinline__ float seg_kth_desc4(float v0, float v1, float v2, flo
   return r == 0 ? a0 : (r == 1 ? a1 : (r == 2 ? a2 : a3));
 }
 
-// Pass-1 summary of a lane: top-2 over its segment in V interleaved parts (part = unit
-// step modulo V).  The parts cover disjoint experts, so V parts give the threshold of the
-// selection as many samples as V times the lanes.
+// Pass-1 summary of a lane: with one part, the top-2 values of its segment; with two
+// interleaved parts (part = unit step modulo 2), in each part the largest and second-largest
+// unit maximum, which are values of two distinct experts (of two units).  s2 is the lane's
+// true second-largest value over its whole segment either way.  The parts cover disjoint
+// experts, so V parts give the threshold of the selection twice V samples per lane.
 struct LaneTop {
   float a1, a2;  // part 0
   float b1, b2;  // part 1 (-inf when V == 1)
+  float s2;      // second-largest value of the segment (= m1() when the largest occurs twice)
   __device__ __forceinline__ float m1() const { return fmaxf(a1, b1); }
-  __device__ __forceinline__ float m2() const { return max3f(fminf(a1, b1), a2, b2); }
+  __device__ __forceinline__ float m2() const { return s2; }
 };
+
+// Second-largest of 4 values.
+__device__ __forceinline__ float second_of4(const float (&v)[4]) {
+  const float h0 = fmaxf(v[0], v[1]), l0 = fminf(v[0], v[1]);
+  const float h1 = fmaxf(v[2], v[3]), l1 = fminf(v[2], v[3]);
+  return max3f(fminf(h0, h1), l0, l1);
+}
+
+// A unit's maximum enters its part's top-2 of unit maxima (best unit in ubest).
+__device__ __forceinline__ void unit_max_insert(float mx, int u, float& m1, float& m2,
+                                                int& ubest) {
+  ubest = (mx > m1) ? u : ubest;
+  m2 = fmaxf(m2, fminf(m1, mx));
+  m1 = fmaxf(m1, mx);
+}
 
 // ------------------------------------------------------------------------ pass 1
 // umax: the warp's unit bounds.  Lanes of an invalid token (or beyond the groups) return
@@ -292,26 +310,51 @@ __device__ __forceinline__ LaneTop seg_pass1(const Row& row, const SegShape& sh,
   static_assert(V == 1 || V == 2, "one or two parts per lane");
   const int ll = lane & (LT - 1);
   const int j = ll >> sh.log2L;
-  LaneTop r{-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  LaneTop r{-INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY};
   if (!token_valid || j >= sh.G) return r;
   const int seg0 = j * sh.g + (ll & (sh.L - 1)) * sh.sl;
   int u = (lane * sh.rot) % sh.nu;
-  int k = 0;
-#pragma unroll (4 / V)
-  for (; k + V <= sh.nu; k += V) {
-#pragma unroll
-    for (int p = 0; p < V; ++p) {
+  if constexpr (V == 1) {
+    // one part: the exact top-2 of every unit enters the running top-2
+#pragma unroll 4
+    for (int k = 0; k < sh.nu; ++k) {
       float v[4];
       row.unit(seg0 + 4 * u, v);
-      umax[ub_index(lane, u)] =
-          ub_half(p == 0 ? top2_unit(v, r.a1, r.a2) : top2_unit(v, r.b1, r.b2));
+      umax[ub_index(lane, u)] = ub_half(top2_unit(v, r.a1, r.a2));
       u = (u + 1 == sh.nu) ? 0 : u + 1;
     }
-  }
-  if (k < sh.nu) {  // odd unit count with two parts
+    r.s2 = r.a2;
+  } else {
+    // two parts: only each unit's maximum enters its part's top-2 (fewer operations per
+    // unit); the segment's second value is then the other part's best, a runner-up unit
+    // maximum, or the second value inside the unit that holds the largest
+    int ua = u, ub = u;  // unit holding a1 / b1
+    int k = 0;
+#pragma unroll 2
+    for (; k + 2 <= sh.nu; k += 2) {
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float v[4];
+        row.unit(seg0 + 4 * u, v);
+        const float mx = max3f(v[0], v[1], fmaxf(v[2], v[3]));
+        if (p == 0)
+          unit_max_insert(mx, u, r.a1, r.a2, ua);
+        else
+          unit_max_insert(mx, u, r.b1, r.b2, ub);
+        umax[ub_index(lane, u)] = ub_half(mx);
+        u = (u + 1 == sh.nu) ? 0 : u + 1;
+      }
+    }
+    if (k < sh.nu) {  // odd unit count
+      float v[4];
+      row.unit(seg0 + 4 * u, v);
+      const float mx = max3f(v[0], v[1], fmaxf(v[2], v[3]));
+      unit_max_insert(mx, u, r.a1, r.a2, ua);
+      umax[ub_index(lane, u)] = ub_half(mx);
+    }
     float v[4];
-    row.unit(seg0 + 4 * u, v);
-    umax[ub_index(lane, u)] = ub_half(top2_unit(v, r.a1, r.a2));
+    row.unit(seg0 + 4 * ((r.a1 >= r.b1) ? ua : ub), v);
+    r.s2 = max3f(fminf(r.a1, r.b1), fmaxf(r.a2, r.b2), second_of4(v));
   }
   return r;
 }
