@@ -24,6 +24,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -248,8 +249,7 @@ class Replica:
         self.w = w
         self.sets = []
         for i in range(n_sets):
-            inp = datagen.make_inputs(datagen.workload(w.name, seed=w.seed + i) if w.name in
-                                      datagen.WORKLOADS else w)
+            inp = datagen.make_inputs(dataclasses.replace(w, seed=w.seed + i))
             logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).cuda()
             bias = torch.from_numpy(inp.bias).cuda()
             out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device="cuda")
@@ -267,7 +267,12 @@ class Replica:
 
 
 def launches_per_call(w) -> int:
-    return 1 if w.T <= 64 else 3
+    """Kernels one route-sort call launches: one for T <= 3 (the one-token or single-CTA
+    kernel), two from 4 to 2048 tokens (the zeroing kernel and a cooperative grid), three
+    above (route, slices, scatter)."""
+    if w.T <= 3:
+        return 1
+    return 2 if w.T <= 2048 else 3
 
 
 def time_graph_steps(rep: Replica, steps: int, warmup: int, world: int, clocks=None):
