@@ -267,10 +267,10 @@ class Replica:
 
 
 def launches_per_call(w) -> int:
-    """Kernels one route-sort call launches: one for T <= 3 (the one-token or single-CTA
-    kernel), two from 4 to 2048 tokens (the zeroing kernel and a cooperative grid), three
+    """Kernels one route-sort call launches: one for T <= 4 (the one-token or single-CTA
+    kernel), two from 5 to 2048 tokens (the zeroing kernel and a cooperative grid), three
     above (route, slices, scatter)."""
-    if w.T <= 3:
+    if w.T <= 4:
         return 1
     return 2 if w.T <= 2048 else 3
 

@@ -322,13 +322,13 @@ int moe_route_sort_proxy_state(int32_t* dst, cudaStream_t stream);
  *                                  every other multi-token path but the warp-per-token grid;
  *                                  2 <= T <= min(320, value));
  *                                  0 turns it off, a negative value restores the default
- *                                  (4 <= T <= 320, when the grid's shared memory fits).
+ *                                  (5 <= T <= 320, when the grid's shared memory fits).
  *   MOE_RS_DEBUG_WARP_GRID_TOKENS  moe_route_sort and moe_route_sort_softmax run calls of
  *                                  more than `value` tokens (and at least 2) on a cooperative
  *                                  grid with one warp per token and up to 16 tokens per CTA
  *                                  (taken before every other multi-token path, while
  *                                  ceil(T / #SMs) <= 16 and its shared memory fits); a negative
- *                                  value restores the default (#SMs < T <= 2048).
+ *                                  value restores the default (128 < T <= 2048).
  *                                  The paths give the same outputs; these hooks let tests
  *                                  compare them on one shape.
  * Returns MOE_RS_OK or MOE_RS_ERR_BAD_DEBUG_KNOB. */

@@ -284,12 +284,15 @@ cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, cudaStream_t st);
 // bounded grid-wide barrier on a.bar; a one-thread kernel ahead of it zeroes a.bar and the
 // status word.  decode_grid_smem: the grid kernel's dynamic shared memory.
 constexpr int kDecodeGridTokens = 320;
-// Default lower end of that path: for two or three tokens the single-CTA kernel is faster
-// (measured: T = 2 7.7 against 9.8 us per call).
-constexpr int kDecodeGridMinTokens = 4;
-// Largest T of the warp-per-token grid path by default (launch_small_grid).  Measured per call
-// (E = 896, K = 16, graph of calls, L2 flushed), against the next path down: T = 512 10.3 against
-// 16.9 us, T = 1536 15.8 against 19.0, T = 2048 18.9 against 19.1.
+// Default lower end of that path: up to four tokens the single-CTA kernel is faster
+// (measured per call: T = 2 7.7 against 9.8 us, T = 4 8.9 against 9.6).
+constexpr int kDecodeGridMinTokens = 5;
+// Default reach of the warp-per-token grid path (launch_small_grid): kWarpGridMinTokens <= T <=
+// kWarpGridTokens, below it the per-token grid.  Measured per call (E = 896, K = 16, graph of
+// calls, L2 flushed): T = 64 9.1 against 8.9 us on the per-token grid, T = 128 9.4 against 9.4,
+// T = 152 9.6 against 9.9; T = 512 10.3 against 16.9 on the three-kernel path, T = 1536 15.8
+// against 19.0, T = 2048 18.9 against 19.1.
+constexpr int kWarpGridMinTokens = 129;
 constexpr int kWarpGridTokens = 2048;
 cudaError_t launch_decode_grid(const DecodeArgs& a, int ctas, cudaStream_t st);
 // One-thread kernel that zeroes a grid path's barrier and status words once the kernel ahead
@@ -317,7 +320,8 @@ bool cluster_reach_sort(int T, int E, int K, int B);
 bool decode_grid_reach(int T);
 // Whether a call of T tokens takes the warp-per-token grid path on a device of `sms` SMs, and
 // with how many tokens per CTA (`per`, at most 16, so that ceil(T / per) <= sms): by default
-// sms < T <= kWarpGridTokens; T > limit (and T >= 2) once the test hook has set a limit.
+// kWarpGridMinTokens <= T <= kWarpGridTokens; T > limit (and T >= 2) once the test hook has
+// set a limit.
 bool warp_grid_reach(int T, int sms, int& per);
 // Identity of the current device and context (the context's unique id, 0 if the driver cannot
 // tell): host caches of device addresses are keyed on it.

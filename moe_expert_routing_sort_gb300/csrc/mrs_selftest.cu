@@ -135,7 +135,7 @@ bool decode_grid_reach(int T) {
 bool warp_grid_reach(int T, int sms, int& per) {
   if (T < 2 || sms < 1) return false;
   const int v = g_warp_grid_tokens.load(std::memory_order_relaxed);
-  if (v < 0 ? (T <= sms || T > kWarpGridTokens) : T <= v) return false;
+  if (v < 0 ? (T < kWarpGridMinTokens || T > kWarpGridTokens) : T <= v) return false;
   per = (T + sms - 1) / sms;
   return per <= 16;
 }

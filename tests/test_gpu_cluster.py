@@ -1,8 +1,8 @@
-"""The one-launch paths of moe_route_sort and moe_sort.  Calls of more than one token per SM
-up to 2048 tokens run on a cooperative grid with one warp per token (up to 16 tokens per CTA);
-calls of 4 tokens up to the SM count (2 to 320 with the test hook) on a cooperative grid with one
-CTA per token (up to four per CTA past the SM count); both exchange the selected ids through
-the workspace around one grid-wide barrier.  For mid-sized calls (by default up to 256 tokens
+"""The one-launch paths of moe_route_sort and moe_sort.  Calls of 129 to 2048 tokens run on a
+cooperative grid with one warp per token (up to 16 tokens per CTA); calls of 5 to 128 tokens
+(2 to 320 with the test hook) on a cooperative grid with one CTA per token (up to four per CTA
+past the SM count); both exchange the selected ids through the workspace around one grid-wide
+barrier.  For mid-sized calls (by default up to 256 tokens
 and at most 512 KiB of logits, segment-shaped groups; the grid paths are switched off in those
 tests) one cluster of 16 CTAs runs the route step and both sort phases in a single launch,
 exchanging per-expert counts through distributed shared memory.  Every case is compared with the CPU oracle bit for
@@ -411,7 +411,10 @@ def test_warp_grid_softmax(T):
     assert out.status_word() == 0
 
 
-@pytest.mark.parametrize("name,T,path", [("prefill_T512_E896", 64, "grid"),
+@pytest.mark.parametrize("name,T,path", [("prefill_T512_E896", 4, "one-launch"),
+                                          ("prefill_T512_E896", 5, "grid"),
+                                          ("prefill_T512_E896", 64, "grid"),
+                                          ("prefill_T512_E896", 129, "grid"),
                                           ("prefill_T512_E896", 512, "grid"),
                                           ("prefill_T512_E896", 2048, "grid"),
                                           ("prefill_T512_E896", 2049, "three"),
