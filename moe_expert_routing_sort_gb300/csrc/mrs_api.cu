@@ -123,6 +123,75 @@ RouteShape make_shape(int E, int G, int Kg, int K, float R) {
   return sh;
 }
 
+// Shared-memory wavefronts of pass 1 (mrs_seg.cuh) over one sweep of the units, for the
+// start rule ((l * rot) >> rsh) % nu: lane l of a token loads 8 bytes of its row at expert
+// e0 = j g + q sl + 4 u (the tokens of a warp step sit in consecutive row buffers; half-warp
+// phases) and the 16 bytes of bias at e0 (quarter-warp phases); a phase costs as many
+// wavefronts as the most distinct words any bank serves.
+int pass1_wavefronts(const SegShape& s, int lanes, int rot, int rsh) {
+  int total = 0;
+  for (int k = 0; k < s.nu; ++k) {
+    for (int width = 16; width >= 8; width >>= 1) {  // 16: row loads, 8: bias loads
+      const int bytes = (width == 16) ? 8 : 16;
+      for (int p0 = 0; p0 < 32; p0 += width) {
+        int words[32][16];
+        int nw[32] = {0};
+        int worst = 1;
+        for (int lane = p0; lane < p0 + width; ++lane) {
+          const int h = lane / lanes, ll = lane % lanes;
+          const int j = ll >> s.log2L, q = ll & (s.L - 1);
+          if (j >= s.G) continue;
+          const int u = (((ll * rot) >> rsh) + k) % s.nu;
+          const long e0 = static_cast<long>(j) * s.g + static_cast<long>(q) * s.sl + 4 * u;
+          const long addr = (width == 16) ? (static_cast<long>(h) * s.E * 2 + 2 * e0) : 4 * e0;
+          const int w = static_cast<int>(addr / bytes);
+          for (int b = 0; b < bytes / 4; ++b) {
+            const int bank = static_cast<int>((addr / 4 + b) % 32);
+            bool seen = false;
+            for (int i = 0; i < nw[bank]; ++i) seen |= (words[bank][i] == w);
+            if (!seen && nw[bank] < 16) words[bank][nw[bank]++] = w;
+            worst = nw[bank] > worst ? nw[bank] : worst;
+          }
+        }
+        total += worst;
+      }
+    }
+  }
+  return total;
+}
+
+// The start rule of pass 1 with the fewest simulated wavefronts (ties keep the plain order,
+// then the smaller rotation); remembered per shape and thread.
+void choose_unit_order(SegShape& s, int lanes) {
+  struct Entry {
+    int E, G, lanes, rot, rsh;
+  };
+  thread_local Entry cache[8] = {};
+  thread_local int next = 0;
+  for (const Entry& c : cache) {
+    if (c.lanes == lanes && c.E == s.E && c.G == s.G) {
+      s.rot = c.rot;
+      s.rsh = c.rsh;
+      return;
+    }
+  }
+  int best_rot = 0, best_rsh = 0, best = pass1_wavefronts(s, lanes, 0, 0);
+  for (int rot = 1; rot <= 3; ++rot) {
+    for (int rsh = 0; rsh <= 3; ++rsh) {
+      const int c = pass1_wavefronts(s, lanes, rot, rsh);
+      if (c < best) {
+        best = c;
+        best_rot = rot;
+        best_rsh = rsh;
+      }
+    }
+  }
+  s.rot = best_rot;
+  s.rsh = best_rsh;
+  cache[next] = Entry{s.E, s.G, lanes, best_rot, best_rsh};
+  next = (next + 1) % 8;
+}
+
 // Segment layout of the route step (see mrs_seg.cuh) for `lanes` lanes per token: groups
 // split into L lanes of equal, 4-expert-aligned segments.  False when the shape does not
 // allow it.
@@ -144,9 +213,7 @@ bool make_seg_shape(int E, int G, int Kg, int K, float R, int lanes, SegShape& s
   while ((1 << s.log2L) < L) ++s.log2L;
   s.sl = sl;
   s.nu = sl / 4;
-  // when segments are a multiple of 128 bytes of keys apart, rotate each lane's unit order
-  // so that lanes of one shared-memory phase hit different banks
-  s.rot = (s.nu % 8 == 0) ? 1 : 0;
+  choose_unit_order(s, lanes);
   s.R = R;
   return true;
 }

@@ -35,7 +35,8 @@ struct SegShape {
   int L, log2L;  // lanes per group (power of two); G * L <= lanes per token
   int sl;        // experts per lane segment (multiple of 4, at most 256)
   int nu;        // units of 4 experts per segment (at most 64)
-  int rot;       // unit order of lane l starts at (l * rot) % nu (spreads smem banks)
+  int rot, rsh;  // unit order of lane l (of its token) starts at ((l * rot) >> rsh) % nu:
+                 // spreads pass 1's shared-memory loads over the banks (chosen per shape)
   float R;
   int softmax;   // 1: values are the logits (LogitRow), weights the renormalised softmax
 };
@@ -313,7 +314,7 @@ __device__ __forceinline__ LaneTop seg_pass1(const Row& row, const SegShape& sh,
   LaneTop r{-INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY};
   if (!token_valid || j >= sh.G) return r;
   const int seg0 = j * sh.g + (ll & (sh.L - 1)) * sh.sl;
-  int u = (lane * sh.rot) % sh.nu;
+  int u = ((ll * sh.rot) >> sh.rsh) % sh.nu;
   if constexpr (V == 1) {
     // one part: the exact top-2 of every unit enters the running top-2
 #pragma unroll 4
