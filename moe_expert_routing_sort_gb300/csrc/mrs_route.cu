@@ -91,14 +91,21 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
         if (idx < total) {
           const int tl = idx / nv, v = idx - tl * nv;
           const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-          float* kr = keys + tl * E + 8 * v;
-          float* sr = svals + tl * E + 8 * v;
+          float k8[8], s8[8];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            kr[2 * j] = score_key(__uint_as_float(wd[j] << 16), bb[u][2 * j], sm, sr[2 * j]);
-            kr[2 * j + 1] = score_key(__uint_as_float(wd[j] & 0xffff0000u), bb[u][2 * j + 1],
-                                      sm, sr[2 * j + 1]);
+            k8[2 * j] = score_key(__uint_as_float(wd[j] << 16), bb[u][2 * j], sm, s8[2 * j]);
+            k8[2 * j + 1] = score_key(__uint_as_float(wd[j] & 0xffff0000u), bb[u][2 * j + 1],
+                                      sm, s8[2 * j + 1]);
           }
+          // 16-byte stores (E % 8 == 0 keeps every row's 8-key chunks 32-byte aligned): a
+          // warp's scalar stores 32 bytes apart would hit only 4 banks
+          float4* kr = reinterpret_cast<float4*>(keys + tl * E + 8 * v);
+          float4* sr = reinterpret_cast<float4*>(svals + tl * E + 8 * v);
+          kr[0] = make_float4(k8[0], k8[1], k8[2], k8[3]);
+          kr[1] = make_float4(k8[4], k8[5], k8[6], k8[7]);
+          sr[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
+          sr[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
         }
       }
     }
