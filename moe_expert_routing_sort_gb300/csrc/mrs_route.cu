@@ -72,6 +72,8 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
     // 16-byte vectors of 8 logits; the matching 8 biases come from global alongside
     const int nv = E >> 3;
     const int total = nt * nv;
+    // a 16-byte aligned bias (the usual case) comes as two 16-byte vectors per chunk
+    const bool b16 = !sm && (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0u;
     for (int base = threadIdx.x; base < total; base += kSmallThreads * 4) {
       uint4 q[4];
       float bb[4][8];
@@ -81,8 +83,21 @@ __device__ __forceinline__ void small_scores(const SmallArgs& a, int t0, int nt,
         if (idx < total) {
           const int tl = idx / nv, v = idx - tl * nv;
           q[u] = reinterpret_cast<const uint4*>(a.logits + static_cast<size_t>(t0 + tl) * E)[v];
+          if (b16) {
+            const float4 b0 = reinterpret_cast<const float4*>(a.bias)[2 * v];
+            const float4 b1 = reinterpret_cast<const float4*>(a.bias)[2 * v + 1];
+            bb[u][0] = b0.x;
+            bb[u][1] = b0.y;
+            bb[u][2] = b0.z;
+            bb[u][3] = b0.w;
+            bb[u][4] = b1.x;
+            bb[u][5] = b1.y;
+            bb[u][6] = b1.z;
+            bb[u][7] = b1.w;
+          } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) bb[u][j] = sm ? 0.0f : a.bias[8 * v + j];
+            for (int j = 0; j < 8; ++j) bb[u][j] = sm ? 0.0f : a.bias[8 * v + j];
+          }
         }
       }
 #pragma unroll
