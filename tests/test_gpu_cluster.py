@@ -425,3 +425,20 @@ def test_default_dispatch(name, T, path):
     out, _ = _run(w, inp, -1, grid=-1, warp=-1)
     assert _path(out) == path
     _assert_matches(out, ref, w)
+
+
+@pytest.mark.parametrize("T", [3, 300])
+def test_bias_not_16_byte_aligned(T):
+    # the exact-key step reads 16-byte bias vectors only from a 16-byte aligned bias; a bias one
+    # float into a buffer takes the 4-byte loads
+    w, inp, ref = _case("prefill_T512_E896", T)
+    logits = torch.from_numpy(inp.logits_bf16.view(np.int16)).view(torch.bfloat16).to(DEV)
+    store = torch.zeros(w.E + 1, dtype=torch.float32, device=DEV)
+    store[1:] = torch.from_numpy(inp.bias).to(DEV)
+    bias = store[1:]
+    assert bias.data_ptr() % 16 != 0
+    out = mrs.RouteSortBuffers.allocate(w.T, w.E, w.topk, w.block_m, device=DEV)
+    mrs.route_sort(logits, bias, w.n_group, w.topk_group, w.topk, w.routed_scale, w.block_m,
+                   out=out)
+    torch.cuda.synchronize()
+    _assert_matches(out, ref, w)
