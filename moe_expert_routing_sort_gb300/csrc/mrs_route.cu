@@ -516,13 +516,24 @@ __global__ void __launch_bounds__(512) mrs_route_kernel(const RouteArgs a) {
       for (int v = lane; v < nv; v += 32) {
         const uint4 q = __ldcs(r4 + v);
         const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        // 16-byte shared-memory accesses (the bias and the per-warp key and score rows are
+        // 16-byte aligned, E % 8 == 0): scalar ones 32 bytes apart would hit 4 banks
+        const float4 b0 = reinterpret_cast<const float4*>(bias_s)[2 * v];
+        const float4 b1 = reinterpret_cast<const float4*>(bias_s)[2 * v + 1];
+        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        float k8[8], s8[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int e = v * 8 + 2 * j;
-          key[e] = score_key(__uint_as_float(wd[j] << 16), bias_s[e], sm, sv[e]);
-          key[e + 1] =
-              score_key(__uint_as_float(wd[j] & 0xffff0000u), bias_s[e + 1], sm, sv[e + 1]);
+          k8[2 * j] = score_key(__uint_as_float(wd[j] << 16), bb[2 * j], sm, s8[2 * j]);
+          k8[2 * j + 1] =
+              score_key(__uint_as_float(wd[j] & 0xffff0000u), bb[2 * j + 1], sm, s8[2 * j + 1]);
         }
+        float4* kr = reinterpret_cast<float4*>(key + 8 * v);
+        float4* sr = reinterpret_cast<float4*>(sv + 8 * v);
+        kr[0] = make_float4(k8[0], k8[1], k8[2], k8[3]);
+        kr[1] = make_float4(k8[4], k8[5], k8[6], k8[7]);
+        sr[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
+        sr[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
       }
     } else {
       for (int e = lane; e < E; e += 32) {
