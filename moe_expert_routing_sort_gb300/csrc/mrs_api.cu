@@ -123,14 +123,14 @@ RouteShape make_shape(int E, int G, int Kg, int K, float R) {
   return sh;
 }
 
-// Shared-memory wavefronts of pass 1 (mrs_seg.cuh) over one sweep of the units, for the
-// start rule ((l * rot) >> rsh) % nu: lane l of a token loads 8 bytes of its row at expert
-// e0 = j g + q sl + 4 u (the tokens of a warp step sit in consecutive row buffers; half-warp
-// phases) and the 16 bytes of bias at e0 (quarter-warp phases); a phase costs as many
-// wavefronts as the most distinct words any bank serves.
+// Shared-memory wavefronts of pass 1 (mrs_seg.cuh) over its first 16 unit steps (the pattern
+// repeats after nu), for the start rule ((l * rot) >> rsh) % nu: lane l of a token loads 8
+// bytes of its row at expert e0 = j g + q sl + 4 u (the tokens of a warp step sit in
+// consecutive row buffers; half-warp phases) and the 16 bytes of bias at e0 (quarter-warp
+// phases); a phase costs as many wavefronts as the most distinct words any bank serves.
 int pass1_wavefronts(const SegShape& s, int lanes, int rot, int rsh) {
   int total = 0;
-  for (int k = 0; k < s.nu; ++k) {
+  for (int k = 0; k < (s.nu < 16 ? s.nu : 16); ++k) {
     for (int width = 16; width >= 8; width >>= 1) {  // 16: row loads, 8: bias loads
       const int bytes = (width == 16) ? 8 : 16;
       for (int p0 = 0; p0 < 32; p0 += width) {
@@ -160,8 +160,9 @@ int pass1_wavefronts(const SegShape& s, int lanes, int rot, int rsh) {
   return total;
 }
 
-// The start rule of pass 1 with the fewest simulated wavefronts (ties keep the plain order,
-// then the smaller rotation); remembered per shape and thread.
+// The start rule of pass 1 with the fewest simulated wavefronts among rot 0 and rot 1 with a
+// shift of 0 to 3 (ties keep the plain order, then the smaller shift); remembered per shape
+// and thread.  The first call of a shape spends at most about 0.15 ms of host time on it.
 void choose_unit_order(SegShape& s, int lanes) {
   struct Entry {
     int E, G, lanes, rot, rsh;
@@ -176,14 +177,12 @@ void choose_unit_order(SegShape& s, int lanes) {
     }
   }
   int best_rot = 0, best_rsh = 0, best = pass1_wavefronts(s, lanes, 0, 0);
-  for (int rot = 1; rot <= 3; ++rot) {
-    for (int rsh = 0; rsh <= 3; ++rsh) {
-      const int c = pass1_wavefronts(s, lanes, rot, rsh);
-      if (c < best) {
-        best = c;
-        best_rot = rot;
-        best_rsh = rsh;
-      }
+  for (int rsh = 0; rsh <= 3; ++rsh) {
+    const int c = pass1_wavefronts(s, lanes, 1, rsh);
+    if (c < best) {
+      best = c;
+      best_rot = 1;
+      best_rsh = rsh;
     }
   }
   s.rot = best_rot;
